@@ -1,0 +1,138 @@
+/*
+ * qwp -- batched-prefill GEMM over 4-bit quantized weights on GB300 (sm_103a).
+ *
+ * C ABI.  Every pointer argument named *_dev is a device pointer; every call
+ * is asynchronous and ordered on `stream` (a cudaStream_t passed as void*,
+ * NULL = the legacy default stream) and never synchronizes the host, except
+ * qwp_device_status.  The caller owns and allocates every buffer; no entry
+ * point allocates device memory.  Every entry point returns QWP_OK (0) or a
+ * negative qwp_status; none throws.  Calls are thread-safe.
+ *
+ * The method (web pages, by title and section):
+ *  - "The dequant scratch round-trip is ZINC's last RDNA4 prefill tax",
+ *    sections "The two passes hiding inside one matmul" and "What the
+ *    roofline says": y = x . W^T where each 4-bit weight block is read from
+ *    memory once (0.5625 byte per Q4_K weight), unpacked on chip and consumed
+ *    by the matmul tile; no 16-bit copy of the weights is ever written.
+ *  - "How ZINC's RDNA4 batched prefill went from 42 to 208 tok/s", sections
+ *    "The two prefill paths" and "The fix: K-parallel batched DMMV": each
+ *    weight row is read once per chunk of prompt tokens and applied to all of
+ *    them; a stripe decodes as factor * q - bias.
+ *  - "[ROCm][Perf] W4A16: packed fp16 prefill dequant", section "1. Packed
+ *    fp16 dequant": the interleaved int4 word and the exact 0x6400|n unpack.
+ *
+ * Shapes.  x is [M, K] row-major, W is [N, K] (K contiguous within a row),
+ * y is [M, N] row-major fp32 and is overwritten (y = x . W^T).
+ */
+#ifndef QWP_H
+#define QWP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QWP_API __attribute__((visibility("default")))
+#else
+#define QWP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QWP_OK = 0,
+    QWP_ERR_INVALID_ARG = -1,      /* null pointer, negative size, bad group size      */
+    QWP_ERR_UNSUPPORTED_SHAPE = -2,/* K not a multiple of 256 (Q4_K) or of 64/group     */
+    QWP_ERR_MISALIGNED = -3,       /* a device pointer is not 16-byte aligned            */
+    QWP_ERR_CUDA = -4,             /* a CUDA runtime/driver call or a launch failed      */
+    QWP_ERR_DEVICE = -5,           /* the current device is not an sm_103 GPU            */
+    QWP_ERR_TIMEOUT = -6           /* a kernel's bounded wait expired (qwp_device_status) */
+} qwp_status;
+
+/* Human-readable name of a status code (static string). */
+QWP_API const char *qwp_status_string(int status);
+
+/*
+ * Q4_K (GGML super-blocks of 256 weights along K, 144 bytes each: fp16 d,
+ * fp16 dmin, 12 bytes of packed 6-bit scales[8]/mins[8], 128 bytes of
+ * nibbles; w = d*sc_j*q - dmin*m_j).  Source: the GGML block format and the
+ * "factor * q - bias" stripe of "How ZINC's RDNA4 batched prefill went from
+ * 42 to 208 tok/s", section "The fix: K-parallel batched DMMV".
+ */
+
+/* Bytes of a repacked Q4_K matrix: N*K/256*144 (the repack is a byte permutation). */
+QWP_API int q4k_repacked_bytes(int64_t N, int64_t K, size_t *out_bytes);
+
+/*
+ * Load-time repack of GGML Q4_K rows (w_ggml_dev: N rows of K/256 blocks,
+ * row-major, N*K/256*144 bytes) into the tile-major order the GEMM streams
+ * (w_tiled_dev, same size, caller-allocated, must not alias w_ggml_dev):
+ * rows in tiles of 128; per tile and super-block a 16-byte header plane and
+ * four 32-byte nibble planes.  K % 256 == 0.  Both pointers 16-byte aligned.
+ */
+QWP_API int q4k_repack(const void *w_ggml_dev, void *w_tiled_dev, int64_t N, int64_t K, void *stream);
+
+/*
+ * Test entry point: dequantize a repacked Q4_K matrix to fp32 w_out_dev[N][K].
+ * Each value is the correctly rounded fp32 of d*sc*q - dmin*m (exact for all
+ * finite fp16 d, dmin whose products fit fp32's range), computed by the same
+ * unpack the GEMM uses.
+ */
+QWP_API int q4k_dequant(const void *w_tiled_dev, float *w_out_dev, int64_t N, int64_t K, void *stream);
+
+/*
+ * y_dev[M][N] (fp32) = x_dev[M][K] (bf16) . W^T, W the repacked Q4_K matrix.
+ * Each weight is rounded once to bf16 after an exact fp32 dequant and fed to
+ * the tensor cores (tcgen05, fp32 accumulation in tensor memory).  K % 256 ==
+ * 0; M, N >= 0 (M == 0 or N == 0 is a no-op); x_dev, w_tiled_dev and y_dev
+ * 16-byte aligned; x rows contiguous (row stride K).
+ */
+QWP_API int q4k_gemm(const void *w_tiled_dev, const void *x_dev, float *y_dev,
+             int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * W4A16 (group-wise asymmetric int4): wq[N][K/8] int32 words, each holding
+ * 8 codes along K with val[2p] at bits 4p..4p+3 and val[2p+1] at bits
+ * 16+4p..19+4p; scales[N][K/group] fp16; zeros[N][K/group] uint8 in 0..15;
+ * w = s * (q - zp).  Source: "[ROCm][Perf] W4A16: packed fp16 prefill
+ * dequant", sections "1. Packed fp16 dequant" and "2. dtype-aware gfx1151
+ * tile selection" (a K-block never straddles a group).  Requirements:
+ * group % 64 == 0, K % group == 0.
+ */
+
+/* Bytes of a repacked W4A16 code matrix: N*K/2. */
+QWP_API int w4a16_repacked_bytes(int64_t N, int64_t K, size_t *out_bytes);
+
+/* Load-time repack of wq_dev [N][K/8] words into 128-row tiles of 64-wide K-blocks (same size). */
+QWP_API int w4a16_repack(const void *wq_dev, void *wq_tiled_dev, int64_t N, int64_t K, void *stream);
+
+/* Test entry point: exact fp32 s*(q - zp) of the repacked matrix into w_out_dev[N][K]. */
+QWP_API int w4a16_dequant(const void *wq_tiled_dev, const void *scales_dev, const uint8_t *zeros_dev,
+                  float *w_out_dev, int64_t N, int64_t K, int64_t group, void *stream);
+
+/*
+ * y_dev[M][N] (fp32) = x_dev[M][K] (fp16) . W^T.  Each weight is unpacked
+ * with the exact 0x6400|n trick, (1024+q) - (1024+zp) exactly, then one fp16
+ * multiply by the scale, and fed to the tensor cores (fp16 operands, fp32
+ * accumulation).  Same alignment rules as q4k_gemm.
+ */
+QWP_API int w4a16_gemm(const void *wq_tiled_dev, const void *scales_dev, const uint8_t *zeros_dev,
+               const void *x_dev, float *y_dev, int64_t M, int64_t N, int64_t K, int64_t group,
+               void *stream);
+
+/*
+ * Synchronize `stream`, then read and clear the library's device status word
+ * on the current device.  Returns QWP_OK, QWP_ERR_TIMEOUT if a kernel's
+ * bounded wait on an mbarrier expired (the kernel then released its tensor
+ * memory and exited; its output is invalid), or QWP_ERR_CUDA.  While the
+ * word holds an error, every GEMM launch on that device exits at once without
+ * writing y; reading it here clears it.
+ */
+QWP_API int qwp_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QWP_H */

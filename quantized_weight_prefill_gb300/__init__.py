@@ -1,0 +1,180 @@
+"""Batched-prefill GEMM over 4-bit quantized weights (Q4_K, W4A16) on GB300.
+
+Thin Python binding over the C ABI of ``libqwp.so`` (declared in
+``include/qwp.h``).  Every function here only marshals arguments: it checks
+that tensors live on the GPU with the right dtype and layout, allocates the
+output with torch when none is given, and passes raw pointers, sizes and the
+current CUDA stream to the library.  All arithmetic runs in the library's CUDA
+kernels; there is no CPU fallback, and a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "QwpError", "library", "q4k_repacked_bytes", "q4k_repack", "q4k_dequant", "q4k_gemm",
+    "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "device_status",
+    "EXPORTED_SYMBOLS",
+]
+
+# Every symbol include/qwp.h declares.
+EXPORTED_SYMBOLS = (
+    "qwp_status_string", "q4k_repacked_bytes", "q4k_repack", "q4k_dequant", "q4k_gemm",
+    "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "qwp_device_status",
+)
+
+_lib = None
+
+
+class QwpError(RuntimeError):
+    def __init__(self, code: int, name: str, what: str):
+        super().__init__(f"{what}: {name} ({code})")
+        self.code = code
+        self.name = name
+
+
+def library() -> ctypes.CDLL:
+    """The loaded libqwp.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(
+                f"{_build.LIB} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                "g.build()\"` (nvcc, sm_103a); there is no fallback path")
+        lib = ctypes.CDLL(_build.LIB)
+        i64, p, sz = ctypes.c_int64, ctypes.c_void_p, ctypes.POINTER(ctypes.c_size_t)
+        lib.qwp_status_string.argtypes = [ctypes.c_int]
+        lib.qwp_status_string.restype = ctypes.c_char_p
+        lib.q4k_repacked_bytes.argtypes = [i64, i64, sz]
+        lib.w4a16_repacked_bytes.argtypes = [i64, i64, sz]
+        lib.q4k_repack.argtypes = [p, p, i64, i64, p]
+        lib.q4k_dequant.argtypes = [p, p, i64, i64, p]
+        lib.q4k_gemm.argtypes = [p, p, p, i64, i64, i64, p]
+        lib.w4a16_repack.argtypes = [p, p, i64, i64, p]
+        lib.w4a16_dequant.argtypes = [p, p, p, p, i64, i64, i64, p]
+        lib.w4a16_gemm.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p]
+        lib.qwp_device_status.argtypes = [p]
+        for name in EXPORTED_SYMBOLS:
+            if name != "qwp_status_string":
+                getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise QwpError(rc, library().qwp_status_string(rc).decode(), what)
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _dev(t: torch.Tensor, dtype, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def q4k_repacked_bytes(N: int, K: int) -> int:
+    out = ctypes.c_size_t()
+    _check(library().q4k_repacked_bytes(N, K, ctypes.byref(out)), "q4k_repacked_bytes")
+    return out.value
+
+
+def w4a16_repacked_bytes(N: int, K: int) -> int:
+    out = ctypes.c_size_t()
+    _check(library().w4a16_repacked_bytes(N, K, ctypes.byref(out)), "w4a16_repacked_bytes")
+    return out.value
+
+
+def q4k_repack(w_ggml: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """GGML Q4_K rows (uint8, N*K/256*144 bytes) -> tile-major repacked bytes."""
+    _dev(w_ggml, torch.uint8, "w_ggml")
+    nbytes = q4k_repacked_bytes(N, K)
+    if w_ggml.numel() != nbytes:
+        raise ValueError("w_ggml size does not match N, K")
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=w_ggml.device)
+    _dev(out, torch.uint8, "out")
+    _check(library().q4k_repack(_ptr(w_ggml), _ptr(out), N, K, _stream(w_ggml)), "q4k_repack")
+    return out
+
+
+def q4k_dequant(w_tiled: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    _dev(w_tiled, torch.uint8, "w_tiled")
+    if out is None:
+        out = torch.empty(N, K, dtype=torch.float32, device=w_tiled.device)
+    _dev(out, torch.float32, "out")
+    _check(library().q4k_dequant(_ptr(w_tiled), _ptr(out), N, K, _stream(w_tiled)), "q4k_dequant")
+    return out
+
+
+def q4k_gemm(w_tiled: torch.Tensor, x: torch.Tensor, N: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """y[M, N] (fp32) = x[M, K] (bf16) . W^T with W the repacked Q4_K matrix."""
+    _dev(w_tiled, torch.uint8, "w_tiled")
+    _dev(x, torch.bfloat16, "x")
+    M, K = x.shape
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.float32, device=x.device)
+    _dev(out, torch.float32, "out")
+    _check(library().q4k_gemm(_ptr(w_tiled), _ptr(x), _ptr(out), M, N, K, _stream(x)), "q4k_gemm")
+    return out
+
+
+def w4a16_repack(wq: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Interleaved int4 words [N, K/8] (int32) -> tile-major repacked words (same size)."""
+    _dev(wq, torch.int32, "wq")
+    N, K8 = wq.shape
+    if out is None:
+        out = torch.empty_like(wq)
+    _dev(out, torch.int32, "out")
+    _check(library().w4a16_repack(_ptr(wq), _ptr(out), N, K8 * 8, _stream(wq)), "w4a16_repack")
+    return out
+
+
+def w4a16_dequant(wq_tiled, scales, zeros, N: int, K: int, group: int, out=None) -> torch.Tensor:
+    _dev(wq_tiled, torch.int32, "wq_tiled")
+    _dev(scales, torch.float16, "scales")
+    _dev(zeros, torch.uint8, "zeros")
+    if out is None:
+        out = torch.empty(N, K, dtype=torch.float32, device=wq_tiled.device)
+    _dev(out, torch.float32, "out")
+    _check(library().w4a16_dequant(_ptr(wq_tiled), _ptr(scales), _ptr(zeros), _ptr(out), N, K, group,
+                                   _stream(wq_tiled)), "w4a16_dequant")
+    return out
+
+
+def w4a16_gemm(wq_tiled, scales, zeros, x: torch.Tensor, N: int, group: int, out=None) -> torch.Tensor:
+    """y[M, N] (fp32) = x[M, K] (fp16) . W^T with W the repacked W4A16 matrix."""
+    _dev(wq_tiled, torch.int32, "wq_tiled")
+    _dev(scales, torch.float16, "scales")
+    _dev(zeros, torch.uint8, "zeros")
+    _dev(x, torch.float16, "x")
+    M, K = x.shape
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.float32, device=x.device)
+    _dev(out, torch.float32, "out")
+    _check(library().w4a16_gemm(_ptr(wq_tiled), _ptr(scales), _ptr(zeros), _ptr(x), _ptr(out), M, N, K,
+                                group, _stream(x)), "w4a16_gemm")
+    return out
+
+
+def device_status(device=None) -> int:
+    """Synchronize the current stream and return (and clear) the library's device status code."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(library().qwp_device_status(ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)))

@@ -1,0 +1,257 @@
+// Load-time repack kernels, the dequant test entry points, the device status
+// word and the device check.
+#include <atomic>
+
+#include "qwp_format.cuh"
+#include "qwp_internal.h"
+
+namespace qwp {
+
+// Status word written by kernels whose bounded waits expire (0 = no error).
+__device__ uint32_t g_qwp_status;
+
+int check_device() {
+    static std::atomic<int> cache[64];  // 0 unknown, 1 sm_103, 2 other
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QWP_ERR_CUDA;
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c) return c == 1 ? QWP_OK : QWP_ERR_DEVICE;
+    }
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return QWP_ERR_CUDA;
+    const bool ok = (major == 10 && minor == 3);
+    if (dev >= 0 && dev < 64) cache[dev].store(ok ? 1 : 2, std::memory_order_relaxed);
+    return ok ? QWP_OK : QWP_ERR_DEVICE;
+}
+
+uint32_t *status_word() {
+    static std::atomic<uint32_t *> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    if (dev >= 0 && dev < 64) {
+        uint32_t *p = cache[dev].load(std::memory_order_acquire);
+        if (p) return p;
+    }
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_qwp_status) != cudaSuccess) return nullptr;
+    if (dev >= 0 && dev < 64) cache[dev].store(static_cast<uint32_t *>(p), std::memory_order_release);
+    return static_cast<uint32_t *>(p);
+}
+
+// ---------------------------------------------------------------- Q4_K repack
+
+// One warp per (row n, super-block b): lanes 0..3 copy the 16 header bytes,
+// lane l builds word v = l%8 of chunk c = l/8 from the GGML nibble bytes
+// (element e < 32 of chunk c is the low nibble of byte 32c+e, element e >= 32
+// the high nibble of byte 32c+e-32).
+__global__ void q4k_repack_kernel(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst,
+                                  int64_t N, int64_t K) {
+    const int64_t nb = K / Q4K_BLOCK;
+    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (gw >= N * nb) return;
+    const int lane = threadIdx.x & 31;
+    const int64_t n = gw / nb, b = gw % nb;
+    const int64_t tile = n / TILE_ROWS;
+    const int i = static_cast<int>(n % TILE_ROWS);
+    const int R = tile_rows(N, tile);
+    const uint8_t *blk = src + (n * nb + b) * Q4K_BLOCK_BYTES;
+    uint8_t *grp = dst + q4k_group_offset(K, tile, R, b);
+    if (lane < 4)
+        *reinterpret_cast<uint32_t *>(grp + Q4K_HEADER_BYTES * i + 4 * lane) =
+            *reinterpret_cast<const uint32_t *>(blk + 4 * lane);
+    const int c = lane >> 3, v = lane & 7;
+    const uint8_t *qs = blk + Q4K_HEADER_BYTES + 32 * c;
+    uint32_t word = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int e = 8 * v + u;
+        const uint32_t byte = qs[e & 31];
+        const uint32_t nib = (e < 32) ? (byte & 15u) : (byte >> 4);
+        word |= nib << (4 * u);
+    }
+    *reinterpret_cast<uint32_t *>(grp + q4k_word_offset(R, i, c, v)) = word;
+}
+
+// One warp per (row, super-block); lane l dequantizes elements 8l..8l+7 and
+// writes them with two 16-byte stores, so a warp writes 1 KiB contiguously.
+__global__ void q4k_dequant_kernel(const uint8_t *__restrict__ w, float *__restrict__ out,
+                                   int64_t N, int64_t K) {
+    const int64_t nb = K / Q4K_BLOCK;
+    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (gw >= N * nb) return;
+    const int lane = threadIdx.x & 31;
+    const int64_t n = gw / nb, b = gw % nb;
+    const int64_t tile = n / TILE_ROWS;
+    const int i = static_cast<int>(n % TILE_ROWS);
+    const int R = tile_rows(N, tile);
+    const uint8_t *grp = w + q4k_group_offset(K, tile, R, b);
+    const uint4 hdr = *reinterpret_cast<const uint4 *>(grp + Q4K_HEADER_BYTES * i);
+    const int c = lane >> 3, v = lane & 7;
+    float dl, ml;
+    q4k_subblock_scale(hdr, 2 * c + (v >> 2), dl, ml);
+    const uint32_t word = *reinterpret_cast<const uint32_t *>(grp + q4k_word_offset(R, i, c, v));
+    float vals[8];
+    q4k_word_f32(word, dl, ml, vals);
+    float4 *o = reinterpret_cast<float4 *>(out + n * K + b * Q4K_BLOCK + 8 * lane);
+    o[0] = make_float4(vals[0], vals[1], vals[2], vals[3]);
+    o[1] = make_float4(vals[4], vals[5], vals[6], vals[7]);
+}
+
+// ---------------------------------------------------------------- W4A16 repack
+
+// One thread per word; consecutive threads read consecutive source words.
+__global__ void w4_repack_kernel(const uint32_t *__restrict__ src, uint8_t *__restrict__ dst,
+                                 int64_t N, int64_t K) {
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t wpr = K / 8;
+    if (idx >= N * wpr) return;
+    const int64_t n = idx / wpr, rem = idx % wpr;
+    const int64_t j = rem / 8;
+    const int v = static_cast<int>(rem % 8);
+    const int64_t tile = n / TILE_ROWS;
+    const int i = static_cast<int>(n % TILE_ROWS);
+    const int R = tile_rows(N, tile);
+    *reinterpret_cast<uint32_t *>(dst + w4_plane_offset(K, tile, R, j) + w4_word_offset(R, i, v)) =
+        src[idx];
+}
+
+// One thread per word: the exact (1024+q) - (1024+zp) of the GEMM's unpack,
+// then an exact fp32 product with the scale (at most 11 + 5 significant bits).
+__global__ void w4_dequant_kernel(const uint8_t *__restrict__ w, const __half *__restrict__ scales,
+                                  const uint8_t *__restrict__ zeros, float *__restrict__ out,
+                                  int64_t N, int64_t K, int64_t group) {
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t wpr = K / 8;
+    if (idx >= N * wpr) return;
+    const int64_t n = idx / wpr, rem = idx % wpr;
+    const int64_t j = rem / 8;
+    const int v = static_cast<int>(rem % 8);
+    const int64_t tile = n / TILE_ROWS;
+    const int i = static_cast<int>(n % TILE_ROWS);
+    const int R = tile_rows(N, tile);
+    const uint32_t word = *reinterpret_cast<const uint32_t *>(
+        w + w4_plane_offset(K, tile, R, j) + w4_word_offset(R, i, v));
+    const int64_t k0 = CHUNK_K * j + 8 * v;
+    const int64_t g = k0 / group;
+    const float s = __half2float(scales[n * (K / group) + g]);
+    const __half2 mz = w4_magic_zero(zeros[n * (K / group) + g]);
+    float vals[8];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const float2 qz = __half22float2(w4_pair_minus_zero(word, p, mz));
+        vals[2 * p] = qz.x * s;
+        vals[2 * p + 1] = qz.y * s;
+    }
+    float4 *o = reinterpret_cast<float4 *>(out + n * K + k0);
+    o[0] = make_float4(vals[0], vals[1], vals[2], vals[3]);
+    o[1] = make_float4(vals[4], vals[5], vals[6], vals[7]);
+}
+
+static unsigned grid_for(int64_t threads, int block) {
+    return static_cast<unsigned>((threads + block - 1) / block);
+}
+
+}  // namespace qwp
+
+using namespace qwp;
+
+extern "C" const char *qwp_status_string(int status) {
+    switch (status) {
+        case QWP_OK: return "QWP_OK";
+        case QWP_ERR_INVALID_ARG: return "QWP_ERR_INVALID_ARG";
+        case QWP_ERR_UNSUPPORTED_SHAPE: return "QWP_ERR_UNSUPPORTED_SHAPE";
+        case QWP_ERR_MISALIGNED: return "QWP_ERR_MISALIGNED";
+        case QWP_ERR_CUDA: return "QWP_ERR_CUDA";
+        case QWP_ERR_DEVICE: return "QWP_ERR_DEVICE";
+        case QWP_ERR_TIMEOUT: return "QWP_ERR_TIMEOUT";
+        default: return "QWP_ERR_UNKNOWN";
+    }
+}
+
+extern "C" int q4k_repacked_bytes(int64_t N, int64_t K, size_t *out_bytes) {
+    if (!out_bytes || N < 0 || K < 0) return QWP_ERR_INVALID_ARG;
+    if (K % Q4K_BLOCK) return QWP_ERR_UNSUPPORTED_SHAPE;
+    *out_bytes = static_cast<size_t>(N) * static_cast<size_t>(K / Q4K_BLOCK) * Q4K_BLOCK_BYTES;
+    return QWP_OK;
+}
+
+extern "C" int w4a16_repacked_bytes(int64_t N, int64_t K, size_t *out_bytes) {
+    if (!out_bytes || N < 0 || K < 0) return QWP_ERR_INVALID_ARG;
+    if (K % CHUNK_K) return QWP_ERR_UNSUPPORTED_SHAPE;
+    *out_bytes = static_cast<size_t>(N) * static_cast<size_t>(K) / 2;
+    return QWP_OK;
+}
+
+static int q4k_common_checks(const void *a, const void *b, int64_t N, int64_t K) {
+    if (N < 0 || K < 0) return QWP_ERR_INVALID_ARG;
+    if (K % Q4K_BLOCK) return QWP_ERR_UNSUPPORTED_SHAPE;
+    if (N == 0 || K == 0) return QWP_OK;
+    if (!a || !b) return QWP_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b)) return QWP_ERR_MISALIGNED;
+    if (a == b) return QWP_ERR_INVALID_ARG;  // outputs never alias inputs
+    return check_device();
+}
+
+extern "C" int q4k_repack(const void *w_ggml, void *w_tiled, int64_t N, int64_t K, void *stream) {
+    int rc = q4k_common_checks(w_ggml, w_tiled, N, K);
+    if (rc || N == 0 || K == 0) return rc;
+    const int64_t threads = N * (K / Q4K_BLOCK) * 32;
+    q4k_repack_kernel<<<grid_for(threads, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t *>(w_ggml), static_cast<uint8_t *>(w_tiled), N, K);
+    return launch_status();
+}
+
+extern "C" int q4k_dequant(const void *w_tiled, float *w_out, int64_t N, int64_t K, void *stream) {
+    int rc = q4k_common_checks(w_tiled, w_out, N, K);
+    if (rc || N == 0 || K == 0) return rc;
+    const int64_t threads = N * (K / Q4K_BLOCK) * 32;
+    q4k_dequant_kernel<<<grid_for(threads, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t *>(w_tiled), w_out, N, K);
+    return launch_status();
+}
+
+static int w4_common_checks(const void *a, const void *b, int64_t N, int64_t K) {
+    if (N < 0 || K < 0) return QWP_ERR_INVALID_ARG;
+    if (K % CHUNK_K) return QWP_ERR_UNSUPPORTED_SHAPE;
+    if (N == 0 || K == 0) return QWP_OK;
+    if (!a || !b) return QWP_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b)) return QWP_ERR_MISALIGNED;
+    if (a == b) return QWP_ERR_INVALID_ARG;  // outputs never alias inputs
+    return check_device();
+}
+
+extern "C" int w4a16_repack(const void *wq, void *wq_tiled, int64_t N, int64_t K, void *stream) {
+    int rc = w4_common_checks(wq, wq_tiled, N, K);
+    if (rc || N == 0 || K == 0) return rc;
+    const int64_t threads = N * (K / 8);
+    w4_repack_kernel<<<grid_for(threads, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint32_t *>(wq), static_cast<uint8_t *>(wq_tiled), N, K);
+    return launch_status();
+}
+
+extern "C" int w4a16_dequant(const void *wq_tiled, const void *scales, const uint8_t *zeros,
+                             float *w_out, int64_t N, int64_t K, int64_t group, void *stream) {
+    if (group <= 0 || group % CHUNK_K) return QWP_ERR_INVALID_ARG;
+    if (K % group) return QWP_ERR_UNSUPPORTED_SHAPE;
+    if (N > 0 && K > 0 && (!scales || !zeros)) return QWP_ERR_INVALID_ARG;
+    int rc = w4_common_checks(wq_tiled, w_out, N, K);
+    if (rc || N == 0 || K == 0) return rc;
+    const int64_t threads = N * (K / 8);
+    w4_dequant_kernel<<<grid_for(threads, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t *>(wq_tiled), static_cast<const __half *>(scales), zeros, w_out, N,
+        K, group);
+    return launch_status();
+}
+
+extern "C" int qwp_device_status(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return QWP_ERR_CUDA;
+    uint32_t *p = status_word();
+    if (!p) return QWP_ERR_CUDA;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return QWP_ERR_CUDA;
+    if (v && cudaMemset(p, 0, sizeof(v)) != cudaSuccess) return QWP_ERR_CUDA;
+    return v ? QWP_ERR_TIMEOUT : QWP_OK;
+}

@@ -1,0 +1,27 @@
+// Host-side helpers shared by the translation units of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qwp.h"
+
+namespace qwp {
+
+// QWP_OK if the current device is an sm_103 GPU (cached per device), else QWP_ERR_DEVICE / QWP_ERR_CUDA.
+int check_device();
+
+// Device address of the library's status word on the current device (nullptr on failure).
+uint32_t *status_word();
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch errors of the last launch on this thread, as a qwp_status.
+inline int launch_status() {
+    return cudaGetLastError() == cudaSuccess ? QWP_OK : QWP_ERR_CUDA;
+}
+
+// Default bound on any single mbarrier wait inside a kernel.
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
+
+}  // namespace qwp

@@ -1,0 +1,105 @@
+"""Shared test helpers: moving the seeded inputs to the GPU, the chunked oracle,
+the error-bound check, and a numpy statement of the documented repack layouts
+(used only to check the CUDA repack byte for byte)."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+
+TOL_REL = 1e-3
+TOL_ABS = 1e-5
+
+
+# --- documented tile-major layouts (numpy restatement, test side) ----------------
+
+def q4k_tiled_reference(blocks: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Tile-major Q4_K order: per 128-row tile and super-block, a 16-byte header plane
+    and four nibble planes [h][row][16 bytes]; word v of a row's 64-wide chunk holds
+    chunk elements 8v..8v+7 in bits 4u..4u+3."""
+    nb = K // 256
+    raw = blocks.reshape(N, nb, 144)
+    out = np.zeros(N * nb * 144, np.uint8)
+    for t0 in range(0, N, 128):
+        R = min(128, N - t0)
+        for b in range(nb):
+            base = t0 * nb * 144 + b * R * 144
+            grp = out[base:base + R * 144]
+            grp[:16 * R] = raw[t0:t0 + R, b, :16].reshape(-1)
+            qs = raw[t0:t0 + R, b, 16:].astype(np.uint32)            # [R, 128]
+            for c in range(4):
+                lo = qs[:, 32 * c:32 * c + 32] & 15                     # elements 0..31
+                hi = qs[:, 32 * c:32 * c + 32] >> 4                     # elements 32..63
+                elems = np.concatenate([lo, hi], axis=1)                # [R, 64]
+                words = np.zeros((R, 8), np.uint32)
+                for u in range(8):
+                    words |= elems[:, u::8] << (4 * u)
+                plane = words.reshape(R, 2, 4).transpose(1, 0, 2)        # [h][row][4 words]
+                start = 16 * R + 32 * R * c
+                grp[start:start + 32 * R] = plane.astype("<u4").reshape(-1).view(np.uint8)
+    return out
+
+
+def w4a16_tiled_reference(wq: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Tile-major W4A16 order: per 128-row tile and 64-wide K-block, a plane [h][row][4 words]."""
+    words = wq.view(np.uint32).reshape(N, K // 8)
+    out = np.zeros(N * K // 8, np.uint32)
+    for t0 in range(0, N, 128):
+        R = min(128, N - t0)
+        for j in range(K // 64):
+            blk = words[t0:t0 + R, 8 * j:8 * j + 8].reshape(R, 2, 4).transpose(1, 0, 2)
+            base = (t0 * K // 2 + j * R * 32) // 4
+            out[base:base + 8 * R] = blk.reshape(-1)
+    return out
+
+
+# --- oracle on row samples ---------------------------------------------------------
+
+def q4k_oracle_rows(blocks: np.ndarray, xb_rows: np.ndarray, N: int, K: int, chunk: int = 2048):
+    """Oracle y and sum|x*w| for the given bf16 activation rows, dequantizing W in row chunks."""
+    x = oracle.bf16_to_f64(xb_rows).reshape(-1, K)
+    raw = blocks.reshape(N, -1)
+    ys, ms = [], []
+    for n0 in range(0, N, chunk):
+        n1 = min(N, n0 + chunk)
+        w = oracle.q4k_dequant(raw[n0:n1], n1 - n0, K)
+        y, a = oracle.gemm(x, w)
+        ys.append(y)
+        ms.append(a)
+    return np.concatenate(ys, axis=1), np.concatenate(ms, axis=1)
+
+
+def w4a16_oracle_rows(wq, s, z, xh_rows, N: int, K: int, group: int, chunk: int = 2048):
+    x = oracle.half_to_f64(np.asarray(xh_rows).view(np.uint16)).reshape(-1, K)
+    ys, ms = [], []
+    for n0 in range(0, N, chunk):
+        n1 = min(N, n0 + chunk)
+        w = oracle.w4a16_dequant(wq[n0:n1], s[n0:n1], z[n0:n1], n1 - n0, K, group)
+        y, a = oracle.gemm(x, w)
+        ys.append(y)
+        ms.append(a)
+    return np.concatenate(ys, axis=1), np.concatenate(ms, axis=1)
+
+
+def sample_rows(M: int, count: int = 64, seed: int = 0) -> np.ndarray:
+    """First 16, last 16 and random rows in between (all rows if M is small)."""
+    if M <= count:
+        return np.arange(M)
+    rng = np.random.default_rng(seed)
+    head = np.arange(16)
+    tail = np.arange(M - 16, M)
+    mid = rng.choice(np.arange(16, M - 16), size=count - 32, replace=False)
+    return np.unique(np.concatenate([head, mid, tail]))
+
+
+def check_bound(y_gpu: np.ndarray, y_ref: np.ndarray, mag: np.ndarray, what: str) -> float:
+    """Assert |y_gpu - y_ref| <= 1e-3 * sum|x*w| + 1e-5 elementwise; return the worst err/bound."""
+    err = np.abs(y_gpu.astype(np.float64) - y_ref)
+    bound = TOL_REL * mag + TOL_ABS
+    ratio = float((err / bound).max()) if err.size else 0.0
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {err.size} outside the bound, "
+                           f"worst err/bound {ratio:.3f}, first at {np.argwhere(bad)[0].tolist()}")
+    assert np.isfinite(y_gpu).all(), f"{what}: non-finite output"
+    return ratio
+

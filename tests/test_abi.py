@@ -1,0 +1,87 @@
+"""The C-ABI library loads, exports every symbol include/qwp.h declares, and its
+host-side argument checks return the documented codes (no GPU work is issued:
+each call below is rejected before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_weight_prefill_gb300 as qwp
+from quantized_weight_prefill_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qwp.h")
+
+OK, INVALID, SHAPE, MISALIGNED = 0, -1, -2, -3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if _build.is_stale():
+        _build.build()
+    return qwp.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return set(re.findall(r"^QWP_API\s+(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, re.M))
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_functions() == set(qwp.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    # and nothing else: internal helpers are hidden
+    out = os.popen(f"nm -D --defined-only {_build.LIB}").read().split("\n")
+    exported = {line.split()[-1] for line in out if " T " in line}
+    assert exported == declared_functions()
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "QWP_OK"), (-1, "QWP_ERR_INVALID_ARG"), (-2, "QWP_ERR_UNSUPPORTED_SHAPE"),
+                       (-3, "QWP_ERR_MISALIGNED"), (-4, "QWP_ERR_CUDA"), (-5, "QWP_ERR_DEVICE"),
+                       (-6, "QWP_ERR_TIMEOUT")]:
+        assert lib.qwp_status_string(code).decode() == name
+
+
+def test_repacked_bytes(lib):
+    assert qwp.q4k_repacked_bytes(4096, 4096) == 4096 * 16 * 144
+    assert qwp.q4k_repacked_bytes(3, 512) == 3 * 2 * 144
+    assert qwp.w4a16_repacked_bytes(12288, 4096) == 12288 * 4096 // 2
+    with pytest.raises(qwp.QwpError) as e:
+        qwp.q4k_repacked_bytes(4, 100)
+    assert e.value.code == SHAPE
+    out = ctypes.c_size_t()
+    assert lib.q4k_repacked_bytes(-1, 256, ctypes.byref(out)) == INVALID
+    assert lib.q4k_repacked_bytes(1, 256, None) == INVALID
+
+
+def _p(v):
+    return ctypes.c_void_p(v)
+
+
+def test_gemm_argument_checks_before_any_cuda_call(lib):
+    a16 = _p(0x1000)
+    # shape errors
+    assert lib.q4k_gemm(a16, a16, a16, 8, 8, 100, None) == SHAPE
+    assert lib.q4k_gemm(a16, a16, a16, -1, 8, 256, None) == INVALID
+    assert lib.w4a16_gemm(a16, a16, a16, a16, a16, 8, 8, 256, 100, None) == INVALID   # group % 64
+    assert lib.w4a16_gemm(a16, a16, a16, a16, a16, 8, 8, 320, 128, None) == SHAPE     # K % group
+    # null and misaligned pointers
+    assert lib.q4k_gemm(None, a16, a16, 8, 8, 256, None) == INVALID
+    assert lib.q4k_gemm(_p(0x1004), a16, a16, 8, 8, 256, None) == MISALIGNED
+    assert lib.q4k_gemm(a16, _p(0x1002), a16, 8, 8, 256, None) == MISALIGNED
+    assert lib.w4a16_gemm(a16, None, a16, a16, a16, 8, 8, 256, 128, None) == INVALID
+    # empty problems are no-ops
+    assert lib.q4k_gemm(None, None, None, 0, 8, 256, None) == OK
+    assert lib.q4k_gemm(None, None, None, 8, 0, 256, None) == OK
+    # repack / dequant checks
+    assert lib.q4k_repack(a16, a16, 4, 256, None) == INVALID          # aliasing
+    assert lib.q4k_repack(a16, _p(0x2008), 4, 256, None) == MISALIGNED
+    assert lib.q4k_dequant(a16, a16, 4, 300, None) == SHAPE
+    assert lib.w4a16_repack(a16, a16, 4, 96, None) == SHAPE
+    assert lib.w4a16_dequant(a16, a16, a16, a16, 4, 256, 96, None) == INVALID

@@ -1,0 +1,204 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+* repacks byte-exact against the documented layouts,
+* dequant entry points bit-exact against the oracle's fp64 values rounded to fp32,
+* GEMMs within |y - y_oracle| <= 1e-3 * sum|x*w| + 1e-5 elementwise, on tiny
+  shapes with ragged tails, on every workload shape (sampled token rows at the
+  large ones) and on edge cases (empty, misaligned, guard bands).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_weight_prefill_gb300 as qwp
+import synth
+from helpers import (check_bound, q4k_oracle_rows, q4k_tiled_reference, sample_rows,
+                     w4a16_oracle_rows, w4a16_tiled_reference)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _q4k_on_gpu(N, K, seed):
+    blocks = synth.q4k_weights(N, K, seed=seed)
+    w = qwp.q4k_repack(torch.from_numpy(blocks.reshape(-1)).to(DEV), N, K)
+    return blocks, w
+
+
+def _bf16_on_gpu(xb):
+    return torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).to(DEV).view(torch.bfloat16)
+
+
+def _w4_on_gpu(N, K, g, seed):
+    wq, s, z = synth.w4a16_weights(N, K, g, seed=seed)
+    wt = qwp.w4a16_repack(torch.from_numpy(wq.view(np.int32)).to(DEV))
+    return (wq, s, z), (wt, torch.from_numpy(s).to(DEV), torch.from_numpy(z).to(DEV))
+
+
+@pytest.fixture(autouse=True)
+def _status_clean():
+    yield
+    assert qwp.device_status() == 0, "a kernel reported a timeout"
+
+
+# --- repack and dequant ------------------------------------------------------------
+
+@pytest.mark.parametrize("N,K", [(1, 256), (5, 512), (128, 256), (130, 768), (300, 1024)])
+def test_q4k_repack_layout(N, K):
+    blocks, w = _q4k_on_gpu(N, K, seed=N + K)
+    assert np.array_equal(w.cpu().numpy(), q4k_tiled_reference(blocks, N, K))
+
+
+@pytest.mark.parametrize("N,K", [(1, 64), (5, 128), (130, 512), (257, 1024)])
+def test_w4a16_repack_layout(N, K):
+    (wq, _, _), (wt, _, _) = _w4_on_gpu(N, K, 64, seed=N + K)
+    assert np.array_equal(wt.cpu().numpy().view(np.uint32).reshape(-1), w4a16_tiled_reference(wq, N, K))
+
+
+@pytest.mark.parametrize("N,K", [(1, 256), (7, 512), (130, 1024), (4096, 12288)])
+def test_q4k_dequant_bit_exact(N, K):
+    blocks, w = _q4k_on_gpu(N, K, seed=3 * N + K)
+    got = qwp.q4k_dequant(w, N, K).cpu().numpy()
+    ref = oracle.q4k_dequant(blocks, N, K).astype(np.float32)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_q4k_dequant_extreme_scales_bit_exact():
+    """Subnormal, tiny and large fp16 d/dmin still give the correctly rounded fp32 value."""
+    N, K = 64, 512
+    blocks = synth.q4k_weights(N, K, seed=77).reshape(-1, 144).copy()
+    rng = np.random.default_rng(78)
+    special = np.array([0x0001, 0x03FF, 0x0400, 0x1400, 0x3C00, 0x5BFF, 0x7BFF, 0x8001, 0xBC00],
+                       np.uint16)
+    d = rng.choice(special, size=blocks.shape[0])
+    dm = rng.choice(special, size=blocks.shape[0])
+    blocks[:, 0:2] = d.astype("<u2").view(np.uint8).reshape(-1, 2)
+    blocks[:, 2:4] = dm.astype("<u2").view(np.uint8).reshape(-1, 2)
+    w = qwp.q4k_repack(torch.from_numpy(blocks.reshape(-1)).to(DEV), N, K)
+    got = qwp.q4k_dequant(w, N, K).cpu().numpy()
+    ref = oracle.q4k_dequant(blocks.reshape(-1), N, K).astype(np.float32)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("N,K,g", [(1, 64, 64), (9, 256, 128), (130, 512, 128), (4096, 12288, 128)])
+def test_w4a16_dequant_bit_exact(N, K, g):
+    (wq, s, z), (wt, sd, zd) = _w4_on_gpu(N, K, g, seed=5 * N + K)
+    got = qwp.w4a16_dequant(wt, sd, zd, N, K, g).cpu().numpy()
+    ref = oracle.w4a16_dequant(wq, s, z, N, K, g).astype(np.float32)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+# --- GEMM: tiny shapes with ragged tails ------------------------------------------
+
+TINY = [(1, 1, 256), (7, 5, 256), (16, 128, 512), (33, 130, 768), (105, 256, 1024),
+        (200, 384, 512), (300, 136, 256), (257, 129, 512), (64, 1000, 256)]
+
+
+@pytest.mark.parametrize("M,N,K", TINY)
+def test_q4k_gemm_tiny(M, N, K):
+    blocks, w = _q4k_on_gpu(N, K, seed=M * 7 + N)
+    xb = synth.activations_bf16(M, K, seed=M + 1)
+    y = qwp.q4k_gemm(w, _bf16_on_gpu(xb), N).cpu().numpy()
+    ref, mag = oracle.q4k_gemm(blocks, xb, N, K)
+    check_bound(y, ref, mag, f"q4k M{M} N{N} K{K}")
+
+
+@pytest.mark.parametrize("M,N,K,g", [(1, 1, 64, 64), (7, 5, 256, 128), (33, 130, 768, 64),
+                                     (105, 256, 1024, 128), (300, 136, 512, 256), (257, 200, 320, 64)])
+def test_w4a16_gemm_tiny(M, N, K, g):
+    (wq, s, z), (wt, sd, zd) = _w4_on_gpu(N, K, g, seed=M * 11 + N)
+    xh = synth.activations_f16(M, K, seed=M + 2)
+    y = qwp.w4a16_gemm(wt, sd, zd, torch.from_numpy(xh).to(DEV), N, g).cpu().numpy()
+    ref, mag = oracle.w4a16_gemm(wq, s, z, xh, N, K, g)
+    check_bound(y, ref, mag, f"w4a16 M{M} N{N} K{K} g{g}")
+
+
+# --- GEMM: the workload shapes -------------------------------------------------------
+
+def _q4k_workload(M, N, K, seed, rows=None):
+    blocks, w = _q4k_on_gpu(N, K, seed=seed)
+    xb = synth.activations_bf16(M, K, seed=seed + 1000)
+    y = qwp.q4k_gemm(w, _bf16_on_gpu(xb), N)
+    sel = np.arange(M) if rows is None else rows
+    ys = y[torch.from_numpy(sel).to(DEV)].cpu().numpy()
+    ref, mag = q4k_oracle_rows(blocks, xb[sel], N, K)
+    return check_bound(ys, ref, mag, f"q4k M{M} N{N} K{K}")
+
+
+def test_q4k_skinny_m_full():
+    """M=32 tokens, N=2048, K=2048: every output element."""
+    _q4k_workload(32, 2048, 2048, seed=1)
+
+
+@pytest.mark.parametrize("name,K,N", synth.QWEN3_8B_LAYER)
+def test_q4k_qwen3_8b_layer_m105(name, K, N):
+    """The 105-token layer the benchmark times: every output element of every projection."""
+    _q4k_workload(105, N, K, seed={"qkv": 2, "o": 3, "gate_up": 4, "down": 5}[name])
+
+
+@pytest.mark.parametrize("M", [658, 2048])
+@pytest.mark.parametrize("name,K,N", synth.QWEN3_8B_LAYER)
+def test_q4k_qwen3_8b_layer_large_m(M, name, K, N):
+    _q4k_workload(M, N, K, seed=M + len(name), rows=sample_rows(M, seed=M))
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 32, 4096), (8192, 12288, 4096)])
+def test_q4k_stress(M, N, K):
+    _q4k_workload(M, N, K, seed=M + N, rows=sample_rows(M, seed=N))
+
+
+@pytest.mark.parametrize("K,N", [(4096, 12288), (12288, 4096)])
+def test_w4a16_m2048(K, N):
+    M, g = 2048, 128
+    (wq, s, z), (wt, sd, zd) = _w4_on_gpu(N, K, g, seed=K + 5)
+    xh = synth.activations_f16(M, K, seed=K + 6)
+    y = qwp.w4a16_gemm(wt, sd, zd, torch.from_numpy(xh).to(DEV), N, g)
+    rows = sample_rows(M, seed=K)
+    ys = y[torch.from_numpy(rows).to(DEV)].cpu().numpy()
+    ref, mag = w4a16_oracle_rows(wq, s, z, xh[rows], N, K, g)
+    check_bound(ys, ref, mag, f"w4a16 M{M} N{N} K{K}")
+
+
+# --- edge cases -----------------------------------------------------------------------
+
+def test_empty_problems_are_noops():
+    blocks, w = _q4k_on_gpu(8, 256, seed=9)
+    y = torch.full((0, 8), float("nan"), device=DEV)
+    qwp.q4k_gemm(w, torch.empty(0, 256, dtype=torch.bfloat16, device=DEV), 8, out=y)
+    y2 = torch.full((4, 0), 1.0, device=DEV)
+    qwp.q4k_gemm(w, torch.zeros(4, 256, dtype=torch.bfloat16, device=DEV), 0, out=y2)
+
+
+def test_guard_band_untouched():
+    """Output writes stay inside [M, N] even with ragged row and token tiles."""
+    M, N, K = 37, 131, 512
+    blocks, w = _q4k_on_gpu(N, K, seed=12)
+    xb = synth.activations_bf16(M, K, seed=13)
+    buf = torch.full((M * N + 4096,), float("nan"), device=DEV)
+    y = buf[:M * N].view(M, N)
+    qwp.q4k_gemm(w, _bf16_on_gpu(xb), N, out=y)
+    assert torch.isnan(buf[M * N:]).all()
+    ref, mag = oracle.q4k_gemm(blocks, xb, N, K)
+    check_bound(y.cpu().numpy(), ref, mag, "guard band")
+
+
+def test_misaligned_and_bad_shapes_rejected():
+    blocks, w = _q4k_on_gpu(8, 256, seed=14)
+    x = torch.zeros(5, 256, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(qwp.QwpError) as e:  # output starting 4 bytes into an allocation
+        qwp.q4k_gemm(w, x, 8, out=torch.empty(5 * 8 + 1, device=DEV)[1:].view(5, 8))
+    assert e.value.code == -3
+    with pytest.raises(qwp.QwpError) as e:
+        qwp.q4k_gemm(w, torch.zeros(4, 300, dtype=torch.bfloat16, device=DEV), 8)
+    assert e.value.code == -2
+
+
+def test_repeat_calls_are_deterministic():
+    M, N, K = 96, 256, 1024
+    blocks, w = _q4k_on_gpu(N, K, seed=15)
+    x = _bf16_on_gpu(synth.activations_bf16(M, K, seed=16))
+    y1 = qwp.q4k_gemm(w, x, N)
+    y2 = qwp.q4k_gemm(w, x, N)
+    assert torch.equal(y1, y2)
