@@ -1,0 +1,400 @@
+#!/usr/bin/env python3
+"""Benchmark: Qwen3-8B-shaped layer prefill through the fused Q4_K GEMM.
+
+One step = one pass of the hot path over one batch: the four Q4_K projections
+of one Qwen3-8B-shaped layer (qkv K4096->N6144, o K4096->N4096, gate+up
+K4096->N24576, down K12288->N4096) for M=105 prompt tokens, bf16 activations,
+fp32 outputs.  Inputs are synthetic (seeded Q4_K blocks with d, dmin uniform in
+[1e-3, 4e-3], N(0,1) bf16 activations).  Weights rotate over enough copies that
+every step reads them from HBM (working set > 2x the 126 MB L2).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+(fp64 dequant + naive GEMM) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Fused Q4_K GEMM TFLOP/s (% bf16 TC peak); Qwen3-8B-shape layer prefill tok/s"
+LAYER = (("qkv", 4096, 6144), ("o", 4096, 4096), ("gate_up", 4096, 24576), ("down", 12288, 4096))
+M_TOKENS = 105
+DOMINANT = "gate_up"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def layer_flops(M):
+    return sum(2.0 * M * N * K for _, K, N in LAYER)
+
+
+def layer_bytes(M):
+    return sum(0.5625 * N * K + 2.0 * M * K + 4.0 * M * N for _, K, N in LAYER)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_weight_prefill_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = self.samples
+        if self.window:
+            inside = [r for r in rows if self.window[0] - 0.2 <= r[0] <= self.window[1] + 0.2]
+            rows = inside or rows
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for _, p in rows if num(p[1]) is not None]
+        smax = [num(p[2]) for _, p in rows if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, p in rows for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(n_gpus):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------- oracle leg
+
+def oracle_layer_tokens_per_s(tokens: int, seed: int = 7):
+    """Time the CPU oracle (exact fp64 dequant of every layer weight + naive fp64 GEMM)
+    for `tokens` rows of the layer; returns (tok/s, seconds, threads)."""
+    import oracle
+    import synth
+
+    inputs = []
+    for i, (_, K, N) in enumerate(LAYER):
+        inputs.append((synth.q4k_weights(N, K, seed=seed + i), synth.activations_bf16(tokens, K, seed=seed + 10 + i),
+                       N, K))
+    t0 = time.perf_counter()
+    for blocks, xb, N, K in inputs:
+        x = oracle.bf16_to_f64(xb)
+        raw = blocks.reshape(N, -1)
+        for n0 in range(0, N, 2048):
+            n1 = min(N, n0 + 2048)
+            w = oracle.q4k_dequant(raw[n0:n1], n1 - n0, K)
+            oracle.gemm(x, w, with_abs=False)
+    dt = time.perf_counter() - t0
+    return tokens / dt, dt, oracle.num_threads()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    tokens = 4
+    for _ in range(args.warmup):
+        oracle_layer_tokens_per_s(tokens)
+    times = []
+    threads = 1
+    for _ in range(args.steps):
+        _, dt, threads = oracle_layer_tokens_per_s(tokens)
+        times.append(dt)
+    total = sum(times)
+    value = tokens * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"Qwen3-8B-shape layer (qkv, o, gate+up, down), Q4_K, bf16 x, "
+                               f"M={M_TOKENS} tokens; each step a {tokens}-token sample",
+                   "global_batch": tokens, "parallelism": "none (host cores)"},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{tokens} of {M_TOKENS} tokens per step, every weight of the layer "
+                                   "dequantized exactly in fp64 then naive fp64 GEMM"},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------------- GPU leg
+
+def run_gpu(args):
+    import torch
+
+    import quantized_weight_prefill_gb300 as qwp
+    import synth
+
+    rank, local, world = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+
+    M = M_TOKENS
+    layer_w_bytes = sum(N * K // 256 * 144 for _, K, N in LAYER)
+    copies = max(3, int(np.ceil(2.5 * l2 / layer_w_bytes)))
+    weights = []  # [copy][proj] repacked Q4_K on the device
+    for c in range(copies):
+        per = []
+        for i, (_, K, N) in enumerate(LAYER):
+            blocks = synth.q4k_weights(N, K, seed=1000 * c + 10 * rank + i)
+            g = torch.from_numpy(blocks.reshape(-1)).to(dev)
+            per.append(qwp.q4k_repack(g, N, K))
+            del g
+        weights.append(per)
+    xs = []
+    for i, (_, K, N) in enumerate(LAYER):
+        xb = synth.activations_bf16(M, K, seed=50 + 10 * rank + i)
+        xs.append(torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16))
+    ys = [torch.empty(M, N, dtype=torch.float32, device=dev) for _, _, N in LAYER]
+    torch.cuda.synchronize()
+
+    dom = [n for n, _, _ in LAYER].index(DOMINANT)
+    dom_events = []
+
+    def step(s, record=False):
+        w = weights[s % copies]
+        for i, (_, K, N) in enumerate(LAYER):
+            if record and i == dom:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                qwp.q4k_gemm(w[i], xs[i], N, out=ys[i])
+                e1.record(stream)
+                dom_events.append((e0, e1))
+            else:
+                qwp.q4k_gemm(w[i], xs[i], N, out=ys[i])
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    if qwp.device_status() != 0:
+        raise RuntimeError("kernel timeout during warm-up")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    start.record(stream)
+    for s in range(args.steps):
+        step(s, record=True)
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier(world)
+    sampler.mark(wall0, wall1)
+    ms_total = start.elapsed_time(end)
+    ms_total = max_over_ranks(ms_total, world)
+    if qwp.device_status() != 0:
+        raise RuntimeError("kernel timeout during the timed region")
+    dom_ms = float(np.mean([a.elapsed_time(b) for a, b in dom_events]))
+
+    # ---- end to end: host buffers, copies inside the timed region
+    x_host = [x.cpu().pin_memory() for x in xs]
+    y_host = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys]
+    x_dev = [torch.empty_like(x) for x in xs]
+    h2d = sum(x.numel() * x.element_size() for x in x_host)
+    d2h = sum(y.numel() * y.element_size() for y in y_host)
+
+    def e2e_step(s):
+        w = weights[s % copies]
+        for i, (_, K, N) in enumerate(LAYER):
+            x_dev[i].copy_(x_host[i], non_blocking=True)
+            qwp.q4k_gemm(w[i], x_dev[i], N, out=ys[i])
+            y_host[i].copy_(ys[i], non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 2000))
+    for s in range(args.warmup):
+        e2e_step(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(e2e_steps):
+        e2e_step(s)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    sampler.stop()
+
+    if rank != 0:
+        return 0
+
+    hbm, tc_burst, tc_sust, peak_kind = measured_peaks()
+    ms_step = ms_total / args.steps
+    value = world * M * args.steps / (ms_total * 1e-3)
+    tflops_layer = layer_flops(M) / (ms_step * 1e-3) / 1e12
+    _, Kd, Nd = LAYER[dom]
+    dom_flops = 2.0 * M * Nd * Kd
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    traffic = None
+    if os.path.exists(TRAFFIC_FILE):
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        if tr.get("kernel_hash") == kernel_source_hash() and tr.get("workload") == f"M{M} N{Nd} K{Kd}":
+            traffic = tr.get("bytes_per_launch")
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        tok_s, dt, threads = oracle_layer_tokens_per_s(args.cpu_tokens)
+        cpu = {"value": tok_s, "unit": "tok/s", "cores": threads, "kind": "oracle",
+               "sample": f"{args.cpu_tokens} of {M} tokens through the whole layer "
+                         f"(every weight dequantized exactly in fp64, naive fp64 GEMM), {dt:.1f} s"}
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"Qwen3-8B-shape layer prefill: qkv K4096->N6144, o K4096->N4096, "
+                        f"gate+up K4096->N24576, down K12288->N4096; Q4_K weights, bf16 x, fp32 y",
+            "global_batch": M * world, "seq_len": M, "parallelism": f"replicas x{world}",
+            "l2": f"weights rotate over {copies} copies ({copies * layer_w_bytes / 1e6:.0f} MB > 2x L2)",
+        },
+        "layer_tflops": tflops_layer,
+        "layer_pct_bf16_peak": 100.0 * tflops_layer / tc_burst,
+        "layer_roofline_frac": (max(layer_flops(M) / (tc_burst * 1e12), layer_bytes(M) / (hbm * 1e9))
+                                / (ms_step * 1e-3)),
+        "roofline": {
+            "kernel": f"qwp_gemm_kernel<Q4_K> {DOMINANT} M{M} N{Nd} K{Kd}",
+            "bound": "tensor", "achieved": achieved, "peak": tc_burst, "unit": "TFLOP/s",
+            "frac": achieved / tc_burst, "traffic": traffic,
+            "peak_source": f"{peak_kind} bf16 dense (burst)",
+            "hbm_gbs": (0.5625 * Nd * Kd + 2.0 * M * Kd + 4.0 * M * Nd) / (dom_ms * 1e-3) / 1e9,
+            "ms_per_launch": dom_ms,
+        },
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * M * e2e_steps / (e2e_ms * 1e-3), "unit": "tok/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": len(LAYER) * args.steps,
+        "clocks": sampler.summary(),
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

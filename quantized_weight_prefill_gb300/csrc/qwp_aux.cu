@@ -93,11 +93,11 @@ __global__ void q4k_dequant_kernel(const uint8_t *__restrict__ w, float *__restr
     float dl, ml;
     q4k_subblock_scale(hdr, 2 * c + (v >> 2), dl, ml);
     const uint32_t word = *reinterpret_cast<const uint32_t *>(grp + q4k_word_offset(R, i, c, v));
-    float vals[8];
-    q4k_word_f32(word, dl, ml, vals);
+    float2 vals[4];
+    q4k_word_f32(word, q4k_sub_consts(dl, ml), vals);
     float4 *o = reinterpret_cast<float4 *>(out + n * K + b * Q4K_BLOCK + 8 * lane);
-    o[0] = make_float4(vals[0], vals[1], vals[2], vals[3]);
-    o[1] = make_float4(vals[4], vals[5], vals[6], vals[7]);
+    o[0] = make_float4(vals[0].x, vals[0].y, vals[1].x, vals[1].y);
+    o[1] = make_float4(vals[2].x, vals[2].y, vals[3].x, vals[3].y);
 }
 
 // ---------------------------------------------------------------- W4A16 repack

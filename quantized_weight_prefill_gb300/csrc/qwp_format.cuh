@@ -64,36 +64,6 @@ __host__ __device__ __forceinline__ int w4_word_offset(int R, int i, int v) {
 
 // ---------------------------------------------------------------- Q4_K unpack
 
-// The 6-bit scales and mins of the 8 sub-blocks from the 12 packed bytes
-// (GGML packing: values 0..3 are the low 6 bits of bytes 0..3 / 4..7; values
-// 4..7 take the low (scale) or high (min) nibble of bytes 8..11 and, as bits
-// 4-5, the top two bits of bytes 0..3 (scale) / 4..7 (min)).
-struct Q4kScales {
-    float dl[8];  // d * sc_j, exact in fp32 (11 x 6 significant bits)
-    float ml[8];  // dmin * m_j, exact in fp32
-};
-
-__device__ __forceinline__ void q4k_decode_header(uint4 h, Q4kScales &s) {
-    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x & 0xFFFFu)));
-    const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x >> 16)));
-    const uint32_t s03 = h.y;  // packed bytes 0..3
-    const uint32_t s47 = h.z;  // packed bytes 4..7
-    const uint32_t s8b = h.w;  // packed bytes 8..11
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t b_lo = (s03 >> (8 * j)) & 0xFFu;
-        const uint32_t b_mid = (s47 >> (8 * j)) & 0xFFu;
-        const uint32_t b_hi = (s8b >> (8 * j)) & 0xFFu;
-        const uint32_t sc_lo = b_lo & 63u, m_lo = b_mid & 63u;
-        const uint32_t sc_hi = (b_hi & 15u) | ((b_lo >> 6) << 4);
-        const uint32_t m_hi = (b_hi >> 4) | ((b_mid >> 6) << 4);
-        s.dl[j] = d * static_cast<float>(sc_lo);
-        s.ml[j] = dmin * static_cast<float>(m_lo);
-        s.dl[j + 4] = d * static_cast<float>(sc_hi);
-        s.ml[j + 4] = dmin * static_cast<float>(m_hi);
-    }
-}
-
 // dl = d*sc_j and ml = dmin*m_j of one sub-block j (0..7), both exact in fp32.
 __device__ __forceinline__ void q4k_subblock_scale(uint4 h, int j, float &dl, float &ml) {
     const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x & 0xFFFFu)));
@@ -114,25 +84,75 @@ __device__ __forceinline__ void q4k_subblock_scale(uint4 h, int j, float &dl, fl
     ml = dmin * static_cast<float>(m);
 }
 
-// Exact integer value of nibble u of `word` as fp32: 0x4B000000 | q is 2^23 + q.
-__device__ __forceinline__ float nibble_f32(uint32_t word, int u) {
-    return __uint_as_float(0x4B000000u | ((word >> (4 * u)) & 15u)) - 8388608.0f;
+// Packed fp32x2 arithmetic (two independent lanes per instruction, sm_100+).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
 }
 
-// The 8 weights of one word: fmaf(dl, q, -ml) rounds the exact d*sc*q - dmin*m once.
-__device__ __forceinline__ void q4k_word_f32(uint32_t word, float dl, float ml, float (&w)[8]) {
-#pragma unroll
-    for (int u = 0; u < 8; ++u) w[u] = fmaf(dl, nibble_f32(word, u), -ml);
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// Per-sub-block constants of the word unpack below.  A nibble q at bits
+// 4u..4u+3 of a word, OR-ed into the fp32 pattern 0x4B000000, reads as
+// v = 2^23 + q*16^u exactly.  With s = dl*16^-u (exact: a power-of-two scale)
+// fma(v, s, -2^23*s) = q*dl exactly (q*dl has at most 21 significant bits),
+// and adding -ml rounds once: the result is the correctly rounded fp32 of
+// d*sc*q - dmin*m.
+struct Q4kSub {
+    float2 s01, s23;  // multipliers of nibbles (0,1) and (2,3) of a half-word
+    float2 c01, c23;  // -2^23 * s
+    float2 nml;       // (-ml, -ml)
+};
+
+__device__ __forceinline__ Q4kSub q4k_sub_consts(float dl, float ml) {
+    Q4kSub k;
+    k.s01 = make_float2(dl, dl * 0.0625f);
+    k.s23 = make_float2(dl * 0.00390625f, dl * 0.000244140625f);
+    k.c01 = make_float2(-8388608.0f * k.s01.x, -8388608.0f * k.s01.y);
+    k.c23 = make_float2(-8388608.0f * k.s23.x, -8388608.0f * k.s23.y);
+    k.nml = make_float2(-ml, -ml);
+    return k;
+}
+
+// The 8 weights of one word (element u in bits 4u..4u+3) as fp32, each the
+// correctly rounded d*sc*q - dmin*m; returned as K-adjacent pairs.
+__device__ __forceinline__ void q4k_word_f32(uint32_t word, const Q4kSub &k, float2 (&w)[4]) {
+    const uint32_t hi = word >> 16;
+    const float2 v01 = make_float2(__uint_as_float((word & 0x000Fu) | 0x4B000000u),
+                                   __uint_as_float((word & 0x00F0u) | 0x4B000000u));
+    const float2 v23 = make_float2(__uint_as_float((word & 0x0F00u) | 0x4B000000u),
+                                   __uint_as_float((word & 0xF000u) | 0x4B000000u));
+    const float2 v45 = make_float2(__uint_as_float((hi & 0x000Fu) | 0x4B000000u),
+                                   __uint_as_float((hi & 0x00F0u) | 0x4B000000u));
+    const float2 v67 = make_float2(__uint_as_float((hi & 0x0F00u) | 0x4B000000u),
+                                   __uint_as_float((hi & 0xF000u) | 0x4B000000u));
+    w[0] = fadd2(ffma2(v01, k.s01, k.c01), k.nml);
+    w[1] = fadd2(ffma2(v23, k.s23, k.c23), k.nml);
+    w[2] = fadd2(ffma2(v45, k.s01, k.c01), k.nml);
+    w[3] = fadd2(ffma2(v67, k.s23, k.c23), k.nml);
 }
 
 // The same 8 weights rounded once more to bf16, packed K-adjacent in pairs
 // (lower K in the low half).
-__device__ __forceinline__ void q4k_word_bf16x2(uint32_t word, float dl, float ml, uint32_t (&p)[4]) {
-    float w[8];
-    q4k_word_f32(word, dl, ml, w);
+__device__ __forceinline__ void q4k_word_bf16x2(uint32_t word, const Q4kSub &k, uint32_t (&p)[4]) {
+    float2 w[4];
+    q4k_word_f32(word, k, w);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        __nv_bfloat162 v = __floats2bfloat162_rn(w[2 * i], w[2 * i + 1]);
+        __nv_bfloat162 v = __floats2bfloat162_rn(w[i].x, w[i].y);
         p[i] = *reinterpret_cast<uint32_t *>(&v);
     }
 }

@@ -9,27 +9,32 @@
 // tok/s", section "The two prefill paths": each weight row is applied to a
 // whole chunk of prompt tokens per read.
 //
-// One CTA computes a 128-row (weights) x BN-token (BN <= 256) tile of y^T:
-//   warp 0        producer: one thread issues a bulk copy per 256-wide K
-//                 stage of packed weights and a 2-D TMA load (128-byte swizzle)
-//                 per 64-wide K block of x;
-//   warp 1        allocates tensor memory and one thread issues tcgen05.mma;
-//   warps 2..9    transform: thread (quarter q, half h) owns weight row 32q+lane
-//                 and half of each 64-wide K block; it unpacks its 32 weights to
-//                 bf16 (Q4_K) or fp16 (W4A16) and stores them with tcgen05.st
-//                 into the A operand ring in tensor memory;
-//                 afterwards the same warps drain the fp32 accumulator
-//                 (tcgen05.ld) into y.
+// One CTA computes a 128-row (weights) x BN-token (BN <= 256) tile of y^T over
+// a range of K:
+//   warp 0        x producer: one thread issues a 2-D TMA load (128-byte
+//                 swizzle) per 64-wide K block of x into the x ring;
+//   warp 1        allocates tensor memory; one thread issues tcgen05.mma;
+//   warp 2        weight producer: one bulk copy per 256-wide K stage of packed
+//                 weights into the weight ring;
+//   warps 3..18   transform: two groups of 8 warps take alternate K blocks; warp
+//                 (quarter q, half h) owns weight rows 32q..32q+31 (its tensor-
+//                 memory lane quarter) and half of the block's 64 K columns; it
+//                 unpacks its 32 weights to bf16 (Q4_K) or fp16 (W4A16) and stores
+//                 them with tcgen05.st into the A ring in tensor memory; the same
+//                 warps later drain the fp32 accumulator (tcgen05.ld) into y.
 // Tensor memory (512 columns): accumulator [128 lanes x BN] at column 0, an
 // 8-deep ring of A operand blocks (128 lanes x 64 K = 32 columns) at 256.
 // The MMA is D[128 x BN] += A[128 x 16] (tensor memory) . B[BN x 16]^T (shared
 // memory), so weights are the M side and tokens the N side: a tile reuses each
-// unpacked weight for BN tokens.
+// unpacked weight for BN tokens.  When the grid would leave SMs idle, K is split
+// across a thread-block cluster and the partial tiles are summed in rank order
+// through distributed shared memory.
 //
 // Every mbarrier wait is bounded: on expiry the thread records a timeout in
 // the library's status word and sets a CTA-wide abort flag; all roles then
 // wait (bounded) for their own copies and MMAs in flight, the tensor memory is
 // released and the CTA exits.
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -39,28 +44,29 @@
 
 namespace qwp {
 
-constexpr int NUM_XFORM_WARPS = 8;
-constexpr int NUM_THREADS = 64 + 32 * NUM_XFORM_WARPS;
-constexpr int X_STAGES = 4;
-constexpr int W_STAGES = 3;
+constexpr int XFORM_GROUPS = 2;                    // groups take alternate K blocks
+constexpr int NUM_XFORM_WARPS = 8 * XFORM_GROUPS;  // 8 warps cover one K block (4 lane quarters x 2 halves)
+constexpr int FIRST_XFORM_WARP = 3;
+constexpr int NUM_THREADS = 32 * (FIRST_XFORM_WARP + NUM_XFORM_WARPS);
+constexpr int X_MAX_STAGES = 12;
+constexpr int W_MAX_STAGES = 8;
 constexpr int A_STAGES = 8;
 constexpr int BN_MAX = 256;
-constexpr int X_STAGE_BYTES = BN_MAX * 128;
-constexpr int W_STAGE_BYTES = TILE_ROWS * Q4K_BLOCK_BYTES;  // 18432 (W4A16 stages use 16384)
-constexpr int KB_PER_STAGE = 4;                             // 64-wide K blocks per weight stage
+constexpr int KB_PER_STAGE = 4;  // 64-wide K blocks per weight stage
+constexpr int MAX_SPLITS = 8;    // portable cluster size
 constexpr uint32_t ACC_COL = 0;
 constexpr uint32_t A_COL = 256;
 constexpr uint32_t TMEM_COLS = 512;
 
-constexpr int OFF_X = 0;
-constexpr int OFF_W = OFF_X + X_STAGES * X_STAGE_BYTES;
-constexpr int OFF_BAR = OFF_W + W_STAGES * W_STAGE_BYTES;
-constexpr int NUM_BARS = 2 * X_STAGES + 2 * W_STAGES + 2 * A_STAGES + 2;
+// Shared memory: a ring region (x stages, then weight stages; reused for the
+// split-K partial sums after the main loop), then the mbarriers and misc words.
+constexpr int RING_BYTES = 224 * 1024;
+constexpr int OFF_BAR = RING_BYTES;
+constexpr int NUM_BARS = 2 * X_MAX_STAGES + 2 * W_MAX_STAGES + 2 * A_STAGES + 2;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int SMEM_USED = OFF_MISC + 16;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
+constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(OFF_W % 1024 == 0 && X_STAGE_BYTES % 1024 == 0, "swizzle atoms need 1 KiB alignment");
+static_assert(512 * BN_MAX <= RING_BYTES, "split-K partials must fit the ring region");
 
 struct GemmArgs {
     const uint8_t *w;       // repacked weights
@@ -70,7 +76,10 @@ struct GemmArgs {
     uint32_t *status;       // library status word
     int M, N, K, group;
     int bn;                 // token tile = MMA N (multiple of 16, <= 256)
-    int kb_per_split;       // 64-wide K blocks per CTA along K
+    int kb_per_split;       // 64-wide K blocks per CTA along K (multiple of 4)
+    int splits;             // CTAs along K = cluster size (1 = no reduction)
+    int x_stages, w_stages;
+    int x_stage_bytes, w_stage_bytes;
     uint64_t timeout_ns;
 };
 
@@ -86,24 +95,52 @@ struct Ctl {
     uint64_t timeout_ns;
 };
 
-// Bounded wait on phase `parity` of `bar`.  False if it timed out or another
-// thread of the CTA aborted; a timeout records `where` in the status word.
+// Bounded wait on phase `parity` of `bar`.  False if it timed out or the CTA is
+// aborting (this CTA or, through the status word, any other); a timeout
+// records `where` in the status word.  The loop mostly sits in try_wait (which
+// suspends the thread in hardware); the clock and the global status word are
+// looked at only every 64 polls.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl &ctl,
                                          uint32_t where, bool honour_abort = true) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    while (true) {
+    for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (honour_abort && (*reinterpret_cast<volatile uint32_t *>(ctl.abort) ||
-                             *reinterpret_cast<volatile uint32_t *>(ctl.status))) {
-            *reinterpret_cast<volatile uint32_t *>(ctl.abort) = 1u;  // another CTA already failed
-            return false;
+        if (honour_abort && *reinterpret_cast<volatile uint32_t *>(ctl.abort)) return false;
+        if ((it & 63u) == 0) {
+            if (honour_abort && *reinterpret_cast<volatile uint32_t *>(ctl.status)) {
+                *reinterpret_cast<volatile uint32_t *>(ctl.abort) = 1u;  // another CTA failed
+                return false;
+            }
+            if (global_timer_ns() - t0 > ctl.timeout_ns) {
+                *reinterpret_cast<volatile uint32_t *>(ctl.abort) = 1u;
+                atomicCAS(ctl.status, 0u, 0x100u | where);
+                return false;
+            }
         }
-        if (global_timer_ns() - t0 > ctl.timeout_ns) {
-            *reinterpret_cast<volatile uint32_t *>(ctl.abort) = 1u;
-            atomicCAS(ctl.status, 0u, 0x100u | where);
-            return false;
-        }
+    }
+}
+
+__device__ __forceinline__ bool aborted(const Ctl &ctl) {
+    return *reinterpret_cast<volatile uint32_t *>(ctl.abort) != 0;
+}
+
+// Unpack one row's half of a 64-wide K block (4 words = 32 weights) into 16
+// packed 16-bit pairs for the A operand.
+template <bool kQ4K>
+__device__ __forceinline__ void unpack_quarter(uint4 wv, float dl, float ml, __half2 mz, __half2 s2,
+                                               uint32_t (&regs)[16]) {
+    const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+    const Q4kSub ks = q4k_sub_consts(dl, ml);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t p[4];
+        if (kQ4K)
+            q4k_word_bf16x2(w[i], ks, p);
+        else
+            w4_word_f16x2(w[i], mz, s2, p);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) regs[4 * i + e] = p[e];
     }
 }
 
@@ -124,38 +161,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int kb_end = min(nkb_total, kb_begin + args.kb_per_split);
     const int nkb = kb_end - kb_begin;
     const int nstage = (nkb + KB_PER_STAGE - 1) / KB_PER_STAGE;
+    const int XS = args.x_stages, WS = args.w_stages;
+    uint8_t *const x_ring = smem;
+    uint8_t *const w_ring = smem + XS * args.x_stage_bytes;
 
     const uint32_t bar0 = smem_u32(smem + OFF_BAR);
-    const uint32_t x_full = bar0, x_empty = x_full + 8 * X_STAGES;
-    const uint32_t w_full = x_empty + 8 * X_STAGES, w_empty = w_full + 8 * W_STAGES;
-    const uint32_t a_full = w_empty + 8 * W_STAGES, a_empty = a_full + 8 * A_STAGES;
+    const uint32_t x_full = bar0, x_empty = x_full + 8 * X_MAX_STAGES;
+    const uint32_t w_full = x_empty + 8 * X_MAX_STAGES, w_empty = w_full + 8 * W_MAX_STAGES;
+    const uint32_t a_full = w_empty + 8 * W_MAX_STAGES, a_empty = a_full + 8 * A_STAGES;
     const uint32_t acc_full = a_empty + 8 * A_STAGES, drain = acc_full + 8;
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + OFF_MISC);  // [0] tmem base, [1] abort
     const Ctl ctl{misc + 1, args.status, args.timeout_ns};
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < X_STAGES; ++s) {
+        for (int s = 0; s < X_MAX_STAGES; ++s) {
             mbar_init(x_full + 8 * s, 1);
             mbar_init(x_empty + 8 * s, 1);
         }
-        for (int s = 0; s < W_STAGES; ++s) {
+        for (int s = 0; s < W_MAX_STAGES; ++s) {
             mbar_init(w_full + 8 * s, 1);
             mbar_init(w_empty + 8 * s, NUM_XFORM_WARPS);
         }
         for (int s = 0; s < A_STAGES; ++s) {
-            mbar_init(a_full + 8 * s, NUM_XFORM_WARPS);
+            mbar_init(a_full + 8 * s, NUM_XFORM_WARPS / XFORM_GROUPS);
             mbar_init(a_empty + 8 * s, 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(drain, 1);
         // A failure recorded earlier (and not yet read by qwp_device_status) makes
-        // every later launch exit at once instead of waiting out its own timeouts.
+        // every later launch skip its work instead of waiting out its own timeouts.
         misc[1] = *reinterpret_cast<volatile uint32_t *>(args.status) ? 1u : 0u;
         fence_mbar_init();
         prefetch_tensormap(&tmap_x);
     }
-    __syncthreads();
-    if (misc[1]) return;
     if (warp == 1) {
         tmem_alloc(smem_u32(misc), TMEM_COLS);
         tmem_relinquish();
@@ -164,14 +202,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
+    const bool skip = misc[1] != 0;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            int issued_x = 0, issued_w = 0;
+        // ------------------------------------------------------------ x producer
+        if (lane == 0 && !skip) {
+            int issued = 0;
+            for (int j = 0; j < nkb; ++j) {
+                const int xs = j % XS;
+                if (!wait_bar(x_empty + 8 * xs, ((j / XS) & 1) ^ 1, ctl, WAIT_X_EMPTY)) break;
+                mbar_arrive_expect_tx(x_full + 8 * xs, static_cast<uint32_t>(args.bn) * 128u);
+                tma_load_2d(smem_u32(x_ring + xs * args.x_stage_bytes), &tmap_x,
+                            (kb_begin + j) * CHUNK_K, m0, x_full + 8 * xs);
+                issued = j + 1;
+            }
+            // Every copy issued above lands before the CTA may exit.
+            for (int j = max(0, issued - XS); j < issued; ++j)
+                wait_bar(x_full + 8 * (j % XS), (j / XS) & 1, ctl, WAIT_DRAIN, false);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ weight producer
+        if (lane == 0 && !skip) {
+            int issued = 0;
             for (int s = 0; s < nstage; ++s) {
-                const int ws = s % W_STAGES;
-                if (!wait_bar(w_empty + 8 * ws, ((s / W_STAGES) & 1) ^ 1, ctl, WAIT_W_EMPTY)) break;
+                const int ws = s % WS;
+                if (!wait_bar(w_empty + 8 * ws, ((s / WS) & 1) ^ 1, ctl, WAIT_W_EMPTY)) break;
                 const int kb0 = kb_begin + KB_PER_STAGE * s;
                 const int nblk = min(KB_PER_STAGE, kb_end - kb0);
                 const uint8_t *src;
@@ -184,41 +239,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     bytes = static_cast<uint32_t>(R) * CHUNK_ROW_BYTES * nblk;
                 }
                 mbar_arrive_expect_tx(w_full + 8 * ws, bytes);
-                bulk_copy_g2s(smem_u32(smem + OFF_W + ws * W_STAGE_BYTES), src, bytes, w_full + 8 * ws);
-                issued_w = s + 1;
-                bool ok = true;
-                for (int c = 0; c < nblk; ++c) {
-                    const int j = KB_PER_STAGE * s + c;
-                    const int xs = j % X_STAGES;
-                    if (!wait_bar(x_empty + 8 * xs, ((j / X_STAGES) & 1) ^ 1, ctl, WAIT_X_EMPTY)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(x_full + 8 * xs, static_cast<uint32_t>(args.bn) * 128u);
-                    tma_load_2d(smem_u32(smem + OFF_X + xs * X_STAGE_BYTES), &tmap_x,
-                                (kb0 + c) * CHUNK_K, m0, x_full + 8 * xs);
-                    issued_x = j + 1;
-                }
-                if (!ok) break;
+                bulk_copy_g2s(smem_u32(w_ring + ws * args.w_stage_bytes), src, bytes, w_full + 8 * ws);
+                issued = s + 1;
             }
-            // Every copy issued above has landed before the CTA may exit.
-            for (int j = max(0, issued_x - X_STAGES); j < issued_x; ++j)
-                wait_bar(x_full + 8 * (j % X_STAGES), (j / X_STAGES) & 1, ctl, WAIT_DRAIN, false);
-            for (int s = max(0, issued_w - W_STAGES); s < issued_w; ++s)
-                wait_bar(w_full + 8 * (s % W_STAGES), (s / W_STAGES) & 1, ctl, WAIT_DRAIN, false);
+            for (int s = max(0, issued - WS); s < issued; ++s)
+                wait_bar(w_full + 8 * (s % WS), (s / WS) & 1, ctl, WAIT_DRAIN, false);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && !skip) {
             const uint32_t idesc = make_idesc_f16(kQ4K, TILE_ROWS, static_cast<uint32_t>(args.bn));
             bool ok = true;
-            for (int j = 0; j < nkb && ok; ++j) {
-                const int xs = j % X_STAGES, as = j % A_STAGES;
-                ok = wait_bar(x_full + 8 * xs, (j / X_STAGES) & 1, ctl, WAIT_X_FULL) &&
+            for (int j = 0; j < nkb; ++j) {
+                const int xs = j % XS, as = j % A_STAGES;
+                ok = wait_bar(x_full + 8 * xs, (j / XS) & 1, ctl, WAIT_X_FULL) &&
                      wait_bar(a_full + 8 * as, (j / A_STAGES) & 1, ctl, WAIT_A_FULL);
                 if (!ok) break;
                 tc_fence_after();
-                const uint64_t bdesc = smem_desc_sw128(smem_u32(smem + OFF_X + xs * X_STAGE_BYTES));
+                const uint64_t bdesc = smem_desc_sw128(smem_u32(x_ring + xs * args.x_stage_bytes));
 #pragma unroll
                 for (int kk = 0; kk < CHUNK_K / 16; ++kk)
                     mma_ts(tmem + ACC_COL, tmem + A_COL + 32u * as + 8u * kk, bdesc + 2u * kk, idesc,
@@ -235,99 +273,104 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else {
         // ------------------------------------------------------------ transform + epilogue
-        const uint32_t xw = warp - 2;
-        const uint32_t quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31
-        const int half = static_cast<int>(xw >> 2);
+        const uint32_t xw = warp - FIRST_XFORM_WARP;
+        const int grp = static_cast<int>(xw >> 3);          // this warp's K blocks: j % XFORM_GROUPS == grp
+        const uint32_t quarter = warp & 3;                   // tensor-memory lanes 32*quarter .. +31
+        const int half = static_cast<int>((xw >> 2) & 1);    // which 32 of the block's 64 K columns
         const int r = static_cast<int>(quarter * 32 + lane);
         const bool valid = r < R;
         const int64_t n = static_cast<int64_t>(tile) * TILE_ROWS + r;
         const uint32_t lane_base = (quarter * 32u) << 16;
-        bool ok = true;
-        for (int s = 0; s < nstage && ok; ++s) {
-            const int ws = s % W_STAGES;
-            // Every lane waits; the warp moves on together (tcgen05.st/ld are warp-collective).
-            if (!__all_sync(0xffffffffu, wait_bar(w_full + 8 * ws, (s / W_STAGES) & 1, ctl, WAIT_W_FULL))) {
-                ok = false;
-                break;
-            }
-            const uint8_t *wst = smem + OFF_W + ws * W_STAGE_BYTES;
+        bool ok = !skip;
+        uint4 hdr = make_uint4(0, 0, 0, 0);  // Q4_K header of the current weight stage
+
+        // Unpack K block j of this thread's row into `regs`; waits for its weight
+        // stage when j opens one and releases the stage after its last block.
+        auto prepare = [&](int j, uint32_t (&regs)[16]) -> bool {
+            const int s = j / KB_PER_STAGE, c = j % KB_PER_STAGE;
+            const int ws = s % WS;
+            const uint8_t *wst = w_ring + ws * args.w_stage_bytes;
             const int kb0 = kb_begin + KB_PER_STAGE * s;
             const int nblk = min(KB_PER_STAGE, kb_end - kb0);
-            uint4 hdr = make_uint4(0, 0, 0, 0);
-            if (kQ4K && valid) hdr = *reinterpret_cast<const uint4 *>(wst + Q4K_HEADER_BYTES * r);
-#pragma unroll
-            for (int c = 0; c < KB_PER_STAGE; ++c) {
-                if (c >= nblk) break;
-                const int j = KB_PER_STAGE * s + c;
-                const int as = j % A_STAGES;
-                uint32_t regs[16];
-                if (kQ4K) {
-                    uint4 wv = make_uint4(0, 0, 0, 0);
-                    if (valid)
-                        wv = *reinterpret_cast<const uint4 *>(wst + Q4K_HEADER_BYTES * R +
-                                                              CHUNK_ROW_BYTES * R * c +
-                                                              (half * R + r) * 16);
-                    float dl, ml;
-                    q4k_subblock_scale(hdr, 2 * c + half, dl, ml);
-                    uint32_t p[4];
-                    q4k_word_bf16x2(wv.x, dl, ml, p);
-                    regs[0] = p[0]; regs[1] = p[1]; regs[2] = p[2]; regs[3] = p[3];
-                    q4k_word_bf16x2(wv.y, dl, ml, p);
-                    regs[4] = p[0]; regs[5] = p[1]; regs[6] = p[2]; regs[7] = p[3];
-                    q4k_word_bf16x2(wv.z, dl, ml, p);
-                    regs[8] = p[0]; regs[9] = p[1]; regs[10] = p[2]; regs[11] = p[3];
-                    q4k_word_bf16x2(wv.w, dl, ml, p);
-                    regs[12] = p[0]; regs[13] = p[1]; regs[14] = p[2]; regs[15] = p[3];
-                } else {
-                    uint4 wv = make_uint4(0, 0, 0, 0);
-                    __half2 s2 = __float2half2_rn(0.f);
-                    __half2 mz = w4_magic_zero(0);
-                    if (valid) {
-                        wv = *reinterpret_cast<const uint4 *>(wst + CHUNK_ROW_BYTES * R * c +
-                                                              (half * R + r) * 16);
-                        const int64_t ng = args.K / args.group;
-                        const int64_t g = (static_cast<int64_t>(kb0 + c) * CHUNK_K) / args.group;
-                        s2 = __half2half2(args.scales[n * ng + g]);
-                        mz = w4_magic_zero(args.zeros[n * ng + g]);
-                    }
-                    uint32_t p[4];
-                    w4_word_f16x2(wv.x, mz, s2, p);
-                    regs[0] = p[0]; regs[1] = p[1]; regs[2] = p[2]; regs[3] = p[3];
-                    w4_word_f16x2(wv.y, mz, s2, p);
-                    regs[4] = p[0]; regs[5] = p[1]; regs[6] = p[2]; regs[7] = p[3];
-                    w4_word_f16x2(wv.z, mz, s2, p);
-                    regs[8] = p[0]; regs[9] = p[1]; regs[10] = p[2]; regs[11] = p[3];
-                    w4_word_f16x2(wv.w, mz, s2, p);
-                    regs[12] = p[0]; regs[13] = p[1]; regs[14] = p[2]; regs[15] = p[3];
-                }
-                if (!__all_sync(0xffffffffu,
-                                wait_bar(a_empty + 8 * as, ((j / A_STAGES) & 1) ^ 1, ctl, WAIT_A_EMPTY))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                tmem_st_x16(tmem + lane_base + A_COL + 32u * as + 16u * half, regs);
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(a_full + 8 * as);
+            if (c == grp) {  // this warp's first block of the stage
+                // Every lane waits; the warp moves on together (tcgen05.st/ld are warp-collective).
+                if (!__all_sync(0xffffffffu, wait_bar(w_full + 8 * ws, (s / WS) & 1, ctl, WAIT_W_FULL)))
+                    return false;
+                if (kQ4K && valid) hdr = *reinterpret_cast<const uint4 *>(wst + Q4K_HEADER_BYTES * r);
             }
+            uint4 wv = make_uint4(0, 0, 0, 0);
+            float dl = 0.f, ml = 0.f;
+            __half2 s2 = __float2half2_rn(0.f), mz = w4_magic_zero(0);
+            if (kQ4K) {
+                if (valid)
+                    wv = *reinterpret_cast<const uint4 *>(wst + Q4K_HEADER_BYTES * R + CHUNK_ROW_BYTES * R * c +
+                                                          (half * R + r) * 16);
+                q4k_subblock_scale(hdr, 2 * c + half, dl, ml);
+            } else if (valid) {
+                wv = *reinterpret_cast<const uint4 *>(wst + CHUNK_ROW_BYTES * R * c + (half * R + r) * 16);
+                const int64_t ng = args.K / args.group;
+                const int64_t g = (static_cast<int64_t>(kb0 + c) * CHUNK_K) / args.group;
+                s2 = __half2half2(args.scales[n * ng + g]);
+                mz = w4_magic_zero(args.zeros[n * ng + g]);
+            }
+            // This warp's last block of the stage: its reads of the stage are done.  (A
+            // warp with no block in a partial last stage never arrives; nothing refills it.)
+            if (c + XFORM_GROUPS >= nblk) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(w_empty + 8 * ws);
+            }
+            unpack_quarter<kQ4K>(wv, dl, ml, mz, s2, regs);
+            return true;
+        };
+        // Store block j into its A ring slot once the MMA has released the slot.
+        auto issue = [&](int j, const uint32_t (&regs)[16]) -> bool {
+            const int as = j % A_STAGES;
+            if (!__all_sync(0xffffffffu, wait_bar(a_empty + 8 * as, ((j / A_STAGES) & 1) ^ 1, ctl, WAIT_A_EMPTY)))
+                return false;
+            tc_fence_after();
+            tmem_st_x16(tmem + lane_base + A_COL + 32u * as + 16u * half, regs);
+            return true;
+        };
+        // Publish block j to the MMA issuer once its tensor-memory store has landed.
+        auto finish = [&](int j) {
+            tmem_wait_st();
+            tc_fence_before();
             __syncwarp();
-            if (ok && lane == 0) mbar_arrive(w_empty + 8 * ws);
+            if (lane == 0) mbar_arrive(a_full + 8 * (j % A_STAGES));
+        };
+
+        // Software pipeline over this warp's blocks j = grp, grp+G, ...: the unpack of
+        // the next block overlaps the tensor-memory store of the current one.
+        constexpr int G = XFORM_GROUPS;
+        uint32_t ra[16], rb[16];
+        if (ok && grp < nkb) ok = prepare(grp, ra);
+        for (int j = grp; ok && j < nkb; j += 2 * G) {
+            if (!(ok = issue(j, ra))) break;
+            if (j + G < nkb && !(ok = prepare(j + G, rb))) break;
+            finish(j);
+            if (j + G >= nkb) break;
+            if (!(ok = issue(j + G, rb))) break;
+            if (j + 2 * G < nkb && !(ok = prepare(j + 2 * G, ra))) break;
+            finish(j + G);
         }
+        tmem_wait_st();  // no tensor-memory store may be in flight past this point
         __syncwarp();
         if (ok && __all_sync(0xffffffffu, wait_bar(acc_full, 0, ctl, WAIT_ACC_FULL))) {
             tc_fence_after();
-            for (int ci = half; ci < args.bn / 16; ci += 2) {
+            float *part = reinterpret_cast<float *>(smem);  // [bn][128] partial tile (split-K)
+            for (int ci = static_cast<int>(xw >> 2); ci < args.bn / 16; ci += NUM_XFORM_WARPS / 4) {
                 uint32_t v[16];
                 tmem_ld_x16(tmem + lane_base + ACC_COL + 16u * ci, v);
                 tmem_wait_ld();
-                if (valid) {
+                if (args.splits > 1) {
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) part[(16 * ci + t) * TILE_ROWS + r] = __uint_as_float(v[t]);
+                } else if (valid) {
                     const int mb = m0 + 16 * ci;
 #pragma unroll
                     for (int t = 0; t < 16; ++t)
                         if (mb + t < args.M)
-                            args.y[static_cast<int64_t>(mb + t) * args.N + n] = __uint_as_float(v[t]);
+                            __stcs(args.y + static_cast<int64_t>(mb + t) * args.N + n, __uint_as_float(v[t]));
                 }
             }
         }
@@ -335,6 +378,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 
     __syncthreads();
+    if (args.splits > 1) {
+        // Deterministic split-K reduction through distributed shared memory: CTA
+        // `rank` of the cluster sums, in rank order, every CTA's partial for its
+        // share of the tile's tokens and writes y.  Every CTA reaches both cluster
+        // barriers whatever happened above (all waits before them are bounded).
+        cluster_sync();
+        const int S = args.splits;
+        const uint32_t rank = cluster_ctarank();
+        const int per = (args.bn + S - 1) / S;
+        const int t0 = min(args.bn, static_cast<int>(rank) * per);
+        const int t1 = min(args.bn, t0 + per);
+        if (!aborted(ctl)) {
+            const uint32_t part0 = smem_u32(smem);
+            const int items = (t1 - t0) * (TILE_ROWS / 4);
+            for (int it = threadIdx.x; it < items; it += NUM_THREADS) {
+                const int t = t0 + it / (TILE_ROWS / 4);
+                const int r4 = 4 * (it % (TILE_ROWS / 4));
+                const uint32_t off = static_cast<uint32_t>((t * TILE_ROWS + r4) * 4);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int q = 0; q < S; ++q) {
+                    const float4 v = ld_shared_cluster_f4(map_shared_rank(part0 + off, q));
+                    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+                }
+                const int m = m0 + t;
+                if (m < args.M) {
+                    float *yr = args.y + static_cast<int64_t>(m) * args.N + static_cast<int64_t>(tile) * TILE_ROWS;
+                    const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (r4 + e < R) __stcs(yr + r4 + e, a4[e]);
+                }
+            }
+        }
+        cluster_sync();
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
@@ -384,18 +462,68 @@ static int choose_bn(int64_t M) {
     return static_cast<int>((per + 15) / 16 * 16);
 }
 
+struct DeviceInfo {
+    int sms = 0;
+    int slots[2][MAX_SPLITS + 1] = {};  // [kQ4K][S]: CTAs resident at once with clusters of S
+    bool ready[2] = {false, false};
+};
+
 template <bool kQ4K>
-static int set_smem_attr() {
-    static std::atomic<uint64_t> done_mask{0};
+static int device_info(DeviceInfo *&out) {
+    static DeviceInfo info[64];
+    static std::mutex mu;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return QWP_ERR_CUDA;
-    const uint64_t bit = 1ull << (dev & 63);
-    if (done_mask.load() & bit) return QWP_OK;
-    if (cudaFuncSetAttribute(qwp_gemm_kernel<kQ4K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES) != cudaSuccess)
-        return QWP_ERR_CUDA;
-    done_mask.fetch_or(bit);
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QWP_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    DeviceInfo &d = info[dev];
+    if (!d.ready[kQ4K]) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return QWP_ERR_CUDA;
+        if (cudaFuncSetAttribute(qwp_gemm_kernel<kQ4K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES) != cudaSuccess)
+            return QWP_ERR_CUDA;
+        d.slots[kQ4K][1] = d.sms;
+        for (int S = 2; S <= MAX_SPLITS; ++S) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(1, 1, S * 64);
+            cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+            cfg.dynamicSmemBytes = SMEM_BYTES;
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = 1;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = S;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, qwp_gemm_kernel<kQ4K>, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                clusters = 0;
+            }
+            d.slots[kQ4K][S] = clusters * S;
+        }
+        d.ready[kQ4K] = true;
+    }
+    out = &d;
     return QWP_OK;
+}
+
+// Split-K factor: model the time as (waves of resident CTAs) x (fixed cost of
+// two weight stages + the K stages per split) and take the cheapest.
+static int choose_splits(const int *slots, int64_t base_ctas, int nstages) {
+    int best = 1;
+    double best_cost = 1e30;
+    for (int S = 1; S <= MAX_SPLITS && S <= nstages; ++S) {
+        const int per = (nstages + S - 1) / S;
+        if ((nstages + per - 1) / per != S || slots[S] <= 0) continue;  // no empty or duplicate splits
+        const int64_t waves = (base_ctas * S + slots[S] - 1) / slots[S];
+        const double cost = static_cast<double>(waves) * (2.0 + per);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = S;
+        }
+    }
+    return best;
 }
 
 template <bool kQ4K>
@@ -404,12 +532,14 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
                        uint64_t timeout_ns) {
     int rc = check_device();
     if (rc) return rc;
-    if ((rc = set_smem_attr<kQ4K>())) return rc;
+    DeviceInfo *info = nullptr;
+    if ((rc = device_info<kQ4K>(info))) return rc;
     uint32_t *status = status_word();
     if (!status) return QWP_ERR_CUDA;
     const int bn = choose_bn(M);
     CUtensorMap map;
     if ((rc = encode_x_map(&map, x, kQ4K, M, K, bn))) return rc;
+
     GemmArgs a;
     a.w = static_cast<const uint8_t *>(w);
     a.scales = static_cast<const __half *>(scales);
@@ -421,12 +551,40 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     a.K = static_cast<int>(K);
     a.group = static_cast<int>(group);
     a.bn = bn;
-    a.kb_per_split = static_cast<int>(K / CHUNK_K);
     a.timeout_ns = timeout_ns;
-    dim3 grid(static_cast<unsigned>((N + TILE_ROWS - 1) / TILE_ROWS),
-              static_cast<unsigned>((M + bn - 1) / bn), 1);
-    qwp_gemm_kernel<kQ4K><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(map, a);
-    return launch_status();
+    a.x_stage_bytes = bn * 128;
+    a.w_stage_bytes = kQ4K ? TILE_ROWS * Q4K_BLOCK_BYTES : TILE_ROWS * CHUNK_ROW_BYTES * KB_PER_STAGE;
+    a.w_stages = 4;
+    a.x_stages = std::min(X_MAX_STAGES, (RING_BYTES - a.w_stages * a.w_stage_bytes) / a.x_stage_bytes);
+    if (a.x_stages == X_MAX_STAGES)
+        a.w_stages = std::min(W_MAX_STAGES, (RING_BYTES - a.x_stages * a.x_stage_bytes) / a.w_stage_bytes);
+
+    const int64_t row_tiles = (N + TILE_ROWS - 1) / TILE_ROWS;
+    const int64_t tok_tiles = (M + bn - 1) / bn;
+    const int nkb = static_cast<int>(K / CHUNK_K);
+    const int nstages = (nkb + KB_PER_STAGE - 1) / KB_PER_STAGE;
+    const int S = choose_splits(info->slots[kQ4K], row_tiles * tok_tiles, nstages);
+    a.splits = S;
+    a.kb_per_split = ((nstages + S - 1) / S) * KB_PER_STAGE;
+    if (row_tiles > 0x7fffffff || tok_tiles > 65535) return QWP_ERR_UNSUPPORTED_SHAPE;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(row_tiles), static_cast<unsigned>(tok_tiles), S);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 1;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = S;
+    cfg.attrs = &attr;
+    cfg.numAttrs = S > 1 ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, qwp_gemm_kernel<kQ4K>, map, a) != cudaSuccess) {
+        cudaGetLastError();
+        return QWP_ERR_CUDA;
+    }
+    return QWP_OK;
 }
 
 }  // namespace qwp
