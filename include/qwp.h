@@ -47,7 +47,8 @@ typedef enum {
     QWP_ERR_MISALIGNED = -3,       /* a device pointer is not 16-byte aligned            */
     QWP_ERR_CUDA = -4,             /* a CUDA runtime/driver call or a launch failed      */
     QWP_ERR_DEVICE = -5,           /* the current device is not an sm_103 GPU            */
-    QWP_ERR_TIMEOUT = -6           /* a kernel's bounded wait expired (qwp_device_status) */
+    QWP_ERR_TIMEOUT = -6,          /* a kernel's bounded wait expired (qwp_device_status) */
+    QWP_ERR_RANGE = -7             /* an activation overflowed fp16 (qwp_device_status)   */
 } qwp_status;
 
 /* Human-readable name of a status code (static string). */
@@ -82,14 +83,28 @@ QWP_API int q4k_repack(const void *w_ggml_dev, void *w_tiled_dev, int64_t N, int
 QWP_API int q4k_dequant(const void *w_tiled_dev, float *w_out_dev, int64_t N, int64_t K, void *stream);
 
 /*
- * y_dev[M][N] (fp32) = x_dev[M][K] (bf16) . W^T, W the repacked Q4_K matrix.
- * Each weight is rounded once to bf16 after an exact fp32 dequant and fed to
- * the tensor cores (tcgen05, fp32 accumulation in tensor memory).  K % 256 ==
- * 0; M, N >= 0 (M == 0 or N == 0 is a no-op); x_dev, w_tiled_dev and y_dev
- * 16-byte aligned; x rows contiguous (row stride K).
+ * y_dev[M][N] (fp32) = x_dev[M][K] (fp16) . W^T, W the repacked Q4_K matrix.
+ * Each weight is unpacked on chip to an fp16 tensor-core operand: q*sc exactly
+ * (from the 0x6400|n form of the nibble), then d*(q*sc) - RN(dmin*m) rounded
+ * once to fp16 (requires |d|*sc*15 < 65504, true of any practical block);
+ * fp32 accumulation in tensor memory.  K % 256 == 0; M, N >= 0 (M == 0 or
+ * N == 0 is a no-op); x_dev, w_tiled_dev and y_dev 16-byte aligned; x rows
+ * contiguous (row stride K).  Allocates nothing.
+ */
+QWP_API int q4k_gemm_f16(const void *w_tiled_dev, const void *x_dev, float *y_dev,
+                         int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * The same product for bf16 activations: x is first converted to fp16 (exact
+ * for |x| in [2^-14, 65504]; smaller values lose at most 2^-25 absolutely;
+ * larger ones overflow, which qwp_device_status reports as QWP_ERR_RANGE) into
+ * M*K*2 bytes of scratch taken from a library-owned, stream-ordered memory pool
+ * on the current device and released in stream order after the GEMM; then
+ * q4k_gemm_f16 runs, launched so that its set-up overlaps the conversion.
+ * Same shape and alignment rules as q4k_gemm_f16.
  */
 QWP_API int q4k_gemm(const void *w_tiled_dev, const void *x_dev, float *y_dev,
-             int64_t M, int64_t N, int64_t K, void *stream);
+                     int64_t M, int64_t N, int64_t K, void *stream);
 
 /*
  * W4A16 (group-wise asymmetric int4): wq[N][K/8] int32 words, each holding
@@ -123,11 +138,12 @@ QWP_API int w4a16_gemm(const void *wq_tiled_dev, const void *scales_dev, const u
 
 /*
  * Synchronize `stream`, then read and clear the library's device status word
- * on the current device.  Returns QWP_OK, QWP_ERR_TIMEOUT if a kernel's
+ * on the current device.  Returns QWP_OK; QWP_ERR_TIMEOUT if a kernel's
  * bounded wait on an mbarrier expired (the kernel then released its tensor
- * memory and exited; its output is invalid), or QWP_ERR_CUDA.  While the
- * word holds an error, every GEMM launch on that device exits at once without
- * writing y; reading it here clears it.
+ * memory and exited; its output is invalid; while a timeout is recorded, every
+ * GEMM launch on that device exits at once without writing y); QWP_ERR_RANGE
+ * if q4k_gemm met an activation beyond the fp16 range (y then holds inf/nan);
+ * or QWP_ERR_CUDA.  Reading the word here clears it.
  */
 QWP_API int qwp_device_status(void *stream);
 

@@ -17,14 +17,14 @@ import torch
 from . import _build
 
 __all__ = [
-    "QwpError", "library", "q4k_repacked_bytes", "q4k_repack", "q4k_dequant", "q4k_gemm",
+    "QwpError", "library", "q4k_repacked_bytes", "q4k_repack", "q4k_dequant", "q4k_gemm", "q4k_gemm_f16",
     "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "device_status",
     "EXPORTED_SYMBOLS",
 ]
 
 # Every symbol include/qwp.h declares.
 EXPORTED_SYMBOLS = (
-    "qwp_status_string", "q4k_repacked_bytes", "q4k_repack", "q4k_dequant", "q4k_gemm",
+    "qwp_status_string", "q4k_repacked_bytes", "q4k_repack", "q4k_dequant", "q4k_gemm", "q4k_gemm_f16",
     "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "qwp_device_status",
 )
 
@@ -55,6 +55,7 @@ def library() -> ctypes.CDLL:
         lib.q4k_repack.argtypes = [p, p, i64, i64, p]
         lib.q4k_dequant.argtypes = [p, p, i64, i64, p]
         lib.q4k_gemm.argtypes = [p, p, p, i64, i64, i64, p]
+        lib.q4k_gemm_f16.argtypes = [p, p, p, i64, i64, i64, p]
         lib.w4a16_repack.argtypes = [p, p, i64, i64, p]
         lib.w4a16_dequant.argtypes = [p, p, p, p, i64, i64, i64, p]
         lib.w4a16_gemm.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p]
@@ -132,6 +133,18 @@ def q4k_gemm(w_tiled: torch.Tensor, x: torch.Tensor, N: int, out: torch.Tensor |
         out = torch.empty(M, N, dtype=torch.float32, device=x.device)
     _dev(out, torch.float32, "out")
     _check(library().q4k_gemm(_ptr(w_tiled), _ptr(x), _ptr(out), M, N, K, _stream(x)), "q4k_gemm")
+    return out
+
+
+def q4k_gemm_f16(w_tiled: torch.Tensor, x: torch.Tensor, N: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """y[M, N] (fp32) = x[M, K] (fp16) . W^T with W the repacked Q4_K matrix."""
+    _dev(w_tiled, torch.uint8, "w_tiled")
+    _dev(x, torch.float16, "x")
+    M, K = x.shape
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.float32, device=x.device)
+    _dev(out, torch.float32, "out")
+    _check(library().q4k_gemm_f16(_ptr(w_tiled), _ptr(x), _ptr(out), M, N, K, _stream(x)), "q4k_gemm_f16")
     return out
 
 

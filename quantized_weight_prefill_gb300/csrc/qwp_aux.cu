@@ -1,5 +1,6 @@
 // Load-time repack kernels, the dequant test entry points, the device status
 // word and the device check.
+#include <algorithm>
 #include <atomic>
 
 #include "qwp_format.cuh"
@@ -46,7 +47,8 @@ uint32_t *status_word() {
 // One warp per (row n, super-block b): lanes 0..3 copy the 16 header bytes,
 // lane l builds word v = l%8 of chunk c = l/8 from the GGML nibble bytes
 // (element e < 32 of chunk c is the low nibble of byte 32c+e, element e >= 32
-// the high nibble of byte 32c+e-32).
+// the high nibble of byte 32c+e-32) in the interleaved order: element 8v+2p at
+// bits 4p..4p+3, element 8v+2p+1 at bits 16+4p..19+4p.
 __global__ void q4k_repack_kernel(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst,
                                   int64_t N, int64_t K) {
     const int64_t nb = K / Q4K_BLOCK;
@@ -70,7 +72,7 @@ __global__ void q4k_repack_kernel(const uint8_t *__restrict__ src, uint8_t *__re
         const int e = 8 * v + u;
         const uint32_t byte = qs[e & 31];
         const uint32_t nib = (e < 32) ? (byte & 15u) : (byte >> 4);
-        word |= nib << (4 * u);
+        word |= nib << ((u & 1) ? 16 + 4 * (u >> 1) : 4 * (u >> 1));
     }
     *reinterpret_cast<uint32_t *>(grp + q4k_word_offset(R, i, c, v)) = word;
 }
@@ -94,7 +96,7 @@ __global__ void q4k_dequant_kernel(const uint8_t *__restrict__ w, float *__restr
     q4k_subblock_scale(hdr, 2 * c + (v >> 2), dl, ml);
     const uint32_t word = *reinterpret_cast<const uint32_t *>(grp + q4k_word_offset(R, i, c, v));
     float2 vals[4];
-    q4k_word_f32(word, q4k_sub_consts(dl, ml), vals);
+    q4k_word_f32(word, dl, ml, vals);
     float4 *o = reinterpret_cast<float4 *>(out + n * K + b * Q4K_BLOCK + 8 * lane);
     o[0] = make_float4(vals[0].x, vals[0].y, vals[1].x, vals[1].y);
     o[1] = make_float4(vals[2].x, vals[2].y, vals[3].x, vals[3].y);
@@ -150,6 +152,42 @@ __global__ void w4_dequant_kernel(const uint8_t *__restrict__ w, const __half *_
     o[1] = make_float4(vals[4], vals[5], vals[6], vals[7]);
 }
 
+// Activations bf16 -> fp16 for the fp16 MMA path.  Every bf16 value of
+// magnitude in [2^-14, 65504] converts exactly (8 significant bits fit fp16's
+// 11); smaller values become fp16 subnormals (absolute error <= 2^-25); values
+// that would round to infinity set the range flag in the status word.  Lets the
+// dependent GEMM launch start (programmatic dependent launch) right away.
+__global__ void bf16_to_f16_kernel(const uint4 *__restrict__ in, uint4 *__restrict__ out, int64_t n8,
+                                   uint32_t *status) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    bool overflow = false;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint4 v = in[i];
+        const uint32_t src[4] = {v.x, v.y, v.z, v.w};
+        uint32_t dst[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float lo = __uint_as_float(src[e] << 16);
+            const float hi = __uint_as_float(src[e] & 0xFFFF0000u);
+            overflow |= !(fabsf(lo) < 65520.f) || !(fabsf(hi) < 65520.f);
+            dst[e] = as_u32(__floats2half2_rn(lo, hi));
+        }
+        out[i] = make_uint4(dst[0], dst[1], dst[2], dst[3]);
+    }
+    if (overflow) atomicOr(status, kStatusRangeBit);
+}
+
+int launch_bf16_to_f16(const void *x, void *out, int64_t n, cudaStream_t stream) {
+    uint32_t *status = status_word();
+    if (!status) return QWP_ERR_CUDA;
+    const int64_t n8 = n / 8;
+    const int64_t blocks = std::min<int64_t>((n8 + 255) / 256, 152 * 8);
+    bf16_to_f16_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, stream>>>(
+        static_cast<const uint4 *>(x), static_cast<uint4 *>(out), n8, status);
+    return launch_status();
+}
+
 static unsigned grid_for(int64_t threads, int block) {
     return static_cast<unsigned>((threads + block - 1) / block);
 }
@@ -167,6 +205,7 @@ extern "C" const char *qwp_status_string(int status) {
         case QWP_ERR_CUDA: return "QWP_ERR_CUDA";
         case QWP_ERR_DEVICE: return "QWP_ERR_DEVICE";
         case QWP_ERR_TIMEOUT: return "QWP_ERR_TIMEOUT";
+        case QWP_ERR_RANGE: return "QWP_ERR_RANGE";
         default: return "QWP_ERR_UNKNOWN";
     }
 }
@@ -253,5 +292,6 @@ extern "C" int qwp_device_status(void *stream) {
     uint32_t v = 0;
     if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return QWP_ERR_CUDA;
     if (v && cudaMemset(p, 0, sizeof(v)) != cudaSuccess) return QWP_ERR_CUDA;
-    return v ? QWP_ERR_TIMEOUT : QWP_OK;
+    if (v & kStatusTimeoutMask) return QWP_ERR_TIMEOUT;
+    return v ? QWP_ERR_RANGE : QWP_OK;
 }

@@ -10,8 +10,10 @@
 //   chunk plane c  (c = 0..3, 64 weights each) 32*R bytes at 16*R + 32*R*c,
 //                  laid out [h = 0..1][row i][16 bytes]: the 8 words v = 0..7 of
 //                  (row i, chunk c) sit at ((v/4)*R + i)*16 + 4*(v%4);
-//   word v         element 64c + 8v + u of the super-block (u = 0..7) in bits
-//                  4u..4u+3.
+//   word v         elements 64c + 8v + t (t = 0..7) of the super-block in the
+//                  interleaved nibble order of the W4A16 format: element t = 2p
+//                  in bits 4p..4p+3, element t = 2p+1 in bits 16+4p..19+4p, so
+//                  one AND-OR per pair p yields two K-adjacent fp16 lanes.
 // The repack is a byte permutation: 144 bytes per 256 weights, as in GGML.  A
 // warp of 32 consecutive rows reading one 16-byte quarter of its chunk reads
 // 512 contiguous bytes of shared memory (no bank conflicts), and the whole
@@ -62,108 +64,105 @@ __host__ __device__ __forceinline__ int w4_word_offset(int R, int i, int v) {
     return ((v >> 2) * R + i) * 16 + 4 * (v & 3);
 }
 
-// ---------------------------------------------------------------- Q4_K unpack
+// ---------------------------------------------------------------- nibble pairs
 
-// dl = d*sc_j and ml = dmin*m_j of one sub-block j (0..7), both exact in fp32.
-__device__ __forceinline__ void q4k_subblock_scale(uint4 h, int j, float &dl, float &ml) {
-    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x & 0xFFFFu)));
-    const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x >> 16)));
+// Pair p (p = 0..3) of an interleaved word as raw fp16x2 bits (1024+q_{2p},
+// 1024+q_{2p+1}): fp16 0x6400|n is exactly 1024 + n.
+__device__ __forceinline__ uint32_t nib_pair_magic(uint32_t word, int p) {
+    return ((word >> (4 * p)) & 0x000F000Fu) | 0x64006400u;
+}
+
+__device__ __forceinline__ __half2 as_half2(uint32_t bits) {
+    return *reinterpret_cast<const __half2 *>(&bits);
+}
+
+__device__ __forceinline__ uint32_t as_u32(__half2 h) {
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// ---------------------------------------------------------------- Q4_K scales
+
+// (1024 + sc_j, 1024 + m_j) of sub-block j (0..7) as raw fp16x2 bits, from the
+// GGML packing: values 0..3 are the low 6 bits of packed bytes 0..3 (scales) and
+// 4..7 (mins); values 4..7 take the low (scale) / high (min) nibble of bytes
+// 8..11 and, as bits 4-5, the top two bits of bytes 0..3 (scale) / 4..7 (min).
+__device__ __forceinline__ uint32_t q4k_scmin_magic(uint4 h, int j) {
     const int sh = 8 * (j & 3);
-    const uint32_t b_lo = (h.y >> sh) & 0xFFu;   // packed byte j%4
-    const uint32_t b_mid = (h.z >> sh) & 0xFFu;  // packed byte 4 + j%4
+    const uint32_t b_lo = h.y >> sh;   // packed byte j%4 in bits 0-7
+    const uint32_t b_mid = h.z >> sh;  // packed byte 4 + j%4
     uint32_t sc, m;
     if (j < 4) {
         sc = b_lo & 63u;
         m = b_mid & 63u;
     } else {
-        const uint32_t b_hi = (h.w >> sh) & 0xFFu;  // packed byte 8 + j%4
-        sc = (b_hi & 15u) | ((b_lo >> 6) << 4);
-        m = (b_hi >> 4) | ((b_mid >> 6) << 4);
+        const uint32_t b_hi = h.w >> sh;  // packed byte 8 + j%4
+        sc = (b_hi & 15u) | ((b_lo >> 2) & 0x30u);
+        m = ((b_hi >> 4) & 15u) | ((b_mid >> 2) & 0x30u);
     }
-    dl = d * static_cast<float>(sc);
-    ml = dmin * static_cast<float>(m);
+    return 0x64006400u | sc | (m << 16);
 }
 
-// Packed fp32x2 arithmetic (two independent lanes per instruction, sm_100+).
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
+// Exact (sc_j, m_j) as fp16x2.
+__device__ __forceinline__ __half2 q4k_scmin(uint4 h, int j) {
+    return __hsub2(as_half2(q4k_scmin_magic(h, j)), as_half2(0x64006400u));
 }
 
-__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
+// dl = d*sc_j and ml = dmin*m_j of one sub-block, both exact in fp32.
+__device__ __forceinline__ void q4k_subblock_scale(uint4 h, int j, float &dl, float &ml) {
+    const float2 scm = __half22float2(q4k_scmin(h, j));
+    dl = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x & 0xFFFFu))) * scm.x;
+    ml = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x >> 16))) * scm.y;
 }
 
-// Per-sub-block constants of the word unpack below.  A nibble q at bits
-// 4u..4u+3 of a word, OR-ed into the fp32 pattern 0x4B000000, reads as
-// v = 2^23 + q*16^u exactly.  With s = dl*16^-u (exact: a power-of-two scale)
-// fma(v, s, -2^23*s) = q*dl exactly (q*dl has at most 21 significant bits),
-// and adding -ml rounds once: the result is the correctly rounded fp32 of
-// d*sc*q - dmin*m.
-struct Q4kSub {
-    float2 s01, s23;  // multipliers of nibbles (0,1) and (2,3) of a half-word
-    float2 c01, c23;  // -2^23 * s
-    float2 nml;       // (-ml, -ml)
+// ---------------------------------------------------------------- Q4_K unpack
+
+// The 8 weights of one interleaved word as exact fp32 (the dequant entry point):
+// q exactly from the magic pair, then fmaf(dl, q, -ml) rounds the exact
+// d*sc*q - dmin*m once.  w[i] holds the K-adjacent elements 2i, 2i+1.
+__device__ __forceinline__ void q4k_word_f32(uint32_t word, float dl, float ml, float2 (&w)[4]) {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const float2 q = __half22float2(__hsub2(as_half2(nib_pair_magic(word, p)), as_half2(0x64006400u)));
+        w[p] = make_float2(fmaf(dl, q.x, -ml), fmaf(dl, q.y, -ml));
+    }
+}
+
+// Per-sub-block fp16 constants of the GEMM's unpack.
+struct Q4kSubH {
+    __half2 sc2;   // (sc, sc)
+    __half2 csc2;  // (-1024*sc, -1024*sc), exact
+    __half2 d2;    // (d, d)
+    __half2 nml2;  // (-RN(dmin*m), -RN(dmin*m))
 };
 
-__device__ __forceinline__ Q4kSub q4k_sub_consts(float dl, float ml) {
-    Q4kSub k;
-    k.s01 = make_float2(dl, dl * 0.0625f);
-    k.s23 = make_float2(dl * 0.00390625f, dl * 0.000244140625f);
-    k.c01 = make_float2(-8388608.0f * k.s01.x, -8388608.0f * k.s01.y);
-    k.c23 = make_float2(-8388608.0f * k.s23.x, -8388608.0f * k.s23.y);
-    k.nml = make_float2(-ml, -ml);
+__device__ __forceinline__ Q4kSubH q4k_sub_f16(uint4 h, int j) {
+    Q4kSubH k;
+    const __half2 scm = q4k_scmin(h, j);
+    k.sc2 = __low2half2(scm);
+    k.csc2 = __hmul2(k.sc2, as_half2(0xE400E400u));  // x (-1024)
+    k.d2 = as_half2(__byte_perm(h.x, 0u, 0x1010));
+    const __half2 ndmin2 = as_half2(__byte_perm(h.x, 0u, 0x3232) ^ 0x80008000u);
+    k.nml2 = __hmul2(__high2half2(scm), ndmin2);
     return k;
 }
 
-// The 8 weights of one word (element u in bits 4u..4u+3) as fp32, each the
-// correctly rounded d*sc*q - dmin*m; returned as K-adjacent pairs.
-__device__ __forceinline__ void q4k_word_f32(uint32_t word, const Q4kSub &k, float2 (&w)[4]) {
-    const uint32_t hi = word >> 16;
-    const float2 v01 = make_float2(__uint_as_float((word & 0x000Fu) | 0x4B000000u),
-                                   __uint_as_float((word & 0x00F0u) | 0x4B000000u));
-    const float2 v23 = make_float2(__uint_as_float((word & 0x0F00u) | 0x4B000000u),
-                                   __uint_as_float((word & 0xF000u) | 0x4B000000u));
-    const float2 v45 = make_float2(__uint_as_float((hi & 0x000Fu) | 0x4B000000u),
-                                   __uint_as_float((hi & 0x00F0u) | 0x4B000000u));
-    const float2 v67 = make_float2(__uint_as_float((hi & 0x0F00u) | 0x4B000000u),
-                                   __uint_as_float((hi & 0xF000u) | 0x4B000000u));
-    w[0] = fadd2(ffma2(v01, k.s01, k.c01), k.nml);
-    w[1] = fadd2(ffma2(v23, k.s23, k.c23), k.nml);
-    w[2] = fadd2(ffma2(v45, k.s01, k.c01), k.nml);
-    w[3] = fadd2(ffma2(v67, k.s23, k.c23), k.nml);
-}
-
-// The same 8 weights rounded once more to bf16, packed K-adjacent in pairs
-// (lower K in the low half).
-__device__ __forceinline__ void q4k_word_bf16x2(uint32_t word, const Q4kSub &k, uint32_t (&p)[4]) {
-    float2 w[4];
-    q4k_word_f32(word, k, w);
+// The 8 weights of one word as fp16x2 MMA operands.  (1024+q)*sc - 1024*sc is
+// q*sc exactly (at most 945, inside fp16's 11-bit integer range; the fma does not
+// round its product), and d*(q*sc) - RN(dmin*m) is rounded once to fp16.
+__device__ __forceinline__ void q4k_word_f16x2(uint32_t word, const Q4kSubH &k, uint32_t (&p)[4]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        __nv_bfloat162 v = __floats2bfloat162_rn(w[i].x, w[i].y);
-        p[i] = *reinterpret_cast<uint32_t *>(&v);
+        const __half2 qsc = __hfma2(as_half2(nib_pair_magic(word, i)), k.sc2, k.csc2);
+        p[i] = as_u32(__hfma2(qsc, k.d2, k.nml2));
     }
 }
 
 // ---------------------------------------------------------------- W4A16 unpack
 
 // Pair p (p = 0..3) of an interleaved word as fp16x2 (q_{2p} - zp, q_{2p+1} - zp),
-// exact: 0x6400|n is 1024 + n, and (1024 + n) - (1024 + zp) has no rounding.
+// exact: (1024 + n) - (1024 + zp) has no rounding.
 __device__ __forceinline__ __half2 w4_pair_minus_zero(uint32_t word, int p, __half2 magic_zp) {
-    const uint32_t bits = ((word >> (4 * p)) & 0x000F000Fu) | 0x64006400u;
-    return __hsub2(*reinterpret_cast<const __half2 *>(&bits), magic_zp);
+    return __hsub2(as_half2(nib_pair_magic(word, p)), magic_zp);
 }
 
 // 1024 + zp in both halves.

@@ -48,7 +48,7 @@ constexpr int XFORM_GROUPS = 2;                    // groups take alternate K bl
 constexpr int NUM_XFORM_WARPS = 8 * XFORM_GROUPS;  // 8 warps cover one K block (4 lane quarters x 2 halves)
 constexpr int FIRST_XFORM_WARP = 3;
 constexpr int NUM_THREADS = 32 * (FIRST_XFORM_WARP + NUM_XFORM_WARPS);
-constexpr int X_MAX_STAGES = 12;
+constexpr int X_MAX_STAGES = 8;  // <= A_STAGES: the x ring reuses the mma_done ring (see below)
 constexpr int W_MAX_STAGES = 8;
 constexpr int A_STAGES = 8;
 constexpr int BN_MAX = 256;
@@ -66,6 +66,7 @@ constexpr int NUM_BARS = 2 * X_MAX_STAGES + 2 * W_MAX_STAGES + 2 * A_STAGES + 2;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(X_MAX_STAGES <= A_STAGES, "the x ring is released through the mma_done ring");
 static_assert(512 * BN_MAX <= RING_BYTES, "split-K partials must fit the ring region");
 
 struct GemmArgs {
@@ -79,6 +80,9 @@ struct GemmArgs {
     int kb_per_split;       // 64-wide K blocks per CTA along K (multiple of 4)
     int splits;             // CTAs along K = cluster size (1 = no reduction)
     int x_stages, w_stages;
+    int groups_per_row;     // W4A16: K / group
+    int kb_per_group;       // W4A16: group / 64
+    int kbg_shift;          // log2(kb_per_group) when it is a power of two, else -1
     int x_stage_bytes, w_stage_bytes;
     uint64_t timeout_ns;
 };
@@ -108,7 +112,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
         if (mbar_try_wait(bar, parity)) return true;
         if (honour_abort && *reinterpret_cast<volatile uint32_t *>(ctl.abort)) return false;
         if ((it & 63u) == 0) {
-            if (honour_abort && *reinterpret_cast<volatile uint32_t *>(ctl.status)) {
+            if (honour_abort && (*reinterpret_cast<volatile uint32_t *>(ctl.status) & kStatusTimeoutMask)) {
                 *reinterpret_cast<volatile uint32_t *>(ctl.abort) = 1u;  // another CTA failed
                 return false;
             }
@@ -126,17 +130,16 @@ __device__ __forceinline__ bool aborted(const Ctl &ctl) {
 }
 
 // Unpack one row's half of a 64-wide K block (4 words = 32 weights) into 16
-// packed 16-bit pairs for the A operand.
+// packed fp16 pairs for the A operand.
 template <bool kQ4K>
-__device__ __forceinline__ void unpack_quarter(uint4 wv, float dl, float ml, __half2 mz, __half2 s2,
+__device__ __forceinline__ void unpack_quarter(uint4 wv, const Q4kSubH &ks, __half2 mz, __half2 s2,
                                                uint32_t (&regs)[16]) {
     const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-    const Q4kSub ks = q4k_sub_consts(dl, ml);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         uint32_t p[4];
         if (kQ4K)
-            q4k_word_bf16x2(w[i], ks, p);
+            q4k_word_f16x2(w[i], ks, p);
         else
             w4_word_f16x2(w[i], mz, s2, p);
 #pragma unroll
@@ -166,31 +169,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t *const w_ring = smem + XS * args.x_stage_bytes;
 
     const uint32_t bar0 = smem_u32(smem + OFF_BAR);
-    const uint32_t x_full = bar0, x_empty = x_full + 8 * X_MAX_STAGES;
-    const uint32_t w_full = x_empty + 8 * X_MAX_STAGES, w_empty = w_full + 8 * W_MAX_STAGES;
-    const uint32_t a_full = w_empty + 8 * W_MAX_STAGES, a_empty = a_full + 8 * A_STAGES;
-    const uint32_t acc_full = a_empty + 8 * A_STAGES, drain = acc_full + 8;
+    // mma_done[j % A_STAGES] completes when the MMAs of K block j (and all before it)
+    // are done: one tcgen05.commit per block releases both the block's A slot and its
+    // x slot (the x ring is at most A_STAGES deep, so no phase of it is skipped).
+    const uint32_t x_full = bar0, mma_done = x_full + 8 * X_MAX_STAGES;
+    const uint32_t w_full = mma_done + 8 * X_MAX_STAGES, w_empty = w_full + 8 * W_MAX_STAGES;
+    const uint32_t a_full = w_empty + 8 * W_MAX_STAGES, unused = a_full + 8 * A_STAGES;
+    const uint32_t acc_full = unused + 8 * A_STAGES, drain = acc_full + 8;
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + OFF_MISC);  // [0] tmem base, [1] abort
     const Ctl ctl{misc + 1, args.status, args.timeout_ns};
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < X_MAX_STAGES; ++s) {
-            mbar_init(x_full + 8 * s, 1);
-            mbar_init(x_empty + 8 * s, 1);
-        }
+        for (int s = 0; s < X_MAX_STAGES; ++s) mbar_init(x_full + 8 * s, 1);
+        for (int s = 0; s < A_STAGES; ++s) mbar_init(mma_done + 8 * s, 1);
         for (int s = 0; s < W_MAX_STAGES; ++s) {
             mbar_init(w_full + 8 * s, 1);
             mbar_init(w_empty + 8 * s, NUM_XFORM_WARPS);
         }
         for (int s = 0; s < A_STAGES; ++s) {
             mbar_init(a_full + 8 * s, NUM_XFORM_WARPS / XFORM_GROUPS);
-            mbar_init(a_empty + 8 * s, 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(drain, 1);
         // A failure recorded earlier (and not yet read by qwp_device_status) makes
         // every later launch skip its work instead of waiting out its own timeouts.
-        misc[1] = *reinterpret_cast<volatile uint32_t *>(args.status) ? 1u : 0u;
+        misc[1] = (*reinterpret_cast<volatile uint32_t *>(args.status) & kStatusTimeoutMask) ? 1u : 0u;
         fence_mbar_init();
         prefetch_tensormap(&tmap_x);
     }
@@ -207,14 +210,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ x producer
         if (lane == 0 && !skip) {
+            // x may be written by the grid launched just before this one (the
+            // activation conversion); nothing else here depends on it.
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             int issued = 0;
+            int xs = 0;         // ring slot (running counters: no division in the loop)
+            int dk = 0;         // mma_done slot of block j - XS, and its phase
+            uint32_t dph = 0;
             for (int j = 0; j < nkb; ++j) {
-                const int xs = j % XS;
-                if (!wait_bar(x_empty + 8 * xs, ((j / XS) & 1) ^ 1, ctl, WAIT_X_EMPTY)) break;
+                if (j >= XS) {  // slot xs last held block j - XS
+                    if (!wait_bar(mma_done + 8 * dk, dph, ctl, WAIT_X_EMPTY)) break;
+                    if (++dk == A_STAGES) { dk = 0; dph ^= 1; }
+                }
                 mbar_arrive_expect_tx(x_full + 8 * xs, static_cast<uint32_t>(args.bn) * 128u);
                 tma_load_2d(smem_u32(x_ring + xs * args.x_stage_bytes), &tmap_x,
                             (kb_begin + j) * CHUNK_K, m0, x_full + 8 * xs);
                 issued = j + 1;
+                if (++xs == XS) xs = 0;
             }
             // Every copy issued above lands before the CTA may exit.
             for (int j = max(0, issued - XS); j < issued; ++j)
@@ -224,9 +236,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------------------ weight producer
         if (lane == 0 && !skip) {
             int issued = 0;
+            int ws = 0;
+            uint32_t wph = 0;
             for (int s = 0; s < nstage; ++s) {
-                const int ws = s % WS;
-                if (!wait_bar(w_empty + 8 * ws, ((s / WS) & 1) ^ 1, ctl, WAIT_W_EMPTY)) break;
+                if (s > 0 && ++ws == WS) { ws = 0; wph ^= 1; }
+                if (!wait_bar(w_empty + 8 * ws, wph ^ 1, ctl, WAIT_W_EMPTY)) break;
                 const int kb0 = kb_begin + KB_PER_STAGE * s;
                 const int nblk = min(KB_PER_STAGE, kb_end - kb0);
                 const uint8_t *src;
@@ -248,11 +262,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && !skip) {
-            const uint32_t idesc = make_idesc_f16(kQ4K, TILE_ROWS, static_cast<uint32_t>(args.bn));
+            const uint32_t idesc = make_idesc_f16(false, TILE_ROWS, static_cast<uint32_t>(args.bn));  // fp16 A and B
             bool ok = true;
-            for (int j = 0; j < nkb; ++j) {
-                const int xs = j % XS, as = j % A_STAGES;
-                ok = wait_bar(x_full + 8 * xs, (j / XS) & 1, ctl, WAIT_X_FULL) &&
+            int xs = 0;
+            uint32_t xph = 0;
+            for (int j = 0; j < nkb; ++j, xs = (xs + 1 == XS) ? 0 : xs + 1, xph ^= (xs == 0)) {
+                const int as = j % A_STAGES;
+                ok = wait_bar(x_full + 8 * xs, xph, ctl, WAIT_X_FULL) &&
                      wait_bar(a_full + 8 * as, (j / A_STAGES) & 1, ctl, WAIT_A_FULL);
                 if (!ok) break;
                 tc_fence_after();
@@ -261,8 +277,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int kk = 0; kk < CHUNK_K / 16; ++kk)
                     mma_ts(tmem + ACC_COL, tmem + A_COL + 32u * as + 8u * kk, bdesc + 2u * kk, idesc,
                            (j | kk) != 0);
-                mma_commit(x_empty + 8 * xs);
-                mma_commit(a_empty + 8 * as);
+                mma_commit(mma_done + 8 * as);
             }
             if (ok) {
                 mma_commit(acc_full);
@@ -283,33 +298,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t lane_base = (quarter * 32u) << 16;
         bool ok = !skip;
         uint4 hdr = make_uint4(0, 0, 0, 0);  // Q4_K header of the current weight stage
+        int cur_s = 0, ws = 0;               // weight stage this warp is in, and its ring slot
+        uint32_t wph = 0;                    // phase of that slot
 
         // Unpack K block j of this thread's row into `regs`; waits for its weight
         // stage when j opens one and releases the stage after its last block.
         auto prepare = [&](int j, uint32_t (&regs)[16]) -> bool {
             const int s = j / KB_PER_STAGE, c = j % KB_PER_STAGE;
-            const int ws = s % WS;
+            while (cur_s < s) {  // at most one step: blocks advance by XFORM_GROUPS < KB_PER_STAGE
+                if (++ws == WS) { ws = 0; wph ^= 1; }
+                ++cur_s;
+            }
             const uint8_t *wst = w_ring + ws * args.w_stage_bytes;
             const int kb0 = kb_begin + KB_PER_STAGE * s;
             const int nblk = min(KB_PER_STAGE, kb_end - kb0);
             if (c == grp) {  // this warp's first block of the stage
                 // Every lane waits; the warp moves on together (tcgen05.st/ld are warp-collective).
-                if (!__all_sync(0xffffffffu, wait_bar(w_full + 8 * ws, (s / WS) & 1, ctl, WAIT_W_FULL)))
+                if (!__all_sync(0xffffffffu, wait_bar(w_full + 8 * ws, wph, ctl, WAIT_W_FULL)))
                     return false;
                 if (kQ4K && valid) hdr = *reinterpret_cast<const uint4 *>(wst + Q4K_HEADER_BYTES * r);
             }
             uint4 wv = make_uint4(0, 0, 0, 0);
-            float dl = 0.f, ml = 0.f;
+            Q4kSubH ks;
             __half2 s2 = __float2half2_rn(0.f), mz = w4_magic_zero(0);
             if (kQ4K) {
                 if (valid)
                     wv = *reinterpret_cast<const uint4 *>(wst + Q4K_HEADER_BYTES * R + CHUNK_ROW_BYTES * R * c +
                                                           (half * R + r) * 16);
-                q4k_subblock_scale(hdr, 2 * c + half, dl, ml);
+                ks = q4k_sub_f16(hdr, 2 * c + half);
             } else if (valid) {
                 wv = *reinterpret_cast<const uint4 *>(wst + CHUNK_ROW_BYTES * R * c + (half * R + r) * 16);
-                const int64_t ng = args.K / args.group;
-                const int64_t g = (static_cast<int64_t>(kb0 + c) * CHUNK_K) / args.group;
+                const int64_t ng = args.groups_per_row;
+                const int kbi = kb0 + c;
+                const int64_t g = args.kbg_shift >= 0 ? (kbi >> args.kbg_shift) : (kbi / args.kb_per_group);
                 s2 = __half2half2(args.scales[n * ng + g]);
                 mz = w4_magic_zero(args.zeros[n * ng + g]);
             }
@@ -319,13 +340,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(w_empty + 8 * ws);
             }
-            unpack_quarter<kQ4K>(wv, dl, ml, mz, s2, regs);
+            unpack_quarter<kQ4K>(wv, ks, mz, s2, regs);
             return true;
         };
         // Store block j into its A ring slot once the MMA has released the slot.
         auto issue = [&](int j, const uint32_t (&regs)[16]) -> bool {
             const int as = j % A_STAGES;
-            if (!__all_sync(0xffffffffu, wait_bar(a_empty + 8 * as, ((j / A_STAGES) & 1) ^ 1, ctl, WAIT_A_EMPTY)))
+            if (!__all_sync(0xffffffffu, wait_bar(mma_done + 8 * as, ((j / A_STAGES) & 1) ^ 1, ctl, WAIT_A_EMPTY)))
                 return false;
             tc_fence_after();
             tmem_st_x16(tmem + lane_base + A_COL + 32u * as + 16u * half, regs);
@@ -441,14 +462,14 @@ static EncodeTiledFn encode_fn() {
 }
 
 // x [M][K] 16-bit, box = 64 (K) x bn (rows), 128-byte swizzle, zero fill out of bounds.
-static int encode_x_map(CUtensorMap *map, const void *x, bool bf16, int64_t M, int64_t K, int bn) {
+static int encode_x_map(CUtensorMap *map, const void *x, int64_t M, int64_t K, int bn) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return QWP_ERR_CUDA;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(CHUNK_K), static_cast<cuuint32_t>(bn)};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                     const_cast<void *>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -526,10 +547,13 @@ static int choose_splits(const int *slots, int64_t base_ctas, int nstages) {
     return best;
 }
 
+// x is fp16 [M, K].  `after_prior` launches with programmatic stream
+// serialization so the kernel's set-up and weight prefetch overlap the grid just
+// before it (the x producer waits for that grid with griddepcontrol.wait).
 template <bool kQ4K>
 static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, const void *x,
                        float *y, int64_t M, int64_t N, int64_t K, int64_t group, cudaStream_t stream,
-                       uint64_t timeout_ns) {
+                       uint64_t timeout_ns, bool after_prior) {
     int rc = check_device();
     if (rc) return rc;
     DeviceInfo *info = nullptr;
@@ -538,7 +562,7 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     if (!status) return QWP_ERR_CUDA;
     const int bn = choose_bn(M);
     CUtensorMap map;
-    if ((rc = encode_x_map(&map, x, kQ4K, M, K, bn))) return rc;
+    if ((rc = encode_x_map(&map, x, M, K, bn))) return rc;
 
     GemmArgs a;
     a.w = static_cast<const uint8_t *>(w);
@@ -550,6 +574,11 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
     a.group = static_cast<int>(group);
+    a.groups_per_row = group > 0 ? static_cast<int>(K / group) : 0;
+    a.kb_per_group = group > 0 ? static_cast<int>(group / CHUNK_K) : 1;
+    a.kbg_shift = -1;
+    for (int sh = 0; sh < 31; ++sh)
+        if ((1 << sh) == a.kb_per_group) a.kbg_shift = sh;
     a.bn = bn;
     a.timeout_ns = timeout_ns;
     a.x_stage_bytes = bn * 128;
@@ -573,13 +602,22 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 1;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = S;
-    cfg.attrs = &attr;
-    cfg.numAttrs = S > 1 ? 1 : 0;
+    cudaLaunchAttribute attrs[2];
+    unsigned nattr = 0;
+    if (S > 1) {
+        attrs[nattr].id = cudaLaunchAttributeClusterDimension;
+        attrs[nattr].val.clusterDim.x = 1;
+        attrs[nattr].val.clusterDim.y = 1;
+        attrs[nattr].val.clusterDim.z = S;
+        ++nattr;
+    }
+    if (after_prior) {
+        attrs[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[nattr].val.programmaticStreamSerializationAllowed = 1;
+        ++nattr;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = nattr;
     if (cudaLaunchKernelEx(&cfg, qwp_gemm_kernel<kQ4K>, map, a) != cudaSuccess) {
         cudaGetLastError();
         return QWP_ERR_CUDA;
@@ -601,13 +639,56 @@ static int gemm_shape_checks(const void *w, const void *x, const float *y, int64
     return QWP_OK;
 }
 
+// Scratch for fp16 activations: a library-owned stream-ordered memory pool per
+// device (allocations are freed, in stream order, right after the GEMM).
+static int scratch_pool(cudaMemPool_t *out) {
+    static cudaMemPool_t pools[64];
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QWP_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!pools[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t p;
+        if (cudaMemPoolCreate(&p, &props) != cudaSuccess) return QWP_ERR_CUDA;
+        uint64_t keep = UINT64_MAX;  // keep freed blocks for reuse
+        cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
+        pools[dev] = p;
+    }
+    *out = pools[dev];
+    return QWP_OK;
+}
+
+extern "C" int q4k_gemm_f16(const void *w_tiled, const void *x, float *y, int64_t M, int64_t N,
+                            int64_t K, void *stream) {
+    if (K % Q4K_BLOCK || K == 0) return K < 0 ? QWP_ERR_INVALID_ARG : QWP_ERR_UNSUPPORTED_SHAPE;
+    int rc = gemm_shape_checks(w_tiled, x, y, M, N, K);
+    if (rc || M == 0 || N == 0) return rc;
+    return launch_gemm<true>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0,
+                             static_cast<cudaStream_t>(stream), kDefaultTimeoutNs, false);
+}
+
 extern "C" int q4k_gemm(const void *w_tiled, const void *x, float *y, int64_t M, int64_t N,
                         int64_t K, void *stream) {
     if (K % Q4K_BLOCK || K == 0) return K < 0 ? QWP_ERR_INVALID_ARG : QWP_ERR_UNSUPPORTED_SHAPE;
     int rc = gemm_shape_checks(w_tiled, x, y, M, N, K);
     if (rc || M == 0 || N == 0) return rc;
-    return launch_gemm<true>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0,
-                             static_cast<cudaStream_t>(stream), kDefaultTimeoutNs);
+    if ((rc = check_device())) return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaMemPool_t pool;
+    if ((rc = scratch_pool(&pool))) return rc;
+    void *x16 = nullptr;
+    if (cudaMallocFromPoolAsync(&x16, static_cast<size_t>(M) * K * 2, pool, s) != cudaSuccess) {
+        cudaGetLastError();
+        return QWP_ERR_CUDA;
+    }
+    rc = launch_bf16_to_f16(x, x16, M * K, s);
+    if (!rc) rc = launch_gemm<true>(w_tiled, nullptr, nullptr, x16, y, M, N, K, 0, s, kDefaultTimeoutNs, true);
+    if (cudaFreeAsync(x16, s) != cudaSuccess && !rc) rc = QWP_ERR_CUDA;
+    return rc;
 }
 
 extern "C" int w4a16_gemm(const void *wq_tiled, const void *scales, const uint8_t *zeros,
@@ -619,5 +700,5 @@ extern "C" int w4a16_gemm(const void *wq_tiled, const void *scales, const uint8_
     if (rc || M == 0 || N == 0) return rc;
     if (!scales || !zeros) return QWP_ERR_INVALID_ARG;
     return launch_gemm<false>(wq_tiled, scales, zeros, x, y, M, N, K, group,
-                              static_cast<cudaStream_t>(stream), kDefaultTimeoutNs);
+                              static_cast<cudaStream_t>(stream), kDefaultTimeoutNs, false);
 }

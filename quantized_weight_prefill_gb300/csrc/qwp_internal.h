@@ -21,6 +21,15 @@ inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? QWP_OK : QWP_ERR_CUDA;
 }
 
+// Status word bits: a timeout records 0x100 | (which wait) in the low 16 bits;
+// an activation outside the fp16 range sets kStatusRangeBit.
+constexpr uint32_t kStatusTimeoutMask = 0xFFFFu;
+constexpr uint32_t kStatusRangeBit = 0x10000u;
+
+// Converts n bf16 values (n % 8 == 0, both pointers 16-byte aligned) to fp16 on
+// `stream`; the launch allows a programmatic dependent launch to follow.
+int launch_bf16_to_f16(const void *x, void *out, int64_t n, cudaStream_t stream);
+
 // Default bound on any single mbarrier wait inside a kernel.
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 

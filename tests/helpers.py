@@ -16,7 +16,7 @@ TOL_ABS = 1e-5
 def q4k_tiled_reference(blocks: np.ndarray, N: int, K: int) -> np.ndarray:
     """Tile-major Q4_K order: per 128-row tile and super-block, a 16-byte header plane
     and four nibble planes [h][row][16 bytes]; word v of a row's 64-wide chunk holds
-    chunk elements 8v..8v+7 in bits 4u..4u+3."""
+    chunk elements 8v+t, element t=2p in bits 4p..4p+3 and t=2p+1 in bits 16+4p..19+4p."""
     nb = K // 256
     raw = blocks.reshape(N, nb, 144)
     out = np.zeros(N * nb * 144, np.uint8)
@@ -32,8 +32,9 @@ def q4k_tiled_reference(blocks: np.ndarray, N: int, K: int) -> np.ndarray:
                 hi = qs[:, 32 * c:32 * c + 32] >> 4                     # elements 32..63
                 elems = np.concatenate([lo, hi], axis=1)                # [R, 64]
                 words = np.zeros((R, 8), np.uint32)
-                for u in range(8):
-                    words |= elems[:, u::8] << (4 * u)
+                for t in range(8):
+                    shift = 16 + 4 * (t // 2) if t % 2 else 4 * (t // 2)
+                    words |= elems[:, t::8] << shift
                 plane = words.reshape(R, 2, 4).transpose(1, 0, 2)        # [h][row][4 words]
                 start = 16 * R + 32 * R * c
                 grp[start:start + 32 * R] = plane.astype("<u4").reshape(-1).view(np.uint8)

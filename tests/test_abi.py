@@ -44,7 +44,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_status_strings(lib):
     for code, name in [(0, "QWP_OK"), (-1, "QWP_ERR_INVALID_ARG"), (-2, "QWP_ERR_UNSUPPORTED_SHAPE"),
                        (-3, "QWP_ERR_MISALIGNED"), (-4, "QWP_ERR_CUDA"), (-5, "QWP_ERR_DEVICE"),
-                       (-6, "QWP_ERR_TIMEOUT")]:
+                       (-6, "QWP_ERR_TIMEOUT"), (-7, "QWP_ERR_RANGE")]:
         assert lib.qwp_status_string(code).decode() == name
 
 
@@ -79,6 +79,8 @@ def test_gemm_argument_checks_before_any_cuda_call(lib):
     # empty problems are no-ops
     assert lib.q4k_gemm(None, None, None, 0, 8, 256, None) == OK
     assert lib.q4k_gemm(None, None, None, 8, 0, 256, None) == OK
+    assert lib.q4k_gemm_f16(a16, a16, a16, 8, 8, 100, None) == SHAPE
+    assert lib.q4k_gemm_f16(a16, _p(0x1008), a16, 8, 8, 256, None) == MISALIGNED
     # repack / dequant checks
     assert lib.q4k_repack(a16, a16, 4, 256, None) == INVALID          # aliasing
     assert lib.q4k_repack(a16, _p(0x2008), 4, 256, None) == MISALIGNED

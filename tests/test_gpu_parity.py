@@ -107,6 +107,32 @@ def test_q4k_gemm_tiny(M, N, K):
     check_bound(y, ref, mag, f"q4k M{M} N{N} K{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 1, 256), (33, 130, 768), (105, 256, 1024), (300, 136, 256)])
+def test_q4k_gemm_f16_activations(M, N, K):
+    """The fp16-activation entry point (no conversion pass) against the oracle."""
+    blocks, w = _q4k_on_gpu(N, K, seed=M * 5 + N)
+    xh = synth.activations_f16(M, K, seed=M + 3)
+    y = qwp.q4k_gemm_f16(w, torch.from_numpy(xh).to(DEV), N).cpu().numpy()
+    wf = oracle.q4k_dequant(blocks, N, K)
+    ref, mag = oracle.gemm(oracle.half_to_f64(xh.view(np.uint16)), wf)
+    check_bound(y, ref, mag, f"q4k f16 M{M} N{N} K{K}")
+
+
+def test_q4k_bf16_activation_beyond_fp16_range_is_reported():
+    """An activation that overflows fp16 is reported as QWP_ERR_RANGE, and the next call is clean."""
+    N, K, M = 128, 256, 8
+    blocks, w = _q4k_on_gpu(N, K, seed=31)
+    xb = synth.activations_bf16(M, K, seed=32).copy()
+    xb[3, 17] = 0x4880  # bf16 262144.0, beyond fp16's largest finite value
+    qwp.q4k_gemm(w, _bf16_on_gpu(xb), N)
+    assert qwp.device_status() == -7
+    xb[3, 17] = 0x3F80  # 1.0
+    y = qwp.q4k_gemm(w, _bf16_on_gpu(xb), N).cpu().numpy()
+    assert qwp.device_status() == 0
+    ref, mag = oracle.q4k_gemm(blocks, xb, N, K)
+    check_bound(y, ref, mag, "after a range error")
+
+
 @pytest.mark.parametrize("M,N,K,g", [(1, 1, 64, 64), (7, 5, 256, 128), (33, 130, 768, 64),
                                      (105, 256, 1024, 128), (300, 136, 512, 256), (257, 200, 320, 64)])
 def test_w4a16_gemm_tiny(M, N, K, g):
