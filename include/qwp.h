@@ -4,9 +4,11 @@
  * C ABI.  Every pointer argument named *_dev is a device pointer; every call
  * is asynchronous and ordered on `stream` (a cudaStream_t passed as void*,
  * NULL = the legacy default stream) and never synchronizes the host, except
- * qwp_device_status.  The caller owns and allocates every buffer; no entry
- * point allocates device memory.  Every entry point returns QWP_OK (0) or a
- * negative qwp_status; none throws.  Calls are thread-safe.
+ * qwp_device_status.  The caller owns and allocates every input and output
+ * buffer; the only entry point that takes device memory of its own is
+ * q4k_gemm (activation scratch from a library-owned stream-ordered pool).
+ * Every entry point returns QWP_OK (0) or a negative qwp_status; none throws.
+ * Calls are thread-safe.
  *
  * The method (web pages, by title and section):
  *  - "The dequant scratch round-trip is ZINC's last RDNA4 prefill tax",
