@@ -50,7 +50,8 @@ typedef enum {
     QWP_ERR_CUDA = -4,             /* a CUDA runtime/driver call or a launch failed      */
     QWP_ERR_DEVICE = -5,           /* the current device is not an sm_103 GPU            */
     QWP_ERR_TIMEOUT = -6,          /* a kernel's bounded wait expired (qwp_device_status) */
-    QWP_ERR_RANGE = -7             /* an activation overflowed fp16 (qwp_device_status)   */
+    QWP_ERR_RANGE = -7,            /* an activation overflowed fp16 (qwp_device_status)   */
+    QWP_ERR_SCRATCH_LIMIT = -8     /* M*K beyond QWP_NOALLOC_MAX_X_ELEMS (q4k_gemm_noalloc) */
 } qwp_status;
 
 /* Human-readable name of a status code (static string). */
@@ -107,6 +108,34 @@ QWP_API int q4k_gemm_f16(const void *w_tiled_dev, const void *x_dev, float *y_de
  */
 QWP_API int q4k_gemm(const void *w_tiled_dev, const void *x_dev, float *y_dev,
                      int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * The largest activation q4k_gemm_noalloc accepts: M*K <= 8,388,608 values
+ * (for example M <= 2048 at K = 4096, M <= 682 at K = 12288).
+ */
+#define QWP_NOALLOC_MAX_X_ELEMS 8388608
+
+/*
+ * q4k_gemm without any device allocation, for callers that must not allocate:
+ * engines that reserve all device memory up front and forbid allocation once
+ * they serve, callers whose allocator owns the memory the CUDA pools would
+ * draw from, and latency-bound loops in which an allocation's cost or its
+ * possible failure is not acceptable.  Same arguments, rules and result as
+ * q4k_gemm (the same kernels run); the fp16 copy of x goes into a fixed array
+ * of QWP_NOALLOC_MAX_X_ELEMS fp16 values (16 MiB) that is part of the library
+ * and that every GPU loading the library's device code holds until the process
+ * exits.  M*K beyond that size returns QWP_ERR_SCRATCH_LIMIT before any work.
+ * The first call on each device looks up the array's address on that device
+ * (and loads the library's device code there if it is not loaded yet); make
+ * that first call before any stream capture begins.  Every call on a device
+ * shares the one array and leaves its x in it; each call writes all it reads
+ * first, so nothing needs clearing, but calls whose work overlaps on the GPU
+ * (different streams with no event or other ordering between them) race on
+ * the array and give wrong results.  The method's pages have no counterpart to
+ * this entry point: it exists only for callers that cannot allocate.
+ */
+QWP_API int q4k_gemm_noalloc(const void *w_tiled_dev, const void *x_dev, float *y_dev,
+                             int64_t M, int64_t N, int64_t K, void *stream);
 
 /*
  * W4A16 (group-wise asymmetric int4): wq[N][K/8] int32 words, each holding

@@ -18,6 +18,7 @@ from . import _build
 
 __all__ = [
     "QwpError", "library", "q4k_repacked_bytes", "q4k_repack", "q4k_dequant", "q4k_gemm", "q4k_gemm_f16",
+    "q4k_gemm_noalloc", "NOALLOC_MAX_X_ELEMS",
     "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "device_status",
     "EXPORTED_SYMBOLS",
 ]
@@ -25,8 +26,11 @@ __all__ = [
 # Every symbol include/qwp.h declares.
 EXPORTED_SYMBOLS = (
     "qwp_status_string", "q4k_repacked_bytes", "q4k_repack", "q4k_dequant", "q4k_gemm", "q4k_gemm_f16",
-    "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "qwp_device_status",
+    "q4k_gemm_noalloc", "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "qwp_device_status",
 )
+
+# Largest M*K that q4k_gemm_noalloc accepts (QWP_NOALLOC_MAX_X_ELEMS in the header).
+NOALLOC_MAX_X_ELEMS = 8388608
 
 _lib = None
 
@@ -56,6 +60,7 @@ def library() -> ctypes.CDLL:
         lib.q4k_dequant.argtypes = [p, p, i64, i64, p]
         lib.q4k_gemm.argtypes = [p, p, p, i64, i64, i64, p]
         lib.q4k_gemm_f16.argtypes = [p, p, p, i64, i64, i64, p]
+        lib.q4k_gemm_noalloc.argtypes = [p, p, p, i64, i64, i64, p]
         lib.w4a16_repack.argtypes = [p, p, i64, i64, p]
         lib.w4a16_dequant.argtypes = [p, p, p, p, i64, i64, i64, p]
         lib.w4a16_gemm.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p]
@@ -145,6 +150,20 @@ def q4k_gemm_f16(w_tiled: torch.Tensor, x: torch.Tensor, N: int, out: torch.Tens
         out = torch.empty(M, N, dtype=torch.float32, device=x.device)
     _dev(out, torch.float32, "out")
     _check(library().q4k_gemm_f16(_ptr(w_tiled), _ptr(x), _ptr(out), M, N, K, _stream(x)), "q4k_gemm_f16")
+    return out
+
+
+def q4k_gemm_noalloc(w_tiled: torch.Tensor, x: torch.Tensor, N: int, out: torch.Tensor) -> torch.Tensor:
+    """q4k_gemm into a caller-provided ``out`` [M, N] fp32; the library allocates nothing
+    (x's fp16 copy goes to a fixed array of NOALLOC_MAX_X_ELEMS values)."""
+    _dev(w_tiled, torch.uint8, "w_tiled")
+    _dev(x, torch.bfloat16, "x")
+    _dev(out, torch.float32, "out")
+    M, K = x.shape
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out must be [M, N]")
+    _check(library().q4k_gemm_noalloc(_ptr(w_tiled), _ptr(x), _ptr(out), M, N, K, _stream(x)),
+           "q4k_gemm_noalloc")
     return out
 
 

@@ -206,6 +206,7 @@ extern "C" const char *qwp_status_string(int status) {
         case QWP_ERR_DEVICE: return "QWP_ERR_DEVICE";
         case QWP_ERR_TIMEOUT: return "QWP_ERR_TIMEOUT";
         case QWP_ERR_RANGE: return "QWP_ERR_RANGE";
+        case QWP_ERR_SCRATCH_LIMIT: return "QWP_ERR_SCRATCH_LIMIT";
         default: return "QWP_ERR_UNKNOWN";
     }
 }

@@ -1,0 +1,64 @@
+// q4k_gemm_noalloc: the bf16-activation Q4_K GEMM for callers that may not
+// allocate device memory.  q4k_gemm converts x to fp16 into scratch taken from
+// a stream-ordered pool; here that scratch is a fixed array compiled into the
+// library instead, so a call allocates nothing.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/qwp.h"
+#include "qwp_internal.h"
+
+// The fp16 copy of x.  Every GPU on which this library's device code is loaded
+// holds these QWP_NOALLOC_MAX_X_ELEMS * 2 bytes until the process exits.  In
+// host code the name is only a handle for cudaGetSymbolAddress, never an address.
+static __device__ __align__(256) uint16_t g_x16_scratch[QWP_NOALLOC_MAX_X_ELEMS];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_x16_scratch on the current device, looked up once per
+// device (the lookup also loads this code onto the device if needed).
+int scratch_address(void **out) {
+    static void *addr[kMaxDevices];
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return QWP_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_x16_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return QWP_ERR_CUDA;
+        }
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return QWP_OK;
+}
+
+}  // namespace
+
+extern "C" int q4k_gemm_noalloc(const void *w_tiled, const void *x, float *y, int64_t M, int64_t N,
+                                int64_t K, void *stream) {
+    using namespace qwp;
+    if (K % 256 || K == 0) return K < 0 ? QWP_ERR_INVALID_ARG : QWP_ERR_UNSUPPORTED_SHAPE;
+    if (M < 0 || N < 0) return QWP_ERR_INVALID_ARG;
+    if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30)) return QWP_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || N == 0) return QWP_OK;
+    if (!w_tiled || !x || !y) return QWP_ERR_INVALID_ARG;
+    if (!aligned16(w_tiled) || !aligned16(x) || !aligned16(y)) return QWP_ERR_MISALIGNED;
+    if (M > static_cast<int64_t>(QWP_NOALLOC_MAX_X_ELEMS) / K) return QWP_ERR_SCRATCH_LIMIT;
+    int rc = check_device();
+    if (rc) return rc;
+    void *x16 = nullptr;
+    if ((rc = scratch_address(&x16))) return rc;
+    // The conversion writes all M*K elements the GEMM reads, so nothing left
+    // in the array by an earlier call is ever read.
+    if ((rc = launch_bf16_to_f16(x, x16, M * K, static_cast<cudaStream_t>(stream)))) return rc;
+    return q4k_gemm_f16(w_tiled, x16, y, M, N, K, stream);
+}
