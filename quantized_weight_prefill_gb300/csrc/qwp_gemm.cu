@@ -67,6 +67,7 @@ constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(X_MAX_STAGES <= A_STAGES, "the x ring is released through the mma_done ring");
+static_assert(A_STAGES % 4 == 0, "commit groups of up to 4 blocks tile the A ring");
 static_assert(512 * BN_MAX <= RING_BYTES, "split-K partials must fit the ring region");
 
 struct GemmArgs {
@@ -79,11 +80,12 @@ struct GemmArgs {
     int bn;                 // token tile = MMA N (multiple of 16, <= 256)
     int kb_per_split;       // 64-wide K blocks per CTA along K (multiple of 4)
     int splits;             // CTAs along K = cluster size (1 = no reduction)
-    int x_stages, w_stages;
+    int x_stages, w_stages; // x ring slots (one commit group of K blocks each), weight ring stages
     int groups_per_row;     // W4A16: K / group
     int kb_per_group;       // W4A16: group / 64
     int kbg_shift;          // log2(kb_per_group) when it is a power of two, else -1
     int x_stage_bytes, w_stage_bytes;
+    int cb_shift;           // log2(CB), CB = K blocks per commit group (1, 2 or 4; divides every split's blocks)
     uint64_t timeout_ns;
 };
 
@@ -169,9 +171,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t *const w_ring = smem + XS * args.x_stage_bytes;
 
     const uint32_t bar0 = smem_u32(smem + OFF_BAR);
-    // mma_done[j % A_STAGES] completes when the MMAs of K block j (and all before it)
-    // are done: one tcgen05.commit per block releases both the block's A slot and its
-    // x slot (the x ring is at most A_STAGES deep, so no phase of it is skipped).
+    // The MMA issuer works in commit groups of CB = 2^cb_shift consecutive K blocks:
+    // one x_full wait (the group's CB x tiles share one ring slot and barrier), one
+    // a_full wait (every transform warp arrives once per group), 4*CB MMAs and one
+    // tcgen05.commit.  A single thread issues every MMA of the CTA, and its fixed
+    // cost per loop iteration (waits, fence, bookkeeping) is several hundred cycles
+    // on a busy SM, so it is paid per group rather than per 64-wide block.
+    // mma_done[(j % A_STAGES) >> cb_shift] completes when the MMAs of the group
+    // holding block j (and all before it) are done; that releases the group's A
+    // slots and its x slot (the x ring has at most A_STAGES / CB slots, so no phase
+    // of mma_done is skipped).
+    const int cbs = args.cb_shift;
+    const int dslots = A_STAGES >> cbs;  // commit-group slots of the A ring
+    const int ngroups = nkb >> cbs;      // nkb is a multiple of CB
     const uint32_t x_full = bar0, mma_done = x_full + 8 * X_MAX_STAGES;
     const uint32_t w_full = mma_done + 8 * X_MAX_STAGES, w_empty = w_full + 8 * W_MAX_STAGES;
     const uint32_t a_full = w_empty + 8 * W_MAX_STAGES, unused = a_full + 8 * A_STAGES;
@@ -186,9 +198,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(w_full + 8 * s, 1);
             mbar_init(w_empty + 8 * s, NUM_XFORM_WARPS);
         }
-        for (int s = 0; s < A_STAGES; ++s) {
-            mbar_init(a_full + 8 * s, NUM_XFORM_WARPS / XFORM_GROUPS);
-        }
+        // With CB == 1 a group is one block, done by one transform group.
+        for (int s = 0; s < A_STAGES; ++s)
+            mbar_init(a_full + 8 * s, cbs == 0 ? NUM_XFORM_WARPS / XFORM_GROUPS : NUM_XFORM_WARPS);
         mbar_init(acc_full, 1);
         mbar_init(drain, 1);
         // A failure recorded earlier (and not yet read by qwp_device_status) makes
@@ -215,22 +227,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             asm volatile("griddepcontrol.wait;" ::: "memory");
             int issued = 0;
             int xs = 0;         // ring slot (running counters: no division in the loop)
-            int dk = 0;         // mma_done slot of block j - XS, and its phase
+            int dk = 0;         // mma_done slot of group g - XS, and its phase
             uint32_t dph = 0;
-            for (int j = 0; j < nkb; ++j) {
-                if (j >= XS) {  // slot xs last held block j - XS
+            const uint32_t tile_bytes = static_cast<uint32_t>(args.bn) * 128u;
+            for (int g = 0; g < ngroups; ++g) {
+                if (g >= XS) {  // slot xs last held group g - XS
                     if (!wait_bar(mma_done + 8 * dk, dph, ctl, WAIT_X_EMPTY)) break;
-                    if (++dk == A_STAGES) { dk = 0; dph ^= 1; }
+                    if (++dk == dslots) { dk = 0; dph ^= 1; }
                 }
-                mbar_arrive_expect_tx(x_full + 8 * xs, static_cast<uint32_t>(args.bn) * 128u);
-                tma_load_2d(smem_u32(x_ring + xs * args.x_stage_bytes), &tmap_x,
-                            (kb_begin + j) * CHUNK_K, m0, x_full + 8 * xs);
-                issued = j + 1;
+                mbar_arrive_expect_tx(x_full + 8 * xs, tile_bytes << cbs);
+                for (int c = 0; c < (1 << cbs); ++c)
+                    tma_load_2d(smem_u32(x_ring + xs * args.x_stage_bytes + c * tile_bytes), &tmap_x,
+                                (kb_begin + (g << cbs) + c) * CHUNK_K, m0, x_full + 8 * xs);
+                issued = g + 1;
                 if (++xs == XS) xs = 0;
             }
             // Every copy issued above lands before the CTA may exit.
-            for (int j = max(0, issued - XS); j < issued; ++j)
-                wait_bar(x_full + 8 * (j % XS), (j / XS) & 1, ctl, WAIT_DRAIN, false);
+            for (int g = max(0, issued - XS); g < issued; ++g)
+                wait_bar(x_full + 8 * (g % XS), (g / XS) & 1, ctl, WAIT_DRAIN, false);
         }
     } else if (warp == 2) {
         // ------------------------------------------------------------ weight producer
@@ -264,20 +278,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0 && !skip) {
             const uint32_t idesc = make_idesc_f16(false, TILE_ROWS, static_cast<uint32_t>(args.bn));  // fp16 A and B
             bool ok = true;
-            int xs = 0;
-            uint32_t xph = 0;
-            for (int j = 0; j < nkb; ++j, xs = (xs + 1 == XS) ? 0 : xs + 1, xph ^= (xs == 0)) {
-                const int as = j % A_STAGES;
+            int xs = 0, gs = 0;       // x ring slot; commit-group slot of the A ring
+            uint32_t xph = 0, gph = 0;
+            const uint32_t tile_desc = static_cast<uint32_t>(args.bn) * 128u >> 4;  // one x tile, in descriptor units
+            for (int g = 0; g < ngroups; ++g) {
                 ok = wait_bar(x_full + 8 * xs, xph, ctl, WAIT_X_FULL) &&
-                     wait_bar(a_full + 8 * as, (j / A_STAGES) & 1, ctl, WAIT_A_FULL);
+                     wait_bar(a_full + 8 * gs, gph, ctl, WAIT_A_FULL);
                 if (!ok) break;
                 tc_fence_after();
-                const uint64_t bdesc = smem_desc_sw128(smem_u32(x_ring + xs * args.x_stage_bytes));
+                uint64_t bdesc = smem_desc_sw128(smem_u32(x_ring + xs * args.x_stage_bytes));
+                uint32_t acol = tmem + A_COL + (32u << cbs) * gs;
+                for (int c = 0; c < (1 << cbs); ++c, bdesc += tile_desc, acol += 32u) {
 #pragma unroll
-                for (int kk = 0; kk < CHUNK_K / 16; ++kk)
-                    mma_ts(tmem + ACC_COL, tmem + A_COL + 32u * as + 8u * kk, bdesc + 2u * kk, idesc,
-                           (j | kk) != 0);
-                mma_commit(mma_done + 8 * as);
+                    for (int kk = 0; kk < CHUNK_K / 16; ++kk)
+                        mma_ts(tmem + ACC_COL, acol + 8u * kk, bdesc + 2u * kk, idesc, (g | c | kk) != 0);
+                }
+                mma_commit(mma_done + 8 * gs);
+                if (++xs == XS) { xs = 0; xph ^= 1; }
+                if (++gs == dslots) { gs = 0; gph ^= 1; }
             }
             if (ok) {
                 mma_commit(acc_full);
@@ -346,18 +364,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // Store block j into its A ring slot once the MMA has released the slot.
         auto issue = [&](int j, const uint32_t (&regs)[16]) -> bool {
             const int as = j % A_STAGES;
-            if (!__all_sync(0xffffffffu, wait_bar(mma_done + 8 * as, ((j / A_STAGES) & 1) ^ 1, ctl, WAIT_A_EMPTY)))
+            if (!__all_sync(0xffffffffu,
+                            wait_bar(mma_done + 8 * (as >> cbs), ((j / A_STAGES) & 1) ^ 1, ctl, WAIT_A_EMPTY)))
                 return false;
             tc_fence_after();
             tmem_st_x16(tmem + lane_base + A_COL + 32u * as + 16u * half, regs);
             return true;
         };
-        // Publish block j to the MMA issuer once its tensor-memory store has landed.
+        // Block j's tensor-memory store lands; after this warp's last block of a commit
+        // group, publish the group to the MMA issuer.
         auto finish = [&](int j) {
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(a_full + 8 * (j % A_STAGES));
+            if (j + XFORM_GROUPS >= (((j >> cbs) + 1) << cbs) && lane == 0)
+                mbar_arrive(a_full + 8 * ((j % A_STAGES) >> cbs));
         };
 
         // Software pipeline over this warp's blocks j = grp, grp+G, ...: the unpack of
@@ -581,12 +602,17 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
         if ((1 << sh) == a.kb_per_group) a.kbg_shift = sh;
     a.bn = bn;
     a.timeout_ns = timeout_ns;
-    a.x_stage_bytes = bn * 128;
+    // Commit groups: 4 blocks for short MMAs (N <= 128), else 2; never more than
+    // divides the K blocks (every split's block count is then a multiple too).
+    const int64_t nkb_total = K / CHUNK_K;
+    int cbs = bn <= 128 ? 2 : 1;
+    while (cbs > 0 && nkb_total % (1 << cbs)) --cbs;
+    a.cb_shift = cbs;
+    a.x_stage_bytes = (bn * 128) << cbs;
     a.w_stage_bytes = kQ4K ? TILE_ROWS * Q4K_BLOCK_BYTES : TILE_ROWS * CHUNK_ROW_BYTES * KB_PER_STAGE;
     a.w_stages = 4;
-    a.x_stages = std::min(X_MAX_STAGES, (RING_BYTES - a.w_stages * a.w_stage_bytes) / a.x_stage_bytes);
-    if (a.x_stages == X_MAX_STAGES)
-        a.w_stages = std::min(W_MAX_STAGES, (RING_BYTES - a.x_stages * a.x_stage_bytes) / a.w_stage_bytes);
+    a.x_stages = std::min(A_STAGES >> cbs, (RING_BYTES - a.w_stages * a.w_stage_bytes) / a.x_stage_bytes);
+    a.w_stages = std::min(W_MAX_STAGES, (RING_BYTES - a.x_stages * a.x_stage_bytes) / a.w_stage_bytes);
 
     const int64_t row_tiles = (N + TILE_ROWS - 1) / TILE_ROWS;
     const int64_t tok_tiles = (M + bn - 1) / bn;
