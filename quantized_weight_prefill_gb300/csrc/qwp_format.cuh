@@ -129,17 +129,21 @@ __device__ __forceinline__ void q4k_word_f32(uint32_t word, float dl, float ml, 
 
 // Per-sub-block fp16 constants of the GEMM's unpack.
 struct Q4kSubH {
-    __half2 sc2;   // (sc, sc)
-    __half2 csc2;  // (-1024*sc, -1024*sc), exact
-    __half2 d2;    // (d, d)
-    __half2 nml2;  // (-RN(dmin*m), -RN(dmin*m))
+    __half2 sc2;     // (sc, sc)
+    __half2 csc2;    // (-1024*sc, -1024*sc), exact
+    __half2 sc16_2;  // (sc/16, sc/16), exact
+    __half2 csc16_2; // (-64*sc, -64*sc), exact
+    __half2 d2;      // (d, d)
+    __half2 nml2;    // (-RN(dmin*m), -RN(dmin*m))
 };
 
 __device__ __forceinline__ Q4kSubH q4k_sub_f16(uint4 h, int j) {
     Q4kSubH k;
     const __half2 scm = q4k_scmin(h, j);
     k.sc2 = __low2half2(scm);
-    k.csc2 = __hmul2(k.sc2, as_half2(0xE400E400u));  // x (-1024)
+    k.csc2 = __hmul2(k.sc2, as_half2(0xE400E400u));     // x (-1024)
+    k.sc16_2 = __hmul2(k.sc2, as_half2(0x2C002C00u));   // x (1/16)
+    k.csc16_2 = __hmul2(k.sc2, as_half2(0xD400D400u));  // x (-64)
     k.d2 = as_half2(__byte_perm(h.x, 0u, 0x1010));
     const __half2 ndmin2 = as_half2(__byte_perm(h.x, 0u, 0x3232) ^ 0x80008000u);
     k.nml2 = __hmul2(__high2half2(scm), ndmin2);
@@ -148,13 +152,19 @@ __device__ __forceinline__ Q4kSubH q4k_sub_f16(uint4 h, int j) {
 
 // The 8 weights of one word as fp16x2 MMA operands.  (1024+q)*sc - 1024*sc is
 // q*sc exactly (at most 945, inside fp16's 11-bit integer range; the fma does not
-// round its product), and d*(q*sc) - RN(dmin*m) is rounded once to fp16.
+// round its product), and d*(q*sc) - RN(dmin*m) is rounded once to fp16.  Pairs 1
+// and 3 are read in place from bits 4..7 of each half, as 1024 + 16q, which saves
+// their shifts: (1024+16q)*(sc/16) - 64*sc is the same exact q*sc.
 __device__ __forceinline__ void q4k_word_f16x2(uint32_t word, const Q4kSubH &k, uint32_t (&p)[4]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __half2 qsc = __hfma2(as_half2(nib_pair_magic(word, i)), k.sc2, k.csc2);
-        p[i] = as_u32(__hfma2(qsc, k.d2, k.nml2));
-    }
+    const uint32_t w8 = word >> 8;
+    const __half2 q0 = __hfma2(as_half2((word & 0x000F000Fu) | 0x64006400u), k.sc2, k.csc2);
+    const __half2 q1 = __hfma2(as_half2((word & 0x00F000F0u) | 0x64006400u), k.sc16_2, k.csc16_2);
+    const __half2 q2 = __hfma2(as_half2((w8 & 0x000F000Fu) | 0x64006400u), k.sc2, k.csc2);
+    const __half2 q3 = __hfma2(as_half2((w8 & 0x00F000F0u) | 0x64006400u), k.sc16_2, k.csc16_2);
+    p[0] = as_u32(__hfma2(q0, k.d2, k.nml2));
+    p[1] = as_u32(__hfma2(q1, k.d2, k.nml2));
+    p[2] = as_u32(__hfma2(q2, k.d2, k.nml2));
+    p[3] = as_u32(__hfma2(q3, k.d2, k.nml2));
 }
 
 // ---------------------------------------------------------------- W4A16 unpack

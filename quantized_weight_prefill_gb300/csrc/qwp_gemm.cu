@@ -16,12 +16,12 @@
 //   warp 1        allocates tensor memory; one thread issues tcgen05.mma;
 //   warp 2        weight producer: one bulk copy per 256-wide K stage of packed
 //                 weights into the weight ring;
-//   warps 3..18   transform: two groups of 8 warps take alternate K blocks; warp
-//                 (quarter q, half h) owns weight rows 32q..32q+31 (its tensor-
-//                 memory lane quarter) and half of the block's 64 K columns; it
-//                 unpacks its 32 weights to bf16 (Q4_K) or fp16 (W4A16) and stores
-//                 them with tcgen05.st into the A ring in tensor memory; the same
-//                 warps later drain the fp32 accumulator (tcgen05.ld) into y.
+//   warps 3..18   transform: four groups of 4 warps; group g owns K block g of
+//                 every weight stage (4 blocks of 64); warp (group g, quarter q)
+//                 unpacks rows 32q..32q+31 (its tensor-memory lane quarter) of
+//                 that block, 64 weights per thread, to fp16 and stores them with
+//                 one tcgen05.st into the A ring in tensor memory; the same warps
+//                 later drain the fp32 accumulator (tcgen05.ld) into y.
 // Tensor memory (512 columns): accumulator [128 lanes x BN] at column 0, an
 // 8-deep ring of A operand blocks (128 lanes x 64 K = 32 columns) at 256.
 // The MMA is D[128 x BN] += A[128 x 16] (tensor memory) . B[BN x 16]^T (shared
@@ -44,8 +44,8 @@
 
 namespace qwp {
 
-constexpr int XFORM_GROUPS = 2;                    // groups take alternate K blocks
-constexpr int NUM_XFORM_WARPS = 8 * XFORM_GROUPS;  // 8 warps cover one K block (4 lane quarters x 2 halves)
+constexpr int XFORM_GROUPS = 4;                    // groups take K blocks in turn, one per weight stage
+constexpr int NUM_XFORM_WARPS = 4 * XFORM_GROUPS;  // 4 warps (one per lane quarter) cover one K block
 constexpr int FIRST_XFORM_WARP = 3;
 constexpr int NUM_THREADS = 32 * (FIRST_XFORM_WARP + NUM_XFORM_WARPS);
 constexpr int X_MAX_STAGES = 8;  // <= A_STAGES: the x ring reuses the mma_done ring (see below)
@@ -68,6 +68,7 @@ constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base t
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(X_MAX_STAGES <= A_STAGES, "the x ring is released through the mma_done ring");
 static_assert(A_STAGES % 4 == 0, "commit groups of up to 4 blocks tile the A ring");
+static_assert(XFORM_GROUPS == KB_PER_STAGE, "each transform warp owns one K block of every weight stage");
 static_assert(512 * BN_MAX <= RING_BYTES, "split-K partials must fit the ring region");
 
 struct GemmArgs {
@@ -132,10 +133,10 @@ __device__ __forceinline__ bool aborted(const Ctl &ctl) {
 }
 
 // Unpack one row's half of a 64-wide K block (4 words = 32 weights) into 16
-// packed fp16 pairs for the A operand.
+// packed fp16 pairs regs[off .. off+15] of the A operand.
 template <bool kQ4K>
 __device__ __forceinline__ void unpack_quarter(uint4 wv, const Q4kSubH &ks, __half2 mz, __half2 s2,
-                                               uint32_t (&regs)[16]) {
+                                               uint32_t (&regs)[32], int off) {
     const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -145,7 +146,7 @@ __device__ __forceinline__ void unpack_quarter(uint4 wv, const Q4kSubH &ks, __ha
         else
             w4_word_f16x2(w[i], mz, s2, p);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) regs[4 * i + e] = p[e];
+        for (int e = 0; e < 4; ++e) regs[off + 4 * i + e] = p[e];
     }
 }
 
@@ -198,9 +199,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(w_full + 8 * s, 1);
             mbar_init(w_empty + 8 * s, NUM_XFORM_WARPS);
         }
-        // With CB == 1 a group is one block, done by one transform group.
+        // A commit group of CB <= XFORM_GROUPS blocks is stored by CB transform groups.
         for (int s = 0; s < A_STAGES; ++s)
-            mbar_init(a_full + 8 * s, cbs == 0 ? NUM_XFORM_WARPS / XFORM_GROUPS : NUM_XFORM_WARPS);
+            mbar_init(a_full + 8 * s, (NUM_XFORM_WARPS / XFORM_GROUPS) << cbs);
         mbar_init(acc_full, 1);
         mbar_init(drain, 1);
         // A failure recorded earlier (and not yet read by qwp_device_status) makes
@@ -307,93 +308,82 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         // ------------------------------------------------------------ transform + epilogue
         const uint32_t xw = warp - FIRST_XFORM_WARP;
-        const int grp = static_cast<int>(xw >> 3);          // this warp's K blocks: j % XFORM_GROUPS == grp
-        const uint32_t quarter = warp & 3;                   // tensor-memory lanes 32*quarter .. +31
-        const int half = static_cast<int>((xw >> 2) & 1);    // which 32 of the block's 64 K columns
+        const int grp = static_cast<int>(xw >> 2);   // this warp's K blocks: j % XFORM_GROUPS == grp
+        const uint32_t quarter = warp & 3;            // tensor-memory lanes 32*quarter .. +31
         const int r = static_cast<int>(quarter * 32 + lane);
         const bool valid = r < R;
         const int64_t n = static_cast<int64_t>(tile) * TILE_ROWS + r;
         const uint32_t lane_base = (quarter * 32u) << 16;
         bool ok = !skip;
-        uint4 hdr = make_uint4(0, 0, 0, 0);  // Q4_K header of the current weight stage
-        int cur_s = 0, ws = 0;               // weight stage this warp is in, and its ring slot
-        uint32_t wph = 0;                    // phase of that slot
+        int ws = -1;       // weight ring slot of this warp's current stage, and its phase
+        uint32_t wph = 0;
 
-        // Unpack K block j of this thread's row into `regs`; waits for its weight
-        // stage when j opens one and releases the stage after its last block.
-        auto prepare = [&](int j, uint32_t (&regs)[16]) -> bool {
-            const int s = j / KB_PER_STAGE, c = j % KB_PER_STAGE;
-            while (cur_s < s) {  // at most one step: blocks advance by XFORM_GROUPS < KB_PER_STAGE
-                if (++ws == WS) { ws = 0; wph ^= 1; }
-                ++cur_s;
-            }
+        // Unpack K block j (the block of weight stage j / 4 that this warp owns) of
+        // this thread's row into `regs`: 64 weights as 32 fp16 pairs.  Waits for the
+        // stage and releases it after reading (the warp reads nothing else of it).
+        auto prepare = [&](int j, uint32_t (&regs)[32]) -> bool {
+            const int c = j & (KB_PER_STAGE - 1);
+            if (++ws == WS) { ws = 0; wph ^= 1; }
             const uint8_t *wst = w_ring + ws * args.w_stage_bytes;
-            const int kb0 = kb_begin + KB_PER_STAGE * s;
-            const int nblk = min(KB_PER_STAGE, kb_end - kb0);
-            if (c == grp) {  // this warp's first block of the stage
-                // Every lane waits; the warp moves on together (tcgen05.st/ld are warp-collective).
-                if (!__all_sync(0xffffffffu, wait_bar(w_full + 8 * ws, wph, ctl, WAIT_W_FULL)))
-                    return false;
-                if (kQ4K && valid) hdr = *reinterpret_cast<const uint4 *>(wst + Q4K_HEADER_BYTES * r);
-            }
-            uint4 wv = make_uint4(0, 0, 0, 0);
-            Q4kSubH ks;
+            // Every lane waits; the warp moves on together (tcgen05.st/ld are warp-collective).
+            if (!__all_sync(0xffffffffu, wait_bar(w_full + 8 * ws, wph, ctl, WAIT_W_FULL))) return false;
+            uint4 wv0 = make_uint4(0, 0, 0, 0), wv1 = make_uint4(0, 0, 0, 0);
+            Q4kSubH k0, k1;
             __half2 s2 = __float2half2_rn(0.f), mz = w4_magic_zero(0);
             if (kQ4K) {
-                if (valid)
-                    wv = *reinterpret_cast<const uint4 *>(wst + Q4K_HEADER_BYTES * R + CHUNK_ROW_BYTES * R * c +
-                                                          (half * R + r) * 16);
-                ks = q4k_sub_f16(hdr, 2 * c + half);
+                uint4 hdr = make_uint4(0, 0, 0, 0);
+                if (valid) {
+                    hdr = *reinterpret_cast<const uint4 *>(wst + Q4K_HEADER_BYTES * r);
+                    const uint8_t *cp = wst + Q4K_HEADER_BYTES * R + CHUNK_ROW_BYTES * R * c + r * 16;
+                    wv0 = *reinterpret_cast<const uint4 *>(cp);
+                    wv1 = *reinterpret_cast<const uint4 *>(cp + 16 * R);
+                }
+                k0 = q4k_sub_f16(hdr, 2 * c);
+                k1 = q4k_sub_f16(hdr, 2 * c + 1);
             } else if (valid) {
-                wv = *reinterpret_cast<const uint4 *>(wst + CHUNK_ROW_BYTES * R * c + (half * R + r) * 16);
+                const uint8_t *cp = wst + CHUNK_ROW_BYTES * R * c + r * 16;
+                wv0 = *reinterpret_cast<const uint4 *>(cp);
+                wv1 = *reinterpret_cast<const uint4 *>(cp + 16 * R);
                 const int64_t ng = args.groups_per_row;
-                const int kbi = kb0 + c;
+                const int kbi = kb_begin + j;
                 const int64_t g = args.kbg_shift >= 0 ? (kbi >> args.kbg_shift) : (kbi / args.kb_per_group);
                 s2 = __half2half2(args.scales[n * ng + g]);
                 mz = w4_magic_zero(args.zeros[n * ng + g]);
             }
-            // This warp's last block of the stage: its reads of the stage are done.  (A
-            // warp with no block in a partial last stage never arrives; nothing refills it.)
-            if (c + XFORM_GROUPS >= nblk) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(w_empty + 8 * ws);
-            }
-            unpack_quarter<kQ4K>(wv, ks, mz, s2, regs);
+            // This warp's reads of the stage are done.
+            __syncwarp();
+            if (lane == 0) mbar_arrive(w_empty + 8 * ws);
+            unpack_quarter<kQ4K>(wv0, k0, mz, s2, regs, 0);
+            unpack_quarter<kQ4K>(wv1, k1, mz, s2, regs, 16);
             return true;
         };
-        // Store block j into its A ring slot once the MMA has released the slot.
-        auto issue = [&](int j, const uint32_t (&regs)[16]) -> bool {
+        // Store block j into its A ring slot once the MMAs of the block that last
+        // used the slot (j - A_STAGES) are done.
+        auto issue = [&](int j, const uint32_t (&regs)[32]) -> bool {
             const int as = j % A_STAGES;
             if (!__all_sync(0xffffffffu,
                             wait_bar(mma_done + 8 * (as >> cbs), ((j / A_STAGES) & 1) ^ 1, ctl, WAIT_A_EMPTY)))
                 return false;
             tc_fence_after();
-            tmem_st_x16(tmem + lane_base + A_COL + 32u * as + 16u * half, regs);
+            tmem_st_x32(tmem + lane_base + A_COL + 32u * as, regs);
             return true;
         };
-        // Block j's tensor-memory store lands; after this warp's last block of a commit
-        // group, publish the group to the MMA issuer.
+        // Block j's tensor-memory store lands; publish it to the MMA issuer.
         auto finish = [&](int j) {
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (j + XFORM_GROUPS >= (((j >> cbs) + 1) << cbs) && lane == 0)
-                mbar_arrive(a_full + 8 * ((j % A_STAGES) >> cbs));
+            if (lane == 0) mbar_arrive(a_full + 8 * ((j % A_STAGES) >> cbs));
         };
 
-        // Software pipeline over this warp's blocks j = grp, grp+G, ...: the unpack of
-        // the next block overlaps the tensor-memory store of the current one.
-        constexpr int G = XFORM_GROUPS;
-        uint32_t ra[16], rb[16];
-        if (ok && grp < nkb) ok = prepare(grp, ra);
-        for (int j = grp; ok && j < nkb; j += 2 * G) {
-            if (!(ok = issue(j, ra))) break;
-            if (j + G < nkb && !(ok = prepare(j + G, rb))) break;
+        // This warp's blocks are j = grp, grp + 4, ...: one per weight stage.  The
+        // unpack of the next block overlaps the tensor-memory store of the current one.
+        uint32_t regs[32];
+        if (ok && grp < nkb) ok = prepare(grp, regs);
+        for (int j = grp; ok && j < nkb; j += XFORM_GROUPS) {
+            if (!(ok = issue(j, regs))) break;
+            if (j + XFORM_GROUPS < nkb && !(ok = prepare(j + XFORM_GROUPS, regs))) break;
             finish(j);
-            if (j + G >= nkb) break;
-            if (!(ok = issue(j + G, rb))) break;
-            if (j + 2 * G < nkb && !(ok = prepare(j + 2 * G, ra))) break;
-            finish(j + G);
         }
         tmem_wait_st();  // no tensor-memory store may be in flight past this point
         __syncwarp();
