@@ -69,7 +69,7 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(X_MAX_STAGES <= A_STAGES, "the x ring is released through the mma_done ring");
 static_assert(A_STAGES % 4 == 0, "commit groups of up to 4 blocks tile the A ring");
 static_assert(XFORM_GROUPS == KB_PER_STAGE, "each transform warp owns one K block of every weight stage");
-static_assert(512 * BN_MAX <= RING_BYTES, "split-K partials must fit the ring region");
+static_assert(512 * (BN_MAX + MAX_SPLITS) <= RING_BYTES, "split-K partials must fit the ring region");
 
 struct GemmArgs {
     const uint8_t *w;       // repacked weights
@@ -192,7 +192,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + OFF_MISC);  // [0] tmem base, [1] abort
     const Ctl ctl{misc + 1, args.status, args.timeout_ns};
 
-    if (threadIdx.x == 0) {
+    // Copy of weight stage s (K blocks 4s.. of this CTA's range) into ring slot ws.
+    auto load_weight_stage = [&](int s, int ws) {
+        const int kb0 = kb_begin + KB_PER_STAGE * s;
+        const int nblk = min(KB_PER_STAGE, kb_end - kb0);
+        const uint8_t *src;
+        uint32_t bytes;
+        if (kQ4K) {
+            src = args.w + q4k_group_offset(args.K, tile, R, kb0 / KB_PER_STAGE);
+            bytes = static_cast<uint32_t>(R) * Q4K_BLOCK_BYTES;
+        } else {
+            src = args.w + w4_plane_offset(args.K, tile, R, kb0);
+            bytes = static_cast<uint32_t>(R) * CHUNK_ROW_BYTES * nblk;
+        }
+        mbar_arrive_expect_tx(w_full + 8 * ws, bytes);
+        bulk_copy_g2s(smem_u32(w_ring + ws * args.w_stage_bytes), src, bytes, w_full + 8 * ws);
+    };
+    // The weight producer's thread sets up the barriers and starts the first weight
+    // copies before the block-wide barrier (their slots are empty).
+    const int w_pre = min(WS, nstage);
+    if (threadIdx.x == 64) {
         for (int s = 0; s < X_MAX_STAGES; ++s) mbar_init(x_full + 8 * s, 1);
         for (int s = 0; s < A_STAGES; ++s) mbar_init(mma_done + 8 * s, 1);
         for (int s = 0; s < W_MAX_STAGES; ++s) {
@@ -206,9 +225,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(drain, 1);
         // A failure recorded earlier (and not yet read by qwp_device_status) makes
         // every later launch skip its work instead of waiting out its own timeouts.
-        misc[1] = (*reinterpret_cast<volatile uint32_t *>(args.status) & kStatusTimeoutMask) ? 1u : 0u;
+        const bool failed = (*reinterpret_cast<volatile uint32_t *>(args.status) & kStatusTimeoutMask) != 0;
+        misc[1] = failed ? 1u : 0u;
         fence_mbar_init();
         prefetch_tensormap(&tmap_x);
+        if (!failed)
+            for (int s = 0; s < w_pre; ++s) load_weight_stage(s, s);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(misc), TMEM_COLS);
@@ -219,6 +241,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const bool skip = misc[1] != 0;
+    bool acc_ok = false;  // transform warps: the accumulator is complete
 
     if (warp == 0) {
         // ------------------------------------------------------------ x producer
@@ -250,26 +273,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 2) {
         // ------------------------------------------------------------ weight producer
         if (lane == 0 && !skip) {
-            int issued = 0;
+            int issued = w_pre;  // stages 0 .. w_pre-1 went out before the block-wide barrier
             int ws = 0;
-            uint32_t wph = 0;
-            for (int s = 0; s < nstage; ++s) {
-                if (s > 0 && ++ws == WS) { ws = 0; wph ^= 1; }
+            uint32_t wph = 1;    // stage w_pre reuses slot 0 (second use: wait for its first release)
+            for (int s = w_pre; s < nstage; ++s) {
                 if (!wait_bar(w_empty + 8 * ws, wph ^ 1, ctl, WAIT_W_EMPTY)) break;
-                const int kb0 = kb_begin + KB_PER_STAGE * s;
-                const int nblk = min(KB_PER_STAGE, kb_end - kb0);
-                const uint8_t *src;
-                uint32_t bytes;
-                if (kQ4K) {
-                    src = args.w + q4k_group_offset(args.K, tile, R, kb0 / KB_PER_STAGE);
-                    bytes = static_cast<uint32_t>(R) * Q4K_BLOCK_BYTES;
-                } else {
-                    src = args.w + w4_plane_offset(args.K, tile, R, kb0);
-                    bytes = static_cast<uint32_t>(R) * CHUNK_ROW_BYTES * nblk;
-                }
-                mbar_arrive_expect_tx(w_full + 8 * ws, bytes);
-                bulk_copy_g2s(smem_u32(w_ring + ws * args.w_stage_bytes), src, bytes, w_full + 8 * ws);
+                load_weight_stage(s, ws);
                 issued = s + 1;
+                if (++ws == WS) { ws = 0; wph ^= 1; }
             }
             for (int s = max(0, issued - WS); s < issued; ++s)
                 wait_bar(w_full + 8 * (s % WS), (s / WS) & 1, ctl, WAIT_DRAIN, false);
@@ -378,26 +389,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
         // This warp's blocks are j = grp, grp + 4, ...: one per weight stage.  The
         // unpack of the next block overlaps the tensor-memory store of the current one.
+        // (The first block is published before the next one is unpacked, so that the
+        // MMAs can start as early as possible.)
         uint32_t regs[32];
         if (ok && grp < nkb) ok = prepare(grp, regs);
         for (int j = grp; ok && j < nkb; j += XFORM_GROUPS) {
             if (!(ok = issue(j, regs))) break;
+            if (j == grp) finish(j);
             if (j + XFORM_GROUPS < nkb && !(ok = prepare(j + XFORM_GROUPS, regs))) break;
-            finish(j);
+            if (j != grp) finish(j);
         }
         tmem_wait_st();  // no tensor-memory store may be in flight past this point
         __syncwarp();
-        if (ok && __all_sync(0xffffffffu, wait_bar(acc_full, 0, ctl, WAIT_ACC_FULL))) {
+        acc_ok = ok && __all_sync(0xffffffffu, wait_bar(acc_full, 0, ctl, WAIT_ACC_FULL));
+        if (acc_ok && args.splits == 1) {
             tc_fence_after();
-            float *part = reinterpret_cast<float *>(smem);  // [bn][128] partial tile (split-K)
-            for (int ci = static_cast<int>(xw >> 2); ci < args.bn / 16; ci += NUM_XFORM_WARPS / 4) {
+            for (int ci = grp; ci < args.bn / 16; ci += NUM_XFORM_WARPS / 4) {
                 uint32_t v[16];
                 tmem_ld_x16(tmem + lane_base + ACC_COL + 16u * ci, v);
                 tmem_wait_ld();
-                if (args.splits > 1) {
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) part[(16 * ci + t) * TILE_ROWS + r] = __uint_as_float(v[t]);
-                } else if (valid) {
+                if (valid) {
                     const int mb = m0 + 16 * ci;
 #pragma unroll
                     for (int t = 0; t < 16; ++t)
@@ -411,29 +422,58 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     __syncthreads();
     if (args.splits > 1) {
-        // Deterministic split-K reduction through distributed shared memory: CTA
-        // `rank` of the cluster sums, in rank order, every CTA's partial for its
-        // share of the tile's tokens and writes y.  Every CTA reaches both cluster
-        // barriers whatever happened above (all waits before them are bounded).
-        cluster_sync();
+        // Deterministic split-K reduction through distributed shared memory.  CTA
+        // `rank` of the cluster owns tokens [rank*per, rank*per + per) of the tile.
+        // Once every CTA is past its main loop (its ring region is free), each CTA
+        // pushes its partial accumulator for every token straight from tensor memory
+        // into the owner's ring region, laid out [source rank][token][row]; after the
+        // second cluster barrier each owner sums its tokens over the source ranks in
+        // rank order and writes y.  Every CTA reaches both barriers whatever happened
+        // above (all waits before them are bounded).
         const int S = args.splits;
         const uint32_t rank = cluster_ctarank();
         const int per = (args.bn + S - 1) / S;
+        const uint32_t buf = smem_u32(smem);
+        cluster_sync();
+        if (acc_ok && !aborted(ctl)) {
+            tc_fence_after();
+            const uint32_t xw = warp - FIRST_XFORM_WARP;
+            const uint32_t quarter = warp & 3;
+            const int row = static_cast<int>(quarter * 32 + lane);
+            const uint32_t lane_base = (quarter * 32u) << 16;
+            for (int ci = static_cast<int>(xw >> 2); ci < args.bn / 16; ci += NUM_XFORM_WARPS / 4) {
+                uint32_t v[16];
+                tmem_ld_x16(tmem + lane_base + ACC_COL + 16u * ci, v);
+                tmem_wait_ld();
+                int owner = (16 * ci) / per, tt = 16 * ci - owner * per;
+                uint32_t dst = map_shared_rank(buf, owner);
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    st_shared_cluster_f32(dst + static_cast<uint32_t>(((static_cast<int>(rank) * per + tt) * TILE_ROWS + row) * 4),
+                                          __uint_as_float(v[t]));
+                    if (++tt == per && t < 15) {
+                        tt = 0;
+                        dst = map_shared_rank(buf, ++owner);
+                    }
+                }
+            }
+            tc_fence_before();
+        }
+        cluster_sync();
         const int t0 = min(args.bn, static_cast<int>(rank) * per);
         const int t1 = min(args.bn, t0 + per);
         if (!aborted(ctl)) {
-            const uint32_t part0 = smem_u32(smem);
+            const float *part = reinterpret_cast<const float *>(smem);
             const int items = (t1 - t0) * (TILE_ROWS / 4);
             for (int it = threadIdx.x; it < items; it += NUM_THREADS) {
-                const int t = t0 + it / (TILE_ROWS / 4);
+                const int tt = it / (TILE_ROWS / 4);
                 const int r4 = 4 * (it % (TILE_ROWS / 4));
-                const uint32_t off = static_cast<uint32_t>((t * TILE_ROWS + r4) * 4);
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                 for (int q = 0; q < S; ++q) {
-                    const float4 v = ld_shared_cluster_f4(map_shared_rank(part0 + off, q));
+                    const float4 v = *reinterpret_cast<const float4 *>(part + (q * per + tt) * TILE_ROWS + r4);
                     acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
                 }
-                const int m = m0 + t;
+                const int m = m0 + t0 + tt;
                 if (m < args.M) {
                     float *yr = args.y + static_cast<int64_t>(m) * args.N + static_cast<int64_t>(tile) * TILE_ROWS;
                     const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
@@ -443,7 +483,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
-        cluster_sync();
     }
     if (warp == 1) {
         tc_fence_after();
