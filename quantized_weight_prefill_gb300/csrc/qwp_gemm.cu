@@ -9,10 +9,13 @@
 // tok/s", section "The two prefill paths": each weight row is applied to a
 // whole chunk of prompt tokens per read.
 //
-// One CTA computes a 128-row (weights) x BN-token (BN <= 256) tile of y^T over
-// a range of K:
-//   warp 0        x producer: one thread issues a 2-D TMA load (128-byte
-//                 swizzle) per 64-wide K block of x into the x ring;
+// The grid is persistent: one CTA per SM (a cluster of S CTAs when K is split S
+// ways) loops over units, a unit being a 128-row (weights) x BN-token (BN <= 256)
+// tile of y^T; CTA rank s of a cluster computes K range s of every unit.  The
+// rings run on across units, so the copies and unpacking of the next unit
+// overlap the end of the current one.  Roles:
+//   warp 0        x producer: one thread issues 2-D TMA loads (128-byte swizzle),
+//                 one per 64-wide K block, into the x ring;
 //   warp 1        allocates tensor memory; one thread issues tcgen05.mma;
 //   warp 2        weight producer: one bulk copy per 256-wide K stage of packed
 //                 weights into the weight ring;
@@ -20,15 +23,16 @@
 //                 every weight stage (4 blocks of 64); warp (group g, quarter q)
 //                 unpacks rows 32q..32q+31 (its tensor-memory lane quarter) of
 //                 that block, 64 weights per thread, to fp16 and stores them with
-//                 one tcgen05.st into the A ring in tensor memory; the same warps
-//                 later drain the fp32 accumulator (tcgen05.ld) into y.
-// Tensor memory (512 columns): accumulator [128 lanes x BN] at column 0, an
-// 8-deep ring of A operand blocks (128 lanes x 64 K = 32 columns) at 256.
-// The MMA is D[128 x BN] += A[128 x 16] (tensor memory) . B[BN x 16]^T (shared
-// memory), so weights are the M side and tokens the N side: a tile reuses each
-// unpacked weight for BN tokens.  When the grid would leave SMs idle, K is split
-// across a thread-block cluster and the partial tiles are summed in rank order
-// through distributed shared memory.
+//                 one tcgen05.st into the A ring in tensor memory;
+//   warps 19..22  epilogue: drain the fp32 accumulator (tcgen05.ld) into y, or,
+//                 with split-K, into the owning CTA of the cluster, which sums
+//                 the partials in rank order (deterministic) and writes y.
+// Tensor memory (512 columns): the A ring (8 blocks of 128 lanes x 64 K = 32
+// columns) at column 256; below it one accumulator [128 lanes x BN], or two of
+// 128 columns when BN <= 128, so that the epilogue of a unit overlaps the MMAs of
+// the next.  The MMA is D[128 x BN] += A[128 x 16] (tensor memory) .
+// B[BN x 16]^T (shared memory): weights are the M side and tokens the N side, so
+// a tile reuses each unpacked weight for BN tokens.
 //
 // Every mbarrier wait is bounded: on expiry the thread records a timeout in
 // the library's status word and sets a CTA-wide abort flag; all roles then
@@ -47,7 +51,9 @@ namespace qwp {
 constexpr int XFORM_GROUPS = 4;                    // groups take K blocks in turn, one per weight stage
 constexpr int NUM_XFORM_WARPS = 4 * XFORM_GROUPS;  // 4 warps (one per lane quarter) cover one K block
 constexpr int FIRST_XFORM_WARP = 3;
-constexpr int NUM_THREADS = 32 * (FIRST_XFORM_WARP + NUM_XFORM_WARPS);
+constexpr int FIRST_EPI_WARP = FIRST_XFORM_WARP + NUM_XFORM_WARPS;
+constexpr int NUM_EPI_WARPS = 4;                   // one per tensor-memory lane quarter
+constexpr int NUM_THREADS = 32 * (FIRST_EPI_WARP + NUM_EPI_WARPS);
 constexpr int X_MAX_STAGES = 8;  // <= A_STAGES: the x ring reuses the mma_done ring (see below)
 constexpr int W_MAX_STAGES = 8;
 constexpr int A_STAGES = 8;
@@ -55,21 +61,22 @@ constexpr int BN_MAX = 256;
 constexpr int KB_PER_STAGE = 4;  // 64-wide K blocks per weight stage
 constexpr int MAX_SPLITS = 8;    // portable cluster size
 constexpr uint32_t ACC_COL = 0;
+constexpr uint32_t ACC_STRIDE = 128;  // second accumulator buffer (token tiles of <= 128)
 constexpr uint32_t A_COL = 256;
 constexpr uint32_t TMEM_COLS = 512;
 
-// Shared memory: a ring region (x stages, then weight stages; reused for the
-// split-K partial sums after the main loop), then the mbarriers and misc words.
+// Shared memory: a ring region (x slots, then weight stages, then, with split-K,
+// the buffer that receives the cluster's partial sums), then mbarriers and misc words.
 constexpr int RING_BYTES = 224 * 1024;
 constexpr int OFF_BAR = RING_BYTES;
-constexpr int NUM_BARS = 2 * X_MAX_STAGES + 2 * W_MAX_STAGES + 2 * A_STAGES + 2;
+constexpr int NUM_BARS = X_MAX_STAGES + 2 * W_MAX_STAGES + 2 * A_STAGES + 4 + 3;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(X_MAX_STAGES <= A_STAGES, "the x ring is released through the mma_done ring");
 static_assert(A_STAGES % 4 == 0, "commit groups of up to 4 blocks tile the A ring");
 static_assert(XFORM_GROUPS == KB_PER_STAGE, "each transform warp owns one K block of every weight stage");
-static_assert(512 * (BN_MAX + MAX_SPLITS) <= RING_BYTES, "split-K partials must fit the ring region");
+static_assert(2 * ACC_STRIDE <= A_COL, "two accumulator buffers of 128 columns fit below the A ring");
 
 struct GemmArgs {
     const uint8_t *w;       // repacked weights
@@ -87,13 +94,17 @@ struct GemmArgs {
     int kbg_shift;          // log2(kb_per_group) when it is a power of two, else -1
     int x_stage_bytes, w_stage_bytes;
     int cb_shift;           // log2(CB), CB = K blocks per commit group (1, 2 or 4; divides every split's blocks)
+    int n_units;            // row tiles x token tiles; cluster c runs units c, c + gridDim.x, ...
+    int row_tiles;
+    int acc_bufs;           // 2 when two accumulators fit (bn <= 128), else 1
+    int part_off;           // shared-memory offset of the split-K partial buffer
     uint64_t timeout_ns;
 };
 
 // Status codes recorded on a timeout: which wait gave up.
 enum : uint32_t {
     WAIT_W_EMPTY = 1, WAIT_X_EMPTY, WAIT_X_FULL, WAIT_A_FULL, WAIT_W_FULL, WAIT_A_EMPTY,
-    WAIT_ACC_FULL, WAIT_DRAIN
+    WAIT_ACC_FULL, WAIT_DRAIN, WAIT_ACC_EMPTY, WAIT_PART
 };
 
 struct Ctl {
@@ -107,12 +118,17 @@ struct Ctl {
 // records `where` in the status word.  The loop mostly sits in try_wait (which
 // suspends the thread in hardware); the clock and the global status word are
 // looked at only every 64 polls.
+// kLazy waits sleep between polls (roles off the critical path, which should
+// not take issue slots from the warps that are on it).
+template <bool kCluster = false, bool kLazy = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl &ctl,
                                          uint32_t where, bool honour_abort = true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto poll = [&] { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (poll()) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (kLazy) __nanosleep(256);
+        if (poll()) return true;
         if (honour_abort && *reinterpret_cast<volatile uint32_t *>(ctl.abort)) return false;
         if ((it & 63u) == 0) {
             if (honour_abort && (*reinterpret_cast<volatile uint32_t *>(ctl.status) & kStatusTimeoutMask)) {
@@ -126,6 +142,12 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
             }
         }
     }
+}
+
+// A wait on a barrier that peers of the cluster arrive on (acquire at cluster
+// scope), by the epilogue warps (lazy).
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, const Ctl &ctl, uint32_t where) {
+    return wait_bar<true, true>(bar, parity, ctl, where);
 }
 
 __device__ __forceinline__ bool aborted(const Ctl &ctl) {
@@ -159,9 +181,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t warp = warp_id();
     const uint32_t lane = lane_id();
 
-    const int tile = blockIdx.x;
-    const int R = tile_rows(args.N, tile);
-    const int m0 = blockIdx.y * args.bn;
+    // This CTA's K range (its cluster rank along K) is the same for every unit.
+    const int S = args.splits;
     const int nkb_total = args.K / CHUNK_K;
     const int kb_begin = blockIdx.z * args.kb_per_split;
     const int kb_end = min(nkb_total, kb_begin + args.kb_per_split);
@@ -170,30 +191,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int XS = args.x_stages, WS = args.w_stages;
     uint8_t *const x_ring = smem;
     uint8_t *const w_ring = smem + XS * args.x_stage_bytes;
+    const int nbufs = args.acc_bufs;
+    const int units0 = static_cast<int>(blockIdx.x);  // units units0, units0 + gridDim.x, ...
+    const int ustep = static_cast<int>(gridDim.x);
+    const int nunits = args.n_units;
+    const int n_mine = units0 < nunits ? (nunits - 1 - units0) / ustep + 1 : 0;  // units of this CTA
+    // Row tile and token tile of unit u: consecutive units share a token tile, so
+    // concurrently running CTAs read the same activation tile (one read, L2 hits);
+    // the packed weights are the smaller stream per unit.
+    auto unit_tile = [&](int u) { return u % args.row_tiles; };
+    auto unit_m0 = [&](int u) { return (u / args.row_tiles) * args.bn; };
 
     const uint32_t bar0 = smem_u32(smem + OFF_BAR);
     // The MMA issuer works in commit groups of CB = 2^cb_shift consecutive K blocks:
-    // one x_full wait (the group's CB x tiles share one ring slot and barrier), one
-    // a_full wait (every transform warp arrives once per group), 4*CB MMAs and one
-    // tcgen05.commit.  A single thread issues every MMA of the CTA, and its fixed
-    // cost per loop iteration (waits, fence, bookkeeping) is several hundred cycles
-    // on a busy SM, so it is paid per group rather than per 64-wide block.
-    // mma_done[(j % A_STAGES) >> cb_shift] completes when the MMAs of the group
-    // holding block j (and all before it) are done; that releases the group's A
-    // slots and its x slot (the x ring has at most A_STAGES / CB slots, so no phase
-    // of mma_done is skipped).
+    // one a_full wait (every transform warp of the group's blocks arrives), one
+    // x_full wait (the group's CB x tiles share one ring slot and barrier), 4*CB
+    // MMAs and one tcgen05.commit.  A single thread issues every MMA of the CTA,
+    // and its fixed cost per loop iteration (waits, fence, bookkeeping) is several
+    // hundred cycles on a busy SM, so it is paid per group rather than per block.
+    // mma_done[(J % A_STAGES) >> cb_shift] completes when the MMAs of the group
+    // holding the CTA's J-th block (counted over all its units) are done; that
+    // releases the group's A slots and its x slot (the x ring has at most
+    // A_STAGES / CB slots, so no phase of mma_done is skipped).
     const int cbs = args.cb_shift;
     const int dslots = A_STAGES >> cbs;  // commit-group slots of the A ring
     const int ngroups = nkb >> cbs;      // nkb is a multiple of CB
     const uint32_t x_full = bar0, mma_done = x_full + 8 * X_MAX_STAGES;
-    const uint32_t w_full = mma_done + 8 * X_MAX_STAGES, w_empty = w_full + 8 * W_MAX_STAGES;
-    const uint32_t a_full = w_empty + 8 * W_MAX_STAGES, unused = a_full + 8 * A_STAGES;
-    const uint32_t acc_full = unused + 8 * A_STAGES, drain = acc_full + 8;
+    const uint32_t w_full = mma_done + 8 * A_STAGES, w_empty = w_full + 8 * W_MAX_STAGES;
+    const uint32_t a_full = w_empty + 8 * W_MAX_STAGES, acc_full = a_full + 8 * A_STAGES;
+    const uint32_t acc_empty = acc_full + 16, part_full = acc_empty + 16, part_free = part_full + 8;
+    const uint32_t drain = part_free + 8;
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + OFF_MISC);  // [0] tmem base, [1] abort
     const Ctl ctl{misc + 1, args.status, args.timeout_ns};
 
-    // Copy of weight stage s (K blocks 4s.. of this CTA's range) into ring slot ws.
-    auto load_weight_stage = [&](int s, int ws) {
+    // Copy of weight stage s (K blocks kb_begin + 4s ..) of row tile `tile` into ring slot ws.
+    auto load_weight_stage = [&](int tile, int s, int ws) {
+        const int R = tile_rows(args.N, tile);
         const int kb0 = kb_begin + KB_PER_STAGE * s;
         const int nblk = min(KB_PER_STAGE, kb_end - kb0);
         const uint8_t *src;
@@ -209,8 +242,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bulk_copy_g2s(smem_u32(w_ring + ws * args.w_stage_bytes), src, bytes, w_full + 8 * ws);
     };
     // The weight producer's thread sets up the barriers and starts the first weight
-    // copies before the block-wide barrier (their slots are empty).
-    const int w_pre = min(WS, nstage);
+    // copies of its first unit before the block-wide barrier (their slots are empty).
+    const int w_pre = units0 < nunits ? min(WS, nstage) : 0;
     if (threadIdx.x == 64) {
         for (int s = 0; s < X_MAX_STAGES; ++s) mbar_init(x_full + 8 * s, 1);
         for (int s = 0; s < A_STAGES; ++s) mbar_init(mma_done + 8 * s, 1);
@@ -221,7 +254,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // A commit group of CB <= XFORM_GROUPS blocks is stored by CB transform groups.
         for (int s = 0; s < A_STAGES; ++s)
             mbar_init(a_full + 8 * s, (NUM_XFORM_WARPS / XFORM_GROUPS) << cbs);
-        mbar_init(acc_full, 1);
+        // The accumulator is drained by the transform warps when there is one, by
+        // the epilogue warps when there are two.
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full + 8 * b, 1);
+            mbar_init(acc_empty + 8 * b, nbufs == 2 ? NUM_EPI_WARPS : NUM_XFORM_WARPS);
+        }
+        // Split-K: every epilogue warp of every CTA of the cluster arrives once per unit.
+        mbar_init(part_full, NUM_EPI_WARPS * S);
+        mbar_init(part_free, NUM_EPI_WARPS * S);
         mbar_init(drain, 1);
         // A failure recorded earlier (and not yet read by qwp_device_status) makes
         // every later launch skip its work instead of waiting out its own timeouts.
@@ -230,7 +271,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         fence_mbar_init();
         prefetch_tensormap(&tmap_x);
         if (!failed)
-            for (int s = 0; s < w_pre; ++s) load_weight_stage(s, s);
+            for (int s = 0; s < w_pre; ++s) load_weight_stage(unit_tile(units0), s, s);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(misc), TMEM_COLS);
@@ -238,10 +279,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_before();
     }
     __syncthreads();
+    // Before its last unit a CTA's epilogue warps push split-K partials into peers
+    // and arrive on their barriers, which must be initialised cluster-wide first.
+    // (The last unit is reduced behind cluster barriers of its own.)
+    if (S > 1 && n_mine > 1) cluster_sync();
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const bool skip = misc[1] != 0;
-    bool acc_ok = false;  // transform warps: the accumulator is complete
+    bool xform_ok = false;  // transform warps: every unit's blocks were stored
 
     if (warp == 0) {
         // ------------------------------------------------------------ x producer
@@ -249,22 +294,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // x may be written by the grid launched just before this one (the
             // activation conversion); nothing else here depends on it.
             asm volatile("griddepcontrol.wait;" ::: "memory");
-            int issued = 0;
+            int issued = 0;     // groups issued over all units
             int xs = 0;         // ring slot (running counters: no division in the loop)
-            int dk = 0;         // mma_done slot of group g - XS, and its phase
+            int dk = 0;         // mma_done slot of group `issued - XS`, and its phase
             uint32_t dph = 0;
+            bool ok = true;
             const uint32_t tile_bytes = static_cast<uint32_t>(args.bn) * 128u;
-            for (int g = 0; g < ngroups; ++g) {
-                if (g >= XS) {  // slot xs last held group g - XS
-                    if (!wait_bar(mma_done + 8 * dk, dph, ctl, WAIT_X_EMPTY)) break;
-                    if (++dk == dslots) { dk = 0; dph ^= 1; }
+            for (int u = units0; ok && u < nunits; u += ustep) {
+                const int m0 = unit_m0(u);
+                for (int g = 0; g < ngroups; ++g) {
+                    if (issued >= XS) {  // slot xs last held group issued - XS
+                        if (!(ok = wait_bar(mma_done + 8 * dk, dph, ctl, WAIT_X_EMPTY))) break;
+                        if (++dk == dslots) { dk = 0; dph ^= 1; }
+                    }
+                    mbar_arrive_expect_tx(x_full + 8 * xs, tile_bytes << cbs);
+                    for (int c = 0; c < (1 << cbs); ++c)
+                        tma_load_2d(smem_u32(x_ring + xs * args.x_stage_bytes + c * tile_bytes), &tmap_x,
+                                    (kb_begin + (g << cbs) + c) * CHUNK_K, m0, x_full + 8 * xs);
+                    ++issued;
+                    if (++xs == XS) xs = 0;
                 }
-                mbar_arrive_expect_tx(x_full + 8 * xs, tile_bytes << cbs);
-                for (int c = 0; c < (1 << cbs); ++c)
-                    tma_load_2d(smem_u32(x_ring + xs * args.x_stage_bytes + c * tile_bytes), &tmap_x,
-                                (kb_begin + (g << cbs) + c) * CHUNK_K, m0, x_full + 8 * xs);
-                issued = g + 1;
-                if (++xs == XS) xs = 0;
             }
             // Every copy issued above lands before the CTA may exit.
             for (int g = max(0, issued - XS); g < issued; ++g)
@@ -273,14 +322,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 2) {
         // ------------------------------------------------------------ weight producer
         if (lane == 0 && !skip) {
-            int issued = w_pre;  // stages 0 .. w_pre-1 went out before the block-wide barrier
+            int issued = 0;  // stages over all units; the first w_pre went out above
             int ws = 0;
-            uint32_t wph = 1;    // stage w_pre reuses slot 0 (second use: wait for its first release)
-            for (int s = w_pre; s < nstage; ++s) {
-                if (!wait_bar(w_empty + 8 * ws, wph ^ 1, ctl, WAIT_W_EMPTY)) break;
-                load_weight_stage(s, ws);
-                issued = s + 1;
-                if (++ws == WS) { ws = 0; wph ^= 1; }
+            uint32_t wph = 0;
+            bool ok = true;
+            for (int u = units0; ok && u < nunits; u += ustep) {
+                const int tile = unit_tile(u);
+                for (int s = 0; s < nstage; ++s) {
+                    if (issued >= w_pre) {
+                        if (issued >= WS && !(ok = wait_bar(w_empty + 8 * ws, wph ^ 1, ctl, WAIT_W_EMPTY))) break;
+                        load_weight_stage(tile, s, ws);
+                    }
+                    ++issued;
+                    if (++ws == WS) { ws = 0; wph ^= 1; }
+                }
             }
             for (int s = max(0, issued - WS); s < issued; ++s)
                 wait_bar(w_full + 8 * (s % WS), (s / WS) & 1, ctl, WAIT_DRAIN, false);
@@ -293,197 +348,385 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int xs = 0, gs = 0;       // x ring slot; commit-group slot of the A ring
             uint32_t xph = 0, gph = 0;
             const uint32_t tile_desc = static_cast<uint32_t>(args.bn) * 128u >> 4;  // one x tile, in descriptor units
-            for (int g = 0; g < ngroups; ++g) {
-                ok = wait_bar(x_full + 8 * xs, xph, ctl, WAIT_X_FULL) &&
-                     wait_bar(a_full + 8 * gs, gph, ctl, WAIT_A_FULL);
-                if (!ok) break;
+            int it = 0;
+            for (int u = units0; ok && u < nunits; u += ustep, ++it) {
+                // The unit accumulates into buffer b once the epilogue has drained b.
+                const int b = nbufs == 2 ? (it & 1) : 0;
+                const int use = nbufs == 2 ? (it >> 1) : it;  // earlier uses of buffer b
+                if (!(ok = wait_bar(acc_empty + 8 * b, (use & 1) ^ 1, ctl, WAIT_ACC_EMPTY))) break;
                 tc_fence_after();
-                uint64_t bdesc = smem_desc_sw128(smem_u32(x_ring + xs * args.x_stage_bytes));
-                uint32_t acol = tmem + A_COL + (32u << cbs) * gs;
-                for (int c = 0; c < (1 << cbs); ++c, bdesc += tile_desc, acol += 32u) {
+                const uint32_t dcol = tmem + ACC_COL + ACC_STRIDE * static_cast<uint32_t>(b);
+                for (int g = 0; g < ngroups; ++g) {
+                    ok = wait_bar(x_full + 8 * xs, xph, ctl, WAIT_X_FULL) &&
+                         wait_bar(a_full + 8 * gs, gph, ctl, WAIT_A_FULL);
+                    if (!ok) break;
+                    tc_fence_after();
+                    uint64_t bdesc = smem_desc_sw128(smem_u32(x_ring + xs * args.x_stage_bytes));
+                    uint32_t acol = tmem + A_COL + (32u << cbs) * gs;
+                    for (int c = 0; c < (1 << cbs); ++c, bdesc += tile_desc, acol += 32u) {
 #pragma unroll
-                    for (int kk = 0; kk < CHUNK_K / 16; ++kk)
-                        mma_ts(tmem + ACC_COL, acol + 8u * kk, bdesc + 2u * kk, idesc, (g | c | kk) != 0);
+                        for (int kk = 0; kk < CHUNK_K / 16; ++kk)
+                            mma_ts(dcol, acol + 8u * kk, bdesc + 2u * kk, idesc, (g | c | kk) != 0);
+                    }
+                    mma_commit(mma_done + 8 * gs);
+                    if (++xs == XS) { xs = 0; xph ^= 1; }
+                    if (++gs == dslots) { gs = 0; gph ^= 1; }
                 }
-                mma_commit(mma_done + 8 * gs);
-                if (++xs == XS) { xs = 0; xph ^= 1; }
-                if (++gs == dslots) { gs = 0; gph ^= 1; }
+                if (ok) mma_commit(acc_full + 8 * b);
             }
-            if (ok) {
-                mma_commit(acc_full);
-            } else {
+            if (!ok) {
                 mma_commit(drain);
                 wait_bar(drain, 0, ctl, WAIT_DRAIN, false);
             }
         }
-    } else {
-        // ------------------------------------------------------------ transform + epilogue
+    } else if (warp < FIRST_EPI_WARP) {
+        // ------------------------------------------------------------ transform
         const uint32_t xw = warp - FIRST_XFORM_WARP;
-        const int grp = static_cast<int>(xw >> 2);   // this warp's K blocks: j % XFORM_GROUPS == grp
+        const int grp = static_cast<int>(xw >> 2);   // this warp's block of every weight stage
         const uint32_t quarter = warp & 3;            // tensor-memory lanes 32*quarter .. +31
         const int r = static_cast<int>(quarter * 32 + lane);
-        const bool valid = r < R;
-        const int64_t n = static_cast<int64_t>(tile) * TILE_ROWS + r;
         const uint32_t lane_base = (quarter * 32u) << 16;
         bool ok = !skip;
         int ws = -1;       // weight ring slot of this warp's current stage, and its phase
         uint32_t wph = 0;
 
-        // Unpack K block j (the block of weight stage j / 4 that this warp owns) of
-        // this thread's row into `regs`: 64 weights as 32 fp16 pairs.  Waits for the
-        // stage and releases it after reading (the warp reads nothing else of it).
-        auto prepare = [&](int j, uint32_t (&regs)[32]) -> bool {
-            const int c = j & (KB_PER_STAGE - 1);
+        // Weight stage s of row tile `tile`: wait for it; if it holds this warp's block
+        // (block 4s + grp of the CTA's range; a short last stage may not), unpack the
+        // thread's row of it into `regs` (64 weights as 32 fp16 pairs); release the
+        // stage.  Returns false on timeout or abort.
+        auto prepare = [&](int tile, int s, uint32_t (&regs)[32], bool &has_block) -> bool {
             if (++ws == WS) { ws = 0; wph ^= 1; }
             const uint8_t *wst = w_ring + ws * args.w_stage_bytes;
             // Every lane waits; the warp moves on together (tcgen05.st/ld are warp-collective).
             if (!__all_sync(0xffffffffu, wait_bar(w_full + 8 * ws, wph, ctl, WAIT_W_FULL))) return false;
+            const int R = tile_rows(args.N, tile);
+            const bool valid = r < R;
+            const int jj = KB_PER_STAGE * s + grp;  // block index within the CTA's range
+            has_block = jj < nkb;
             uint4 wv0 = make_uint4(0, 0, 0, 0), wv1 = make_uint4(0, 0, 0, 0);
             Q4kSubH k0, k1;
             __half2 s2 = __float2half2_rn(0.f), mz = w4_magic_zero(0);
-            if (kQ4K) {
-                uint4 hdr = make_uint4(0, 0, 0, 0);
-                if (valid) {
-                    hdr = *reinterpret_cast<const uint4 *>(wst + Q4K_HEADER_BYTES * r);
-                    const uint8_t *cp = wst + Q4K_HEADER_BYTES * R + CHUNK_ROW_BYTES * R * c + r * 16;
+            if (has_block) {
+                if (kQ4K) {
+                    uint4 hdr = make_uint4(0, 0, 0, 0);
+                    if (valid) {
+                        hdr = *reinterpret_cast<const uint4 *>(wst + Q4K_HEADER_BYTES * r);
+                        const uint8_t *cp = wst + Q4K_HEADER_BYTES * R + CHUNK_ROW_BYTES * R * grp + r * 16;
+                        wv0 = *reinterpret_cast<const uint4 *>(cp);
+                        wv1 = *reinterpret_cast<const uint4 *>(cp + 16 * R);
+                    }
+                    k0 = q4k_sub_f16(hdr, 2 * grp);
+                    k1 = q4k_sub_f16(hdr, 2 * grp + 1);
+                } else if (valid) {
+                    const uint8_t *cp = wst + CHUNK_ROW_BYTES * R * grp + r * 16;
                     wv0 = *reinterpret_cast<const uint4 *>(cp);
                     wv1 = *reinterpret_cast<const uint4 *>(cp + 16 * R);
+                    const int64_t n = static_cast<int64_t>(tile) * TILE_ROWS + r;
+                    const int64_t ng = args.groups_per_row;
+                    const int kbi = kb_begin + jj;
+                    const int64_t g = args.kbg_shift >= 0 ? (kbi >> args.kbg_shift) : (kbi / args.kb_per_group);
+                    s2 = __half2half2(args.scales[n * ng + g]);
+                    mz = w4_magic_zero(args.zeros[n * ng + g]);
                 }
-                k0 = q4k_sub_f16(hdr, 2 * c);
-                k1 = q4k_sub_f16(hdr, 2 * c + 1);
-            } else if (valid) {
-                const uint8_t *cp = wst + CHUNK_ROW_BYTES * R * c + r * 16;
-                wv0 = *reinterpret_cast<const uint4 *>(cp);
-                wv1 = *reinterpret_cast<const uint4 *>(cp + 16 * R);
-                const int64_t ng = args.groups_per_row;
-                const int kbi = kb_begin + j;
-                const int64_t g = args.kbg_shift >= 0 ? (kbi >> args.kbg_shift) : (kbi / args.kb_per_group);
-                s2 = __half2half2(args.scales[n * ng + g]);
-                mz = w4_magic_zero(args.zeros[n * ng + g]);
             }
             // This warp's reads of the stage are done.
             __syncwarp();
             if (lane == 0) mbar_arrive(w_empty + 8 * ws);
-            unpack_quarter<kQ4K>(wv0, k0, mz, s2, regs, 0);
-            unpack_quarter<kQ4K>(wv1, k1, mz, s2, regs, 16);
+            if (has_block) {
+                unpack_quarter<kQ4K>(wv0, k0, mz, s2, regs, 0);
+                unpack_quarter<kQ4K>(wv1, k1, mz, s2, regs, 16);
+            }
             return true;
         };
-        // Store block j into its A ring slot once the MMAs of the block that last
-        // used the slot (j - A_STAGES) are done.
-        auto issue = [&](int j, const uint32_t (&regs)[32]) -> bool {
-            const int as = j % A_STAGES;
-            if (!__all_sync(0xffffffffu,
-                            wait_bar(mma_done + 8 * (as >> cbs), ((j / A_STAGES) & 1) ^ 1, ctl, WAIT_A_EMPTY)))
+        // Store the CTA's J-th block into its A ring slot once the MMAs of block
+        // J - A_STAGES (the slot's previous content) are done.
+        auto issue = [&](int J, const uint32_t (&regs)[32]) -> bool {
+            const int as = J & (A_STAGES - 1);
+            if (!__all_sync(0xffffffffu, wait_bar(mma_done + 8 * (as >> cbs), ((J / A_STAGES) & 1) ^ 1, ctl,
+                                                  WAIT_A_EMPTY)))
                 return false;
             tc_fence_after();
             tmem_st_x32(tmem + lane_base + A_COL + 32u * as, regs);
             return true;
         };
-        // Block j's tensor-memory store lands; publish it to the MMA issuer.
-        auto finish = [&](int j) {
+        // Block J's tensor-memory store lands; publish it to the MMA issuer.
+        auto finish = [&](int J) {
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(a_full + 8 * ((j % A_STAGES) >> cbs));
+            if (lane == 0) mbar_arrive(a_full + 8 * ((J & (A_STAGES - 1)) >> cbs));
         };
 
-        // This warp's blocks are j = grp, grp + 4, ...: one per weight stage.  The
-        // unpack of the next block overlaps the tensor-memory store of the current one.
-        // (The first block is published before the next one is unpacked, so that the
-        // MMAs can start as early as possible.)
-        uint32_t regs[32];
-        if (ok && grp < nkb) ok = prepare(grp, regs);
-        for (int j = grp; ok && j < nkb; j += XFORM_GROUPS) {
-            if (!(ok = issue(j, regs))) break;
-            if (j == grp) finish(j);
-            if (j + XFORM_GROUPS < nkb && !(ok = prepare(j + XFORM_GROUPS, regs))) break;
-            if (j != grp) finish(j);
-        }
-        tmem_wait_st();  // no tensor-memory store may be in flight past this point
-        __syncwarp();
-        acc_ok = ok && __all_sync(0xffffffffu, wait_bar(acc_full, 0, ctl, WAIT_ACC_FULL));
-        if (acc_ok && args.splits == 1) {
+        // With one accumulator the transform warps drain it into y between units
+        // (the MMAs of the next unit wait for that anyway): unit `uu`, the CTA's
+        // `itx`-th, split-K never applies (it needs two accumulators).
+        auto drain_unit = [&](int uu, int itx) -> bool {
+            if (!__all_sync(0xffffffffu, wait_bar(acc_full, itx & 1, ctl, WAIT_ACC_FULL))) return false;
             tc_fence_after();
-            for (int ci = grp; ci < args.bn / 16; ci += NUM_XFORM_WARPS / 4) {
-                uint32_t v[16];
-                tmem_ld_x16(tmem + lane_base + ACC_COL + 16u * ci, v);
+            const int tile = unit_tile(uu), m0 = unit_m0(uu);
+            const int R = tile_rows(args.N, tile);
+            const int64_t n = static_cast<int64_t>(tile) * TILE_ROWS + r;
+            // 8 columns at a time: this warp's 32 unpacked weights stay live meanwhile.
+            for (int ci = grp; ci < args.bn / 8; ci += NUM_XFORM_WARPS / 4) {
+                uint32_t v[8];
+                tmem_ld_x8(tmem + lane_base + ACC_COL + 8u * ci, v);
                 tmem_wait_ld();
-                if (valid) {
-                    const int mb = m0 + 16 * ci;
+                if (r < R) {
+                    const int mb = m0 + 8 * ci;
 #pragma unroll
-                    for (int t = 0; t < 16; ++t)
+                    for (int t = 0; t < 8; ++t)
                         if (mb + t < args.M)
                             __stcs(args.y + static_cast<int64_t>(mb + t) * args.N + n, __uint_as_float(v[t]));
                 }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+            return true;
+        };
+
+        // The warp walks the weight stages of all its units in order; per stage it
+        // owns at most one block.  A block is stored (issue) before the next stage is
+        // unpacked into the same registers, and published (finish) after that, so the
+        // unpack overlaps the tensor-memory store; the very first block is published
+        // at once so that the MMAs can start early.
+        uint32_t regs[32];
+        bool have = false, pend = false;  // regs hold block have_J; block pend_J is stored, unpublished
+        int have_J = 0, pend_J = 0;
+        bool first = true;
+        int it = 0;
+        for (int u = units0; ok && u < nunits; u += ustep, ++it) {
+            const int tile = unit_tile(u);
+            for (int s = 0; s < nstage; ++s) {
+                if (have) {
+                    if (!(ok = issue(have_J, regs))) break;
+                    if (first) {
+                        finish(have_J);
+                        first = false;
+                    } else {
+                        pend = true;
+                        pend_J = have_J;
+                    }
+                    have = false;
+                }
+                bool nb = false;
+                if (!(ok = prepare(tile, s, regs, nb))) break;
+                if (pend) {
+                    finish(pend_J);
+                    pend = false;
+                }
+                // One accumulator: the previous unit is complete once its last block
+                // (just published) has gone through the MMAs; drain it while this
+                // unit's first block waits in registers.
+                if (nbufs == 1 && s == 0 && it > 0 && !(ok = drain_unit(u - ustep, it - 1))) break;
+                if (nb) {
+                    have = true;
+                    have_J = it * nkb + KB_PER_STAGE * s + grp;
+                }
+            }
+        }
+        if (ok && have && (ok = issue(have_J, regs))) finish(have_J);
+        if (ok && nbufs == 1 && it > 0) ok = drain_unit(units0 + (it - 1) * ustep, it - 1);
+        xform_ok = ok;
+        tmem_wait_st();  // no tensor-memory store may be in flight past this point
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const uint32_t quarter = warp & 3;
+        const int row = static_cast<int>(quarter * 32 + lane);
+        const uint32_t lane_base = (quarter * 32u) << 16;
+        const uint32_t rank = S > 1 ? cluster_ctarank() : 0u;
+        const int per = (args.bn + S - 1) / S;  // tokens owned by each cluster rank
+        const uint32_t part = smem_u32(smem + args.part_off);
+        // Two accumulators: these warps finish every unit but the CTA's last one
+        // (which all transform warps finish together after the main loop).
+        bool ok = !skip && nbufs == 2;
+        int it = 0;
+        for (int u = units0; ok && u + ustep < nunits; u += ustep, ++it) {
+            const int tile = unit_tile(u), m0 = unit_m0(u);
+            const int R = tile_rows(args.N, tile);
+            const int b = nbufs == 2 ? (it & 1) : 0;
+            const int use = nbufs == 2 ? (it >> 1) : it;
+            if (!(ok = __all_sync(0xffffffffu, wait_bar<false, true>(acc_full + 8 * b, use & 1, ctl, WAIT_ACC_FULL))))
+                break;
+            tc_fence_after();
+            const uint32_t dcol = tmem + lane_base + ACC_COL + ACC_STRIDE * static_cast<uint32_t>(b);
+            if (S == 1) {
+                const int64_t n = static_cast<int64_t>(tile) * TILE_ROWS + row;
+                for (int c0 = 0; c0 < args.bn; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld_x16(dcol + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
+                    const bool two = c0 + 16 < args.bn;
+                    if (two) tmem_ld_x16(dcol + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+                    tmem_wait_ld();
+                    if (row < R) {
+                        float *yc = args.y + static_cast<int64_t>(m0 + c0) * args.N + n;
+                        const int nt = min(two ? 32 : 16, args.M - (m0 + c0));
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            if (t < nt) __stcs(yc + static_cast<int64_t>(t) * args.N, __uint_as_float(v[t]));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty + 8 * b);
+            } else {
+                // Split-K through distributed shared memory.  Rank q owns tokens
+                // [q*per, q*per + per) of the tile.  Each CTA pushes its partial for
+                // every token into the owner's buffer [source rank][token][row] once the
+                // owners have consumed the previous unit (part_free), then tells the
+                // owners (part_full); each owner sums its tokens over the source ranks
+                // in rank order (deterministic) and writes y.
+                if (it > 0 && !(ok = __all_sync(0xffffffffu, wait_bar_cluster(part_free, (it - 1) & 1, ctl, WAIT_PART))))
+                    break;
+                for (int c0 = 0; c0 < args.bn; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld_x16(dcol + c0, v);
+                    tmem_wait_ld();
+                    int owner = c0 / per, tt = c0 - owner * per;
+                    uint32_t dst = map_shared_rank(part, owner);
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        st_shared_cluster_f32(dst + static_cast<uint32_t>(((static_cast<int>(rank) * per + tt) * TILE_ROWS + row) * 4),
+                                              __uint_as_float(v[t]));
+                        if (++tt == per && t < 15) {
+                            tt = 0;
+                            dst = map_shared_rank(part, ++owner);
+                        }
+                    }
+                }
+                tc_fence_before();
+                fence_acq_rel_cluster();  // every lane's remote stores before lane 0's release
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(acc_empty + 8 * b);
+                    for (int q = 0; q < S; ++q) mbar_arrive_remote(map_shared_rank(part_full, q));
+                }
+                if (!(ok = __all_sync(0xffffffffu, wait_bar_cluster(part_full, it & 1, ctl, WAIT_PART)))) break;
+                const int t0 = min(args.bn, static_cast<int>(rank) * per);
+                const int t1 = min(args.bn, t0 + per);
+                const float *pbuf = reinterpret_cast<const float *>(smem + args.part_off);
+                const int items = (t1 - t0) * (TILE_ROWS / 4);
+                const int et = static_cast<int>((warp - FIRST_EPI_WARP) * 32 + lane);
+                for (int itm = et; itm < items; itm += NUM_EPI_WARPS * 32) {
+                    const int tt = itm / (TILE_ROWS / 4);
+                    const int r4 = 4 * (itm % (TILE_ROWS / 4));
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int q = 0; q < S; ++q) {
+                        const float4 pv = *reinterpret_cast<const float4 *>(pbuf + (q * per + tt) * TILE_ROWS + r4);
+                        acc.x += pv.x; acc.y += pv.y; acc.z += pv.z; acc.w += pv.w;
+                    }
+                    const int m = m0 + t0 + tt;
+                    if (m < args.M) {
+                        float *yr = args.y + static_cast<int64_t>(m) * args.N + static_cast<int64_t>(tile) * TILE_ROWS;
+                        const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (r4 + e < R) __stcs(yr + r4 + e, a4[e]);
+                    }
+                }
+                // The buffer may be refilled once every epilogue warp here has read it.
+                fence_acq_rel_cluster();
+                __syncwarp();
+                if (lane == 0)
+                    for (int q = 0; q < S; ++q) mbar_arrive_remote(map_shared_rank(part_free, q));
             }
         }
         tc_fence_before();
     }
 
     __syncthreads();
-    if (args.splits > 1) {
-        // Deterministic split-K reduction through distributed shared memory.  CTA
-        // `rank` of the cluster owns tokens [rank*per, rank*per + per) of the tile.
-        // Once every CTA is past its main loop (its ring region is free), each CTA
-        // pushes its partial accumulator for every token straight from tensor memory
-        // into the owner's ring region, laid out [source rank][token][row]; after the
-        // second cluster barrier each owner sums its tokens over the source ranks in
-        // rank order and writes y.  Every CTA reaches both barriers whatever happened
-        // above (all waits before them are bounded).
-        const int S = args.splits;
-        const uint32_t rank = cluster_ctarank();
-        const int per = (args.bn + S - 1) / S;
-        const uint32_t buf = smem_u32(smem);
-        cluster_sync();
-        if (acc_ok && !aborted(ctl)) {
-            tc_fence_after();
-            const uint32_t xw = warp - FIRST_XFORM_WARP;
-            const uint32_t quarter = warp & 3;
-            const int row = static_cast<int>(quarter * 32 + lane);
-            const uint32_t lane_base = (quarter * 32u) << 16;
-            for (int ci = static_cast<int>(xw >> 2); ci < args.bn / 16; ci += NUM_XFORM_WARPS / 4) {
-                uint32_t v[16];
-                tmem_ld_x16(tmem + lane_base + ACC_COL + 16u * ci, v);
-                tmem_wait_ld();
-                int owner = (16 * ci) / per, tt = 16 * ci - owner * per;
-                uint32_t dst = map_shared_rank(buf, owner);
+    // Two accumulators: the CTA's last unit, finished by the transform warps (all
+    // other roles are done).  With split-K the epilogue warps of every CTA of the
+    // cluster are past all earlier units once the first cluster barrier completes,
+    // so the partial buffers are free; the partials are pushed as above, and after
+    // the second barrier every CTA sums its share in rank order and writes y.
+    if (nbufs == 2 && n_mine > 0) {
+        const int lit = n_mine - 1;
+        const int lu = units0 + lit * ustep;
+        const int tile = unit_tile(lu), m0 = unit_m0(lu);
+        const int R = tile_rows(args.N, tile);
+        const int b = lit & 1;
+        const bool xf = warp >= FIRST_XFORM_WARP && warp < FIRST_EPI_WARP;
+        const uint32_t xw = warp - FIRST_XFORM_WARP;
+        const int grp = static_cast<int>(xw >> 2);
+        const uint32_t quarter = warp & 3;
+        const int row = static_cast<int>(quarter * 32 + lane);
+        const uint32_t dcol = tmem + ((quarter * 32u) << 16) + ACC_COL + ACC_STRIDE * static_cast<uint32_t>(b);
+        bool acc_ok = false;
+        if (xf && xform_ok)
+            acc_ok = __all_sync(0xffffffffu, wait_bar(acc_full + 8 * b, (lit >> 1) & 1, ctl, WAIT_ACC_FULL));
+        if (S == 1) {
+            if (acc_ok) {
+                tc_fence_after();
+                const int64_t n = static_cast<int64_t>(tile) * TILE_ROWS + row;
+                for (int ci = grp; ci < args.bn / 16; ci += NUM_XFORM_WARPS / 4) {
+                    uint32_t v[16];
+                    tmem_ld_x16(dcol + 16u * ci, v);
+                    tmem_wait_ld();
+                    if (row < R) {
+                        const int mb = m0 + 16 * ci;
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    st_shared_cluster_f32(dst + static_cast<uint32_t>(((static_cast<int>(rank) * per + tt) * TILE_ROWS + row) * 4),
-                                          __uint_as_float(v[t]));
-                    if (++tt == per && t < 15) {
-                        tt = 0;
-                        dst = map_shared_rank(buf, ++owner);
+                        for (int t = 0; t < 16; ++t)
+                            if (mb + t < args.M)
+                                __stcs(args.y + static_cast<int64_t>(mb + t) * args.N + n, __uint_as_float(v[t]));
                     }
                 }
+                tc_fence_before();
             }
-            tc_fence_before();
-        }
-        cluster_sync();
-        const int t0 = min(args.bn, static_cast<int>(rank) * per);
-        const int t1 = min(args.bn, t0 + per);
-        if (!aborted(ctl)) {
-            const float *part = reinterpret_cast<const float *>(smem);
-            const int items = (t1 - t0) * (TILE_ROWS / 4);
-            for (int it = threadIdx.x; it < items; it += NUM_THREADS) {
-                const int tt = it / (TILE_ROWS / 4);
-                const int r4 = 4 * (it % (TILE_ROWS / 4));
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int q = 0; q < S; ++q) {
-                    const float4 v = *reinterpret_cast<const float4 *>(part + (q * per + tt) * TILE_ROWS + r4);
-                    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-                }
-                const int m = m0 + t0 + tt;
-                if (m < args.M) {
-                    float *yr = args.y + static_cast<int64_t>(m) * args.N + static_cast<int64_t>(tile) * TILE_ROWS;
-                    const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+        } else {
+            const uint32_t rank = cluster_ctarank();
+            const int per = (args.bn + S - 1) / S;
+            const uint32_t part = smem_u32(smem + args.part_off);
+            cluster_sync();
+            if (acc_ok && !aborted(ctl)) {
+                tc_fence_after();
+                for (int ci = grp; ci < args.bn / 16; ci += NUM_XFORM_WARPS / 4) {
+                    uint32_t v[16];
+                    tmem_ld_x16(dcol + 16u * ci, v);
+                    tmem_wait_ld();
+                    int owner = (16 * ci) / per, tt = 16 * ci - owner * per;
+                    uint32_t dst = map_shared_rank(part, owner);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if (r4 + e < R) __stcs(yr + r4 + e, a4[e]);
+                    for (int t = 0; t < 16; ++t) {
+                        st_shared_cluster_f32(dst + static_cast<uint32_t>(((static_cast<int>(rank) * per + tt) * TILE_ROWS + row) * 4),
+                                              __uint_as_float(v[t]));
+                        if (++tt == per && t < 15) {
+                            tt = 0;
+                            dst = map_shared_rank(part, ++owner);
+                        }
+                    }
+                }
+                tc_fence_before();
+            }
+            cluster_sync();
+            const int t0 = min(args.bn, static_cast<int>(rank) * per);
+            const int t1 = min(args.bn, t0 + per);
+            if (!aborted(ctl)) {
+                const float *pbuf = reinterpret_cast<const float *>(smem + args.part_off);
+                const int items = (t1 - t0) * (TILE_ROWS / 4);
+                for (int itm = threadIdx.x; itm < items; itm += NUM_THREADS) {
+                    const int tt = itm / (TILE_ROWS / 4);
+                    const int r4 = 4 * (itm % (TILE_ROWS / 4));
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int q = 0; q < S; ++q) {
+                        const float4 pv = *reinterpret_cast<const float4 *>(pbuf + (q * per + tt) * TILE_ROWS + r4);
+                        acc.x += pv.x; acc.y += pv.y; acc.z += pv.z; acc.w += pv.w;
+                    }
+                    const int m = m0 + t0 + tt;
+                    if (m < args.M) {
+                        float *yr = args.y + static_cast<int64_t>(m) * args.N + static_cast<int64_t>(tile) * TILE_ROWS;
+                        const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (r4 + e < R) __stcs(yr + r4 + e, a4[e]);
+                    }
                 }
             }
         }
     }
+    // (With split-K the last unit's second cluster barrier above is the last point
+    // at which peers touch this CTA: no further barrier is needed before exit.)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
@@ -526,9 +769,9 @@ static int encode_x_map(CUtensorMap *map, const void *x, int64_t M, int64_t K, i
     return r == CUDA_SUCCESS ? QWP_OK : QWP_ERR_CUDA;
 }
 
-// Token tile: the fewest tiles of at most 256 tokens, each a multiple of 16.
-static int choose_bn(int64_t M) {
-    const int64_t tiles = (M + BN_MAX - 1) / BN_MAX;
+// Token tile: the fewest tiles of at most `cap` tokens, each a multiple of 16.
+static int choose_bn(int64_t M, int cap) {
+    const int64_t tiles = (M + cap - 1) / cap;
     const int64_t per = (M + tiles - 1) / tiles;
     return static_cast<int>((per + 15) / 16 * 16);
 }
@@ -579,20 +822,63 @@ static int device_info(DeviceInfo *&out) {
     return QWP_OK;
 }
 
-// Split-K factor: model the time as (waves of resident CTAs) x (fixed cost of
-// two weight stages + the K stages per split) and take the cheapest.
-static int choose_splits(const int *slots, int64_t base_ctas, int nstages) {
-    int best = 1;
-    double best_cost = 1e30;
+// Launch plan of one GEMM: split-K factor S (cluster size), number of resident
+// clusters, commit-group size and the shared-memory layout.
+struct Plan {
+    int S = 1, clusters = 0, cbs = 0, x_stages = 0, w_stages = 0, part_off = 0;
+    double cost = 1e30;
+};
+
+// Shared-memory layout for a given split and commit-group size; false if the
+// rings would be too shallow.  The split-K partial buffer gets space of its own
+// only when CTAs run several units (`reserve`); with one unit per CTA it overlays
+// the rings, which are idle by the time partials arrive.
+static bool layout(int bn, int S, int cbs, int w_stage_bytes, bool reserve, Plan &p) {
+    const int x_stage = (bn * 128) << cbs;
+    int avail = RING_BYTES;
+    if (S > 1 && reserve) {
+        const int per = (bn + S - 1) / S;
+        const int part_bytes = S * per * TILE_ROWS * 4;
+        avail = (RING_BYTES - part_bytes) & ~1023;
+    }
+    // Keep room for 4 weight stages if the x ring still gets 2 slots, else for 2.
+    int xs = std::min(A_STAGES >> cbs, (avail - 4 * w_stage_bytes) / x_stage);
+    if (xs < 2) xs = std::min(A_STAGES >> cbs, (avail - 2 * w_stage_bytes) / x_stage);
+    if (xs < 2 && !(xs == 1 && cbs == 0)) return false;
+    if (xs < 1) return false;
+    const int ws = std::min(W_MAX_STAGES, (avail - xs * x_stage) / w_stage_bytes);
+    if (ws < 2) return false;
+    p.cbs = cbs;
+    p.x_stages = xs;
+    p.w_stages = ws;
+    p.part_off = (S > 1 && reserve) ? avail : 0;
+    return true;
+}
+
+// Units are (row tile, token tile) pairs; a cluster of S CTAs splits each unit's
+// K range S ways and the clusters loop over the units.  Time is modelled as
+// (rounds of units per cluster) x (weight stages per CTA and unit + a small
+// per-unit cost), plus a fixed cost for the reduction when S > 1; the cheapest
+// plan wins.  Commit groups are 4 blocks for short MMAs (N <= 128), else 2,
+// never more than divides the K blocks (every split's block count is then a
+// multiple too) and smaller if the x ring would not fit.
+static Plan choose_plan(const int *slots, int64_t units, int nstages, int64_t nkb_total, int bn,
+                        int w_stage_bytes) {
+    Plan best;
     for (int S = 1; S <= MAX_SPLITS && S <= nstages; ++S) {
         const int per = (nstages + S - 1) / S;
-        if ((nstages + per - 1) / per != S || slots[S] <= 0) continue;  // no empty or duplicate splits
-        const int64_t waves = (base_ctas * S + slots[S] - 1) / slots[S];
-        const double cost = static_cast<double>(waves) * (2.0 + per);
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best = S;
-        }
+        if ((nstages + per - 1) / per != S || slots[S] < S) continue;  // no empty or duplicate splits
+        if (S > 1 && bn > static_cast<int>(ACC_STRIDE)) continue;      // partial buffer too large
+        Plan p;
+        p.S = S;
+        p.clusters = static_cast<int>(std::min<int64_t>(units, slots[S] / S));
+        const int64_t rounds = (units + p.clusters - 1) / p.clusters;
+        int cbs = bn <= 128 ? 2 : 1;
+        while (cbs > 0 && nkb_total % (1 << cbs)) --cbs;
+        while (!layout(bn, S, cbs, w_stage_bytes, rounds > 1, p) && cbs > 0) --cbs;
+        if (p.w_stages == 0) continue;
+        p.cost = static_cast<double>(rounds) * (per + 0.25) + (S > 1 ? 1.0 : 0.0);
+        if (p.cost < best.cost - 1e-9) best = p;
     }
     return best;
 }
@@ -610,7 +896,30 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     if ((rc = device_info<kQ4K>(info))) return rc;
     uint32_t *status = status_word();
     if (!status) return QWP_ERR_CUDA;
-    const int bn = choose_bn(M);
+    const int64_t row_tiles = (N + TILE_ROWS - 1) / TILE_ROWS;
+    const int64_t nkb_total = K / CHUNK_K;
+    const int nstages = static_cast<int>((nkb_total + KB_PER_STAGE - 1) / KB_PER_STAGE);
+    const int w_stage_bytes = kQ4K ? TILE_ROWS * Q4K_BLOCK_BYTES : TILE_ROWS * CHUNK_ROW_BYTES * KB_PER_STAGE;
+    // Token tile: the widest (fewest tiles of <= 256 tokens) unless tiles of <= 128,
+    // which allow split-K and two accumulators, give a cheaper plan (few units).
+    int bn = choose_bn(M, BN_MAX);
+    int64_t tok_tiles = (M + bn - 1) / bn;
+    if (row_tiles * tok_tiles > 0x7fffffff) return QWP_ERR_UNSUPPORTED_SHAPE;
+    Plan plan = choose_plan(info->slots[kQ4K], row_tiles * tok_tiles, nstages, nkb_total, bn, w_stage_bytes);
+    if (bn > static_cast<int>(ACC_STRIDE)) {
+        const int bn2 = choose_bn(M, static_cast<int>(ACC_STRIDE));
+        const int64_t tt2 = (M + bn2 - 1) / bn2;
+        if (row_tiles * tt2 <= 0x7fffffff) {
+            const Plan p2 = choose_plan(info->slots[kQ4K], row_tiles * tt2, nstages, nkb_total, bn2, w_stage_bytes);
+            if (p2.cost < plan.cost - 1e-9) {
+                plan = p2;
+                bn = bn2;
+                tok_tiles = tt2;
+            }
+        }
+    }
+    if (plan.clusters <= 0) return QWP_ERR_UNSUPPORTED_SHAPE;
+    const int64_t units = row_tiles * tok_tiles;
     CUtensorMap map;
     if ((rc = encode_x_map(&map, x, M, K, bn))) return rc;
 
@@ -631,39 +940,30 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
         if ((1 << sh) == a.kb_per_group) a.kbg_shift = sh;
     a.bn = bn;
     a.timeout_ns = timeout_ns;
-    // Commit groups: 4 blocks for short MMAs (N <= 128), else 2; never more than
-    // divides the K blocks (every split's block count is then a multiple too).
-    const int64_t nkb_total = K / CHUNK_K;
-    int cbs = bn <= 128 ? 2 : 1;
-    while (cbs > 0 && nkb_total % (1 << cbs)) --cbs;
-    a.cb_shift = cbs;
-    a.x_stage_bytes = (bn * 128) << cbs;
-    a.w_stage_bytes = kQ4K ? TILE_ROWS * Q4K_BLOCK_BYTES : TILE_ROWS * CHUNK_ROW_BYTES * KB_PER_STAGE;
-    a.w_stages = 4;
-    a.x_stages = std::min(A_STAGES >> cbs, (RING_BYTES - a.w_stages * a.w_stage_bytes) / a.x_stage_bytes);
-    a.w_stages = std::min(W_MAX_STAGES, (RING_BYTES - a.x_stages * a.x_stage_bytes) / a.w_stage_bytes);
-
-    const int64_t row_tiles = (N + TILE_ROWS - 1) / TILE_ROWS;
-    const int64_t tok_tiles = (M + bn - 1) / bn;
-    const int nkb = static_cast<int>(K / CHUNK_K);
-    const int nstages = (nkb + KB_PER_STAGE - 1) / KB_PER_STAGE;
-    const int S = choose_splits(info->slots[kQ4K], row_tiles * tok_tiles, nstages);
-    a.splits = S;
-    a.kb_per_split = ((nstages + S - 1) / S) * KB_PER_STAGE;
-    if (row_tiles > 0x7fffffff || tok_tiles > 65535) return QWP_ERR_UNSUPPORTED_SHAPE;
+    a.cb_shift = plan.cbs;
+    a.x_stage_bytes = (bn * 128) << plan.cbs;
+    a.w_stage_bytes = w_stage_bytes;
+    a.x_stages = plan.x_stages;
+    a.w_stages = plan.w_stages;
+    a.part_off = plan.part_off;
+    a.splits = plan.S;
+    a.kb_per_split = ((nstages + plan.S - 1) / plan.S) * KB_PER_STAGE;
+    a.n_units = static_cast<int>(units);
+    a.row_tiles = static_cast<int>(row_tiles);
+    a.acc_bufs = bn <= static_cast<int>(ACC_STRIDE) ? 2 : 1;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(row_tiles), static_cast<unsigned>(tok_tiles), S);
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.clusters), 1, plan.S);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];
     unsigned nattr = 0;
-    if (S > 1) {
+    if (plan.S > 1) {
         attrs[nattr].id = cudaLaunchAttributeClusterDimension;
         attrs[nattr].val.clusterDim.x = 1;
         attrs[nattr].val.clusterDim.y = 1;
-        attrs[nattr].val.clusterDim.z = S;
+        attrs[nattr].val.clusterDim.z = plan.S;
         ++nattr;
     }
     if (after_prior) {

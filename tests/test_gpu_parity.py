@@ -143,6 +143,17 @@ def test_w4a16_gemm_tiny(M, N, K, g):
     check_bound(y, ref, mag, f"w4a16 M{M} N{N} K{K} g{g}")
 
 
+def test_w4a16_more_units_than_ctas_with_short_last_stage():
+    """157 row tiles on at most one CTA per SM: CTAs run several units in turn, and K = 320
+    leaves a last weight stage of one block (the other transform warps only release it)."""
+    M, N, K, g = 33, 20000, 320, 64
+    (wq, s, z), (wt, sd, zd) = _w4_on_gpu(N, K, g, seed=77)
+    xh = synth.activations_f16(M, K, seed=78)
+    y = qwp.w4a16_gemm(wt, sd, zd, torch.from_numpy(xh).to(DEV), N, g).cpu().numpy()
+    ref, mag = oracle.w4a16_gemm(wq, s, z, xh, N, K, g)
+    check_bound(y, ref, mag, f"w4a16 M{M} N{N} K{K} g{g}")
+
+
 # --- GEMM: the workload shapes -------------------------------------------------------
 
 def _q4k_workload(M, N, K, seed, rows=None):
