@@ -69,7 +69,7 @@ constexpr uint32_t TMEM_COLS = 512;
 // the buffer that receives the cluster's partial sums), then mbarriers and misc words.
 constexpr int RING_BYTES = 224 * 1024;
 constexpr int OFF_BAR = RING_BYTES;
-constexpr int NUM_BARS = X_MAX_STAGES + 2 * W_MAX_STAGES + 2 * A_STAGES + 4 + 3;
+constexpr int NUM_BARS = X_MAX_STAGES + 2 * W_MAX_STAGES + 2 * A_STAGES + 4 + 4;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -98,6 +98,7 @@ struct GemmArgs {
     int row_tiles;
     int acc_bufs;           // 2 when two accumulators fit (bn <= 128), else 1
     int part_off;           // shared-memory offset of the split-K partial buffer
+    int part_overlay;       // 1: one unit per CTA, the partial buffer overlays the idle rings
     uint64_t timeout_ns;
 };
 
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t w_full = mma_done + 8 * A_STAGES, w_empty = w_full + 8 * W_MAX_STAGES;
     const uint32_t a_full = w_empty + 8 * W_MAX_STAGES, acc_full = a_full + 8 * A_STAGES;
     const uint32_t acc_empty = acc_full + 16, part_full = acc_empty + 16, part_free = part_full + 8;
-    const uint32_t drain = part_free + 8;
+    const uint32_t part_last = part_free + 8, drain = part_last + 8;
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + OFF_MISC);  // [0] tmem base, [1] abort
     const Ctl ctl{misc + 1, args.status, args.timeout_ns};
 
@@ -263,15 +264,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // Split-K: every epilogue warp of every CTA of the cluster arrives once per unit.
         mbar_init(part_full, NUM_EPI_WARPS * S);
         mbar_init(part_free, NUM_EPI_WARPS * S);
+        mbar_init(part_last, NUM_XFORM_WARPS * S);  // the last unit: every transform warp of every rank
         mbar_init(drain, 1);
         // A failure recorded earlier (and not yet read by qwp_device_status) makes
-        // every later launch skip its work instead of waiting out its own timeouts.
-        const bool failed = (*reinterpret_cast<volatile uint32_t *>(args.status) & kStatusTimeoutMask) != 0;
-        misc[1] = failed ? 1u : 0u;
+        // every later launch skip its work instead of waiting out its own timeouts
+        // (the weight copies started below are still waited for).
+        misc[1] = (*reinterpret_cast<volatile uint32_t *>(args.status) & kStatusTimeoutMask) ? 1u : 0u;
         fence_mbar_init();
         prefetch_tensormap(&tmap_x);
-        if (!failed)
-            for (int s = 0; s < w_pre; ++s) load_weight_stage(unit_tile(units0), s, s);
+        for (int s = 0; s < w_pre; ++s) load_weight_stage(unit_tile(units0), s, s);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(misc), TMEM_COLS);
@@ -279,10 +280,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_before();
     }
     __syncthreads();
-    // Before its last unit a CTA's epilogue warps push split-K partials into peers
-    // and arrive on their barriers, which must be initialised cluster-wide first.
-    // (The last unit is reduced behind cluster barriers of its own.)
-    if (S > 1 && n_mine > 1) cluster_sync();
+    // Split-K with a partial buffer of its own: peers arrive on this CTA's
+    // barriers and write into the buffer, so the barriers must be initialised
+    // cluster-wide before any thread touches another CTA.  Every thread arrives
+    // here and waits once, just before its first remote access (epilogue warps) or
+    // at the last unit (the others).  (With the buffer overlaying the rings, the
+    // last unit is reduced between two cluster barriers instead.)
+    const bool split_mbar = S > 1 && !args.part_overlay;
+    if (split_mbar) cluster_arrive_relaxed();
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const bool skip = misc[1] != 0;
@@ -321,6 +326,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp == 2) {
         // ------------------------------------------------------------ weight producer
+        if (lane == 0 && skip)
+            for (int s = 0; s < w_pre; ++s) wait_bar(w_full + 8 * s, 0, ctl, WAIT_DRAIN, false);
         if (lane == 0 && !skip) {
             int issued = 0;  // stages over all units; the first w_pre went out above
             int ws = 0;
@@ -540,6 +547,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t part = smem_u32(smem + args.part_off);
         // Two accumulators: these warps finish every unit but the CTA's last one
         // (which all transform warps finish together after the main loop).
+        if (split_mbar) cluster_wait();
         bool ok = !skip && nbufs == 2;
         int it = 0;
         for (int u = units0; ok && u + ustep < nunits; u += ustep, ++it) {
@@ -637,10 +645,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     __syncthreads();
     // Two accumulators: the CTA's last unit, finished by the transform warps (all
-    // other roles are done).  With split-K the epilogue warps of every CTA of the
-    // cluster are past all earlier units once the first cluster barrier completes,
-    // so the partial buffers are free; the partials are pushed as above, and after
-    // the second barrier every CTA sums its share in rank order and writes y.
+    // other roles are done).  With split-K each transform warp pushes its partials
+    // into the owners' buffers and every CTA then sums its tokens over the ranks in
+    // rank order and writes y.  With a buffer of its own: the push waits until the
+    // owners have consumed the previous unit (part_free), each warp then arrives on
+    // the owners' part_last barrier and every thread of a CTA waits for all ranks'
+    // pushes into it; once part_last has completed nothing touches this CTA any
+    // more, so it may exit.  With the buffer overlaying the rings (one unit per
+    // CTA), a first cluster barrier makes sure every CTA's rings are idle before
+    // the push and a second one that the pushes have landed.
     if (nbufs == 2 && n_mine > 0) {
         const int lit = n_mine - 1;
         const int lu = units0 + lit * ustep;
@@ -678,31 +691,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t rank = cluster_ctarank();
             const int per = (args.bn + S - 1) / S;
             const uint32_t part = smem_u32(smem + args.part_off);
-            cluster_sync();
-            if (acc_ok && !aborted(ctl)) {
-                tc_fence_after();
-                for (int ci = grp; ci < args.bn / 16; ci += NUM_XFORM_WARPS / 4) {
-                    uint32_t v[16];
-                    tmem_ld_x16(dcol + 16u * ci, v);
-                    tmem_wait_ld();
-                    int owner = (16 * ci) / per, tt = 16 * ci - owner * per;
-                    uint32_t dst = map_shared_rank(part, owner);
+            if (split_mbar) {
+                if (warp < FIRST_EPI_WARP) cluster_wait();  // (the epilogue warps waited already)
+            } else {
+                cluster_sync();
+            }
+            if (xf) {
+                bool push_ok = acc_ok;
+                if (push_ok && n_mine > 1)
+                    push_ok = __all_sync(0xffffffffu, wait_bar_cluster(part_free, (n_mine - 2) & 1, ctl, WAIT_PART));
+                if (push_ok && !aborted(ctl)) {
+                    tc_fence_after();
+                    for (int ci = grp; ci < args.bn / 16; ci += NUM_XFORM_WARPS / 4) {
+                        uint32_t v[16];
+                        tmem_ld_x16(dcol + 16u * ci, v);
+                        tmem_wait_ld();
+                        int owner = (16 * ci) / per, tt = 16 * ci - owner * per;
+                        uint32_t dst = map_shared_rank(part, owner);
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        st_shared_cluster_f32(dst + static_cast<uint32_t>(((static_cast<int>(rank) * per + tt) * TILE_ROWS + row) * 4),
-                                              __uint_as_float(v[t]));
-                        if (++tt == per && t < 15) {
-                            tt = 0;
-                            dst = map_shared_rank(part, ++owner);
+                        for (int t = 0; t < 16; ++t) {
+                            st_shared_cluster_f32(dst + static_cast<uint32_t>(((static_cast<int>(rank) * per + tt) * TILE_ROWS + row) * 4),
+                                                  __uint_as_float(v[t]));
+                            if (++tt == per && t < 15) {
+                                tt = 0;
+                                dst = map_shared_rank(part, ++owner);
+                            }
                         }
                     }
+                    tc_fence_before();
                 }
-                tc_fence_before();
+                // Arrive even after a failure (the status word already says so), so
+                // that the owners need not wait out their own timeouts.
+                if (split_mbar) {
+                    fence_acq_rel_cluster();
+                    __syncwarp();
+                    if (lane == 0)
+                        for (int q = 0; q < S; ++q) mbar_arrive_remote(map_shared_rank(part_last, q));
+                }
             }
-            cluster_sync();
+            bool all_in = true;
+            if (split_mbar)
+                all_in = __all_sync(0xffffffffu, wait_bar_cluster(part_last, 0, ctl, WAIT_PART));
+            else
+                cluster_sync();
             const int t0 = min(args.bn, static_cast<int>(rank) * per);
             const int t1 = min(args.bn, t0 + per);
-            if (!aborted(ctl)) {
+            if (all_in && !aborted(ctl)) {
                 const float *pbuf = reinterpret_cast<const float *>(smem + args.part_off);
                 const int items = (t1 - t0) * (TILE_ROWS / 4);
                 for (int itm = threadIdx.x; itm < items; itm += NUM_THREADS) {
@@ -826,13 +860,14 @@ static int device_info(DeviceInfo *&out) {
 // clusters, commit-group size and the shared-memory layout.
 struct Plan {
     int S = 1, clusters = 0, cbs = 0, x_stages = 0, w_stages = 0, part_off = 0;
+    bool overlay = false;
     double cost = 1e30;
 };
 
 // Shared-memory layout for a given split and commit-group size; false if the
-// rings would be too shallow.  The split-K partial buffer gets space of its own
-// only when CTAs run several units (`reserve`); with one unit per CTA it overlays
-// the rings, which are idle by the time partials arrive.
+// rings would be too shallow.  With split-K and several units per CTA (`reserve`)
+// the partial buffer gets space of its own (peers push into it while this CTA's
+// rings are busy); with one unit per CTA it overlays the rings, idle by then.
 static bool layout(int bn, int S, int cbs, int w_stage_bytes, bool reserve, Plan &p) {
     const int x_stage = (bn * 128) << cbs;
     int avail = RING_BYTES;
@@ -876,6 +911,7 @@ static Plan choose_plan(const int *slots, int64_t units, int nstages, int64_t nk
         int cbs = bn <= 128 ? 2 : 1;
         while (cbs > 0 && nkb_total % (1 << cbs)) --cbs;
         while (!layout(bn, S, cbs, w_stage_bytes, rounds > 1, p) && cbs > 0) --cbs;
+        p.overlay = S > 1 && rounds == 1;
         if (p.w_stages == 0) continue;
         p.cost = static_cast<double>(rounds) * (per + 0.25) + (S > 1 ? 1.0 : 0.0);
         if (p.cost < best.cost - 1e-9) best = p;
@@ -946,6 +982,7 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     a.x_stages = plan.x_stages;
     a.w_stages = plan.w_stages;
     a.part_off = plan.part_off;
+    a.part_overlay = plan.overlay ? 1 : 0;
     a.splits = plan.S;
     a.kb_per_split = ((nstages + plan.S - 1) / plan.S) * KB_PER_STAGE;
     a.n_units = static_cast<int>(units);

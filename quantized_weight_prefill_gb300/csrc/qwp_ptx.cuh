@@ -240,6 +240,17 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     return r;
 }
 
+// Split cluster barrier: every thread arrives once (relaxed: only the mbarrier
+// initialisations before it need to be visible, and those are fenced) and waits
+// once, later, before its first access to another CTA.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
