@@ -214,6 +214,105 @@ def run_reference(args):
     return 0
 
 
+# ------------------------------------------------------------------------- single GEMMs
+
+# Every GEMM shape of the workloads: Q4_K M=32 2048x2048; the Qwen3-8B-shaped
+# layer at M = 105, 658, 2048; W4A16 (group 128) at M=2048; the stress sweep.
+SWEEP = (["q4k:32:2048:2048"]
+         + [f"q4k:{m}:{n}:{k}" for m in (105, 658, 2048) for _, k, n in LAYER]
+         + ["w4a16:2048:12288:4096:128", "w4a16:2048:4096:12288:128",
+            "q4k:4096:32:4096", "q4k:8192:12288:4096"])
+
+
+def parse_gemm(spec):
+    parts = spec.split(":")
+    kind = parts[0]
+    if kind == "q4k" and len(parts) == 4:
+        M, N, K = map(int, parts[1:])
+        return kind, M, N, K, 0
+    if kind == "w4a16" and len(parts) == 5:
+        M, N, K, g = map(int, parts[1:])
+        return kind, M, N, K, g
+    raise ValueError(f"bad --gemm spec {spec!r}: q4k:M:N:K or w4a16:M:N:K:group")
+
+
+def run_gemms(args, specs):
+    """One JSON line per GEMM shape: graph replays of the library call (Q4_K: bf16 x,
+    conversion included; W4A16: fp16 x), weights rotating over copies larger than
+    2x L2, CUDA events around the timed replays."""
+    import torch
+
+    import quantized_weight_prefill_gb300 as qwp
+    import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
+    hbm, tc_burst, _, peak_kind = measured_peaks()
+    for spec in specs:
+        kind, M, N, K, g = parse_gemm(spec)
+        wbytes = N * K // 256 * 144 if kind == "q4k" else N * K // 2 + (N * K // g) * 3
+        copies = max(2, min(64, int(np.ceil(2.5 * l2 / wbytes))))
+        ws = []
+        for c in range(copies):
+            if kind == "q4k":
+                blocks = synth.q4k_weights(N, K, seed=100 + c)
+                ws.append((qwp.q4k_repack(torch.from_numpy(blocks.reshape(-1)).to(dev), N, K),))
+            else:
+                wq, sc, z = synth.w4a16_weights(N, K, g, seed=100 + c)
+                ws.append((qwp.w4a16_repack(torch.from_numpy(wq.view(np.int32)).to(dev)),
+                           torch.from_numpy(sc).to(dev), torch.from_numpy(z).to(dev)))
+        if kind == "q4k":
+            x = torch.from_numpy(synth.activations_bf16(M, K, seed=7).view(np.int16)).to(dev).view(torch.bfloat16)
+        else:
+            x = torch.from_numpy(synth.activations_f16(M, K, seed=7)).to(dev)
+        y = torch.empty(M, N, dtype=torch.float32, device=dev)
+
+        def call(c):
+            if kind == "q4k":
+                qwp.q4k_gemm(ws[c][0], x, N, out=y)
+            else:
+                qwp.w4a16_gemm(ws[c][0], ws[c][1], ws[c][2], x, N, g, out=y)
+
+        for s in range(args.warmup):
+            call(s % copies)
+        torch.cuda.synchronize()
+        graphs = []
+        for c in range(copies):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                call(c)
+            graphs.append(gr)
+        for gr in graphs:
+            gr.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(args.steps):
+            graphs[s % copies].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if qwp.device_status() != 0:
+            raise RuntimeError(f"kernel timeout in {spec}")
+        t = e0.elapsed_time(e1) * 1e-3 / args.steps
+        flops = 2.0 * M * N * K
+        xbytes = 2.0 * M * K
+        byts = wbytes + xbytes + 4.0 * M * N
+        t_roof = max(flops / (tc_burst * 1e12), byts / (hbm * 1e9))
+        print(json.dumps({
+            "gemm": spec, "us": t * 1e6, "tflops": flops / t / 1e12,
+            "pct_bf16_peak": 100.0 * flops / t / 1e12 / tc_burst,
+            "gbs": byts / t / 1e9, "bound": "tensor" if flops / (tc_burst * 1e12) >= byts / (hbm * 1e9) else "hbm",
+            "roofline_frac": t_roof / t, "peak_source": peak_kind, "steps": args.steps,
+            "weight_copies": copies, "launches_per_call": 2 if kind == "q4k" else 1,
+        }), flush=True)
+        del ws, graphs
+        torch.cuda.empty_cache()
+    return 0
+
+
 # ------------------------------------------------------------------------- GPU leg
 
 def run_gpu(args):
@@ -432,11 +531,18 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gemm", action="append", default=[],
+                    help="time single GEMMs instead of the layer: q4k:M:N:K or w4a16:M:N:K:group")
+    ap.add_argument("--sweep", action="store_true", help="time every GEMM shape of the workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.gemm or args.sweep:
+        if args.steps == ap.get_default("steps"):
+            args.steps = 200
+        return run_gemms(args, args.gemm + (SWEEP if args.sweep else []))
     return run_gpu(args)
 
 
