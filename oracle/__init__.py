@@ -115,15 +115,16 @@ def q4k_dequant(blocks: np.ndarray, N: int, K: int) -> np.ndarray:
     return w
 
 
-def w4a16_dequant(wq: np.ndarray, scales: np.ndarray, zeros: np.ndarray,
+def w4a16_dequant(wq: np.ndarray, scales: np.ndarray, zeros,
                   N: int, K: int, group: int) -> np.ndarray:
-    """Interleaved int4 words [N, K/8] + fp16 scales/uint8 zeros [N, K/group] -> fp64 [N, K]."""
+    """Interleaved int4 words [N, K/8] + fp16 scales/uint8 zeros [N, K/group] -> fp64 [N, K].
+    zeros=None: the symmetric form (zero point 8)."""
     q = np.ascontiguousarray(np.asarray(wq).view(np.uint32).reshape(N, K // 8))
     s = np.ascontiguousarray(np.asarray(scales).view(np.uint16).reshape(N, K // group))
-    z = np.ascontiguousarray(np.asarray(zeros, dtype=np.uint8).reshape(N, K // group))
+    z = None if zeros is None else np.ascontiguousarray(np.asarray(zeros, dtype=np.uint8).reshape(N, K // group))
     w = np.empty((N, K), np.float64)
-    _check(_load().oracle_w4a16_dequant(_ptr(q), _ptr(s), _ptr(z), N, K, group, _ptr(w)),
-           "w4a16_dequant")
+    _check(_load().oracle_w4a16_dequant(_ptr(q), _ptr(s), _ptr(z) if z is not None else None, N, K, group,
+                                        _ptr(w)), "w4a16_dequant")
     return w
 
 
@@ -150,7 +151,14 @@ def q4k_gemm(blocks: np.ndarray, x_bf16_bits: np.ndarray, N: int, K: int, with_a
 
 
 def w4a16_gemm(wq, scales, zeros, x_f16, N: int, K: int, group: int, with_abs: bool = True):
-    """Plain definition of the W4A16 GEMM in fp64."""
+    """Plain definition of the W4A16 GEMM in fp64 (fp16 activations; zeros=None: symmetric)."""
     w = w4a16_dequant(wq, scales, zeros, N, K, group)
     x = half_to_f64(np.asarray(x_f16).view(np.uint16))
+    return gemm(x.reshape(-1, K), w, with_abs)
+
+
+def w4a16_gemm_bf16(wq, scales, zeros, x_bf16, N: int, K: int, group: int, with_abs: bool = True):
+    """The W4A16 GEMM with bf16 activations, in fp64."""
+    w = w4a16_dequant(wq, scales, zeros, N, K, group)
+    x = bf16_to_f64(np.asarray(x_bf16).view(np.uint16))
     return gemm(x.reshape(-1, K), w, with_abs)

@@ -31,7 +31,9 @@
  *  - "[ROCm][Perf] W4A16: packed fp16 prefill dequant", section "1. Packed
  *    fp16 dequant": an int32 holds val[2p] at bits 4p..4p+3 and val[2p+1] at
  *    bits 16+4p..19+4p (p = 0..3); w = s * (q - zp); section "2." keeps a
- *    K-block inside one quantisation group (groups run along K).
+ *    K-block inside one quantisation group (groups run along K); the
+ *    measurements table and "Duplicate-work check" name a symmetric variant
+ *    without zero points (read here as zp = 8).
  */
 #include <math.h>
 #include <stdint.h>
@@ -149,8 +151,11 @@ int oracle_q4k_dequant(const uint8_t *blocks, int64_t N, int64_t K, double *w)
 }
 
 /*
- * Dequantize group-wise asymmetric 4-bit weights: wq[N][K/8] int32 words in
- * the interleaved order, scales[N][K/group] fp16 bits, zeros[N][K/group] in 0..15.
+ * Dequantize group-wise 4-bit weights: wq[N][K/8] int32 words in the
+ * interleaved order, scales[N][K/group] fp16 bits, zeros[N][K/group] in 0..15
+ * (asymmetric), or zeros == NULL for the symmetric form, whose zero point is
+ * the middle code 8 (the pages name a symmetric path with no zero points;
+ * centring the unsigned 4-bit code at 8 is the reading taken here).
  */
 int oracle_w4a16_dequant(const uint32_t *wq, const uint16_t *scales, const uint8_t *zeros,
                          int64_t N, int64_t K, int64_t group, double *w)
@@ -170,7 +175,7 @@ int oracle_w4a16_dequant(const uint32_t *wq, const uint16_t *scales, const uint8
                 int64_t k = 8 * i + t;
                 int64_t g = k / group;
                 double s = oracle_half_to_double(scales[n * ng + g]);
-                int z = zeros[n * ng + g];
+                int z = zeros ? zeros[n * ng + g] : 8;
                 if (!isfinite(s))
                     status = ORACLE_ERR_NONFINITE;
                 if (z > 15)

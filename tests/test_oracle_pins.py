@@ -164,6 +164,33 @@ def test_w4a16_handbuilt(case):
     assert np.array_equal(w[0], _rle(case["expect"])), case["source"]
 
 
+def test_w4a16_symmetric_handbuilt():
+    """zeros=None is the symmetric form w = s*(q - 8).  Word 0x76543210 holds, in K order,
+    the codes 0,4,1,5,2,6,3,7 (val[2p] at bits 4p, val[2p+1] at bits 16+4p), worked by hand."""
+    K, g = 64, 64
+    words = np.full(K // 8, 0x88888888, np.uint32)  # code 8 everywhere: w = 0
+    words[0] = 0x76543210
+    words[7] = 0xFFFF0000  # elements 56..63: codes 0,15,0,15,0,15,0,15
+    for sbits, s in ((0x3C00, 1.0), (0x3800, 0.5)):
+        w = oracle.w4a16_dequant(words[None], np.array([[sbits]], np.uint16), None, 1, K, g)[0]
+        expect = np.zeros(K)
+        expect[0:8] = s * (np.array([0, 4, 1, 5, 2, 6, 3, 7]) - 8)
+        expect[56:64] = s * (np.array([0, 15, 0, 15, 0, 15, 0, 15]) - 8)
+        assert np.array_equal(w, expect)
+
+
+def test_w4a16_bf16_gemm_one_hot():
+    """bf16 activations: x = e_k picks column k of W; x = 2^-3 scales it exactly."""
+    N, K, g = 3, 128, 64
+    wq, s, z = synth.w4a16_weights(N, K, g, seed=11)
+    w = oracle.w4a16_dequant(wq, s, z, N, K, g)
+    for k in (0, 37, 127):
+        xb = np.zeros((1, K), np.uint16)
+        xb[0, k] = 0x3E00  # bf16 0.125
+        y, a = oracle.w4a16_gemm_bf16(wq, s, z, xb, N, K, g)
+        assert np.array_equal(y[0], 0.125 * w[:, k]) and np.array_equal(a[0], 0.125 * np.abs(w[:, k]))
+
+
 # --- the pages' exact fp16 identity (used by the kernels' unpack) ----------------
 
 def test_fp16_magic_identity():
