@@ -5,8 +5,8 @@
  * is asynchronous and ordered on `stream` (a cudaStream_t passed as void*,
  * NULL = the legacy default stream) and never synchronizes the host, except
  * qwp_device_status.  The caller owns and allocates every input and output
- * buffer; the only entry point that takes device memory of its own is
- * q4k_gemm (activation scratch from a library-owned stream-ordered pool).
+ * buffer; the entry points that take device memory of their own are q4k_gemm
+ * and w4a16_gemm_bf16 (activation scratch from a library-owned stream-ordered pool).
  * Every entry point returns QWP_OK (0) or a negative qwp_status; none throws.
  * Calls are thread-safe.
  *
@@ -138,12 +138,14 @@ QWP_API int q4k_gemm_noalloc(const void *w_tiled_dev, const void *x_dev, float *
                              int64_t M, int64_t N, int64_t K, void *stream);
 
 /*
- * W4A16 (group-wise asymmetric int4): wq[N][K/8] int32 words, each holding
- * 8 codes along K with val[2p] at bits 4p..4p+3 and val[2p+1] at bits
- * 16+4p..19+4p; scales[N][K/group] fp16; zeros[N][K/group] uint8 in 0..15;
- * w = s * (q - zp).  Source: "[ROCm][Perf] W4A16: packed fp16 prefill
- * dequant", sections "1. Packed fp16 dequant" and "2. dtype-aware gfx1151
- * tile selection" (a K-block never straddles a group).  Requirements:
+ * W4A16 (group-wise int4): wq[N][K/8] int32 words, each holding 8 codes along
+ * K with val[2p] at bits 4p..4p+3 and val[2p+1] at bits 16+4p..19+4p;
+ * scales[N][K/group] fp16; zeros[N][K/group] uint8 in 0..15 (asymmetric,
+ * w = s * (q - zp)), or zeros_dev = NULL for the symmetric form w = s * (q - 8).
+ * Source: "[ROCm][Perf] W4A16: packed fp16 prefill dequant", sections "1.
+ * Packed fp16 dequant" and "2. dtype-aware gfx1151 tile selection" (a K-block
+ * never straddles a group); its results table and "Duplicate-work check" name
+ * the symmetric variant and the bf16-activation arm.  Requirements:
  * group % 64 == 0, K % group == 0.
  */
 
@@ -153,7 +155,7 @@ QWP_API int w4a16_repacked_bytes(int64_t N, int64_t K, size_t *out_bytes);
 /* Load-time repack of wq_dev [N][K/8] words into 128-row tiles of 64-wide K-blocks (same size). */
 QWP_API int w4a16_repack(const void *wq_dev, void *wq_tiled_dev, int64_t N, int64_t K, void *stream);
 
-/* Test entry point: exact fp32 s*(q - zp) of the repacked matrix into w_out_dev[N][K]. */
+/* Test entry point: exact fp32 s*(q - zp) of the repacked matrix into w_out_dev[N][K] (zeros_dev may be NULL). */
 QWP_API int w4a16_dequant(const void *wq_tiled_dev, const void *scales_dev, const uint8_t *zeros_dev,
                   float *w_out_dev, int64_t N, int64_t K, int64_t group, void *stream);
 
@@ -166,6 +168,17 @@ QWP_API int w4a16_dequant(const void *wq_tiled_dev, const void *scales_dev, cons
 QWP_API int w4a16_gemm(const void *wq_tiled_dev, const void *scales_dev, const uint8_t *zeros_dev,
                const void *x_dev, float *y_dev, int64_t M, int64_t N, int64_t K, int64_t group,
                void *stream);
+
+/*
+ * The same product for bf16 activations (the pages' bf16 arm): x is first
+ * converted to fp16 into M*K*2 bytes of scratch from the library-owned,
+ * stream-ordered pool (exact for |x| in [2^-14, 65504]; an overflow is reported
+ * by qwp_device_status as QWP_ERR_RANGE), then w4a16_gemm runs, launched so that
+ * its set-up overlaps the conversion.  Same rules as w4a16_gemm.
+ */
+QWP_API int w4a16_gemm_bf16(const void *wq_tiled_dev, const void *scales_dev, const uint8_t *zeros_dev,
+                    const void *x_dev, float *y_dev, int64_t M, int64_t N, int64_t K, int64_t group,
+                    void *stream);
 
 /*
  * Synchronize `stream`, then read and clear the library's device status word

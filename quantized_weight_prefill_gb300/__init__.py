@@ -19,14 +19,15 @@ from . import _build
 __all__ = [
     "QwpError", "library", "q4k_repacked_bytes", "q4k_repack", "q4k_dequant", "q4k_gemm", "q4k_gemm_f16",
     "q4k_gemm_noalloc", "NOALLOC_MAX_X_ELEMS",
-    "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "device_status",
-    "EXPORTED_SYMBOLS",
+    "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_bf16",
+    "device_status", "EXPORTED_SYMBOLS",
 ]
 
 # Every symbol include/qwp.h declares.
 EXPORTED_SYMBOLS = (
     "qwp_status_string", "q4k_repacked_bytes", "q4k_repack", "q4k_dequant", "q4k_gemm", "q4k_gemm_f16",
-    "q4k_gemm_noalloc", "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "qwp_device_status",
+    "q4k_gemm_noalloc", "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_bf16",
+    "qwp_device_status",
 )
 
 # Largest M*K that q4k_gemm_noalloc accepts (QWP_NOALLOC_MAX_X_ELEMS in the header).
@@ -64,6 +65,7 @@ def library() -> ctypes.CDLL:
         lib.w4a16_repack.argtypes = [p, p, i64, i64, p]
         lib.w4a16_dequant.argtypes = [p, p, p, p, i64, i64, i64, p]
         lib.w4a16_gemm.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p]
+        lib.w4a16_gemm_bf16.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p]
         lib.qwp_device_status.argtypes = [p]
         for name in EXPORTED_SYMBOLS:
             if name != "qwp_status_string":
@@ -179,9 +181,11 @@ def w4a16_repack(wq: torch.Tensor, out: torch.Tensor | None = None) -> torch.Ten
 
 
 def w4a16_dequant(wq_tiled, scales, zeros, N: int, K: int, group: int, out=None) -> torch.Tensor:
+    """Exact fp32 s*(q - zp) of a repacked W4A16 matrix; zeros=None is the symmetric form (zp = 8)."""
     _dev(wq_tiled, torch.int32, "wq_tiled")
     _dev(scales, torch.float16, "scales")
-    _dev(zeros, torch.uint8, "zeros")
+    if zeros is not None:
+        _dev(zeros, torch.uint8, "zeros")
     if out is None:
         out = torch.empty(N, K, dtype=torch.float32, device=wq_tiled.device)
     _dev(out, torch.float32, "out")
@@ -190,19 +194,30 @@ def w4a16_dequant(wq_tiled, scales, zeros, N: int, K: int, group: int, out=None)
     return out
 
 
-def w4a16_gemm(wq_tiled, scales, zeros, x: torch.Tensor, N: int, group: int, out=None) -> torch.Tensor:
-    """y[M, N] (fp32) = x[M, K] (fp16) . W^T with W the repacked W4A16 matrix."""
+def _w4a16_gemm_call(entry, x_dtype, wq_tiled, scales, zeros, x, N, group, out):
     _dev(wq_tiled, torch.int32, "wq_tiled")
     _dev(scales, torch.float16, "scales")
-    _dev(zeros, torch.uint8, "zeros")
-    _dev(x, torch.float16, "x")
+    if zeros is not None:
+        _dev(zeros, torch.uint8, "zeros")
+    _dev(x, x_dtype, "x")
     M, K = x.shape
     if out is None:
         out = torch.empty(M, N, dtype=torch.float32, device=x.device)
     _dev(out, torch.float32, "out")
-    _check(library().w4a16_gemm(_ptr(wq_tiled), _ptr(scales), _ptr(zeros), _ptr(x), _ptr(out), M, N, K,
-                                group, _stream(x)), "w4a16_gemm")
+    _check(getattr(library(), entry)(_ptr(wq_tiled), _ptr(scales), _ptr(zeros), _ptr(x), _ptr(out), M, N, K,
+                                     group, _stream(x)), entry)
     return out
+
+
+def w4a16_gemm(wq_tiled, scales, zeros, x: torch.Tensor, N: int, group: int, out=None) -> torch.Tensor:
+    """y[M, N] (fp32) = x[M, K] (fp16) . W^T with W the repacked W4A16 matrix
+    (zeros=None: symmetric, zero point 8)."""
+    return _w4a16_gemm_call("w4a16_gemm", torch.float16, wq_tiled, scales, zeros, x, N, group, out)
+
+
+def w4a16_gemm_bf16(wq_tiled, scales, zeros, x: torch.Tensor, N: int, group: int, out=None) -> torch.Tensor:
+    """As w4a16_gemm with bf16 activations (converted to fp16 on the GPU first)."""
+    return _w4a16_gemm_call("w4a16_gemm_bf16", torch.bfloat16, wq_tiled, scales, zeros, x, N, group, out)
 
 
 def device_status(device=None) -> int:

@@ -122,6 +122,7 @@ __global__ void w4_repack_kernel(const uint32_t *__restrict__ src, uint8_t *__re
 
 // One thread per word: the exact (1024+q) - (1024+zp) of the GEMM's unpack,
 // then an exact fp32 product with the scale (at most 11 + 5 significant bits).
+// zeros == NULL: symmetric, zero point 8.
 __global__ void w4_dequant_kernel(const uint8_t *__restrict__ w, const __half *__restrict__ scales,
                                   const uint8_t *__restrict__ zeros, float *__restrict__ out,
                                   int64_t N, int64_t K, int64_t group) {
@@ -139,7 +140,7 @@ __global__ void w4_dequant_kernel(const uint8_t *__restrict__ w, const __half *_
     const int64_t k0 = CHUNK_K * j + 8 * v;
     const int64_t g = k0 / group;
     const float s = __half2float(scales[n * (K / group) + g]);
-    const __half2 mz = w4_magic_zero(zeros[n * (K / group) + g]);
+    const __half2 mz = w4_magic_zero(zeros ? zeros[n * (K / group) + g] : 8u);
     float vals[8];
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
@@ -276,7 +277,7 @@ extern "C" int w4a16_dequant(const void *wq_tiled, const void *scales, const uin
                              float *w_out, int64_t N, int64_t K, int64_t group, void *stream) {
     if (group <= 0 || group % CHUNK_K) return QWP_ERR_INVALID_ARG;
     if (K % group) return QWP_ERR_UNSUPPORTED_SHAPE;
-    if (N > 0 && K > 0 && (!scales || !zeros)) return QWP_ERR_INVALID_ARG;
+    if (N > 0 && K > 0 && !scales) return QWP_ERR_INVALID_ARG;
     int rc = w4_common_checks(wq_tiled, w_out, N, K);
     if (rc || N == 0 || K == 0) return rc;
     const int64_t threads = N * (K / 8);

@@ -81,7 +81,7 @@ static_assert(2 * ACC_STRIDE <= A_COL, "two accumulator buffers of 128 columns f
 struct GemmArgs {
     const uint8_t *w;       // repacked weights
     const __half *scales;   // W4A16: [N][K/group]
-    const uint8_t *zeros;   // W4A16: [N][K/group]
+    const uint8_t *zeros;   // W4A16: [N][K/group], or null: symmetric (zero point 8)
     float *y;               // [M][N]
     uint32_t *status;       // library status word
     int M, N, K, group;
@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int kbi = kb_begin + jj;
                     const int64_t g = args.kbg_shift >= 0 ? (kbi >> args.kbg_shift) : (kbi / args.kb_per_group);
                     s2 = __half2half2(args.scales[n * ng + g]);
-                    mz = w4_magic_zero(args.zeros[n * ng + g]);
+                    mz = w4_magic_zero(args.zeros ? args.zeros[n * ng + g] : 8u);  // no zeros: symmetric
                 }
             }
             // This warp's reads of the stage are done.
@@ -1090,7 +1090,30 @@ extern "C" int w4a16_gemm(const void *wq_tiled, const void *scales, const uint8_
     if (K % group || K == 0) return K < 0 ? QWP_ERR_INVALID_ARG : QWP_ERR_UNSUPPORTED_SHAPE;
     int rc = gemm_shape_checks(wq_tiled, x, y, M, N, K);
     if (rc || M == 0 || N == 0) return rc;
-    if (!scales || !zeros) return QWP_ERR_INVALID_ARG;
+    if (!scales) return QWP_ERR_INVALID_ARG;
     return launch_gemm<false>(wq_tiled, scales, zeros, x, y, M, N, K, group,
                               static_cast<cudaStream_t>(stream), kDefaultTimeoutNs, false);
+}
+
+extern "C" int w4a16_gemm_bf16(const void *wq_tiled, const void *scales, const uint8_t *zeros,
+                               const void *x, float *y, int64_t M, int64_t N, int64_t K, int64_t group,
+                               void *stream) {
+    if (group <= 0 || group % CHUNK_K) return QWP_ERR_INVALID_ARG;
+    if (K % group || K == 0) return K < 0 ? QWP_ERR_INVALID_ARG : QWP_ERR_UNSUPPORTED_SHAPE;
+    int rc = gemm_shape_checks(wq_tiled, x, y, M, N, K);
+    if (rc || M == 0 || N == 0) return rc;
+    if (!scales) return QWP_ERR_INVALID_ARG;
+    if ((rc = check_device())) return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaMemPool_t pool;
+    if ((rc = scratch_pool(&pool))) return rc;
+    void *x16 = nullptr;
+    if (cudaMallocFromPoolAsync(&x16, static_cast<size_t>(M) * K * 2, pool, s) != cudaSuccess) {
+        cudaGetLastError();
+        return QWP_ERR_CUDA;
+    }
+    rc = launch_bf16_to_f16(x, x16, M * K, s);
+    if (!rc) rc = launch_gemm<false>(wq_tiled, scales, zeros, x16, y, M, N, K, group, s, kDefaultTimeoutNs, true);
+    if (cudaFreeAsync(x16, s) != cudaSuccess && !rc) rc = QWP_ERR_CUDA;
+    return rc;
 }

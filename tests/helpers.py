@@ -70,12 +70,14 @@ def q4k_oracle_rows(blocks: np.ndarray, xb_rows: np.ndarray, N: int, K: int, chu
     return np.concatenate(ys, axis=1), np.concatenate(ms, axis=1)
 
 
-def w4a16_oracle_rows(wq, s, z, xh_rows, N: int, K: int, group: int, chunk: int = 2048):
-    x = oracle.half_to_f64(np.asarray(xh_rows).view(np.uint16)).reshape(-1, K)
+def w4a16_oracle_rows(wq, s, z, xh_rows, N: int, K: int, group: int, chunk: int = 2048, bf16: bool = False):
+    """Oracle rows of the W4A16 GEMM (z None: symmetric; bf16: x holds bf16 bits, else fp16)."""
+    bits = np.asarray(xh_rows).view(np.uint16)
+    x = (oracle.bf16_to_f64(bits) if bf16 else oracle.half_to_f64(bits)).reshape(-1, K)
     ys, ms = [], []
     for n0 in range(0, N, chunk):
         n1 = min(N, n0 + chunk)
-        w = oracle.w4a16_dequant(wq[n0:n1], s[n0:n1], z[n0:n1], n1 - n0, K, group)
+        w = oracle.w4a16_dequant(wq[n0:n1], s[n0:n1], None if z is None else z[n0:n1], n1 - n0, K, group)
         y, a = oracle.gemm(x, w)
         ys.append(y)
         ms.append(a)

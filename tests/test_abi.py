@@ -76,6 +76,11 @@ def test_gemm_argument_checks_before_any_cuda_call(lib):
     assert lib.q4k_gemm(_p(0x1004), a16, a16, 8, 8, 256, None) == MISALIGNED
     assert lib.q4k_gemm(a16, _p(0x1002), a16, 8, 8, 256, None) == MISALIGNED
     assert lib.w4a16_gemm(a16, None, a16, a16, a16, 8, 8, 256, 128, None) == INVALID
+    assert lib.w4a16_gemm_bf16(a16, None, None, a16, a16, 8, 8, 256, 128, None) == INVALID  # scales required
+    assert lib.w4a16_gemm_bf16(a16, a16, None, a16, a16, 8, 8, 256, 100, None) == INVALID   # group % 64
+    assert lib.w4a16_gemm_bf16(a16, a16, None, a16, a16, 8, 8, 320, 128, None) == SHAPE     # K % group
+    assert lib.w4a16_gemm_bf16(a16, a16, None, _p(0x1002), a16, 8, 8, 256, 128, None) == MISALIGNED
+    assert lib.w4a16_gemm_bf16(None, None, None, None, None, 0, 8, 256, 128, None) == OK
     # empty problems are no-ops
     assert lib.q4k_gemm(None, None, None, 0, 8, 256, None) == OK
     assert lib.q4k_gemm(None, None, None, 8, 0, 256, None) == OK

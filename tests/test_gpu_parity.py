@@ -154,6 +154,53 @@ def test_w4a16_more_units_than_ctas_with_short_last_stage():
     check_bound(y, ref, mag, f"w4a16 M{M} N{N} K{K} g{g}")
 
 
+@pytest.mark.parametrize("N,K,g", [(1, 64, 64), (130, 512, 128), (4096, 4096, 128)])
+def test_w4a16_symmetric_dequant_bit_exact(N, K, g):
+    """No zero points: w = s * (q - 8)."""
+    (wq, s, _), (wt, sd, _) = _w4_on_gpu(N, K, g, seed=9 * N + K)
+    got = qwp.w4a16_dequant(wt, sd, None, N, K, g).cpu().numpy()
+    ref = oracle.w4a16_dequant(wq, s, None, N, K, g).astype(np.float32)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("M,N,K,g", [(1, 1, 64, 64), (33, 130, 768, 64), (105, 256, 1024, 128),
+                                     (257, 200, 320, 64)])
+def test_w4a16_symmetric_gemm_tiny(M, N, K, g):
+    (wq, s, _), (wt, sd, _) = _w4_on_gpu(N, K, g, seed=M * 13 + N)
+    xh = synth.activations_f16(M, K, seed=M + 3)
+    y = qwp.w4a16_gemm(wt, sd, None, torch.from_numpy(xh).to(DEV), N, g).cpu().numpy()
+    ref, mag = oracle.w4a16_gemm(wq, s, None, xh, N, K, g)
+    check_bound(y, ref, mag, f"w4a16 sym M{M} N{N} K{K} g{g}")
+
+
+@pytest.mark.parametrize("symmetric", [False, True])
+@pytest.mark.parametrize("M,N,K,g", [(1, 1, 64, 64), (7, 5, 256, 128), (105, 256, 1024, 128),
+                                     (300, 136, 512, 256)])
+def test_w4a16_bf16_gemm_tiny(M, N, K, g, symmetric):
+    (wq, s, z), (wt, sd, zd) = _w4_on_gpu(N, K, g, seed=M * 17 + N)
+    if symmetric:
+        z = zd = None
+    xb = synth.activations_bf16(M, K, seed=M + 4)
+    y = qwp.w4a16_gemm_bf16(wt, sd, zd, _bf16_on_gpu(xb), N, g).cpu().numpy()
+    ref, mag = oracle.w4a16_gemm_bf16(wq, s, z, xb, N, K, g)
+    check_bound(y, ref, mag, f"w4a16 bf16 sym={symmetric} M{M} N{N} K{K} g{g}")
+
+
+def test_w4a16_bf16_activation_beyond_fp16_range_is_reported():
+    """An activation that overflows fp16 is reported as QWP_ERR_RANGE, and the next call is clean."""
+    M, N, K, g = 8, 128, 256, 128
+    (wq, s, z), (wt, sd, zd) = _w4_on_gpu(N, K, g, seed=31)
+    xb = synth.activations_bf16(M, K, seed=32).copy()
+    xb[3, 17] = 0x4880  # bf16 262144.0, beyond fp16's largest finite value
+    qwp.w4a16_gemm_bf16(wt, sd, zd, _bf16_on_gpu(xb), N, g)
+    assert qwp.device_status() == -7
+    xb[3, 17] = 0x3F80  # 1.0
+    y = qwp.w4a16_gemm_bf16(wt, sd, zd, _bf16_on_gpu(xb), N, g).cpu().numpy()
+    assert qwp.device_status() == 0
+    ref, mag = oracle.w4a16_gemm_bf16(wq, s, z, xb, N, K, g)
+    check_bound(y, ref, mag, "w4a16 bf16 after a range error")
+
+
 # --- GEMM: the workload shapes -------------------------------------------------------
 
 def _q4k_workload(M, N, K, seed, rows=None):
@@ -188,16 +235,25 @@ def test_q4k_stress(M, N, K):
     _q4k_workload(M, N, K, seed=M + N, rows=sample_rows(M, seed=N))
 
 
-@pytest.mark.parametrize("K,N", [(4096, 12288), (12288, 4096)])
-def test_w4a16_m2048(K, N):
+@pytest.mark.parametrize("K,N,arm", [(4096, 12288, "f16"), (12288, 4096, "f16"),
+                                     (4096, 12288, "f16_symmetric"), (12288, 4096, "bf16"),
+                                     (4096, 12288, "bf16_symmetric")])
+def test_w4a16_m2048(K, N, arm):
     M, g = 2048, 128
     (wq, s, z), (wt, sd, zd) = _w4_on_gpu(N, K, g, seed=K + 5)
-    xh = synth.activations_f16(M, K, seed=K + 6)
-    y = qwp.w4a16_gemm(wt, sd, zd, torch.from_numpy(xh).to(DEV), N, g)
+    if arm.endswith("symmetric"):
+        z = zd = None
     rows = sample_rows(M, seed=K)
+    if arm.startswith("bf16"):
+        xb = synth.activations_bf16(M, K, seed=K + 6)
+        y = qwp.w4a16_gemm_bf16(wt, sd, zd, _bf16_on_gpu(xb), N, g)
+        ref, mag = w4a16_oracle_rows(wq, s, z, xb[rows], N, K, g, bf16=True)
+    else:
+        xh = synth.activations_f16(M, K, seed=K + 6)
+        y = qwp.w4a16_gemm(wt, sd, zd, torch.from_numpy(xh).to(DEV), N, g)
+        ref, mag = w4a16_oracle_rows(wq, s, z, xh[rows], N, K, g)
     ys = y[torch.from_numpy(rows).to(DEV)].cpu().numpy()
-    ref, mag = w4a16_oracle_rows(wq, s, z, xh[rows], N, K, g)
-    check_bound(ys, ref, mag, f"w4a16 M{M} N{N} K{K}")
+    check_bound(ys, ref, mag, f"w4a16 {arm} M{M} N{N} K{K}")
 
 
 # --- edge cases -----------------------------------------------------------------------
