@@ -10,14 +10,19 @@ Functions (each follows the passage cited in ``qwp_oracle.c``):
   half_to_f64 / bf16_to_f64   exact IEEE decode of stored 16-bit values
   q4k_scale_min               the 6-bit (scale, min) pair of one sub-block
   q4k_dequant                 GGML Q4_K super-blocks -> fp64 weights [N, K]
+  q6k_code / q6k_dequant      GGML Q6_K blocks: one 6-bit code / fp64 weights [N, K]
   w4a16_dequant               interleaved int4 words + fp16 scales + zeros -> fp64
   gemm                        y = x @ w.T and a = |x| @ |w|.T, both fp64, naive loops
-  q4k_gemm / w4a16_gemm       decode + dequant + gemm in one call
+  q4k_gemm / q6k_gemm / w4a16_gemm   decode + dequant + gemm in one call
 
 Parity pins: see ``tests/test_oracle_pins.py``.  The exact GGML bit layout of
 the 6-bit scale/min packing is not printed on the source pages and is
 "parity unpinned" beyond the invariants tested there (every one of the 96
-packed bits reaches exactly one 6-bit value).
+packed bits reaches exactly one 6-bit value).  The same holds for the Q6_K bit
+layout (the pages name Q6_K but print no layout): the pins check that the 1536
+code bits of a block reach each of the 256 codes exactly six times, one bit per
+power of two, that each int8 scale covers exactly 16 consecutive weights, and
+hand-worked blocks of the GGML reading.
 """
 from __future__ import annotations
 
@@ -50,6 +55,8 @@ def _load():
         lib.oracle_q4k_scale_min.argtypes = [p, ctypes.c_int, p, p]
         lib.oracle_q4k_scale_min.restype = None
         lib.oracle_q4k_dequant.argtypes = [p, i64, i64, p]
+        lib.oracle_q6k_code.argtypes = [p, ctypes.c_int]
+        lib.oracle_q6k_dequant.argtypes = [p, i64, i64, p]
         lib.oracle_w4a16_dequant.argtypes = [p, p, p, i64, i64, i64, p]
         lib.oracle_gemm.argtypes = [p, p, i64, i64, i64, p, p]
         lib.oracle_num_threads.argtypes = []
@@ -115,6 +122,22 @@ def q4k_dequant(blocks: np.ndarray, N: int, K: int) -> np.ndarray:
     return w
 
 
+def q6k_code(block: np.ndarray, e: int) -> int:
+    """The 6-bit code (0..63) of element e of one 210-byte GGML Q6_K block."""
+    b = np.ascontiguousarray(np.asarray(block, dtype=np.uint8).reshape(210))
+    return int(_load().oracle_q6k_code(_ptr(b), int(e)))
+
+
+def q6k_dequant(blocks: np.ndarray, N: int, K: int) -> np.ndarray:
+    """GGML Q6_K rows (N * K/256 * 210 bytes) -> exact fp64 weights [N, K]."""
+    b = np.ascontiguousarray(np.asarray(blocks, dtype=np.uint8).reshape(-1))
+    if b.size != N * (K // 256) * 210 or K % 256:
+        raise ValueError("Q6_K buffer size does not match N, K")
+    w = np.empty((N, K), np.float64)
+    _check(_load().oracle_q6k_dequant(_ptr(b), N, K, _ptr(w)), "q6k_dequant")
+    return w
+
+
 def w4a16_dequant(wq: np.ndarray, scales: np.ndarray, zeros,
                   N: int, K: int, group: int) -> np.ndarray:
     """Interleaved int4 words [N, K/8] + fp16 scales/uint8 zeros [N, K/group] -> fp64 [N, K].
@@ -146,6 +169,13 @@ def gemm(x: np.ndarray, w: np.ndarray, with_abs: bool = True):
 def q4k_gemm(blocks: np.ndarray, x_bf16_bits: np.ndarray, N: int, K: int, with_abs: bool = True):
     """Plain definition of the Q4_K prefill GEMM: y[M,N] = x[M,K] . W[N,K]^T in fp64."""
     w = q4k_dequant(blocks, N, K)
+    x = bf16_to_f64(x_bf16_bits)
+    return gemm(x.reshape(-1, K), w, with_abs)
+
+
+def q6k_gemm(blocks: np.ndarray, x_bf16_bits: np.ndarray, N: int, K: int, with_abs: bool = True):
+    """Plain definition of the Q6_K prefill GEMM: y[M,N] = x[M,K] . W[N,K]^T in fp64 (bf16 x)."""
+    w = q6k_dequant(blocks, N, K)
     x = bf16_to_f64(x_bf16_bits)
     return gemm(x.reshape(-1, K), w, with_abs)
 

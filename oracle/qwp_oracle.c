@@ -34,6 +34,14 @@
  *    K-block inside one quantisation group (groups run along K); the
  *    measurements table and "Duplicate-work check" name a symmetric variant
  *    without zero points (read here as zp = 8).
+ *  - "How ZINC's RDNA4 batched prefill went from 42 to 208 tok/s", sections
+ *    "Bug 2: Q6_K had a gate but no dispatcher" and "What changed": Q4_K_M
+ *    checkpoints keep ffn_down and attn_v in Q6_K, and the batched path needs
+ *    a Q6_K kernel beside the Q4_K one.  The pages name the format but do not
+ *    print it; the oracle follows the GGML Q6_K block (parity partly
+ *    unpinned): 256 weights in 210 bytes -- ql[128] (low four bits), qh[64]
+ *    (high two bits), int8 scales[16] (one per 16 weights), fp16 d last;
+ *    w = d * scale * (q - 32) with q the 6-bit code.
  */
 #include <math.h>
 #include <stdint.h>
@@ -145,6 +153,52 @@ int oracle_q4k_dequant(const uint8_t *blocks, int64_t N, int64_t K, double *w)
                     row[64 * c + 32 + l] = d * sc_hi * q_hi - dmin * m_hi;
                 }
             }
+        }
+    }
+    return status;
+}
+
+/*
+ * The 6-bit code of element e (0..255) of one GGML Q6_K block.  The block is
+ * two halves of 128 elements; in half h, element 32*j + l (j = 0..3,
+ * l = 0..31) takes its low four bits from byte 64*h + l + 32*(j % 2) of ql
+ * (the low nibble for j < 2, the high nibble for j >= 2) and its high two
+ * bits from bits 2j..2j+1 of byte 32*h + l of qh.
+ */
+int oracle_q6k_code(const uint8_t *blk, int e)
+{
+    const uint8_t *ql = blk, *qh = blk + 128;
+    int h = e / 128, j = (e % 128) / 32, l = e % 32;
+    int lo_byte = ql[64 * h + l + 32 * (j % 2)];
+    int lo = (j < 2) ? (lo_byte & 15) : (lo_byte >> 4);
+    int hi = (qh[32 * h + l] >> (2 * j)) & 3;
+    return lo | (hi << 4);
+}
+
+/*
+ * Dequantize N rows of K weights stored as GGML Q6_K blocks (row n, block b
+ * at byte offset (n*(K/256) + b) * 210) into w[N][K]: element e of a block is
+ * d * scales[e / 16] * (q_e - 32).
+ */
+int oracle_q6k_dequant(const uint8_t *blocks, int64_t N, int64_t K, double *w)
+{
+    if (N < 0 || K < 0 || K % 256 != 0)
+        return ORACLE_ERR_SHAPE;
+    const int64_t nb = K / 256;
+    int status = ORACLE_OK;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint8_t *blk = blocks + (n * nb + b) * 210;
+            const int8_t *scales = (const int8_t *)(blk + 192);
+            double d = oracle_half_to_double((uint16_t)(blk[208] | (blk[209] << 8)));
+            if (!isfinite(d)) {
+                status = ORACLE_ERR_NONFINITE;
+                continue;
+            }
+            double *row = w + n * K + b * 256;
+            for (int e = 0; e < 256; ++e)
+                row[e] = d * (double)scales[e / 16] * (double)(oracle_q6k_code(blk, e) - 32);
         }
     }
     return status;

@@ -12,6 +12,14 @@ Recipe (the workload definitions fix the value distributions):
                  one 6-bit value, so uniform bytes give independent 6-bit
                  scales/mins uniform in 0..63, and uniform bytes give nibbles
                  uniform in 0..15.
+  Q6_K weights   per 210-byte block: the 128 ql and 64 qh bytes uniform random
+                 bytes (every bit of the 1536 code bits feeds exactly one code,
+                 so the 6-bit codes are uniform in 0..63); the 16 int8 scales
+                 uniform random bytes (uniform in -128..127); d uniform in
+                 [1e-5, 8e-5] rounded to fp16, so that both subnormal and
+                 normal fp16 d occur (GGML puts the block's largest scale near
+                 127, which leaves d small: weights of magnitude ~0.05 give d
+                 ~1e-5).
   W4A16 weights  uniform random 32-bit words (so every 4-bit code is uniform
                  in 0..15 whatever the bit interleave), fp16 scales uniform in
                  [1e-3, 4e-3], uint8 zero points uniform in 0..15.
@@ -24,6 +32,7 @@ import numpy as np
 
 Q4K_BLOCK_BYTES = 144  # bytes per 256-weight super-block (0.5625 byte per weight)
 Q4K_BLOCK_K = 256
+Q6K_BLOCK_BYTES = 210  # ql[128], qh[64], int8 scales[16], fp16 d
 
 
 def _fp16_bits(values: np.ndarray) -> np.ndarray:
@@ -43,6 +52,19 @@ def q4k_weights(N: int, K: int, seed: int, lo: float = 1e-3, hi: float = 4e-3) -
     blk[:, 2:4] = dmin.astype("<u2").view(np.uint8).reshape(nb, 2)
     blk[:, 4:144] = rng.integers(0, 256, size=(nb, 140), dtype=np.uint8)
     return blk.reshape(N, (K // Q4K_BLOCK_K) * Q4K_BLOCK_BYTES)
+
+
+def q6k_weights(N: int, K: int, seed: int, lo: float = 1e-5, hi: float = 8e-5) -> np.ndarray:
+    """GGML Q6_K rows: uint8 array [N, K/256*210]; block b of row n at byte 210*b."""
+    if K % Q4K_BLOCK_K:
+        raise ValueError("K must be a multiple of 256")
+    rng = np.random.default_rng(seed)
+    nb = N * (K // Q4K_BLOCK_K)
+    blk = np.empty((nb, Q6K_BLOCK_BYTES), np.uint8)
+    blk[:, 0:208] = rng.integers(0, 256, size=(nb, 208), dtype=np.uint8)
+    d = _fp16_bits(rng.uniform(lo, hi, nb))
+    blk[:, 208:210] = d.astype("<u2").view(np.uint8).reshape(nb, 2)
+    return blk.reshape(N, (K // Q4K_BLOCK_K) * Q6K_BLOCK_BYTES)
 
 
 def w4a16_weights(N: int, K: int, group: int, seed: int, lo: float = 1e-3, hi: float = 4e-3):

@@ -47,6 +47,25 @@ def _q4k_cases():
         return json.load(f)["cases"]
 
 
+def _q6k_block(spec):
+    blk = np.zeros(210, np.uint8)
+    blk[0:128] = int(spec["ql_fill"], 16)
+    blk[128:192] = int(spec["qh_fill"], 16)
+    for idx, val in spec["ql_set"].items():
+        blk[int(idx)] = int(val, 16)
+    for idx, val in spec["qh_set"].items():
+        blk[128 + int(idx)] = int(val, 16)
+    blk[192:208] = np.frombuffer(bytes.fromhex(spec["scales"]), np.uint8)
+    d = int(spec["d"], 16)
+    blk[208], blk[209] = d & 255, d >> 8
+    return blk
+
+
+def _q6k_cases():
+    with open(os.path.join(GOLDEN, "q6k_handbuilt.json")) as f:
+        return json.load(f)["cases"]
+
+
 def _w4a16_cases():
     with open(os.path.join(GOLDEN, "w4a16_handbuilt.json")) as f:
         return json.load(f)["cases"]
@@ -151,6 +170,97 @@ def test_q4k_rejects_bad_shape():
 
 
 # --- W4A16 dequant ----------------------------------------------------------------
+
+# --- Q6_K dequant -----------------------------------------------------------------
+
+@pytest.mark.parametrize("case", _q6k_cases(), ids=lambda c: c["name"])
+def test_q6k_handbuilt_blocks(case):
+    N, K = case["N"], case["K"]
+    blocks = np.concatenate([_q6k_block(b) for b in case["blocks"]])
+    w = oracle.q6k_dequant(blocks, N, K)
+    for n in range(N):
+        expect = _rle(case["expect"][n])
+        assert expect.size == K
+        assert np.array_equal(w[n], expect), case["source"]
+
+
+def test_q6k_code_bits_are_a_bijection():
+    """Each of the 1536 code bits (ql, qh) reaches exactly one weight, as one power of two.
+
+    256 six-bit codes in 192 bytes leave no spare bit, so the decode must be a
+    permutation of bits with bit weights 1..32: a dropped, duplicated, mis-shifted
+    or mis-indexed term breaks this.  Low-nibble bytes must give weights 1..8, qh
+    bytes weights 16 and 32.
+    """
+    base = np.zeros(210, np.uint8)
+    base[192:208] = 1        # every scale 1
+    base[208:210] = (0x00, 0x3C)  # d = 1.0
+    w0 = oracle.q6k_dequant(base, 1, 256)[0]
+    assert np.array_equal(w0, np.full(256, -32.0))
+    hits = set()
+    for byte in range(192):
+        for bit in range(8):
+            blk = base.copy()
+            blk[byte] = 1 << bit
+            diff = oracle.q6k_dequant(blk, 1, 256)[0] - w0
+            nz = np.flatnonzero(diff)
+            assert nz.size == 1, (byte, bit, nz)
+            v = diff[nz[0]]
+            assert v > 0 and v == 2.0 ** round(np.log2(v)) and v <= 32, (byte, bit, v)
+            k = int(round(np.log2(v)))
+            assert (k < 4) == (byte < 128), (byte, bit, k)
+            key = (int(nz[0]), k)
+            assert key not in hits
+            hits.add(key)
+    assert len(hits) == 1536
+
+
+def test_q6k_each_scale_covers_16_consecutive_weights():
+    """Scale byte s multiplies exactly elements 16s..16s+15 (one-hot scales, codes 0)."""
+    for s in range(16):
+        blk = np.zeros(210, np.uint8)
+        blk[192 + s] = 3
+        blk[208:210] = (0x00, 0x3C)
+        w = oracle.q6k_dequant(blk, 1, 256)[0]
+        nz = np.flatnonzero(w)
+        assert np.array_equal(nz, np.arange(16 * s, 16 * s + 16))
+        assert np.all(w[nz] == -96.0)  # 1 * 3 * (0 - 32)
+
+
+def test_q6k_code_accessor_matches_dequant_and_covers_all_codes():
+    """Random blocks: the one-code accessor agrees with the dequant, and with d = 1 and
+    unit scales every code 0..63 appears (uniform random bytes)."""
+    blk = synth.q6k_weights(1, 256, seed=3).reshape(210).copy()
+    blk[192:208] = 1
+    blk[208:210] = (0x00, 0x3C)
+    w = oracle.q6k_dequant(blk, 1, 256)[0]
+    codes = np.array([oracle.q6k_code(blk, e) for e in range(256)])
+    assert np.array_equal(w, codes - 32.0)
+    many = synth.q6k_weights(64, 256, seed=4).copy()
+    many[:, 192:208] = 1
+    many[:, 208:210] = (0x00, 0x3C)
+    allw = oracle.q6k_dequant(many, 64, 256)
+    assert set(np.unique(allw + 32).astype(int)) == set(range(64))
+
+
+def test_q6k_gemm_closed_form_one_hot_and_ones():
+    """x = e_k picks column k of W; x = ones sums a row (one_scale_per_16: sum = 128)."""
+    case = {c["name"]: c for c in _q6k_cases()}["one_scale_per_16_weights"]
+    blk = _q6k_block(case["blocks"][0])
+    x = np.zeros((2, 256), np.float32)
+    x[0, 37] = 1.0
+    x[1, :] = 1.0
+    xb = (x.view(np.uint32) >> 16).astype(np.uint16)  # exact: 0 and 1 are bf16
+    y, a = oracle.q6k_gemm(blk, xb, 1, 256)
+    assert y[0, 0] == -3.0         # element 37 is in sub-block 2 (scale 3): w = -sc = -3
+    assert y[1, 0] == 128.0        # -(1 - 2 + 3 - ... - 16) * 16 = 128
+    assert a[1, 0] == 16.0 * sum(range(1, 17))
+
+
+def test_q6k_rejects_bad_shape():
+    with pytest.raises(ValueError):
+        oracle.q6k_dequant(np.zeros(210, np.uint8), 1, 300)
+
 
 @pytest.mark.parametrize("case", _w4a16_cases(), ids=lambda c: c["name"])
 def test_w4a16_handbuilt(case):
@@ -295,3 +405,7 @@ def test_synth_value_ranges():
     assert abs(x.mean()) < 0.1 and 0.9 < x.std() < 1.1
     wq, s, z = synth.w4a16_weights(4, 256, 128, seed=3)
     assert z.max() <= 15 and s.astype(np.float64).min() >= 1e-3 * (1 - 2 ** -11)
+    q6 = synth.q6k_weights(64, 1024, seed=4).reshape(-1, 210)
+    d6 = q6[:, 208:210].copy().view("<u2").view(np.float16).astype(np.float64)
+    assert d6.min() >= 1e-5 * (1 - 2 ** -10) and d6.max() <= 8e-5 * (1 + 2 ** -11)
+    assert (d6 < 2.0 ** -14).any() and (d6 >= 2.0 ** -14).any()  # subnormal and normal fp16 d
