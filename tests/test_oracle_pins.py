@@ -169,8 +169,6 @@ def test_q4k_rejects_bad_shape():
         oracle.q4k_dequant(np.zeros(144, np.uint8), 1, 128)
 
 
-# --- W4A16 dequant ----------------------------------------------------------------
-
 # --- Q6_K dequant -----------------------------------------------------------------
 
 @pytest.mark.parametrize("case", _q6k_cases(), ids=lambda c: c["name"])
@@ -261,6 +259,8 @@ def test_q6k_rejects_bad_shape():
     with pytest.raises(ValueError):
         oracle.q6k_dequant(np.zeros(210, np.uint8), 1, 300)
 
+
+# --- W4A16 dequant ----------------------------------------------------------------
 
 @pytest.mark.parametrize("case", _w4a16_cases(), ids=lambda c: c["name"])
 def test_w4a16_handbuilt(case):
