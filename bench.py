@@ -222,19 +222,20 @@ SWEEP = (["q4k:32:2048:2048"]
          + [f"q4k:{m}:{n}:{k}" for m in (105, 658, 2048) for _, k, n in LAYER]
          + ["w4a16:2048:12288:4096:128", "w4a16:2048:4096:12288:128",
             "w4a16:2048:12288:4096:128:sym", "w4a16:2048:12288:4096:128:bf16",
+            "q6k:105:1024:4096", "q6k:105:4096:12288", "q6k:2048:4096:12288",
             "q4k:4096:32:4096", "q4k:8192:12288:4096"])
 
 
 def parse_gemm(spec):
     parts = spec.split(":")
     kind = parts[0]
-    if kind == "q4k" and len(parts) == 4:
+    if kind in ("q4k", "q6k") and len(parts) == 4:
         M, N, K = map(int, parts[1:])
         return kind, M, N, K, 0, set()
     if kind == "w4a16" and len(parts) >= 5 and set(parts[5:]) <= {"sym", "bf16"}:
         M, N, K, g = map(int, parts[1:5])
         return kind, M, N, K, g, set(parts[5:])
-    raise ValueError(f"bad --gemm spec {spec!r}: q4k:M:N:K or w4a16:M:N:K:group[:sym][:bf16]")
+    raise ValueError(f"bad --gemm spec {spec!r}: q4k:M:N:K, q6k:M:N:K or w4a16:M:N:K:group[:sym][:bf16]")
 
 
 def run_gemms(args, specs):
@@ -254,18 +255,24 @@ def run_gemms(args, specs):
     hbm, tc_burst, _, peak_kind = measured_peaks()
     for spec in specs:
         kind, M, N, K, g, flags = parse_gemm(spec)
-        wbytes = N * K // 256 * 144 if kind == "q4k" else N * K // 2 + (N * K // g) * (2 if "sym" in flags else 3)
+        if kind in ("q4k", "q6k"):
+            wbytes = N * K // 256 * (144 if kind == "q4k" else 210)
+        else:
+            wbytes = N * K // 2 + (N * K // g) * (2 if "sym" in flags else 3)
         copies = max(2, min(64, int(np.ceil(2.5 * l2 / wbytes))))
         ws = []
         for c in range(copies):
             if kind == "q4k":
                 blocks = synth.q4k_weights(N, K, seed=100 + c)
                 ws.append((qwp.q4k_repack(torch.from_numpy(blocks.reshape(-1)).to(dev), N, K),))
+            elif kind == "q6k":
+                blocks = synth.q6k_weights(N, K, seed=100 + c)
+                ws.append((qwp.q6k_repack(torch.from_numpy(blocks.reshape(-1)).to(dev), N, K),))
             else:
                 wq, sc, z = synth.w4a16_weights(N, K, g, seed=100 + c)
                 ws.append((qwp.w4a16_repack(torch.from_numpy(wq.view(np.int32)).to(dev)),
                            torch.from_numpy(sc).to(dev), None if "sym" in flags else torch.from_numpy(z).to(dev)))
-        if kind == "q4k" or "bf16" in flags:
+        if kind in ("q4k", "q6k") or "bf16" in flags:
             x = torch.from_numpy(synth.activations_bf16(M, K, seed=7).view(np.int16)).to(dev).view(torch.bfloat16)
         else:
             x = torch.from_numpy(synth.activations_f16(M, K, seed=7)).to(dev)
@@ -274,6 +281,8 @@ def run_gemms(args, specs):
         def call(c):
             if kind == "q4k":
                 qwp.q4k_gemm(ws[c][0], x, N, out=y)
+            elif kind == "q6k":
+                qwp.q6k_gemm(ws[c][0], x, N, out=y)
             else:
                 gemm = qwp.w4a16_gemm_bf16 if "bf16" in flags else qwp.w4a16_gemm
                 gemm(ws[c][0], ws[c][1], ws[c][2], x, N, g, out=y)
@@ -309,7 +318,7 @@ def run_gemms(args, specs):
             "pct_bf16_peak": 100.0 * flops / t / 1e12 / tc_burst,
             "gbs": byts / t / 1e9, "bound": "tensor" if flops / (tc_burst * 1e12) >= byts / (hbm * 1e9) else "hbm",
             "roofline_frac": t_roof / t, "peak_source": peak_kind, "steps": args.steps,
-            "weight_copies": copies, "launches_per_call": 2 if kind == "q4k" or "bf16" in flags else 1,
+            "weight_copies": copies, "launches_per_call": 2 if kind in ("q4k", "q6k") or "bf16" in flags else 1,
         }), flush=True)
         del ws, graphs
         torch.cuda.empty_cache()
@@ -535,7 +544,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gemm", action="append", default=[],
-                    help="time single GEMMs instead of the layer: q4k:M:N:K or w4a16:M:N:K:group")
+                    help="time single GEMMs instead of the layer: q4k:M:N:K, q6k:M:N:K or w4a16:M:N:K:group[:sym][:bf16]")
     ap.add_argument("--sweep", action="store_true", help="time every GEMM shape of the workloads")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -5,8 +5,9 @@
  * is asynchronous and ordered on `stream` (a cudaStream_t passed as void*,
  * NULL = the legacy default stream) and never synchronizes the host, except
  * qwp_device_status.  The caller owns and allocates every input and output
- * buffer; the entry points that take device memory of their own are q4k_gemm
- * and w4a16_gemm_bf16 (activation scratch from a library-owned stream-ordered pool).
+ * buffer; the entry points that take device memory of their own are q4k_gemm,
+ * q6k_gemm and w4a16_gemm_bf16 (activation scratch from a library-owned
+ * stream-ordered pool).
  * Every entry point returns QWP_OK (0) or a negative qwp_status; none throws.
  * Calls are thread-safe.
  *
@@ -136,6 +137,57 @@ QWP_API int q4k_gemm(const void *w_tiled_dev, const void *x_dev, float *y_dev,
  */
 QWP_API int q4k_gemm_noalloc(const void *w_tiled_dev, const void *x_dev, float *y_dev,
                              int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * Q6_K (GGML blocks of 256 weights along K, 210 bytes each: ql[128] low four
+ * bits of the 6-bit codes, qh[64] high two bits, int8 scales[16] (one per 16
+ * weights), fp16 d last; w = d * scale * (q - 32)).  Source: "How ZINC's RDNA4
+ * batched prefill went from 42 to 208 tok/s", sections "Bug 2: Q6_K had a gate
+ * but no dispatcher" and "What changed" (Q4_K_M checkpoints keep ffn_down and
+ * attn_v in Q6_K and the batched path needs a Q6_K kernel); the pages name the
+ * format only, the layout is GGML's.
+ */
+
+/*
+ * Bytes of a repacked Q6_K matrix: (K/256)*210 per stored row, the stored rows
+ * being N rounded up so that the last 128-row tile holds a multiple of 8 rows
+ * (at most 7 zero rows of padding; equal to the GGML size when N % 8 == 0).
+ */
+QWP_API int q6k_repacked_bytes(int64_t N, int64_t K, size_t *out_bytes);
+
+/*
+ * Load-time repack of GGML Q6_K rows (w_ggml_dev: N rows of K/256 blocks,
+ * row-major, N*K/256*210 bytes) into the tile-major order the GEMM streams
+ * (w_tiled_dev, q6k_repacked_bytes bytes, caller-allocated, must not alias):
+ * per 128-row tile and super-block a d plane, a scale plane, four planes of
+ * interleaved low nibbles and four planes of high bits.  K % 256 == 0.  Both
+ * pointers 16-byte aligned.
+ */
+QWP_API int q6k_repack(const void *w_ggml_dev, void *w_tiled_dev, int64_t N, int64_t K, void *stream);
+
+/*
+ * Test entry point: the correctly rounded fp32 of d*scale*(q - 32) of a
+ * repacked Q6_K matrix into w_out_dev[N][K] (d*scale is exact in fp32; one
+ * rounding of the product).
+ */
+QWP_API int q6k_dequant(const void *w_tiled_dev, float *w_out_dev, int64_t N, int64_t K, void *stream);
+
+/*
+ * y_dev[M][N] (fp32) = x_dev[M][K] (fp16) . W^T, W the repacked Q6_K matrix.
+ * Each weight is unpacked on chip to an fp16 tensor-core operand: (q - 32)
+ * exactly, times RN(d*scale) rounded once more to fp16 (two fp16 roundings,
+ * relative error at most 2^-10 for normal results); fp32 accumulation in
+ * tensor memory.  Same shape, alignment and no-allocation rules as q4k_gemm_f16.
+ */
+QWP_API int q6k_gemm_f16(const void *w_tiled_dev, const void *x_dev, float *y_dev,
+                         int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * The same product for bf16 activations, converted to fp16 into pool scratch
+ * first exactly as q4k_gemm does (same rules, same QWP_ERR_RANGE report).
+ */
+QWP_API int q6k_gemm(const void *w_tiled_dev, const void *x_dev, float *y_dev,
+                     int64_t M, int64_t N, int64_t K, void *stream);
 
 /*
  * W4A16 (group-wise int4): wq[N][K/8] int32 words, each holding 8 codes along

@@ -19,6 +19,7 @@ from . import _build
 __all__ = [
     "QwpError", "library", "q4k_repacked_bytes", "q4k_repack", "q4k_dequant", "q4k_gemm", "q4k_gemm_f16",
     "q4k_gemm_noalloc", "NOALLOC_MAX_X_ELEMS",
+    "q6k_repacked_bytes", "q6k_repack", "q6k_dequant", "q6k_gemm", "q6k_gemm_f16",
     "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_bf16",
     "device_status", "EXPORTED_SYMBOLS",
 ]
@@ -26,7 +27,8 @@ __all__ = [
 # Every symbol include/qwp.h declares.
 EXPORTED_SYMBOLS = (
     "qwp_status_string", "q4k_repacked_bytes", "q4k_repack", "q4k_dequant", "q4k_gemm", "q4k_gemm_f16",
-    "q4k_gemm_noalloc", "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_bf16",
+    "q4k_gemm_noalloc", "q6k_repacked_bytes", "q6k_repack", "q6k_dequant", "q6k_gemm", "q6k_gemm_f16",
+    "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_bf16",
     "qwp_device_status",
 )
 
@@ -57,6 +59,11 @@ def library() -> ctypes.CDLL:
         lib.qwp_status_string.restype = ctypes.c_char_p
         lib.q4k_repacked_bytes.argtypes = [i64, i64, sz]
         lib.w4a16_repacked_bytes.argtypes = [i64, i64, sz]
+        lib.q6k_repacked_bytes.argtypes = [i64, i64, sz]
+        lib.q6k_repack.argtypes = [p, p, i64, i64, p]
+        lib.q6k_dequant.argtypes = [p, p, i64, i64, p]
+        lib.q6k_gemm.argtypes = [p, p, p, i64, i64, i64, p]
+        lib.q6k_gemm_f16.argtypes = [p, p, p, i64, i64, i64, p]
         lib.q4k_repack.argtypes = [p, p, i64, i64, p]
         lib.q4k_dequant.argtypes = [p, p, i64, i64, p]
         lib.q4k_gemm.argtypes = [p, p, p, i64, i64, i64, p]
@@ -167,6 +174,57 @@ def q4k_gemm_noalloc(w_tiled: torch.Tensor, x: torch.Tensor, N: int, out: torch.
     _check(library().q4k_gemm_noalloc(_ptr(w_tiled), _ptr(x), _ptr(out), M, N, K, _stream(x)),
            "q4k_gemm_noalloc")
     return out
+
+
+def q6k_repacked_bytes(N: int, K: int) -> int:
+    out = ctypes.c_size_t()
+    _check(library().q6k_repacked_bytes(N, K, ctypes.byref(out)), "q6k_repacked_bytes")
+    return out.value
+
+
+def q6k_repack(w_ggml: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """GGML Q6_K rows (uint8, N*K/256*210 bytes) -> tile-major repacked bytes (q6k_repacked_bytes)."""
+    _dev(w_ggml, torch.uint8, "w_ggml")
+    if K % 256 or w_ggml.numel() != N * (K // 256) * 210:
+        raise ValueError("w_ggml size does not match N, K")
+    nbytes = q6k_repacked_bytes(N, K)
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=w_ggml.device)
+    _dev(out, torch.uint8, "out")
+    if out.numel() != nbytes:
+        raise ValueError("out must hold q6k_repacked_bytes(N, K) bytes")
+    _check(library().q6k_repack(_ptr(w_ggml), _ptr(out), N, K, _stream(w_ggml)), "q6k_repack")
+    return out
+
+
+def q6k_dequant(w_tiled: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    _dev(w_tiled, torch.uint8, "w_tiled")
+    if out is None:
+        out = torch.empty(N, K, dtype=torch.float32, device=w_tiled.device)
+    _dev(out, torch.float32, "out")
+    _check(library().q6k_dequant(_ptr(w_tiled), _ptr(out), N, K, _stream(w_tiled)), "q6k_dequant")
+    return out
+
+
+def _q6k_gemm_call(entry, x_dtype, w_tiled, x, N, out):
+    _dev(w_tiled, torch.uint8, "w_tiled")
+    _dev(x, x_dtype, "x")
+    M, K = x.shape
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.float32, device=x.device)
+    _dev(out, torch.float32, "out")
+    _check(getattr(library(), entry)(_ptr(w_tiled), _ptr(x), _ptr(out), M, N, K, _stream(x)), entry)
+    return out
+
+
+def q6k_gemm(w_tiled: torch.Tensor, x: torch.Tensor, N: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """y[M, N] (fp32) = x[M, K] (bf16) . W^T with W the repacked Q6_K matrix."""
+    return _q6k_gemm_call("q6k_gemm", torch.bfloat16, w_tiled, x, N, out)
+
+
+def q6k_gemm_f16(w_tiled: torch.Tensor, x: torch.Tensor, N: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """y[M, N] (fp32) = x[M, K] (fp16) . W^T with W the repacked Q6_K matrix."""
+    return _q6k_gemm_call("q6k_gemm_f16", torch.float16, w_tiled, x, N, out)
 
 
 def w4a16_repack(wq: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:

@@ -102,6 +102,100 @@ __global__ void q4k_dequant_kernel(const uint8_t *__restrict__ w, float *__restr
     o[1] = make_float4(vals[2].x, vals[2].y, vals[3].x, vals[3].y);
 }
 
+// ---------------------------------------------------------------- Q6_K repack
+
+// Low four bits and high two bits of element e (0..255) of a GGML Q6_K block:
+// in half h, element 32j + l takes its low bits from ql[64h + l + 32(j%2)] (low
+// nibble for j < 2, high nibble for j >= 2) and its high bits from bits 2j..2j+1
+// of qh[32h + l].
+__device__ __forceinline__ uint32_t q6k_src_low(const uint8_t *blk, int e) {
+    const int h = e >> 7, j = (e >> 5) & 3, l = e & 31;
+    const uint32_t byte = blk[64 * h + l + 32 * (j & 1)];
+    return (j < 2) ? (byte & 15u) : (byte >> 4);
+}
+__device__ __forceinline__ uint32_t q6k_src_high(const uint8_t *blk, int e) {
+    const int h = e >> 7, j = (e >> 5) & 3, l = e & 31;
+    return (blk[128 + 32 * h + l] >> (2 * j)) & 3u;
+}
+
+// One warp per (stored row n, super-block b), stored rows running over the
+// padded last tile too (its padding rows are written as zeros).  Lane l builds
+// low word v = l%8 of chunk c = l/8; lanes 0..15 also build high word u = l%4 of
+// chunk l/4; lane 0 copies d, lanes 0..3 four scale bytes each.
+__global__ void q6k_repack_kernel(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst,
+                                  int64_t N, int64_t K, int64_t stored_rows) {
+    const int64_t nb = K / Q4K_BLOCK;
+    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (gw >= stored_rows * nb) return;
+    const int lane = threadIdx.x & 31;
+    const int64_t n = gw / nb, b = gw % nb;
+    const int64_t tile = n / TILE_ROWS;
+    const int i = static_cast<int>(n % TILE_ROWS);
+    const int Rp = q6k_padded_rows(tile_rows(N, tile));
+    const bool real = n < N;
+    const uint8_t *blk = src + (real ? (n * nb + b) * Q6K_BLOCK_BYTES : 0);
+    uint8_t *grp = dst + q6k_group_offset(K, tile, Rp, b);
+    if (lane == 0)
+        *reinterpret_cast<uint16_t *>(grp + 2 * i) =
+            real ? static_cast<uint16_t>(blk[208] | (blk[209] << 8)) : static_cast<uint16_t>(0);
+    if (lane < 4) {
+        uint32_t sc = 0;
+        if (real)
+            for (int t = 0; t < 4; ++t) sc |= static_cast<uint32_t>(blk[192 + 4 * lane + t]) << (8 * t);
+        *reinterpret_cast<uint32_t *>(grp + Q6K_SCALE_PLANE * Rp + 16 * i + 4 * lane) = sc;
+    }
+    {
+        const int c = lane >> 3, v = lane & 7;
+        uint32_t word = 0;
+        if (real)
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+                word |= q6k_src_low(blk, 64 * c + 8 * v + t) << ((t & 1) ? 16 + 4 * (t >> 1) : 4 * (t >> 1));
+        *reinterpret_cast<uint32_t *>(grp + q6k_low_word_offset(Rp, i, c, v)) = word;
+    }
+    if (lane < 16) {
+        const int c = lane >> 2, u = lane & 3;
+        uint32_t word = 0;
+        if (real)
+#pragma unroll
+            for (int t = 0; t < 16; ++t) word |= q6k_src_high(blk, 64 * c + 16 * u + t) << q6k_high_bit(t);
+        *reinterpret_cast<uint32_t *>(grp + q6k_high_word_offset(Rp, i, c, u)) = word;
+    }
+}
+
+// One warp per (row, super-block); lane l dequantizes elements 8l..8l+7 (low
+// word v = l%8 of chunk c = l/8): (q - 32) exactly from the GEMM's magic pair,
+// then one fp32 rounding of d*sc (exact) times (q - 32).
+__global__ void q6k_dequant_kernel(const uint8_t *__restrict__ w, float *__restrict__ out,
+                                   int64_t N, int64_t K) {
+    const int64_t nb = K / Q4K_BLOCK;
+    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (gw >= N * nb) return;
+    const int lane = threadIdx.x & 31;
+    const int64_t n = gw / nb, b = gw % nb;
+    const int64_t tile = n / TILE_ROWS;
+    const int i = static_cast<int>(n % TILE_ROWS);
+    const int Rp = q6k_padded_rows(tile_rows(N, tile));
+    const uint8_t *grp = w + q6k_group_offset(K, tile, Rp, b);
+    const int c = lane >> 3, v = lane & 7;
+    const float d = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(grp + 2 * i)));
+    const int sc = static_cast<int8_t>(grp[Q6K_SCALE_PLANE * Rp + 16 * i + 4 * c + (v >> 1)]);
+    const float dl = d * static_cast<float>(sc);
+    const uint32_t lo = *reinterpret_cast<const uint32_t *>(grp + q6k_low_word_offset(Rp, i, c, v));
+    const uint32_t hi = *reinterpret_cast<const uint32_t *>(grp + q6k_high_word_offset(Rp, i, c, v >> 1));
+    float vals[8];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const uint32_t m = (v & 1) ? q6k_pair_magic<1>(lo, hi, p) : q6k_pair_magic<0>(lo, hi, p);
+        const float2 q = __half22float2(q6k_centered(m));
+        vals[2 * p] = dl * q.x;
+        vals[2 * p + 1] = dl * q.y;
+    }
+    float4 *o = reinterpret_cast<float4 *>(out + n * K + b * Q4K_BLOCK + 8 * lane);
+    o[0] = make_float4(vals[0], vals[1], vals[2], vals[3]);
+    o[1] = make_float4(vals[4], vals[5], vals[6], vals[7]);
+}
+
 // ---------------------------------------------------------------- W4A16 repack
 
 // One thread per word; consecutive threads read consecutive source words.
@@ -219,6 +313,19 @@ extern "C" int q4k_repacked_bytes(int64_t N, int64_t K, size_t *out_bytes) {
     return QWP_OK;
 }
 
+// Stored rows of the Q6_K layout: full tiles plus the last tile padded to a multiple of 8.
+static int64_t q6k_stored_rows(int64_t N) {
+    const int64_t full = N / TILE_ROWS * TILE_ROWS;
+    return full + q6k_padded_rows(static_cast<int>(N - full));
+}
+
+extern "C" int q6k_repacked_bytes(int64_t N, int64_t K, size_t *out_bytes) {
+    if (!out_bytes || N < 0 || K < 0) return QWP_ERR_INVALID_ARG;
+    if (K % Q4K_BLOCK) return QWP_ERR_UNSUPPORTED_SHAPE;
+    *out_bytes = static_cast<size_t>(q6k_stored_rows(N)) * static_cast<size_t>(K / Q4K_BLOCK) * Q6K_BLOCK_BYTES;
+    return QWP_OK;
+}
+
 extern "C" int w4a16_repacked_bytes(int64_t N, int64_t K, size_t *out_bytes) {
     if (!out_bytes || N < 0 || K < 0) return QWP_ERR_INVALID_ARG;
     if (K % CHUNK_K) return QWP_ERR_UNSUPPORTED_SHAPE;
@@ -250,6 +357,25 @@ extern "C" int q4k_dequant(const void *w_tiled, float *w_out, int64_t N, int64_t
     if (rc || N == 0 || K == 0) return rc;
     const int64_t threads = N * (K / Q4K_BLOCK) * 32;
     q4k_dequant_kernel<<<grid_for(threads, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t *>(w_tiled), w_out, N, K);
+    return launch_status();
+}
+
+extern "C" int q6k_repack(const void *w_ggml, void *w_tiled, int64_t N, int64_t K, void *stream) {
+    int rc = q4k_common_checks(w_ggml, w_tiled, N, K);
+    if (rc || N == 0 || K == 0) return rc;
+    const int64_t rows = q6k_stored_rows(N);
+    const int64_t threads = rows * (K / Q4K_BLOCK) * 32;
+    q6k_repack_kernel<<<grid_for(threads, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t *>(w_ggml), static_cast<uint8_t *>(w_tiled), N, K, rows);
+    return launch_status();
+}
+
+extern "C" int q6k_dequant(const void *w_tiled, float *w_out, int64_t N, int64_t K, void *stream) {
+    int rc = q4k_common_checks(w_tiled, w_out, N, K);
+    if (rc || N == 0 || K == 0) return rc;
+    const int64_t threads = N * (K / Q4K_BLOCK) * 32;
+    q6k_dequant_kernel<<<grid_for(threads, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint8_t *>(w_tiled), w_out, N, K);
     return launch_status();
 }

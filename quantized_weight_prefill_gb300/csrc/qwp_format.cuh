@@ -19,6 +19,25 @@
 // 512 contiguous bytes of shared memory (no bank conflicts), and the whole
 // group is one contiguous bulk copy.
 //
+// Q6_K, repacked order.  Same 128-row tiles, but the last tile's R rows are
+// padded to Rp = R rounded up to a multiple of 8 (zero bytes), so that every
+// group is a multiple of 16 bytes; full tiles have Rp = 128.  Tile t starts at
+// byte 128*t * (K/256) * 210.  Inside a tile, super-block b of all Rp rows is
+// one group of Rp*210 bytes at offset b*Rp*210:
+//   d plane        2*Rp bytes: row i's fp16 d at 2*i;
+//   scale plane    16*Rp bytes at 2*Rp: row i's 16 int8 scales at 16*i;
+//   low plane c    (c = 0..3) 32*Rp bytes at 18*Rp + 32*Rp*c, [h][row i][16 B]
+//                  like the Q4_K chunk planes: word v holds the low four bits of
+//                  elements 64c + 8v + t in the interleaved nibble order;
+//   high plane c   16*Rp bytes at 146*Rp + 16*Rp*c, [row i][16 B]: word u (0..3)
+//                  holds the high two bits of elements 64c + 16u + t, t = 0..15:
+//                  t = 2p + o (p = 0..3, o = 0..1) at bits 4+2p+16o, and
+//                  t = 8 + 2p + o at bits (12+2p+16o) mod 32.  Rotating word u
+//                  right by 2p (elements of low word 2u) or 8+2p (low word 2u+1)
+//                  puts pair p's two fields at bits 4-5 and 20-21, just above the
+//                  pair's low nibbles once the low word is shifted right by 4p.
+// 210 bytes per 256 weights as in GGML (plus the row padding of the last tile).
+//
 // W4A16, repacked order.  Same 128-row tiles; tile t starts at 128*t * K/2.
 // Inside, K-block j (64 weights along K) of all R rows is a plane of 32*R bytes
 // at j*32*R, laid out [h][row i][16 bytes] as above, word v being the original
@@ -37,6 +56,10 @@ constexpr int Q4K_BLOCK_BYTES = 144;
 constexpr int Q4K_HEADER_BYTES = 16;
 constexpr int CHUNK_K = 64;          // weights per chunk (one 128-byte row of bf16 / fp16)
 constexpr int CHUNK_ROW_BYTES = 32;  // packed bytes of one row's chunk
+constexpr int Q6K_BLOCK_BYTES = 210;
+constexpr int Q6K_SCALE_PLANE = 2;   // x Rp: byte offset of the scale plane
+constexpr int Q6K_LOW_PLANE = 18;    // x Rp: first low plane
+constexpr int Q6K_HIGH_PLANE = 146;  // x Rp: first high plane
 
 __host__ __device__ __forceinline__ int tile_rows(int64_t N, int64_t tile) {
     int64_t r = N - tile * TILE_ROWS;
@@ -47,6 +70,28 @@ __host__ __device__ __forceinline__ int tile_rows(int64_t N, int64_t tile) {
 __host__ __device__ __forceinline__ int64_t q4k_group_offset(int64_t K, int64_t tile, int R,
                                                              int64_t b) {
     return tile * TILE_ROWS * (K / Q4K_BLOCK) * Q4K_BLOCK_BYTES + b * R * Q4K_BLOCK_BYTES;
+}
+
+// Rows of tile `tile` as stored in the Q6_K layout (a multiple of 8).
+__host__ __device__ __forceinline__ int q6k_padded_rows(int R) { return (R + 7) & ~7; }
+
+// Byte offset of super-block b's group inside the tiled Q6_K matrix (Rp padded rows).
+__host__ __device__ __forceinline__ int64_t q6k_group_offset(int64_t K, int64_t tile, int Rp,
+                                                             int64_t b) {
+    return tile * TILE_ROWS * (K / Q4K_BLOCK) * Q6K_BLOCK_BYTES + b * Rp * Q6K_BLOCK_BYTES;
+}
+
+// Offsets inside a Q6_K group: low word v and high word u of (row i, chunk c).
+__host__ __device__ __forceinline__ int q6k_low_word_offset(int Rp, int i, int c, int v) {
+    return Q6K_LOW_PLANE * Rp + CHUNK_ROW_BYTES * Rp * c + ((v >> 2) * Rp + i) * 16 + 4 * (v & 3);
+}
+__host__ __device__ __forceinline__ int q6k_high_word_offset(int Rp, int i, int c, int u) {
+    return Q6K_HIGH_PLANE * Rp + 16 * Rp * c + i * 16 + 4 * u;
+}
+// Bit position of the high two bits of element t (0..15) inside its high word.
+__host__ __device__ __forceinline__ int q6k_high_bit(int t) {
+    const int p = (t & 7) >> 1, o = t & 1;
+    return (t < 8) ? 4 + 2 * p + 16 * o : (12 + 2 * p + 16 * o) & 31;
 }
 
 // Offset of word v of (row i, chunk c) inside a Q4_K super-block group.
@@ -165,6 +210,40 @@ __device__ __forceinline__ void q4k_word_f16x2(uint32_t word, const Q4kSubH &k, 
     p[1] = as_u32(__hfma2(q1, k.d2, k.nml2));
     p[2] = as_u32(__hfma2(q2, k.d2, k.nml2));
     p[3] = as_u32(__hfma2(q3, k.d2, k.nml2));
+}
+
+// ---------------------------------------------------------------- Q6_K unpack
+
+// Pair p of low word `lo` with its high bits from high word `hi` (set 0: the word's
+// first 8 elements, set 1: the second 8) as raw fp16x2 bits (1024+q, 1024+q').
+template <int kSet>
+__device__ __forceinline__ uint32_t q6k_pair_magic(uint32_t lo, uint32_t hi, int p) {
+    const uint32_t a = lo >> (4 * p);
+    const uint32_t b = __funnelshift_r(hi, hi, (kSet ? 8 : 0) + 2 * p);
+    return (a & 0x000F000Fu) | (b & 0x00300030u) | 0x64006400u;
+}
+
+// (q - 32) of a magic pair, exact: (1024 + q) - 1056.
+__device__ __forceinline__ __half2 q6k_centered(uint32_t magic) {
+    return __hsub2(as_half2(magic), as_half2(0x64206420u));
+}
+
+// The 8 weights of low word `lo` as fp16x2 MMA operands RN(RN(d*sc) * (q - 32)).
+template <int kSet>
+__device__ __forceinline__ void q6k_word_f16x2(uint32_t lo, uint32_t hi, __half2 ds2, uint32_t (&p)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = as_u32(__hmul2(q6k_centered(q6k_pair_magic<kSet>(lo, hi, i)), ds2));
+}
+
+// RN(d * sc_u) for the four sub-blocks u of one 64-wide chunk, as fp16x2 (d is the
+// block's fp16 bits, sc4 its four int8 scales).  d * sc is exact in fp32.
+__device__ __forceinline__ void q6k_chunk_scales(uint32_t dbits, uint32_t sc4, __half2 (&ds)[4]) {
+    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int sc = static_cast<int8_t>(static_cast<uint8_t>(sc4 >> (8 * u)));
+        ds[u] = __float2half2_rn(d * static_cast<float>(sc));
+    }
 }
 
 // ---------------------------------------------------------------- W4A16 unpack

@@ -1,6 +1,6 @@
 // Fused dequant-in-tile GEMM on the 5th-generation tensor cores (tcgen05).
 //
-// y[M,N] = x[M,K] . W[N,K]^T with W in 4-bit form.  Method: "The dequant
+// y[M,N] = x[M,K] . W[N,K]^T with W in 4-bit (Q4_K, W4A16) or 6-bit (Q6_K) form.  Method: "The dequant
 // scratch round-trip is ZINC's last RDNA4 prefill tax", sections "The two
 // passes hiding inside one matmul" and "What the roofline says" -- every
 // packed weight block is read from global memory once, unpacked on chip and
@@ -47,6 +47,9 @@
 #include "qwp_ptx.cuh"
 
 namespace qwp {
+
+// Weight formats (the kernel's template parameter).
+enum : int { FMT_W4A16 = 0, FMT_Q4K = 1, FMT_Q6K = 2, NUM_FMTS = 3 };
 
 constexpr int XFORM_GROUPS = 4;                    // groups take K blocks in turn, one per weight stage
 constexpr int NUM_XFORM_WARPS = 4 * XFORM_GROUPS;  // 4 warps (one per lane quarter) cover one K block
@@ -173,9 +176,30 @@ __device__ __forceinline__ void unpack_quarter(uint4 wv, const Q4kSubH &ks, __ha
     }
 }
 
-template <bool kQ4K>
+// Q6_K: low words 4q..4q+3 of a chunk (wv) with their high words h0 (sub-block
+// 2q) and h1 (sub-block 2q+1) into regs[off .. off+15].
+__device__ __forceinline__ void unpack_q6k_quarter(uint4 wv, uint32_t h0, uint32_t h1, __half2 ds0, __half2 ds1,
+                                                   uint32_t (&regs)[32], int off) {
+    uint32_t p[4];
+    q6k_word_f16x2<0>(wv.x, h0, ds0, p);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) regs[off + e] = p[e];
+    q6k_word_f16x2<1>(wv.y, h0, ds0, p);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) regs[off + 4 + e] = p[e];
+    q6k_word_f16x2<0>(wv.z, h1, ds1, p);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) regs[off + 8 + e] = p[e];
+    q6k_word_f16x2<1>(wv.w, h1, ds1, p);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) regs[off + 12 + e] = p[e];
+}
+
+template <int kFmt>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     qwp_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmArgs args) {
+    constexpr bool kQ4K = kFmt == FMT_Q4K;
+    constexpr bool kQ6K = kFmt == FMT_Q6K;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -235,6 +259,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (kQ4K) {
             src = args.w + q4k_group_offset(args.K, tile, R, kb0 / KB_PER_STAGE);
             bytes = static_cast<uint32_t>(R) * Q4K_BLOCK_BYTES;
+        } else if (kQ6K) {
+            const int Rp = q6k_padded_rows(R);
+            src = args.w + q6k_group_offset(args.K, tile, Rp, kb0 / KB_PER_STAGE);
+            bytes = static_cast<uint32_t>(Rp) * Q6K_BLOCK_BYTES;
         } else {
             src = args.w + w4_plane_offset(args.K, tile, R, kb0);
             bytes = static_cast<uint32_t>(R) * CHUNK_ROW_BYTES * nblk;
@@ -413,8 +441,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint4 wv0 = make_uint4(0, 0, 0, 0), wv1 = make_uint4(0, 0, 0, 0);
             Q4kSubH k0, k1;
             __half2 s2 = __float2half2_rn(0.f), mz = w4_magic_zero(0);
+            uint4 hv = make_uint4(0, 0, 0, 0);  // Q6_K: high-bit words of this block
+            __half2 ds[4];                      // Q6_K: RN(d*sc) of its four sub-blocks
+            if (kQ6K)
+                for (int u = 0; u < 4; ++u) ds[u] = __float2half2_rn(0.f);
             if (has_block) {
-                if (kQ4K) {
+                if (kQ6K) {
+                    if (valid) {
+                        const int Rp = q6k_padded_rows(R);
+                        const uint32_t dbits = *reinterpret_cast<const uint16_t *>(wst + 2 * r);
+                        const uint32_t sc4 =
+                            *reinterpret_cast<const uint32_t *>(wst + Q6K_SCALE_PLANE * Rp + 16 * r + 4 * grp);
+                        const uint8_t *lp = wst + Q6K_LOW_PLANE * Rp + CHUNK_ROW_BYTES * Rp * grp + r * 16;
+                        wv0 = *reinterpret_cast<const uint4 *>(lp);
+                        wv1 = *reinterpret_cast<const uint4 *>(lp + 16 * Rp);
+                        hv = *reinterpret_cast<const uint4 *>(wst + Q6K_HIGH_PLANE * Rp + 16 * Rp * grp + r * 16);
+                        q6k_chunk_scales(dbits, sc4, ds);
+                    }
+                } else if (kQ4K) {
                     uint4 hdr = make_uint4(0, 0, 0, 0);
                     if (valid) {
                         hdr = *reinterpret_cast<const uint4 *>(wst + Q4K_HEADER_BYTES * r);
@@ -440,8 +484,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(w_empty + 8 * ws);
             if (has_block) {
-                unpack_quarter<kQ4K>(wv0, k0, mz, s2, regs, 0);
-                unpack_quarter<kQ4K>(wv1, k1, mz, s2, regs, 16);
+                if (kQ6K) {
+                    unpack_q6k_quarter(wv0, hv.x, hv.y, ds[0], ds[1], regs, 0);
+                    unpack_q6k_quarter(wv1, hv.z, hv.w, ds[2], ds[3], regs, 16);
+                } else {
+                    unpack_quarter<kQ4K>(wv0, k0, mz, s2, regs, 0);
+                    unpack_quarter<kQ4K>(wv1, k1, mz, s2, regs, 16);
+                }
             }
             return true;
         };
@@ -812,11 +861,11 @@ static int choose_bn(int64_t M, int cap) {
 
 struct DeviceInfo {
     int sms = 0;
-    int slots[2][MAX_SPLITS + 1] = {};  // [kQ4K][S]: CTAs resident at once with clusters of S
-    bool ready[2] = {false, false};
+    int slots[NUM_FMTS][MAX_SPLITS + 1] = {};  // [format][S]: CTAs resident at once with clusters of S
+    bool ready[NUM_FMTS] = {};
 };
 
-template <bool kQ4K>
+template <int kFmt>
 static int device_info(DeviceInfo *&out) {
     static DeviceInfo info[64];
     static std::mutex mu;
@@ -824,13 +873,13 @@ static int device_info(DeviceInfo *&out) {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QWP_ERR_CUDA;
     std::lock_guard<std::mutex> lock(mu);
     DeviceInfo &d = info[dev];
-    if (!d.ready[kQ4K]) {
+    if (!d.ready[kFmt]) {
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return QWP_ERR_CUDA;
-        if (cudaFuncSetAttribute(qwp_gemm_kernel<kQ4K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(qwp_gemm_kernel<kFmt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_BYTES) != cudaSuccess)
             return QWP_ERR_CUDA;
-        d.slots[kQ4K][1] = d.sms;
+        d.slots[kFmt][1] = d.sms;
         for (int S = 2; S <= MAX_SPLITS; ++S) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(1, 1, S * 64);
@@ -844,13 +893,13 @@ static int device_info(DeviceInfo *&out) {
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
             int clusters = 0;
-            if (cudaOccupancyMaxActiveClusters(&clusters, qwp_gemm_kernel<kQ4K>, &cfg) != cudaSuccess) {
+            if (cudaOccupancyMaxActiveClusters(&clusters, qwp_gemm_kernel<kFmt>, &cfg) != cudaSuccess) {
                 cudaGetLastError();
                 clusters = 0;
             }
-            d.slots[kQ4K][S] = clusters * S;
+            d.slots[kFmt][S] = clusters * S;
         }
-        d.ready[kQ4K] = true;
+        d.ready[kFmt] = true;
     }
     out = &d;
     return QWP_OK;
@@ -922,31 +971,33 @@ static Plan choose_plan(const int *slots, int64_t units, int nstages, int64_t nk
 // x is fp16 [M, K].  `after_prior` launches with programmatic stream
 // serialization so the kernel's set-up and weight prefetch overlap the grid just
 // before it (the x producer waits for that grid with griddepcontrol.wait).
-template <bool kQ4K>
+template <int kFmt>
 static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, const void *x,
                        float *y, int64_t M, int64_t N, int64_t K, int64_t group, cudaStream_t stream,
                        uint64_t timeout_ns, bool after_prior) {
     int rc = check_device();
     if (rc) return rc;
     DeviceInfo *info = nullptr;
-    if ((rc = device_info<kQ4K>(info))) return rc;
+    if ((rc = device_info<kFmt>(info))) return rc;
     uint32_t *status = status_word();
     if (!status) return QWP_ERR_CUDA;
     const int64_t row_tiles = (N + TILE_ROWS - 1) / TILE_ROWS;
     const int64_t nkb_total = K / CHUNK_K;
     const int nstages = static_cast<int>((nkb_total + KB_PER_STAGE - 1) / KB_PER_STAGE);
-    const int w_stage_bytes = kQ4K ? TILE_ROWS * Q4K_BLOCK_BYTES : TILE_ROWS * CHUNK_ROW_BYTES * KB_PER_STAGE;
+    const int w_stage_bytes = kFmt == FMT_Q4K   ? TILE_ROWS * Q4K_BLOCK_BYTES
+                              : kFmt == FMT_Q6K ? TILE_ROWS * Q6K_BLOCK_BYTES
+                                                : TILE_ROWS * CHUNK_ROW_BYTES * KB_PER_STAGE;
     // Token tile: the widest (fewest tiles of <= 256 tokens) unless tiles of <= 128,
     // which allow split-K and two accumulators, give a cheaper plan (few units).
     int bn = choose_bn(M, BN_MAX);
     int64_t tok_tiles = (M + bn - 1) / bn;
     if (row_tiles * tok_tiles > 0x7fffffff) return QWP_ERR_UNSUPPORTED_SHAPE;
-    Plan plan = choose_plan(info->slots[kQ4K], row_tiles * tok_tiles, nstages, nkb_total, bn, w_stage_bytes);
+    Plan plan = choose_plan(info->slots[kFmt], row_tiles * tok_tiles, nstages, nkb_total, bn, w_stage_bytes);
     if (bn > static_cast<int>(ACC_STRIDE)) {
         const int bn2 = choose_bn(M, static_cast<int>(ACC_STRIDE));
         const int64_t tt2 = (M + bn2 - 1) / bn2;
         if (row_tiles * tt2 <= 0x7fffffff) {
-            const Plan p2 = choose_plan(info->slots[kQ4K], row_tiles * tt2, nstages, nkb_total, bn2, w_stage_bytes);
+            const Plan p2 = choose_plan(info->slots[kFmt], row_tiles * tt2, nstages, nkb_total, bn2, w_stage_bytes);
             if (p2.cost < plan.cost - 1e-9) {
                 plan = p2;
                 bn = bn2;
@@ -1010,7 +1061,7 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     }
     cfg.attrs = attrs;
     cfg.numAttrs = nattr;
-    if (cudaLaunchKernelEx(&cfg, qwp_gemm_kernel<kQ4K>, map, a) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, qwp_gemm_kernel<kFmt>, map, a) != cudaSuccess) {
         cudaGetLastError();
         return QWP_ERR_CUDA;
     }
@@ -1059,7 +1110,7 @@ extern "C" int q4k_gemm_f16(const void *w_tiled, const void *x, float *y, int64_
     if (K % Q4K_BLOCK || K == 0) return K < 0 ? QWP_ERR_INVALID_ARG : QWP_ERR_UNSUPPORTED_SHAPE;
     int rc = gemm_shape_checks(w_tiled, x, y, M, N, K);
     if (rc || M == 0 || N == 0) return rc;
-    return launch_gemm<true>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0,
+    return launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0,
                              static_cast<cudaStream_t>(stream), kDefaultTimeoutNs, false);
 }
 
@@ -1078,7 +1129,36 @@ extern "C" int q4k_gemm(const void *w_tiled, const void *x, float *y, int64_t M,
         return QWP_ERR_CUDA;
     }
     rc = launch_bf16_to_f16(x, x16, M * K, s);
-    if (!rc) rc = launch_gemm<true>(w_tiled, nullptr, nullptr, x16, y, M, N, K, 0, s, kDefaultTimeoutNs, true);
+    if (!rc) rc = launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x16, y, M, N, K, 0, s, kDefaultTimeoutNs, true);
+    if (cudaFreeAsync(x16, s) != cudaSuccess && !rc) rc = QWP_ERR_CUDA;
+    return rc;
+}
+
+extern "C" int q6k_gemm_f16(const void *w_tiled, const void *x, float *y, int64_t M, int64_t N,
+                            int64_t K, void *stream) {
+    if (K % Q4K_BLOCK || K == 0) return K < 0 ? QWP_ERR_INVALID_ARG : QWP_ERR_UNSUPPORTED_SHAPE;
+    int rc = gemm_shape_checks(w_tiled, x, y, M, N, K);
+    if (rc || M == 0 || N == 0) return rc;
+    return launch_gemm<FMT_Q6K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0,
+                                static_cast<cudaStream_t>(stream), kDefaultTimeoutNs, false);
+}
+
+extern "C" int q6k_gemm(const void *w_tiled, const void *x, float *y, int64_t M, int64_t N,
+                        int64_t K, void *stream) {
+    if (K % Q4K_BLOCK || K == 0) return K < 0 ? QWP_ERR_INVALID_ARG : QWP_ERR_UNSUPPORTED_SHAPE;
+    int rc = gemm_shape_checks(w_tiled, x, y, M, N, K);
+    if (rc || M == 0 || N == 0) return rc;
+    if ((rc = check_device())) return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaMemPool_t pool;
+    if ((rc = scratch_pool(&pool))) return rc;
+    void *x16 = nullptr;
+    if (cudaMallocFromPoolAsync(&x16, static_cast<size_t>(M) * K * 2, pool, s) != cudaSuccess) {
+        cudaGetLastError();
+        return QWP_ERR_CUDA;
+    }
+    rc = launch_bf16_to_f16(x, x16, M * K, s);
+    if (!rc) rc = launch_gemm<FMT_Q6K>(w_tiled, nullptr, nullptr, x16, y, M, N, K, 0, s, kDefaultTimeoutNs, true);
     if (cudaFreeAsync(x16, s) != cudaSuccess && !rc) rc = QWP_ERR_CUDA;
     return rc;
 }
@@ -1091,7 +1171,7 @@ extern "C" int w4a16_gemm(const void *wq_tiled, const void *scales, const uint8_
     int rc = gemm_shape_checks(wq_tiled, x, y, M, N, K);
     if (rc || M == 0 || N == 0) return rc;
     if (!scales) return QWP_ERR_INVALID_ARG;
-    return launch_gemm<false>(wq_tiled, scales, zeros, x, y, M, N, K, group,
+    return launch_gemm<FMT_W4A16>(wq_tiled, scales, zeros, x, y, M, N, K, group,
                               static_cast<cudaStream_t>(stream), kDefaultTimeoutNs, false);
 }
 
@@ -1113,7 +1193,7 @@ extern "C" int w4a16_gemm_bf16(const void *wq_tiled, const void *scales, const u
         return QWP_ERR_CUDA;
     }
     rc = launch_bf16_to_f16(x, x16, M * K, s);
-    if (!rc) rc = launch_gemm<false>(wq_tiled, scales, zeros, x16, y, M, N, K, group, s, kDefaultTimeoutNs, true);
+    if (!rc) rc = launch_gemm<FMT_W4A16>(wq_tiled, scales, zeros, x16, y, M, N, K, group, s, kDefaultTimeoutNs, true);
     if (cudaFreeAsync(x16, s) != cudaSuccess && !rc) rc = QWP_ERR_CUDA;
     return rc;
 }

@@ -41,6 +41,73 @@ def q4k_tiled_reference(blocks: np.ndarray, N: int, K: int) -> np.ndarray:
     return out
 
 
+def q6k_codes(blocks: np.ndarray, N: int, K: int) -> np.ndarray:
+    """The 6-bit codes [N, K] of GGML Q6_K rows, read through the oracle's dequant with
+    every scale set to 1 and d to 1.0 (w = q - 32)."""
+    raw = blocks.reshape(N, K // 256, 210).copy()
+    raw[:, :, 192:208] = 1
+    raw[:, :, 208], raw[:, :, 209] = 0x00, 0x3C
+    return (oracle.q6k_dequant(raw.reshape(-1), N, K) + 32).astype(np.uint32)
+
+
+def q6k_high_bit(t: int) -> int:
+    p, o = (t & 7) >> 1, t & 1
+    return 4 + 2 * p + 16 * o if t < 8 else (12 + 2 * p + 16 * o) & 31
+
+
+def q6k_tiled_reference(blocks: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Tile-major Q6_K order: the last tile padded to a multiple of 8 rows; per tile and
+    super-block a d plane [row][2 B], a scale plane [row][16 B], four low planes
+    [h][row][16 B] (interleaved nibbles as in Q4_K) and four high planes [row][16 B]
+    (word u: high bits of chunk elements 16u+t at q6k_high_bit(t))."""
+    nb = K // 256
+    raw = blocks.reshape(N, nb, 210)
+    codes = q6k_codes(blocks, N, K).reshape(N, nb, 256)
+    full = N // 128 * 128
+    stored = full + ((N - full + 7) // 8 * 8)
+    out = np.zeros(stored * nb * 210, np.uint8)
+    for t0 in range(0, N, 128):
+        R = min(128, N - t0)
+        Rp = (R + 7) // 8 * 8
+        for b in range(nb):
+            base = t0 * nb * 210 + b * Rp * 210
+            grp = out[base:base + Rp * 210]
+            grp[:2 * R] = raw[t0:t0 + R, b, 208:210].reshape(-1)
+            grp[2 * Rp:2 * Rp + 16 * R] = raw[t0:t0 + R, b, 192:208].reshape(-1)
+            q = codes[t0:t0 + R, b]                                    # [R, 256]
+            for c in range(4):
+                lo = q[:, 64 * c:64 * c + 64] & 15
+                words = np.zeros((R, 8), np.uint32)
+                for t in range(8):
+                    shift = 16 + 4 * (t // 2) if t % 2 else 4 * (t // 2)
+                    words |= lo[:, t::8] << shift
+                plane = np.zeros((2, Rp, 4), np.uint32)
+                plane[:, :R] = words.reshape(R, 2, 4).transpose(1, 0, 2)
+                start = 18 * Rp + 32 * Rp * c
+                grp[start:start + 32 * Rp] = plane.astype("<u4").reshape(-1).view(np.uint8)
+                hi = q[:, 64 * c:64 * c + 64] >> 4
+                hw = np.zeros((Rp, 4), np.uint32)
+                for t in range(16):
+                    hw[:R] |= hi[:, t::16] << q6k_high_bit(t)
+                start = 146 * Rp + 16 * Rp * c
+                grp[start:start + 16 * Rp] = hw.astype("<u4").reshape(-1).view(np.uint8)
+    return out
+
+
+def q6k_oracle_rows(blocks: np.ndarray, xb_rows: np.ndarray, N: int, K: int, chunk: int = 2048):
+    """Oracle y and sum|x*w| of the Q6_K GEMM for the given bf16 activation rows."""
+    x = oracle.bf16_to_f64(xb_rows).reshape(-1, K)
+    raw = blocks.reshape(N, -1)
+    ys, ms = [], []
+    for n0 in range(0, N, chunk):
+        n1 = min(N, n0 + chunk)
+        w = oracle.q6k_dequant(raw[n0:n1], n1 - n0, K)
+        y, a = oracle.gemm(x, w)
+        ys.append(y)
+        ms.append(a)
+    return np.concatenate(ys, axis=1), np.concatenate(ms, axis=1)
+
+
 def w4a16_tiled_reference(wq: np.ndarray, N: int, K: int) -> np.ndarray:
     """Tile-major W4A16 order: per 128-row tile and 64-wide K-block, a plane [h][row][4 words]."""
     words = wq.view(np.uint32).reshape(N, K // 8)

@@ -52,6 +52,11 @@ def test_repacked_bytes(lib):
     assert qwp.q4k_repacked_bytes(4096, 4096) == 4096 * 16 * 144
     assert qwp.q4k_repacked_bytes(3, 512) == 3 * 2 * 144
     assert qwp.w4a16_repacked_bytes(12288, 4096) == 12288 * 4096 // 2
+    # Q6_K: the last tile is padded to a multiple of 8 rows
+    assert qwp.q6k_repacked_bytes(4096, 12288) == 4096 * 48 * 210
+    assert qwp.q6k_repacked_bytes(130, 256) == (128 + 8) * 210
+    assert qwp.q6k_repacked_bytes(1, 512) == 8 * 2 * 210
+    assert lib.q6k_repacked_bytes(4, 100, ctypes.byref(ctypes.c_size_t())) == SHAPE
     with pytest.raises(qwp.QwpError) as e:
         qwp.q4k_repacked_bytes(4, 100)
     assert e.value.code == SHAPE
@@ -86,6 +91,12 @@ def test_gemm_argument_checks_before_any_cuda_call(lib):
     assert lib.q4k_gemm(None, None, None, 8, 0, 256, None) == OK
     assert lib.q4k_gemm_f16(a16, a16, a16, 8, 8, 100, None) == SHAPE
     assert lib.q4k_gemm_f16(a16, _p(0x1008), a16, 8, 8, 256, None) == MISALIGNED
+    assert lib.q6k_gemm(a16, a16, a16, 8, 8, 100, None) == SHAPE
+    assert lib.q6k_gemm(None, a16, a16, 8, 8, 256, None) == INVALID
+    assert lib.q6k_gemm_f16(a16, _p(0x1004), a16, 8, 8, 256, None) == MISALIGNED
+    assert lib.q6k_gemm(None, None, None, 0, 8, 256, None) == OK
+    assert lib.q6k_repack(a16, a16, 4, 256, None) == INVALID          # aliasing
+    assert lib.q6k_dequant(a16, _p(0x2008), 4, 300, None) == SHAPE
     # repack / dequant checks
     assert lib.q4k_repack(a16, a16, 4, 256, None) == INVALID          # aliasing
     assert lib.q4k_repack(a16, _p(0x2008), 4, 256, None) == MISALIGNED

@@ -13,8 +13,8 @@ import torch
 import oracle
 import quantized_weight_prefill_gb300 as qwp
 import synth
-from helpers import (check_bound, q4k_oracle_rows, q4k_tiled_reference, sample_rows,
-                     w4a16_oracle_rows, w4a16_tiled_reference)
+from helpers import (check_bound, q4k_oracle_rows, q4k_tiled_reference, q6k_oracle_rows, q6k_tiled_reference,
+                     sample_rows, w4a16_oracle_rows, w4a16_tiled_reference)
 
 pytestmark = pytest.mark.gpu
 
@@ -24,6 +24,12 @@ DEV = "cuda"
 def _q4k_on_gpu(N, K, seed):
     blocks = synth.q4k_weights(N, K, seed=seed)
     w = qwp.q4k_repack(torch.from_numpy(blocks.reshape(-1)).to(DEV), N, K)
+    return blocks, w
+
+
+def _q6k_on_gpu(N, K, seed):
+    blocks = synth.q6k_weights(N, K, seed=seed)
+    w = qwp.q6k_repack(torch.from_numpy(blocks.reshape(-1)).to(DEV), N, K)
     return blocks, w
 
 
@@ -199,6 +205,65 @@ def test_w4a16_bf16_activation_beyond_fp16_range_is_reported():
     assert qwp.device_status() == 0
     ref, mag = oracle.w4a16_gemm_bf16(wq, s, z, xb, N, K, g)
     check_bound(y, ref, mag, "w4a16 bf16 after a range error")
+
+
+# --- Q6_K ------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,K", [(1, 256), (5, 512), (130, 256), (300, 768)])
+def test_q6k_repack_layout(N, K):
+    blocks, w = _q6k_on_gpu(N, K, seed=N + K)
+    assert w.numel() == qwp.q6k_repacked_bytes(N, K)
+    assert np.array_equal(w.cpu().numpy(), q6k_tiled_reference(blocks, N, K))
+
+
+@pytest.mark.parametrize("N,K", [(1, 256), (9, 512), (130, 512), (4096, 4096)])
+def test_q6k_dequant_bit_exact(N, K):
+    blocks, w = _q6k_on_gpu(N, K, seed=3 * N + K)
+    got = qwp.q6k_dequant(w, N, K).cpu().numpy()
+    ref = oracle.q6k_dequant(blocks, N, K).astype(np.float32)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("M,N,K", TINY)
+def test_q6k_gemm_tiny(M, N, K):
+    blocks, w = _q6k_on_gpu(N, K, seed=M * 7 + N)
+    xb = synth.activations_bf16(M, K, seed=M + 5)
+    y = qwp.q6k_gemm(w, _bf16_on_gpu(xb), N).cpu().numpy()
+    ref, mag = oracle.q6k_gemm(blocks, xb, N, K)
+    check_bound(y, ref, mag, f"q6k M{M} N{N} K{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 3, 256), (40, 200, 512), (257, 129, 768)])
+def test_q6k_gemm_f16_activations(M, N, K):
+    blocks, w = _q6k_on_gpu(N, K, seed=M + 3 * N)
+    xh = synth.activations_f16(M, K, seed=M + 6)
+    y = qwp.q6k_gemm_f16(w, torch.from_numpy(xh).to(DEV), N).cpu().numpy()
+    ref, mag = oracle.gemm(oracle.half_to_f64(xh.view(np.uint16)), oracle.q6k_dequant(blocks, N, K))
+    check_bound(y, ref, mag, f"q6k f16 M{M} N{N} K{K}")
+
+
+def test_q6k_more_units_than_ctas():
+    """253 row tiles (the last one of 100 rows, padded to 104) over at most one CTA per SM."""
+    M, N, K = 24, 32356, 256
+    blocks, w = _q6k_on_gpu(N, K, seed=91)
+    xb = synth.activations_bf16(M, K, seed=92)
+    y = qwp.q6k_gemm(w, _bf16_on_gpu(xb), N).cpu().numpy()
+    ref, mag = oracle.q6k_gemm(blocks, xb, N, K)
+    check_bound(y, ref, mag, f"q6k M{M} N{N} K{K}")
+
+
+@pytest.mark.parametrize("M,name,K,N", [(105, "attn_v", 4096, 1024), (105, "ffn_down", 12288, 4096),
+                                        (2048, "ffn_down", 12288, 4096), (658, "attn_v", 4096, 1024)])
+def test_q6k_qwen3_8b_projections(M, name, K, N):
+    """The projections a Q4_K_M checkpoint stores in Q6_K, at the workload token counts
+    (every element at M=105, sampled rows beyond)."""
+    blocks, w = _q6k_on_gpu(N, K, seed=K + N + M)
+    xb = synth.activations_bf16(M, K, seed=M + 17)
+    y = qwp.q6k_gemm(w, _bf16_on_gpu(xb), N)
+    rows = np.arange(M) if M <= 128 else sample_rows(M, seed=M)
+    ys = y[torch.from_numpy(rows).to(DEV)].cpu().numpy()
+    ref, mag = q6k_oracle_rows(blocks, xb[rows], N, K)
+    check_bound(ys, ref, mag, f"q6k {name} M{M} N{N} K{K}")
 
 
 # --- GEMM: the workload shapes -------------------------------------------------------
