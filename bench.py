@@ -223,6 +223,9 @@ SWEEP = (["q4k:32:2048:2048"]
          + ["w4a16:2048:12288:4096:128", "w4a16:2048:4096:12288:128",
             "w4a16:2048:12288:4096:128:sym", "w4a16:2048:12288:4096:128:bf16",
             "q6k:105:1024:4096", "q6k:105:4096:12288", "q6k:2048:4096:12288",
+            "q4k:1:6144:4096", "q4k:1:4096:4096", "q4k:1:24576:4096", "q4k:1:4096:12288",
+            "q4k:8:6144:4096", "q4k:8:4096:4096", "q4k:8:24576:4096", "q4k:8:4096:12288",
+            "q6k:1:4096:12288", "w4a16:8:12288:4096:128:sym",
             "q4k:4096:32:4096", "q4k:8192:12288:4096"])
 
 

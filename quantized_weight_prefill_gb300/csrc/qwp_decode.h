@@ -1,0 +1,42 @@
+// Host entry of the decode-shaped (M <= 8 tokens) product kernel.
+#pragma once
+
+#include "qwp_internal.h"
+
+namespace qwp {
+
+// Weight formats of launch_decode (same numbering as the prefill kernel's).
+enum : int { DFMT_W4A16 = 0, DFMT_Q4K = 1, DFMT_Q6K = 2 };
+
+// The largest token count the decode kernel takes (one MMA's N).
+constexpr int64_t DECODE_MAX_TOKENS = 8;
+
+// The decode kernel is used for matrices of at least this many (128-row tile,
+// 256-wide super-block) items; below it (under ~20M weights) the fixed start-up
+// and hand-off costs of the decode kernel exceed what it saves over the prefill
+// kernel (measured on GB300 at 1 to 8 tokens).
+constexpr int64_t DECODE_MIN_ITEMS = 600;
+
+// Whether an M x N x K product takes the decode kernel: 1 <= M <= 8, K % 256 == 0,
+// at least DECODE_MIN_ITEMS items and few enough for its 32-bit work split.
+inline bool decode_fits(int64_t M, int64_t N, int64_t K) {
+    if (M < 1 || M > DECODE_MAX_TOKENS || K % 256 != 0) return false;
+    const int64_t items = (N + 127) / 128 * (K / 256);
+    return items >= DECODE_MIN_ITEMS && items <= (int64_t(1) << 22);
+}
+
+// Device scratch launch_decode needs for an N x K matrix of format `fmt` on the
+// current device (partial sums of tiles shared by two or more CTAs, and one
+// counter per 128-row tile); 0 if the device could not be queried.
+size_t decode_scratch_bytes(int fmt, int64_t N, int64_t K);
+
+// y[M][N] = x[M][K] . W^T for 1 <= M <= 8 and K % 256 == 0, W repacked in format
+// `fmt`; x fp16, or bf16 when x_bf16 (converted in shared memory; an fp16
+// overflow sets the range bit of the status word).  `scratch` (16-byte aligned,
+// at least decode_scratch_bytes) is used in stream order; its counters are
+// cleared on `stream` before the kernel.  Allocates nothing.
+int launch_decode(int fmt, const void *w, const void *scales, const uint8_t *zeros, const void *x, bool x_bf16,
+                  float *y, int64_t M, int64_t N, int64_t K, int64_t group, void *scratch, size_t scratch_bytes,
+                  cudaStream_t stream);
+
+}  // namespace qwp

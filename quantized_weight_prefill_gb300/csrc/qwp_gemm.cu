@@ -42,6 +42,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "qwp_decode.h"
 #include "qwp_format.cuh"
 #include "qwp_internal.h"
 #include "qwp_ptx.cuh"
@@ -49,7 +50,7 @@
 namespace qwp {
 
 // Weight formats (the kernel's template parameter).
-enum : int { FMT_W4A16 = 0, FMT_Q4K = 1, FMT_Q6K = 2, NUM_FMTS = 3 };
+enum : int { FMT_W4A16 = DFMT_W4A16, FMT_Q4K = DFMT_Q4K, FMT_Q6K = DFMT_Q6K, NUM_FMTS = 3 };
 
 constexpr int XFORM_GROUPS = 4;                    // groups take K blocks in turn, one per weight stage
 constexpr int NUM_XFORM_WARPS = 4 * XFORM_GROUPS;  // 4 warps (one per lane quarter) cover one K block
@@ -1105,11 +1106,37 @@ static int scratch_pool(cudaMemPool_t *out) {
     return QWP_OK;
 }
 
+// Decode-shaped calls (at most 8 tokens, K a multiple of 256) go to the decode
+// kernel, which streams the same repacked weights without the tensor-memory
+// pipeline (and converts bf16 activations itself); its scratch comes from the pool.
+static bool decode_shaped(int64_t M, int64_t N, int64_t K) { return decode_fits(M, N, K); }
+
+static int run_decode(int fmt, const void *w, const void *scales, const uint8_t *zeros, const void *x, bool x_bf16,
+                      float *y, int64_t M, int64_t N, int64_t K, int64_t group, cudaStream_t s) {
+    int rc = check_device();
+    if (rc) return rc;
+    const size_t bytes = decode_scratch_bytes(fmt, N, K);
+    if (!bytes) return QWP_ERR_CUDA;
+    cudaMemPool_t pool;
+    if ((rc = scratch_pool(&pool))) return rc;
+    void *scratch = nullptr;
+    if (cudaMallocFromPoolAsync(&scratch, bytes, pool, s) != cudaSuccess) {
+        cudaGetLastError();
+        return QWP_ERR_CUDA;
+    }
+    rc = launch_decode(fmt, w, scales, zeros, x, x_bf16, y, M, N, K, group, scratch, bytes, s);
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && !rc) rc = QWP_ERR_CUDA;
+    return rc;
+}
+
 extern "C" int q4k_gemm_f16(const void *w_tiled, const void *x, float *y, int64_t M, int64_t N,
                             int64_t K, void *stream) {
     if (K % Q4K_BLOCK || K == 0) return K < 0 ? QWP_ERR_INVALID_ARG : QWP_ERR_UNSUPPORTED_SHAPE;
     int rc = gemm_shape_checks(w_tiled, x, y, M, N, K);
     if (rc || M == 0 || N == 0) return rc;
+    if (decode_shaped(M, N, K))
+        return run_decode(DFMT_Q4K, w_tiled, nullptr, nullptr, x, false, y, M, N, K, 0,
+                          static_cast<cudaStream_t>(stream));
     return launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0,
                              static_cast<cudaStream_t>(stream), kDefaultTimeoutNs, false);
 }
@@ -1121,6 +1148,7 @@ extern "C" int q4k_gemm(const void *w_tiled, const void *x, float *y, int64_t M,
     if (rc || M == 0 || N == 0) return rc;
     if ((rc = check_device())) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (decode_shaped(M, N, K)) return run_decode(DFMT_Q4K, w_tiled, nullptr, nullptr, x, true, y, M, N, K, 0, s);
     cudaMemPool_t pool;
     if ((rc = scratch_pool(&pool))) return rc;
     void *x16 = nullptr;
@@ -1139,6 +1167,9 @@ extern "C" int q6k_gemm_f16(const void *w_tiled, const void *x, float *y, int64_
     if (K % Q4K_BLOCK || K == 0) return K < 0 ? QWP_ERR_INVALID_ARG : QWP_ERR_UNSUPPORTED_SHAPE;
     int rc = gemm_shape_checks(w_tiled, x, y, M, N, K);
     if (rc || M == 0 || N == 0) return rc;
+    if (decode_shaped(M, N, K))
+        return run_decode(DFMT_Q6K, w_tiled, nullptr, nullptr, x, false, y, M, N, K, 0,
+                          static_cast<cudaStream_t>(stream));
     return launch_gemm<FMT_Q6K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0,
                                 static_cast<cudaStream_t>(stream), kDefaultTimeoutNs, false);
 }
@@ -1150,6 +1181,7 @@ extern "C" int q6k_gemm(const void *w_tiled, const void *x, float *y, int64_t M,
     if (rc || M == 0 || N == 0) return rc;
     if ((rc = check_device())) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (decode_shaped(M, N, K)) return run_decode(DFMT_Q6K, w_tiled, nullptr, nullptr, x, true, y, M, N, K, 0, s);
     cudaMemPool_t pool;
     if ((rc = scratch_pool(&pool))) return rc;
     void *x16 = nullptr;
@@ -1171,6 +1203,9 @@ extern "C" int w4a16_gemm(const void *wq_tiled, const void *scales, const uint8_
     int rc = gemm_shape_checks(wq_tiled, x, y, M, N, K);
     if (rc || M == 0 || N == 0) return rc;
     if (!scales) return QWP_ERR_INVALID_ARG;
+    if (decode_shaped(M, N, K))
+        return run_decode(DFMT_W4A16, wq_tiled, scales, zeros, x, false, y, M, N, K, group,
+                          static_cast<cudaStream_t>(stream));
     return launch_gemm<FMT_W4A16>(wq_tiled, scales, zeros, x, y, M, N, K, group,
                               static_cast<cudaStream_t>(stream), kDefaultTimeoutNs, false);
 }
@@ -1185,6 +1220,7 @@ extern "C" int w4a16_gemm_bf16(const void *wq_tiled, const void *scales, const u
     if (!scales) return QWP_ERR_INVALID_ARG;
     if ((rc = check_device())) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (decode_shaped(M, N, K)) return run_decode(DFMT_W4A16, wq_tiled, scales, zeros, x, true, y, M, N, K, group, s);
     cudaMemPool_t pool;
     if ((rc = scratch_pool(&pool))) return rc;
     void *x16 = nullptr;

@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "../../include/qwp.h"
+#include "qwp_decode.h"
 #include "qwp_internal.h"
 
 // The fp16 copy of x.  Every GPU on which this library's device code is loaded
@@ -14,14 +15,20 @@
 // host code the name is only a handle for cudaGetSymbolAddress, never an address.
 static __device__ __align__(256) uint16_t g_x16_scratch[QWP_NOALLOC_MAX_X_ELEMS];
 
+// Scratch of decode-shaped calls (M <= 8): partial sums of the 128-row tiles that
+// two or more CTAs share and one counter per tile (4 MiB, held the same way).
+constexpr size_t kDecodeScratchBytes = 4u << 20;
+static __device__ __align__(256) uint8_t g_decode_scratch[kDecodeScratchBytes];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
 
-// Device address of g_x16_scratch on the current device, looked up once per
-// device (the lookup also loads this code onto the device if needed).
-int scratch_address(void **out) {
-    static void *addr[kMaxDevices];
+// Device addresses of g_x16_scratch and g_decode_scratch on the current device,
+// looked up once per device (the lookup also loads this code onto the device if
+// needed).
+int scratch_address(void **out, void **decode_out) {
+    static void *addr[kMaxDevices], *dec_addr[kMaxDevices];
     static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -30,14 +37,17 @@ int scratch_address(void **out) {
     }
     std::lock_guard<std::mutex> lock(mu);
     if (!addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_x16_scratch) != cudaSuccess || !p) {
+        void *p = nullptr, *q = nullptr;
+        if (cudaGetSymbolAddress(&p, g_x16_scratch) != cudaSuccess || !p ||
+            cudaGetSymbolAddress(&q, g_decode_scratch) != cudaSuccess || !q) {
             cudaGetLastError();
             return QWP_ERR_CUDA;
         }
         addr[dev] = p;
+        dec_addr[dev] = q;
     }
     *out = addr[dev];
+    *decode_out = dec_addr[dev];
     return QWP_OK;
 }
 
@@ -55,8 +65,13 @@ extern "C" int q4k_gemm_noalloc(const void *w_tiled, const void *x, float *y, in
     if (M > static_cast<int64_t>(QWP_NOALLOC_MAX_X_ELEMS) / K) return QWP_ERR_SCRATCH_LIMIT;
     int rc = check_device();
     if (rc) return rc;
-    void *x16 = nullptr;
-    if ((rc = scratch_address(&x16))) return rc;
+    void *x16 = nullptr, *dec = nullptr;
+    if ((rc = scratch_address(&x16, &dec))) return rc;
+    // Decode-shaped calls: the decode kernel converts x itself and keeps its
+    // partial sums in the fixed decode array.
+    if (decode_fits(M, N, K))
+        return launch_decode(DFMT_Q4K, w_tiled, nullptr, nullptr, x, true, y, M, N, K, 0, dec, kDecodeScratchBytes,
+                             static_cast<cudaStream_t>(stream));
     // The conversion writes all M*K elements the GEMM reads, so nothing left
     // in the array by an earlier call is ever read.
     if ((rc = launch_bf16_to_f16(x, x16, M * K, static_cast<cudaStream_t>(stream)))) return rc;
