@@ -5,9 +5,19 @@
  * is asynchronous and ordered on `stream` (a cudaStream_t passed as void*,
  * NULL = the legacy default stream) and never synchronizes the host, except
  * qwp_device_status.  The caller owns and allocates every input and output
- * buffer; the entry points that take device memory of their own are q4k_gemm,
- * q6k_gemm and w4a16_gemm_bf16 (activation scratch from a library-owned
- * stream-ordered pool).
+ * buffer.  Device memory of the library's own comes from a library-owned,
+ * stream-ordered pool, released in stream order after the call: the fp16 copy
+ * of x taken by q4k_gemm, q6k_gemm and w4a16_gemm_bf16, and, for decode-shaped
+ * calls of any GEMM entry point (see below), the decode kernel's partial sums.
+ *
+ * Decode-shaped calls.  A GEMM with 1 <= M <= 8 tokens, K % 256 == 0 and at
+ * least 600 (128-row tile, 256-wide super-block) items (ceil(N/128) * K/256)
+ * runs a second kernel made for that regime ("How ZINC's RDNA4 batched prefill
+ * went from 42 to 208 tok/s", section "The fix: K-parallel batched DMMV"): same
+ * weights, same operand rounding and the same error bound, bf16 activations
+ * converted inside the kernel, and G * 8 KiB + ceil(N/128) * 4 bytes of pool
+ * scratch (G <= 2 CTAs per SM) for the tiles its CTAs share.  Results are
+ * deterministic (shared tiles are summed in a fixed order).
  * Every entry point returns QWP_OK (0) or a negative qwp_status; none throws.
  * Calls are thread-safe.
  *
@@ -93,7 +103,8 @@ QWP_API int q4k_dequant(const void *w_tiled_dev, float *w_out_dev, int64_t N, in
  * once to fp16 (requires |d|*sc*15 < 65504, true of any practical block);
  * fp32 accumulation in tensor memory.  K % 256 == 0; M, N >= 0 (M == 0 or
  * N == 0 is a no-op); x_dev, w_tiled_dev and y_dev 16-byte aligned; x rows
- * contiguous (row stride K).  Allocates nothing.
+ * contiguous (row stride K).  Allocates nothing, except the decode kernel's
+ * scratch for decode-shaped calls.
  */
 QWP_API int q4k_gemm_f16(const void *w_tiled_dev, const void *x_dev, float *y_dev,
                          int64_t M, int64_t N, int64_t K, void *stream);
@@ -126,6 +137,8 @@ QWP_API int q4k_gemm(const void *w_tiled_dev, const void *x_dev, float *y_dev,
  * of QWP_NOALLOC_MAX_X_ELEMS fp16 values (16 MiB) that is part of the library
  * and that every GPU loading the library's device code holds until the process
  * exits.  M*K beyond that size returns QWP_ERR_SCRATCH_LIMIT before any work.
+ * Decode-shaped calls keep their partial sums in a second fixed array (4 MiB)
+ * instead and read x directly (no fp16 copy).
  * The first call on each device looks up the array's address on that device
  * (and loads the library's device code there if it is not loaded yet); make
  * that first call before any stream capture begins.  Every call on a device
