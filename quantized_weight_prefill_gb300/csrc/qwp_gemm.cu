@@ -159,6 +159,27 @@ __device__ __forceinline__ bool aborted(const Ctl &ctl) {
     return *reinterpret_cast<volatile uint32_t *>(ctl.abort) != 0;
 }
 
+// One commit group: CB 64-wide K blocks of 4 MMAs (K = 16 each).  A block c sits at
+// tensor-memory column acol + 32c, its x tile at B-descriptor low word
+// b_lo + tile_desc*c; K step kk advances A by 8 columns and B by 32 bytes.  The
+// group accumulates onto D unless it is the first of its unit (acc_in false).
+template <int CB>
+__device__ __forceinline__ void mma_group(uint32_t dcol, uint32_t acol, uint32_t b_lo, uint32_t b_hi,
+                                          uint32_t tile_desc, uint32_t idesc, bool acc_in) {
+    static_assert(CHUNK_K == 64, "4 MMAs of K = 16 per block");
+    if (acc_in)
+        mma_ts_w<true>(dcol, acol, b_lo, b_hi, idesc);
+    else
+        mma_ts_w<false>(dcol, acol, b_lo, b_hi, idesc);
+#pragma unroll
+    for (int kk = 1; kk < 4; ++kk) mma_ts_w<true>(dcol, acol + 8u * kk, b_lo + 2u * kk, b_hi, idesc);
+#pragma unroll
+    for (int c = 1; c < CB; ++c)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_ts_w<true>(dcol, acol + 32u * c + 8u * kk, b_lo + tile_desc * c + 2u * kk, b_hi, idesc);
+}
+
 // Unpack one row's half of a 64-wide K block (4 words = 32 weights) into 16
 // packed fp16 pairs regs[off .. off+15] of the A operand.
 template <bool kQ4K>
@@ -378,42 +399,56 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && !skip) {
+        // The whole warp runs the loop (its values stay warp-uniform) and one elected
+        // lane issues the MMAs and commits: the issuer shares its scheduler with
+        // transform warps, so every instruction it saves per MMA shortens the
+        // MMA stream.
+        if (!skip) {
             const uint32_t idesc = make_idesc_f16(false, TILE_ROWS, static_cast<uint32_t>(args.bn));  // fp16 A and B
             bool ok = true;
             int xs = 0, gs = 0;       // x ring slot; commit-group slot of the A ring
             uint32_t xph = 0, gph = 0;
-            const uint32_t tile_desc = static_cast<uint32_t>(args.bn) * 128u >> 4;  // one x tile, in descriptor units
+            const uint64_t xdesc0 = smem_desc_sw128(smem_u32(x_ring));
+            const uint32_t x_lo0 = static_cast<uint32_t>(xdesc0), x_hi = static_cast<uint32_t>(xdesc0 >> 32);
+            const uint32_t x_step = static_cast<uint32_t>(args.x_stage_bytes) >> 4;  // one x slot, descriptor units
+            const uint32_t tile_desc = static_cast<uint32_t>(args.bn) * 128u >> 4;   // one x tile, descriptor units
             int it = 0;
             for (int u = units0; ok && u < nunits; u += ustep, ++it) {
                 // The unit accumulates into buffer b once the epilogue has drained b.
                 const int b = nbufs == 2 ? (it & 1) : 0;
                 const int use = nbufs == 2 ? (it >> 1) : it;  // earlier uses of buffer b
-                if (!(ok = wait_bar(acc_empty + 8 * b, (use & 1) ^ 1, ctl, WAIT_ACC_EMPTY))) break;
+                if (!(ok = __all_sync(0xffffffffu, wait_bar(acc_empty + 8 * b, (use & 1) ^ 1, ctl, WAIT_ACC_EMPTY))))
+                    break;
                 tc_fence_after();
                 const uint32_t dcol = tmem + ACC_COL + ACC_STRIDE * static_cast<uint32_t>(b);
                 for (int g = 0; g < ngroups; ++g) {
-                    ok = wait_bar(x_full + 8 * xs, xph, ctl, WAIT_X_FULL) &&
-                         wait_bar(a_full + 8 * gs, gph, ctl, WAIT_A_FULL);
+                    ok = __all_sync(0xffffffffu, wait_bar(x_full + 8 * xs, xph, ctl, WAIT_X_FULL) &&
+                                                     wait_bar(a_full + 8 * gs, gph, ctl, WAIT_A_FULL));
                     if (!ok) break;
                     tc_fence_after();
-                    uint64_t bdesc = smem_desc_sw128(smem_u32(x_ring + xs * args.x_stage_bytes));
-                    uint32_t acol = tmem + A_COL + (32u << cbs) * gs;
-                    for (int c = 0; c < (1 << cbs); ++c, bdesc += tile_desc, acol += 32u) {
-#pragma unroll
-                        for (int kk = 0; kk < CHUNK_K / 16; ++kk)
-                            mma_ts(dcol, acol + 8u * kk, bdesc + 2u * kk, idesc, (g | c | kk) != 0);
+                    const uint32_t b_lo = x_lo0 + x_step * static_cast<uint32_t>(xs);
+                    const uint32_t acol = tmem + A_COL + (32u << cbs) * static_cast<uint32_t>(gs);
+                    if (elect_one()) {
+                        if (cbs == 2)
+                            mma_group<4>(dcol, acol, b_lo, x_hi, tile_desc, idesc, g != 0);
+                        else if (cbs == 1)
+                            mma_group<2>(dcol, acol, b_lo, x_hi, tile_desc, idesc, g != 0);
+                        else
+                            mma_group<1>(dcol, acol, b_lo, x_hi, tile_desc, idesc, g != 0);
+                        mma_commit(mma_done + 8 * gs);
                     }
-                    mma_commit(mma_done + 8 * gs);
+                    __syncwarp();
                     if (++xs == XS) { xs = 0; xph ^= 1; }
                     if (++gs == dslots) { gs = 0; gph ^= 1; }
                 }
-                if (ok) mma_commit(acc_full + 8 * b);
+                if (ok && elect_one()) mma_commit(acc_full + 8 * b);
+                __syncwarp();
             }
-            if (!ok) {
+            if (!ok && lane == 0) {
                 mma_commit(drain);
                 wait_bar(drain, 0, ctl, WAIT_DRAIN, false);
             }
+            __syncwarp();
         }
     } else if (warp < FIRST_EPI_WARP) {
         // ------------------------------------------------------------ transform
