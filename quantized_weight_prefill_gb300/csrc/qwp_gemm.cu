@@ -578,37 +578,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         };
 
         // The warp walks the weight stages of all its units in order; per stage it
-        // owns at most one block.  A block is stored (issue) before the next stage is
-        // unpacked into the same registers, and published (finish) after that, so the
-        // unpack overlaps the tensor-memory store; the very first block is published
-        // at once so that the MMAs can start early.
+        // owns at most one block.  A block unpacked into `regs` is stored (issue) and
+        // published (finish) before the next stage is unpacked into the same
+        // registers: publishing at once, rather than after the next unpack, hands the
+        // MMAs their operand a whole unpack earlier, which the shallow A ring needs.
         uint32_t regs[32];
-        bool have = false, pend = false;  // regs hold block have_J; block pend_J is stored, unpublished
-        int have_J = 0, pend_J = 0;
-        bool first = true;
+        bool have = false;  // regs hold block have_J
+        int have_J = 0;
         int it = 0;
         for (int u = units0; ok && u < nunits; u += ustep, ++it) {
             const int tile = unit_tile(u);
             for (int s = 0; s < nstage; ++s) {
                 if (have) {
                     if (!(ok = issue(have_J, regs))) break;
-                    if (first) {
-                        finish(have_J);
-                        first = false;
-                    } else {
-                        pend = true;
-                        pend_J = have_J;
-                    }
+                    finish(have_J);
                     have = false;
                 }
                 bool nb = false;
                 if (!(ok = prepare(tile, s, regs, nb))) break;
-                if (pend) {
-                    finish(pend_J);
-                    pend = false;
-                }
                 // One accumulator: the previous unit is complete once its last block
-                // (just published) has gone through the MMAs; drain it while this
+                // (published above) has gone through the MMAs; drain it while this
                 // unit's first block waits in registers.
                 if (nbufs == 1 && s == 0 && it > 0 && !(ok = drain_unit(u - ustep, it - 1))) break;
                 if (nb) {
