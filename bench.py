@@ -37,6 +37,7 @@ METRIC = "Fused Q4_K GEMM TFLOP/s (% bf16 TC peak); Qwen3-8B-shape layer prefill
 LAYER = (("qkv", 4096, 6144), ("o", 4096, 4096), ("gate_up", 4096, 24576), ("down", 12288, 4096))
 M_TOKENS = 105
 DOMINANT = "gate_up"
+REF_BUDGET_S = 100.0  # reference arm: host seconds for warm-up + steps
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -161,53 +162,90 @@ def max_over_ranks(value: float, world: int) -> float:
 
 # ------------------------------------------------------------------------- oracle leg
 
-def oracle_layer_tokens_per_s(tokens: int, seed: int = 7):
-    """Time the CPU oracle (exact fp64 dequant of every layer weight + naive fp64 GEMM)
-    for `tokens` rows of the layer; returns (tok/s, seconds, threads)."""
-    import oracle
+def layer_workload():
+    return (f"Qwen3-8B-shape layer prefill: qkv K4096->N6144, o K4096->N4096, "
+            f"gate+up K4096->N24576, down K12288->N4096; Q4_K weights, bf16 x, fp32 y")
+
+
+def oracle_layer_sample(frac: float, seed: int = 7):
+    """Inputs of one oracle step over all M_TOKENS tokens and the first
+    max(1, round(frac * N)) weight rows of every projection; returns the inputs and
+    the fraction of the layer's weights they cover (the oracle's time is linear in
+    the rows: every row is dequantized and multiplied once per step)."""
     import synth
 
-    inputs = []
+    inputs, rows_k = [], 0
     for i, (_, K, N) in enumerate(LAYER):
-        inputs.append((synth.q4k_weights(N, K, seed=seed + i), synth.activations_bf16(tokens, K, seed=seed + 10 + i),
-                       N, K))
-    t0 = time.perf_counter()
-    for blocks, xb, N, K in inputs:
+        n = max(1, min(N, int(round(frac * N))))
+        blocks = synth.q4k_weights(N, K, seed=seed + i).reshape(N, -1)[:n]
+        inputs.append((blocks, synth.activations_bf16(M_TOKENS, K, seed=seed + 10 + i), n, K))
+        rows_k += n * K
+    return inputs, rows_k / sum(N * K for _, K, N in LAYER)
+
+
+def oracle_layer_step(inputs):
+    """One step of the CPU oracle (exact fp64 dequant of the rows + naive fp64 GEMM)."""
+    import oracle
+
+    for blocks, xb, n, K in inputs:
         x = oracle.bf16_to_f64(xb)
-        raw = blocks.reshape(N, -1)
-        for n0 in range(0, N, 2048):
-            n1 = min(N, n0 + 2048)
-            w = oracle.q4k_dequant(raw[n0:n1], n1 - n0, K)
-            oracle.gemm(x, w, with_abs=False)
-    dt = time.perf_counter() - t0
-    return tokens / dt, dt, oracle.num_threads()
+        for n0 in range(0, n, 2048):
+            n1 = min(n, n0 + 2048)
+            oracle.gemm(x, oracle.q4k_dequant(blocks[n0:n1], n1 - n0, K), with_abs=False)
+
+
+def oracle_layer_tokens_per_s(min_seconds: float):
+    """The CPU oracle over the whole layer and all M_TOKENS tokens, repeated for at
+    least `min_seconds`; returns (tok/s, seconds, steps, threads)."""
+    import oracle
+
+    inputs, _ = oracle_layer_sample(1.0)
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        oracle_layer_step(inputs)
+        steps += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            return M_TOKENS * steps / dt, dt, steps, oracle.num_threads()
 
 
 def run_reference(args):
+    """The oracle as the reference arm: each step is the whole layer's M_TOKENS tokens
+    over a row slice of every projection, sized (from a timed 1% slice) so that
+    warm-up and steps together take about REF_BUDGET_S seconds on the host cores;
+    tok/s counts the slice's share of the layer."""
+    import oracle
+
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    tokens = 4
+    # calibrate: time a 1% slice, extrapolate to the whole layer
+    probe, probe_share = oracle_layer_sample(0.01)
+    oracle_layer_step(probe)
+    c0 = time.perf_counter()
+    oracle_layer_step(probe)
+    full_step_s = (time.perf_counter() - c0) / probe_share
+    frac = min(1.0, REF_BUDGET_S / (full_step_s * max(1, args.steps + args.warmup)))
+    inputs, share = oracle_layer_sample(frac)
     for _ in range(args.warmup):
-        oracle_layer_tokens_per_s(tokens)
-    times = []
-    threads = 1
+        oracle_layer_step(inputs)
+    t0 = time.perf_counter()
     for _ in range(args.steps):
-        _, dt, threads = oracle_layer_tokens_per_s(tokens)
-        times.append(dt)
-    total = sum(times)
-    value = tokens * args.steps / total
+        oracle_layer_step(inputs)
+    total = time.perf_counter() - t0
+    value = M_TOKENS * share * args.steps / total
+    threads = oracle.num_threads()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"Qwen3-8B-shape layer (qkv, o, gate+up, down), Q4_K, bf16 x, "
-                               f"M={M_TOKENS} tokens; each step a {tokens}-token sample",
-                   "global_batch": tokens, "parallelism": "none (host cores)"},
+        "config": {"workload": layer_workload(), "global_batch": M_TOKENS, "seq_len": M_TOKENS,
+                   "parallelism": "none (host cores)"},
         "cpu_baseline": {"value": value, "unit": "tok/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{tokens} of {M_TOKENS} tokens per step, every weight of the layer "
-                                   "dequantized exactly in fp64 then naive fp64 GEMM"},
+                         "sample": f"per step all {M_TOKENS} tokens over {share:.4%} of the layer's weight rows "
+                                   "(every weight dequantized exactly in fp64, then naive fp64 GEMM), "
+                                   f"{args.steps} steps in {total:.1f} s"},
         "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -496,10 +534,10 @@ def run_gpu(args):
 
     cpu = None
     if not args.no_cpu_baseline:
-        tok_s, dt, threads = oracle_layer_tokens_per_s(args.cpu_tokens)
+        tok_s, dt, nsteps, threads = oracle_layer_tokens_per_s(args.cpu_seconds)
         cpu = {"value": tok_s, "unit": "tok/s", "cores": threads, "kind": "oracle",
-               "sample": f"{args.cpu_tokens} of {M} tokens through the whole layer "
-                         f"(every weight dequantized exactly in fp64, naive fp64 GEMM), {dt:.1f} s"}
+               "sample": f"{nsteps} whole-layer steps of all {M} tokens (every weight dequantized exactly "
+                         f"in fp64, naive fp64 GEMM), {dt:.1f} s"}
 
     line = {
         "metric": METRIC,
@@ -515,8 +553,7 @@ def run_gpu(args):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": f"Qwen3-8B-shape layer prefill: qkv K4096->N6144, o K4096->N4096, "
-                        f"gate+up K4096->N24576, down K12288->N4096; Q4_K weights, bf16 x, fp32 y",
+            "workload": layer_workload(),
             "global_batch": M * world, "seq_len": M, "parallelism": f"replicas x{world}",
             "l2": f"weights rotate over {copies} copies ({copies * layer_w_bytes / 1e6:.0f} MB > 2x L2)",
             "launch": "one CUDA graph of the four library calls per weight copy, replayed per step",
@@ -551,7 +588,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-tokens", type=int, default=8)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gemm", action="append", default=[],
                     help="time single GEMMs instead of the layer: q4k:M:N:K, q6k:M:N:K or w4a16:M:N:K:group[:sym][:bf16]")
