@@ -12,12 +12,15 @@
  *
  * Decode-shaped calls.  A GEMM with 1 <= M <= 8 tokens, K % 256 == 0 and at
  * least 600 (128-row tile, 256-wide super-block) items (ceil(N/128) * K/256)
- * runs a second kernel made for that regime ("How ZINC's RDNA4 batched prefill
- * went from 42 to 208 tok/s", section "The fix: K-parallel batched DMMV"): same
- * weights, same operand rounding and the same error bound, bf16 activations
- * converted inside the kernel, and G * 8 KiB + ceil(N/128) * 4 bytes of pool
- * scratch (G <= 2 CTAs per SM) for the tiles its CTAs share.  Results are
- * deterministic (shared tiles are summed in a fixed order).
+ * can run a second kernel made for that regime ("How ZINC's RDNA4 batched
+ * prefill went from 42 to 208 tok/s", section "The fix: K-parallel batched
+ * DMMV"): same weights, same operand rounding and the same error bound, bf16
+ * activations converted inside the kernel, and G * 8 KiB + ceil(N/128) * 4
+ * bytes of pool scratch (G <= 2 CTAs per SM) for the tiles its CTAs share.
+ * Results are deterministic (shared tiles are summed in a fixed order).  By
+ * default (QWP_DECODE_AUTO) it takes such products only where it measured
+ * faster than the prefill kernel on GB300: M <= 2 and N >= 10240; see
+ * qwp_set_decode_policy.
  * Every entry point returns QWP_OK (0) or a negative qwp_status; none throws.
  * Calls are thread-safe.
  *
@@ -255,6 +258,23 @@ QWP_API int w4a16_gemm_bf16(const void *wq_tiled_dev, const void *scales_dev, co
  * or QWP_ERR_CUDA.  Reading the word here clears it.
  */
 QWP_API int qwp_device_status(void *stream);
+
+/*
+ * Which decode-shaped products (see the top of this file) the GEMM entry points
+ * run on the decode kernel, process-wide: QWP_DECODE_AUTO (the default: M <= 2
+ * and N >= 10240, where it measured faster), QWP_DECODE_NEVER (always the
+ * prefill kernel) or QWP_DECODE_ALWAYS (every decode-shaped product).  Results
+ * meet the same error bound either way.  Returns the previous policy (>= 0) or
+ * QWP_ERR_INVALID_ARG.  Calls already issued keep the kernel they were given;
+ * the setting is read at each call, so a graph captured under one policy keeps
+ * the kernels it captured.
+ */
+enum qwp_decode_policy { QWP_DECODE_AUTO = 0, QWP_DECODE_NEVER = 1, QWP_DECODE_ALWAYS = 2 };
+QWP_API int qwp_set_decode_policy(int policy);
+
+/* 1 if a GEMM call of this shape would run the decode kernel under the current
+ * policy, 0 if the prefill kernel (host-only; no device call). */
+QWP_API int qwp_decode_selected(int64_t M, int64_t N, int64_t K);
 
 #ifdef __cplusplus
 }

@@ -21,7 +21,8 @@ __all__ = [
     "q4k_gemm_noalloc", "NOALLOC_MAX_X_ELEMS",
     "q6k_repacked_bytes", "q6k_repack", "q6k_dequant", "q6k_gemm", "q6k_gemm_f16",
     "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_bf16",
-    "device_status", "EXPORTED_SYMBOLS",
+    "device_status", "set_decode_policy", "decode_selected", "DECODE_AUTO", "DECODE_NEVER", "DECODE_ALWAYS",
+    "EXPORTED_SYMBOLS",
 ]
 
 # Every symbol include/qwp.h declares.
@@ -29,8 +30,11 @@ EXPORTED_SYMBOLS = (
     "qwp_status_string", "q4k_repacked_bytes", "q4k_repack", "q4k_dequant", "q4k_gemm", "q4k_gemm_f16",
     "q4k_gemm_noalloc", "q6k_repacked_bytes", "q6k_repack", "q6k_dequant", "q6k_gemm", "q6k_gemm_f16",
     "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_bf16",
-    "qwp_device_status",
+    "qwp_device_status", "qwp_set_decode_policy", "qwp_decode_selected",
 )
+
+# Decode-kernel dispatch policies (enum qwp_decode_policy in the header).
+DECODE_AUTO, DECODE_NEVER, DECODE_ALWAYS = 0, 1, 2
 
 # Largest M*K that q4k_gemm_noalloc accepts (QWP_NOALLOC_MAX_X_ELEMS in the header).
 NOALLOC_MAX_X_ELEMS = 8388608
@@ -74,6 +78,8 @@ def library() -> ctypes.CDLL:
         lib.w4a16_gemm.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p]
         lib.w4a16_gemm_bf16.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p]
         lib.qwp_device_status.argtypes = [p]
+        lib.qwp_set_decode_policy.argtypes = [ctypes.c_int]
+        lib.qwp_decode_selected.argtypes = [i64, i64, i64]
         for name in EXPORTED_SYMBOLS:
             if name != "qwp_status_string":
                 getattr(lib, name).restype = ctypes.c_int
@@ -283,3 +289,17 @@ def device_status(device=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     with torch.cuda.device(dev):
         return int(library().qwp_device_status(ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)))
+
+
+def set_decode_policy(policy: int) -> int:
+    """Set which decode-shaped products run on the decode kernel (DECODE_AUTO,
+    DECODE_NEVER or DECODE_ALWAYS; process-wide) and return the previous policy."""
+    rc = int(library().qwp_set_decode_policy(int(policy)))
+    if rc < 0:
+        _check(rc, "qwp_set_decode_policy")
+    return rc
+
+
+def decode_selected(M: int, N: int, K: int) -> bool:
+    """Whether a GEMM call of this shape would run the decode kernel now."""
+    return bool(library().qwp_decode_selected(int(M), int(N), int(K)))

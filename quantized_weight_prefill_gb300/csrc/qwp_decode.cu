@@ -35,6 +35,7 @@
 // weights, as in the prefill transform) and reads 64 contiguous bytes of its
 // token's activations.
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "qwp_decode.h"
@@ -686,4 +687,24 @@ int launch_decode(int fmt, const void *w, const void *scales, const uint8_t *zer
     }
 }
 
+static std::atomic<int> g_decode_policy{DECODE_POLICY_AUTO};
+
+int decode_policy() { return g_decode_policy.load(std::memory_order_relaxed); }
+
+bool decode_selected(int64_t M, int64_t N, int64_t K) {
+    switch (decode_policy()) {
+        case DECODE_POLICY_NEVER: return false;
+        case DECODE_POLICY_ALWAYS: return decode_fits(M, N, K);
+        default: return decode_auto(M, N, K);
+    }
+}
+
 }  // namespace qwp
+
+extern "C" int qwp_set_decode_policy(int policy) {
+    if (policy != qwp::DECODE_POLICY_AUTO && policy != qwp::DECODE_POLICY_NEVER && policy != qwp::DECODE_POLICY_ALWAYS)
+        return QWP_ERR_INVALID_ARG;
+    return qwp::g_decode_policy.exchange(policy, std::memory_order_relaxed);
+}
+
+extern "C" int qwp_decode_selected(int64_t M, int64_t N, int64_t K) { return qwp::decode_selected(M, N, K) ? 1 : 0; }

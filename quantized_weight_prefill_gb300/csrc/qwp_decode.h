@@ -25,6 +25,26 @@ inline bool decode_fits(int64_t M, int64_t N, int64_t K) {
     return items >= DECODE_MIN_ITEMS && items <= (int64_t(1) << 22);
 }
 
+// Which products of decode shape the GEMM entry points give the decode kernel
+// (qwp_set_decode_policy): AUTO follows decode_auto, NEVER keeps every product on
+// the prefill kernel, ALWAYS takes every product that decode_fits.
+enum : int { DECODE_POLICY_AUTO = 0, DECODE_POLICY_NEVER = 1, DECODE_POLICY_ALWAYS = 2 };
+
+// The automatic choice, from both kernels timed on GB300 at 1 to 8 tokens (Q4_K,
+// Q6_K and W4A16, N from 2048 to 152064, K from 4096 to 12288): the decode kernel
+// is faster only at one or two tokens and for at least 80 row tiles (N >= 10240),
+// by 3-10%; the prefill kernel wins for narrower matrices (by up to 15% at
+// N = 6144), for K-heavy ones (N = 4096, K = 12288) and from three tokens on.
+constexpr int64_t DECODE_AUTO_MAX_TOKENS = 2;
+constexpr int64_t DECODE_AUTO_MIN_ROWS = 10240;
+inline bool decode_auto(int64_t M, int64_t N, int64_t K) {
+    return decode_fits(M, N, K) && M <= DECODE_AUTO_MAX_TOKENS && N >= DECODE_AUTO_MIN_ROWS;
+}
+
+// The current policy, and the choice it makes for an M x N x K product.
+int decode_policy();
+bool decode_selected(int64_t M, int64_t N, int64_t K);
+
 // Device scratch launch_decode needs for an N x K matrix of format `fmt` on the
 // current device (partial sums of tiles shared by two or more CTAs, and one
 // counter per 128-row tile); 0 if the device could not be queried.

@@ -1133,7 +1133,7 @@ static int scratch_pool(cudaMemPool_t *out) {
 // Decode-shaped calls (at most 8 tokens, K a multiple of 256) go to the decode
 // kernel, which streams the same repacked weights without the tensor-memory
 // pipeline (and converts bf16 activations itself); its scratch comes from the pool.
-static bool decode_shaped(int64_t M, int64_t N, int64_t K) { return decode_fits(M, N, K); }
+static bool decode_shaped(int64_t M, int64_t N, int64_t K) { return decode_selected(M, N, K); }
 
 static int run_decode(int fmt, const void *w, const void *scales, const uint8_t *zeros, const void *x, bool x_bf16,
                       float *y, int64_t M, int64_t N, int64_t K, int64_t group, cudaStream_t s) {

@@ -103,3 +103,33 @@ def test_gemm_argument_checks_before_any_cuda_call(lib):
     assert lib.q4k_dequant(a16, a16, 4, 300, None) == SHAPE
     assert lib.w4a16_repack(a16, a16, 4, 96, None) == SHAPE
     assert lib.w4a16_dequant(a16, a16, a16, a16, 4, 256, 96, None) == INVALID
+
+
+def test_decode_policy_round_trip_and_automatic_rule(lib):
+    """The dispatch between the decode and the prefill kernel is host logic: the
+    automatic rule (1-2 tokens, N >= 10240, plus what the decode kernel needs:
+    K % 256 == 0 and >= 600 tile items), the two forced policies, and the
+    rejection of an unknown policy."""
+    prev = qwp.set_decode_policy(qwp.DECODE_AUTO)
+    try:
+        assert qwp.decode_selected(1, 24576, 4096) and qwp.decode_selected(2, 10240, 4096)
+        assert qwp.decode_selected(1, 152064, 4096)
+        assert not qwp.decode_selected(3, 24576, 4096)      # three tokens: the prefill kernel
+        assert not qwp.decode_selected(1, 10112, 4096)      # 79 row tiles
+        assert not qwp.decode_selected(1, 4096, 12288)      # K-heavy
+        assert not qwp.decode_selected(1, 24576, 4000)      # K % 256 != 0
+        assert not qwp.decode_selected(1, 10240, 1792)      # 80 x 7 = 560 items
+        assert not qwp.decode_selected(0, 24576, 4096)
+        assert qwp.set_decode_policy(qwp.DECODE_ALWAYS) == qwp.DECODE_AUTO
+        assert qwp.decode_selected(8, 4096, 12288) and qwp.decode_selected(5, 2500, 8192)
+        assert not qwp.decode_selected(9, 24576, 4096)      # more than 8 tokens
+        assert not qwp.decode_selected(1, 2048, 2048)       # 16 x 8 = 128 items
+        assert qwp.set_decode_policy(qwp.DECODE_NEVER) == qwp.DECODE_ALWAYS
+        assert not qwp.decode_selected(1, 24576, 4096)
+        assert lib.qwp_set_decode_policy(3) == INVALID and lib.qwp_set_decode_policy(-1) == INVALID
+        with pytest.raises(qwp.QwpError):
+            qwp.set_decode_policy(7)
+        assert qwp.set_decode_policy(qwp.DECODE_AUTO) == qwp.DECODE_NEVER
+    finally:
+        qwp.set_decode_policy(prev)
+

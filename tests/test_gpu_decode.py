@@ -1,12 +1,13 @@
 """GPU parity of the decode-shaped path through the C ABI.
 
-The GEMM entry points route products with 1..8 tokens, K % 256 == 0 and at least
-600 (128-row tile, 256-wide super-block) items to the decode kernel (mma.sync over
-operands unpacked in registers, a stream-K split whose shared tiles are finished
-by the last CTA to arrive); the shapes here are chosen to take that path, with
-ragged row counts and every token count.  Every case is compared element by
-element with the CPU oracle under the same bound as the prefill path:
-|y - y_oracle| <= 1e-3 * sum|x*w| + 1e-5.
+Products with 1..8 tokens, K % 256 == 0 and at least 600 (128-row tile,
+256-wide super-block) items can run the decode kernel (mma.sync over operands
+unpacked in registers, a stream-K split whose shared tiles are finished by the
+last CTA to arrive).  By default only those where it is the faster kernel do;
+these tests set the QWP_DECODE_ALWAYS policy so that every shape here (ragged
+row counts, every token count) takes it, and one test checks the default choice
+end to end.  Every case is compared element by element with the CPU oracle under
+the same bound as the prefill path: |y - y_oracle| <= 1e-3 * sum|x*w| + 1e-5.
 """
 import numpy as np
 import pytest
@@ -32,6 +33,13 @@ def _status_clean():
     assert qwp.device_status() == 0, "a kernel reported an error"
 
 
+@pytest.fixture(autouse=True)
+def _decode_kernel_forced():
+    prev = qwp.set_decode_policy(qwp.DECODE_ALWAYS)
+    yield
+    qwp.set_decode_policy(prev)
+
+
 # (M, N, K): tile items = ceil(N/128) * K/256, all >= 600; N % 128 != 0 except one.
 SHAPES = [(1, 2500, 8192), (2, 1700, 12288), (5, 6000, 4096), (8, 3000, 8192), (3, 9000, 4096),
           (7, 800, 24576), (4, 4096, 4864), (6, 76850, 256)]
@@ -43,6 +51,22 @@ def _items(N, K):
 
 def test_decode_shapes_take_the_decode_path():
     assert all(1 <= M <= 8 and K % 256 == 0 and _items(N, K) >= 600 for M, N, K in SHAPES)
+    assert all(qwp.decode_selected(M, N, K) for M, N, K in SHAPES)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 10240, 2048), (2, 12300, 2048)])
+def test_default_policy_both_kernels(M, N, K):
+    """Under the default policy these shapes take the decode kernel; forced onto the
+    prefill kernel they give results within the same bound."""
+    blocks = synth.q4k_weights(N, K, seed=M * 53 + N)
+    w = qwp.q4k_repack(torch.from_numpy(blocks.reshape(-1)).to(DEV), N, K)
+    xb = synth.activations_bf16(M, K, seed=M + 11)
+    ref, mag = oracle.q4k_gemm(blocks, xb, N, K)
+    for policy, decode in [(qwp.DECODE_AUTO, True), (qwp.DECODE_NEVER, False)]:
+        qwp.set_decode_policy(policy)
+        assert qwp.decode_selected(M, N, K) == decode
+        y = qwp.q4k_gemm(w, _bf16(xb), N).cpu().numpy()
+        check_bound(y, ref, mag, f"policy {policy} M{M} N{N} K{K}")
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)

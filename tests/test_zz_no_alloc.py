@@ -86,3 +86,28 @@ def test_noalloc_at_the_limit_and_one_row_beyond():
     assert e.value.code == SCRATCH_LIMIT
     torch.cuda.synchronize()
     assert bool((y_big == 7.0).all()), "a rejected call must not touch y"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("policy,M,N,K", [(0, 1, 10240, 2048), (2, 7, 2500, 8192)])
+def test_noalloc_decode_shaped(policy, M, N, K):
+    """Decode-shaped calls keep the decode kernel's partial sums in the library's
+    second fixed array: two calls in a row (different activations) each meet the
+    bound against the oracle, by default (one token, wide matrix) and with the
+    decode kernel forced (seven tokens)."""
+    prev = qwp.set_decode_policy(policy)
+    try:
+        assert qwp.decode_selected(M, N, K)
+        blocks = synth.q4k_weights(N, K, seed=906 + M)
+        w = qwp.q4k_repack(torch.from_numpy(blocks.reshape(-1)).to(DEV), N, K)
+        for call, seed in enumerate((907, 908)):
+            xb = synth.activations_bf16(M, K, seed=seed)
+            y = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+            qwp.q4k_gemm_noalloc(w, _bf16_on_gpu(xb), N, out=y)
+            torch.cuda.synchronize()
+            assert qwp.device_status() == 0
+            ref, mag = oracle.q4k_gemm(blocks, xb, N, K)
+            check_bound(y.cpu().numpy(), ref, mag, f"q4k_gemm_noalloc decode-shaped call {call + 1} (M={M})")
+    finally:
+        qwp.set_decode_policy(prev)
+
