@@ -58,6 +58,11 @@ constexpr int FIRST_XFORM_WARP = 3;
 constexpr int FIRST_EPI_WARP = FIRST_XFORM_WARP + NUM_XFORM_WARPS;
 constexpr int NUM_EPI_WARPS = 4;                   // one per tensor-memory lane quarter
 constexpr int NUM_THREADS = 32 * (FIRST_EPI_WARP + NUM_EPI_WARPS);
+// With one accumulator the transform warps drain it and there are no epilogue
+// warps: 19 warps (at most 5 per scheduler) leave 96 registers per thread
+// instead of 80.
+constexpr int NUM_THREADS_1ACC = 32 * FIRST_EPI_WARP;
+__host__ __device__ constexpr int block_threads(bool two_acc) { return two_acc ? NUM_THREADS : NUM_THREADS_1ACC; }
 constexpr int X_MAX_STAGES = 8;  // <= A_STAGES: the x ring reuses the mma_done ring (see below)
 constexpr int W_MAX_STAGES = 8;
 constexpr int A_STAGES = 8;
@@ -73,7 +78,7 @@ constexpr uint32_t TMEM_COLS = 512;
 // the buffer that receives the cluster's partial sums), then mbarriers and misc words.
 constexpr int RING_BYTES = 224 * 1024;
 constexpr int OFF_BAR = RING_BYTES;
-constexpr int NUM_BARS = X_MAX_STAGES + 2 * W_MAX_STAGES + 2 * A_STAGES + 4 + 4;
+constexpr int NUM_BARS = X_MAX_STAGES + 2 * W_MAX_STAGES + 2 * A_STAGES + 4 + 5;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -217,8 +222,11 @@ __device__ __forceinline__ void unpack_q6k_quarter(uint4 wv, uint32_t h0, uint32
     for (int e = 0; e < 4; ++e) regs[off + 12 + e] = p[e];
 }
 
-template <int kFmt>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+// kTwoAcc: token tiles of at most 128, two accumulators, split-K allowed, 23
+// warps; else one accumulator, no split-K and no epilogue warps (the two are
+// compiled apart, so that neither carries the other's code and registers).
+template <int kFmt, bool kTwoAcc>
+__global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
     qwp_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmArgs args) {
     constexpr bool kQ4K = kFmt == FMT_Q4K;
     constexpr bool kQ6K = kFmt == FMT_Q6K;
@@ -229,7 +237,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lane = lane_id();
 
     // This CTA's K range (its cluster rank along K) is the same for every unit.
-    const int S = args.splits;
+    const int S = kTwoAcc ? args.splits : 1;
     const int nkb_total = args.K / CHUNK_K;
     const int kb_begin = blockIdx.z * args.kb_per_split;
     const int kb_end = min(nkb_total, kb_begin + args.kb_per_split);
@@ -238,7 +246,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int XS = args.x_stages, WS = args.w_stages;
     uint8_t *const x_ring = smem;
     uint8_t *const w_ring = smem + XS * args.x_stage_bytes;
-    const int nbufs = args.acc_bufs;
+    const int nbufs = kTwoAcc ? 2 : 1;
     const int units0 = static_cast<int>(blockIdx.x);  // units units0, units0 + gridDim.x, ...
     const int ustep = static_cast<int>(gridDim.x);
     const int nunits = args.n_units;
@@ -267,7 +275,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t w_full = mma_done + 8 * A_STAGES, w_empty = w_full + 8 * W_MAX_STAGES;
     const uint32_t a_full = w_empty + 8 * W_MAX_STAGES, acc_full = a_full + 8 * A_STAGES;
     const uint32_t acc_empty = acc_full + 16, part_full = acc_empty + 16, part_free = part_full + 8;
-    const uint32_t part_last = part_free + 8, drain = part_last + 8;
+    const uint32_t part_last = part_free + 8, drain = part_last + 8, rings_idle = drain + 8;
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + OFF_MISC);  // [0] tmem base, [1] abort
     const Ctl ctl{misc + 1, args.status, args.timeout_ns};
 
@@ -315,6 +323,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(part_full, NUM_EPI_WARPS * S);
         mbar_init(part_free, NUM_EPI_WARPS * S);
         mbar_init(part_last, NUM_XFORM_WARPS * S);  // the last unit: every transform warp of every rank
+        mbar_init(rings_idle, S);                   // the last unit: one arrival per rank
         mbar_init(drain, 1);
         // A failure recorded earlier (and not yet read by qwp_device_status) makes
         // every later launch skip its work instead of waiting out its own timeouts
@@ -557,18 +566,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const int tile = unit_tile(uu), m0 = unit_m0(uu);
             const int R = tile_rows(args.N, tile);
-            const int64_t n = static_cast<int64_t>(tile) * TILE_ROWS + r;
+            const int64_t N = args.N;
+            // Chunk ci (8 token columns) holds tokens m0 + 8ci ..; this warp takes every
+            // fourth chunk from its group's, so its y pointer and the count of tokens
+            // left step by 32 tokens.  (Stepping a pointer rather than forming each
+            // address from the token index keeps this loop cheap: it runs while the
+            // MMAs wait for the accumulator, 8 stores per load.)
+            float *yc = args.y + (static_cast<int64_t>(m0) + 8 * grp) * N + static_cast<int64_t>(tile) * TILE_ROWS + r;
+            const int64_t chunk_step = 8 * (NUM_XFORM_WARPS / 4) * N;
+            int left = args.M - m0 - 8 * grp;
+            const bool row_ok = r < R;
             // 8 columns at a time: this warp's 32 unpacked weights stay live meanwhile.
-            for (int ci = grp; ci < args.bn / 8; ci += NUM_XFORM_WARPS / 4) {
+            for (int ci = grp; ci < args.bn / 8;
+                 ci += NUM_XFORM_WARPS / 4, yc += chunk_step, left -= 8 * (NUM_XFORM_WARPS / 4)) {
                 uint32_t v[8];
                 tmem_ld_x8(tmem + lane_base + ACC_COL + 8u * ci, v);
                 tmem_wait_ld();
-                if (r < R) {
-                    const int mb = m0 + 8 * ci;
+                if (row_ok) {
+                    float *p = yc;
 #pragma unroll
-                    for (int t = 0; t < 8; ++t)
-                        if (mb + t < args.M)
-                            __stcs(args.y + static_cast<int64_t>(mb + t) * args.N + n, __uint_as_float(v[t]));
+                    for (int t = 0; t < 8; ++t, p += N)
+                        if (t < left) __stcs(p, __uint_as_float(v[t]));
                 }
             }
             tc_fence_before();
@@ -714,20 +732,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int q = 0; q < S; ++q) mbar_arrive_remote(map_shared_rank(part_free, q));
             }
         }
+        // The owners arrive on this CTA's part_free once they have read the partials
+        // of the last unit pushed from here: wait for that before the CTA may exit.
+        if (ok && S > 1 && it > 0) __all_sync(0xffffffffu, wait_bar_cluster(part_free, (it - 1) & 1, ctl, WAIT_PART));
         tc_fence_before();
     }
 
-    __syncthreads();
-    // Two accumulators: the CTA's last unit, finished by the transform warps (all
-    // other roles are done).  With split-K each transform warp pushes its partials
-    // into the owners' buffers and every CTA then sums its tokens over the ranks in
-    // rank order and writes y.  With a buffer of its own: the push waits until the
-    // owners have consumed the previous unit (part_free), each warp then arrives on
-    // the owners' part_last barrier and every thread of a CTA waits for all ranks'
-    // pushes into it; once part_last has completed nothing touches this CTA any
-    // more, so it may exit.  With the buffer overlaying the rings (one unit per
-    // CTA), a first cluster barrier makes sure every CTA's rings are idle before
-    // the push and a second one that the pushes have landed.
+    // Two accumulators: the CTA's last unit, finished by the transform warps.  With
+    // split-K each transform warp pushes its partials into the owners' buffers,
+    // arrives on the owners' part_last barrier, and the non-epilogue warps of every
+    // CTA then sum its tokens over the ranks in rank order and write y.  With a
+    // partial buffer of its own (several units per CTA) the epilogue warps may still
+    // be reducing the previous unit through it, so the last unit's partials go to a
+    // second buffer at the start of the owners' rings instead: a CTA's rings are
+    // idle once its last unit's MMAs are done, which it tells every rank through
+    // rings_idle, and the push waits until all ranks have.  With the buffer
+    // overlaying the rings (one unit per CTA), a first cluster barrier makes sure
+    // every CTA's rings are idle before the push and a second one that the pushes
+    // have landed.
+    if (!split_mbar) __syncthreads();
     if (nbufs == 2 && n_mine > 0) {
         const int lit = n_mine - 1;
         const int lu = units0 + lit * ustep;
@@ -764,7 +787,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         } else {
             const uint32_t rank = cluster_ctarank();
             const int per = (args.bn + S - 1) / S;
-            const uint32_t part = smem_u32(smem + args.part_off);
+            const int last_off = split_mbar ? 0 : args.part_off;  // this unit's partial buffer
+            const uint32_t part = smem_u32(smem + last_off);
             if (split_mbar) {
                 if (warp < FIRST_EPI_WARP) cluster_wait();  // (the epilogue warps waited already)
             } else {
@@ -772,8 +796,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (xf) {
                 bool push_ok = acc_ok;
-                if (push_ok && n_mine > 1)
-                    push_ok = __all_sync(0xffffffffu, wait_bar_cluster(part_free, (n_mine - 2) & 1, ctl, WAIT_PART));
+                if (split_mbar) {
+                    // This CTA's MMAs are done (or failed): its rings are idle.
+                    if (warp == FIRST_XFORM_WARP && lane == 0)
+                        for (int q = 0; q < S; ++q) mbar_arrive_remote(map_shared_rank(rings_idle, q));
+                    push_ok = __all_sync(0xffffffffu, wait_bar<true, false>(rings_idle, 0, ctl, WAIT_PART)) && push_ok;
+                }
                 if (push_ok && !aborted(ctl)) {
                     tc_fence_after();
                     for (int ci = grp; ci < args.bn / 16; ci += NUM_XFORM_WARPS / 4) {
@@ -803,17 +831,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int q = 0; q < S; ++q) mbar_arrive_remote(map_shared_rank(part_last, q));
                 }
             }
+            // With split_mbar the epilogue warps take no part: they may still be busy.
+            const bool summer = !split_mbar || warp < FIRST_EPI_WARP;
             bool all_in = true;
             if (split_mbar)
-                all_in = __all_sync(0xffffffffu, wait_bar_cluster(part_last, 0, ctl, WAIT_PART));
+                all_in = summer && __all_sync(0xffffffffu, wait_bar<true, false>(part_last, 0, ctl, WAIT_PART));
             else
                 cluster_sync();
             const int t0 = min(args.bn, static_cast<int>(rank) * per);
             const int t1 = min(args.bn, t0 + per);
-            if (all_in && !aborted(ctl)) {
-                const float *pbuf = reinterpret_cast<const float *>(smem + args.part_off);
+            if (summer && all_in && !aborted(ctl)) {
+                const float *pbuf = reinterpret_cast<const float *>(smem + last_off);
                 const int items = (t1 - t0) * (TILE_ROWS / 4);
-                for (int itm = threadIdx.x; itm < items; itm += NUM_THREADS) {
+                const int nsum = split_mbar ? FIRST_EPI_WARP * 32 : NUM_THREADS;
+                for (int itm = threadIdx.x; itm < items; itm += nsum) {
                     const int tt = itm / (TILE_ROWS / 4);
                     const int r4 = 4 * (itm % (TILE_ROWS / 4));
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -833,8 +864,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
     }
-    // (With split-K the last unit's second cluster barrier above is the last point
-    // at which peers touch this CTA: no further barrier is needed before exit.)
+    // Every read of tensor memory (epilogue and transform warps) is done before it
+    // is released.  (Peers touch this CTA's shared memory no more by now: every
+    // remote write or arrival aimed at it is one that a thread here waited for.)
+    __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
@@ -901,14 +934,16 @@ static int device_info(DeviceInfo *&out) {
     if (!d.ready[kFmt]) {
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return QWP_ERR_CUDA;
-        if (cudaFuncSetAttribute(qwp_gemm_kernel<kFmt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(qwp_gemm_kernel<kFmt, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(qwp_gemm_kernel<kFmt, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_BYTES) != cudaSuccess)
             return QWP_ERR_CUDA;
         d.slots[kFmt][1] = d.sms;
         for (int S = 2; S <= MAX_SPLITS; ++S) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(1, 1, S * 64);
-            cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+            cfg.blockDim = dim3(block_threads(true), 1, 1);
             cfg.dynamicSmemBytes = SMEM_BYTES;
             cudaLaunchAttribute attr;
             attr.id = cudaLaunchAttributeClusterDimension;
@@ -918,7 +953,7 @@ static int device_info(DeviceInfo *&out) {
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
             int clusters = 0;
-            if (cudaOccupancyMaxActiveClusters(&clusters, qwp_gemm_kernel<kFmt>, &cfg) != cudaSuccess) {
+            if (cudaOccupancyMaxActiveClusters(&clusters, qwp_gemm_kernel<kFmt, true>, &cfg) != cudaSuccess) {
                 cudaGetLastError();
                 clusters = 0;
             }
@@ -1067,7 +1102,7 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.clusters), 1, plan.S);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(block_threads(a.acc_bufs == 2), 1, 1);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];
@@ -1086,7 +1121,9 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     }
     cfg.attrs = attrs;
     cfg.numAttrs = nattr;
-    if (cudaLaunchKernelEx(&cfg, qwp_gemm_kernel<kFmt>, map, a) != cudaSuccess) {
+    const cudaError_t le = a.acc_bufs == 2 ? cudaLaunchKernelEx(&cfg, qwp_gemm_kernel<kFmt, true>, map, a)
+                                           : cudaLaunchKernelEx(&cfg, qwp_gemm_kernel<kFmt, false>, map, a);
+    if (le != cudaSuccess) {
         cudaGetLastError();
         return QWP_ERR_CUDA;
     }
