@@ -19,7 +19,7 @@
  * bytes of pool scratch (G <= 2 CTAs per SM) for the tiles its CTAs share.
  * Results are deterministic (shared tiles are summed in a fixed order).  By
  * default (QWP_DECODE_AUTO) it takes such products only where it measured
- * faster than the prefill kernel on GB300: M <= 2 and N >= 10240; see
+ * faster than the prefill kernel on GB300: M == 1 and N >= 65536; see
  * qwp_set_decode_policy.
  * Every entry point returns QWP_OK (0) or a negative qwp_status; none throws.
  * Calls are thread-safe.
@@ -261,8 +261,8 @@ QWP_API int qwp_device_status(void *stream);
 
 /*
  * Which decode-shaped products (see the top of this file) the GEMM entry points
- * run on the decode kernel, process-wide: QWP_DECODE_AUTO (the default: M <= 2
- * and N >= 10240, where it measured faster), QWP_DECODE_NEVER (always the
+ * run on the decode kernel, process-wide: QWP_DECODE_AUTO (the default: M == 1
+ * and N >= 65536, where it measured faster), QWP_DECODE_NEVER (always the
  * prefill kernel) or QWP_DECODE_ALWAYS (every decode-shaped product).  Results
  * meet the same error bound either way.  Returns the previous policy (>= 0) or
  * QWP_ERR_INVALID_ARG.  Calls already issued keep the kernel they were given;

@@ -32,11 +32,12 @@ enum : int { DECODE_POLICY_AUTO = 0, DECODE_POLICY_NEVER = 1, DECODE_POLICY_ALWA
 
 // The automatic choice, from both kernels timed on GB300 at 1 to 8 tokens (Q4_K,
 // Q6_K and W4A16, N from 2048 to 152064, K from 4096 to 12288): the decode kernel
-// is faster only at one or two tokens and for at least 80 row tiles (N >= 10240),
-// by 3-10%; the prefill kernel wins for narrower matrices (by up to 15% at
-// N = 6144), for K-heavy ones (N = 4096, K = 12288) and from three tokens on.
-constexpr int64_t DECODE_AUTO_MAX_TOKENS = 2;
-constexpr int64_t DECODE_AUTO_MIN_ROWS = 10240;
+// is clearly faster only for vocabulary-sized matrices at one token (2% for Q4_K,
+// 7% for Q6_K at N = 152064); from N = 10240 to 24576 the two are within a few
+// percent either way, and the prefill kernel wins for narrower or K-heavy
+// matrices and from two or three tokens on.
+constexpr int64_t DECODE_AUTO_MAX_TOKENS = 1;
+constexpr int64_t DECODE_AUTO_MIN_ROWS = 65536;
 inline bool decode_auto(int64_t M, int64_t N, int64_t K) {
     return decode_fits(M, N, K) && M <= DECODE_AUTO_MAX_TOKENS && N >= DECODE_AUTO_MIN_ROWS;
 }

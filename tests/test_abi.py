@@ -107,19 +107,19 @@ def test_gemm_argument_checks_before_any_cuda_call(lib):
 
 def test_decode_policy_round_trip_and_automatic_rule(lib):
     """The dispatch between the decode and the prefill kernel is host logic: the
-    automatic rule (1-2 tokens, N >= 10240, plus what the decode kernel needs:
+    automatic rule (one token, N >= 65536, plus what the decode kernel needs:
     K % 256 == 0 and >= 600 tile items), the two forced policies, and the
     rejection of an unknown policy."""
     prev = qwp.set_decode_policy(qwp.DECODE_AUTO)
     try:
-        assert qwp.decode_selected(1, 24576, 4096) and qwp.decode_selected(2, 10240, 4096)
-        assert qwp.decode_selected(1, 152064, 4096)
-        assert not qwp.decode_selected(3, 24576, 4096)      # three tokens: the prefill kernel
-        assert not qwp.decode_selected(1, 10112, 4096)      # 79 row tiles
-        assert not qwp.decode_selected(1, 4096, 12288)      # K-heavy
-        assert not qwp.decode_selected(1, 24576, 4000)      # K % 256 != 0
-        assert not qwp.decode_selected(1, 10240, 1792)      # 80 x 7 = 560 items
-        assert not qwp.decode_selected(0, 24576, 4096)
+        assert qwp.decode_selected(1, 152064, 4096) and qwp.decode_selected(1, 65536, 4096)
+        assert qwp.decode_selected(1, 65600, 512)           # 513 x 2 = 1026 items
+        assert not qwp.decode_selected(2, 152064, 4096)     # two tokens: the prefill kernel
+        assert not qwp.decode_selected(1, 65408, 4096)      # 511 row tiles
+        assert not qwp.decode_selected(1, 24576, 4096)
+        assert not qwp.decode_selected(1, 152064, 4000)     # K % 256 != 0
+        assert not qwp.decode_selected(1, 65536, 256)       # 512 x 1 = 512 items
+        assert not qwp.decode_selected(0, 152064, 4096)
         assert qwp.set_decode_policy(qwp.DECODE_ALWAYS) == qwp.DECODE_AUTO
         assert qwp.decode_selected(8, 4096, 12288) and qwp.decode_selected(5, 2500, 8192)
         assert not qwp.decode_selected(9, 24576, 4096)      # more than 8 tokens

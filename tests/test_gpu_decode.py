@@ -54,7 +54,7 @@ def test_decode_shapes_take_the_decode_path():
     assert all(qwp.decode_selected(M, N, K) for M, N, K in SHAPES)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 10240, 2048), (2, 12300, 2048)])
+@pytest.mark.parametrize("M,N,K", [(1, 65600, 512), (1, 66000, 768)])
 def test_default_policy_both_kernels(M, N, K):
     """Under the default policy these shapes take the decode kernel; forced onto the
     prefill kernel they give results within the same bound."""
