@@ -212,7 +212,7 @@ def oracle_layer_tokens_per_s(min_seconds: float):
 def run_reference(args):
     """The oracle as the reference arm: each step is the whole layer's M_TOKENS tokens
     over a row slice of every projection, sized (from a timed 1% slice) so that
-    warm-up and steps together take about REF_BUDGET_S seconds on the host cores;
+    warm-up and steps together take about --ref-seconds on the host cores;
     tok/s counts the slice's share of the layer."""
     import oracle
 
@@ -225,7 +225,7 @@ def run_reference(args):
     c0 = time.perf_counter()
     oracle_layer_step(probe)
     full_step_s = (time.perf_counter() - c0) / probe_share
-    frac = min(1.0, REF_BUDGET_S / (full_step_s * max(1, args.steps + args.warmup)))
+    frac = min(1.0, args.ref_seconds / (full_step_s * max(1, args.steps + args.warmup)))
     inputs, share = oracle_layer_sample(frac)
     for _ in range(args.warmup):
         oracle_layer_step(inputs)
@@ -589,6 +589,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=REF_BUDGET_S,
+                    help="reference arm: host seconds that warm-up and steps together aim at")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gemm", action="append", default=[],
                     help="time single GEMMs instead of the layer: q4k:M:N:K, q6k:M:N:K or w4a16:M:N:K:group[:sym][:bf16]")
