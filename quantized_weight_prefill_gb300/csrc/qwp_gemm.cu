@@ -16,7 +16,8 @@
 // overlap the end of the current one.  Roles:
 //   warp 0        x producer: one thread issues 2-D TMA loads (128-byte swizzle),
 //                 one per 64-wide K block, into the x ring;
-//   warp 1        allocates tensor memory; one thread issues tcgen05.mma;
+//   warp 1        allocates tensor memory; runs the MMA loop, one elected lane
+//                 issuing every tcgen05.mma;
 //   warp 2        weight producer: one bulk copy per 256-wide K stage of packed
 //                 weights into the weight ring;
 //   warps 3..18   transform: four groups of 4 warps; group g owns K block g of
@@ -24,13 +25,16 @@
 //                 unpacks rows 32q..32q+31 (its tensor-memory lane quarter) of
 //                 that block, 64 weights per thread, to fp16 and stores them with
 //                 one tcgen05.st into the A ring in tensor memory;
-//   warps 19..22  epilogue: drain the fp32 accumulator (tcgen05.ld) into y, or,
-//                 with split-K, into the owning CTA of the cluster, which sums
-//                 the partials in rank order (deterministic) and writes y.
+//   warps 19..22  epilogue (two-accumulator kernel only): drain the fp32
+//                 accumulator (tcgen05.ld) into y, or, with split-K, into the
+//                 owning CTA of the cluster, which sums the partials in rank
+//                 order (deterministic) and writes y.
 // Tensor memory (512 columns): the A ring (8 blocks of 128 lanes x 64 K = 32
-// columns) at column 256; below it one accumulator [128 lanes x BN], or two of
-// 128 columns when BN <= 128, so that the epilogue of a unit overlaps the MMAs of
-// the next.  The MMA is D[128 x BN] += A[128 x 16] (tensor memory) .
+// columns) at column 256; below it one accumulator [128 lanes x BN], drained by
+// the transform warps between units (the one-accumulator kernel: BN > 128, 19
+// warps), or two of 128 columns when BN <= 128, so that the epilogue of a unit
+// overlaps the MMAs of the next (the two-accumulator kernel: 23 warps, split-K
+// allowed).  The MMA is D[128 x BN] += A[128 x 16] (tensor memory) .
 // B[BN x 16]^T (shared memory): weights are the M side and tokens the N side, so
 // a tile reuses each unpacked weight for BN tokens.
 //

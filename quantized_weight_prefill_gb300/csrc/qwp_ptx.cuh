@@ -126,20 +126,10 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[tmem] . B[smem]^T, kind::f16 (bf16 or fp16 operands, fp32 accumulate).
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// The same MMA with B's shared-memory descriptor given as its two 32-bit words
-// (the address field is in the low word, so callers step the low word alone) and
-// the accumulate flag fixed at compile time where it is known.
+// D[tmem] (+)= A[tmem] . B[smem]^T, kind::f16 (bf16 or fp16 operands, fp32
+// accumulate).  B's shared-memory descriptor is given as its two 32-bit words (the
+// address field is in the low word, so callers step the low word alone); whether D
+// accumulates is fixed at compile time.
 template <bool kAccumulate>
 __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
                                          uint32_t idesc) {
@@ -163,17 +153,6 @@ __device__ __forceinline__ bool elect_one() {
     return pred != 0;
 }
 
-// D[tmem] (+)= A[smem] . B[smem]^T.
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // Arrive (once) on `bar` when all tcgen05 async operations issued so far by this thread complete.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
@@ -187,16 +166,6 @@ __device__ __forceinline__ void tmem_wait_st() {
 
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Each thread of the warp stores 16 consecutive 32-bit columns of its own lane.
-__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-        "%12, %13, %14, %15, %16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
 }
 
 // Each thread of the warp stores 32 consecutive 32-bit columns of its own lane.
@@ -295,15 +264,6 @@ __device__ __forceinline__ void fence_acq_rel_cluster() {
 
 __device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
 }
 
 }  // namespace qwp
