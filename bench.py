@@ -167,18 +167,22 @@ def layer_workload():
             f"gate+up K4096->N24576, down K12288->N4096; Q4_K weights, bf16 x, fp32 y")
 
 
-def oracle_layer_sample(frac: float, seed: int = 7):
+def oracle_layer_sample(frac: float, seed: int = 7, min_rows: int = 1):
     """Inputs of one oracle step over all M_TOKENS tokens and the first
-    max(1, round(frac * N)) weight rows of every projection; returns the inputs and
-    the fraction of the layer's weights they cover (the oracle's time is linear in
-    the rows: every row is dequantized and multiplied once per step)."""
+    max(min_rows, round(frac * N)) weight rows of every projection (at most N);
+    returns the inputs and
+    the fraction of the layer's weights they cover.  x is decoded to fp64 here,
+    once: a step's time is then linear in the rows (every row is dequantized and
+    multiplied once per step), so a row slice times its share of the layer."""
+    import oracle
     import synth
 
     inputs, rows_k = [], 0
     for i, (_, K, N) in enumerate(LAYER):
-        n = max(1, min(N, int(round(frac * N))))
+        n = min(N, max(min_rows, int(round(frac * N))))
         blocks = synth.q4k_weights(N, K, seed=seed + i).reshape(N, -1)[:n]
-        inputs.append((blocks, synth.activations_bf16(M_TOKENS, K, seed=seed + 10 + i), n, K))
+        x = oracle.bf16_to_f64(synth.activations_bf16(M_TOKENS, K, seed=seed + 10 + i))
+        inputs.append((blocks, x, n, K))
         rows_k += n * K
     return inputs, rows_k / sum(N * K for _, K, N in LAYER)
 
@@ -187,8 +191,7 @@ def oracle_layer_step(inputs):
     """One step of the CPU oracle (exact fp64 dequant of the rows + naive fp64 GEMM)."""
     import oracle
 
-    for blocks, xb, n, K in inputs:
-        x = oracle.bf16_to_f64(xb)
+    for blocks, x, n, K in inputs:
         for n0 in range(0, n, 2048):
             n1 = min(n, n0 + 2048)
             oracle.gemm(x, oracle.q4k_dequant(blocks[n0:n1], n1 - n0, K), with_abs=False)
@@ -212,21 +215,25 @@ def oracle_layer_tokens_per_s(min_seconds: float):
 def run_reference(args):
     """The oracle as the reference arm: each step is the whole layer's M_TOKENS tokens
     over a row slice of every projection, sized (from a timed 1% slice) so that
-    warm-up and steps together take about --ref-seconds on the host cores;
-    tok/s counts the slice's share of the layer."""
+    warm-up and steps together take about --ref-seconds on the host cores, but
+    with at least two rows per oracle thread (at very many steps the run then
+    takes longer); tok/s counts the slice's share of the layer."""
     import oracle
 
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    # The oracle parallelises over weight rows: a slice keeps at least two rows per
+    # thread in every projection, so that it runs at the whole layer's rate.
+    min_rows = 2 * oracle.num_threads()
     # calibrate: time a 1% slice, extrapolate to the whole layer
-    probe, probe_share = oracle_layer_sample(0.01)
+    probe, probe_share = oracle_layer_sample(0.01, min_rows=min_rows)
     oracle_layer_step(probe)
     c0 = time.perf_counter()
     oracle_layer_step(probe)
     full_step_s = (time.perf_counter() - c0) / probe_share
     frac = min(1.0, args.ref_seconds / (full_step_s * max(1, args.steps + args.warmup)))
-    inputs, share = oracle_layer_sample(frac)
+    inputs, share = oracle_layer_sample(frac, min_rows=min_rows)
     for _ in range(args.warmup):
         oracle_layer_step(inputs)
     t0 = time.perf_counter()
