@@ -276,6 +276,20 @@ QWP_API int qwp_set_decode_policy(int policy);
  * policy, 0 if the prefill kernel (host-only; no device call). */
 QWP_API int qwp_decode_selected(int64_t M, int64_t N, int64_t K);
 
+/*
+ * The launch a GEMM call of this shape gets on the current device (host only:
+ * it reads the device's properties but launches nothing).  `format`: 0 W4A16,
+ * 1 Q4_K, 2 Q6_K.  plan_out[6] receives: [0] the kernel (1 the prefill kernel,
+ * 2 the decode kernel, which leaves [1..5] at 0); [1] the split-K factor S (the
+ * cluster size); [2] the clusters launched; [3] the token tile (tokens per
+ * unit); [4] the units (128-row tiles x token tiles); [5] the units per cluster
+ * at most.  Returns QWP_OK, QWP_ERR_INVALID_ARG (NULL plan_out, a size below 1,
+ * an unknown format), QWP_ERR_UNSUPPORTED_SHAPE (K not a multiple of 256 for
+ * Q4_K / Q6_K or of 64 for W4A16, a size above 2^30), QWP_ERR_DEVICE or
+ * QWP_ERR_CUDA.
+ */
+QWP_API int qwp_gemm_plan(int format, int64_t M, int64_t N, int64_t K, int32_t *plan_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,6 +22,7 @@ __all__ = [
     "q6k_repacked_bytes", "q6k_repack", "q6k_dequant", "q6k_gemm", "q6k_gemm_f16",
     "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_bf16",
     "device_status", "set_decode_policy", "decode_selected", "DECODE_AUTO", "DECODE_NEVER", "DECODE_ALWAYS",
+    "gemm_plan",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -30,7 +31,7 @@ EXPORTED_SYMBOLS = (
     "qwp_status_string", "q4k_repacked_bytes", "q4k_repack", "q4k_dequant", "q4k_gemm", "q4k_gemm_f16",
     "q4k_gemm_noalloc", "q6k_repacked_bytes", "q6k_repack", "q6k_dequant", "q6k_gemm", "q6k_gemm_f16",
     "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_bf16",
-    "qwp_device_status", "qwp_set_decode_policy", "qwp_decode_selected",
+    "qwp_device_status", "qwp_set_decode_policy", "qwp_decode_selected", "qwp_gemm_plan",
 )
 
 # Decode-kernel dispatch policies (enum qwp_decode_policy in the header).
@@ -80,6 +81,7 @@ def library() -> ctypes.CDLL:
         lib.qwp_device_status.argtypes = [p]
         lib.qwp_set_decode_policy.argtypes = [ctypes.c_int]
         lib.qwp_decode_selected.argtypes = [i64, i64, i64]
+        lib.qwp_gemm_plan.argtypes = [ctypes.c_int, i64, i64, i64, p]
         for name in EXPORTED_SYMBOLS:
             if name != "qwp_status_string":
                 getattr(lib, name).restype = ctypes.c_int
@@ -303,3 +305,18 @@ def set_decode_policy(policy: int) -> int:
 def decode_selected(M: int, N: int, K: int) -> bool:
     """Whether a GEMM call of this shape would run the decode kernel now."""
     return bool(library().qwp_decode_selected(int(M), int(N), int(K)))
+
+
+_PLAN_FORMATS = {"w4a16": 0, "q4k": 1, "q6k": 2}
+
+
+def gemm_plan(fmt: str, M: int, N: int, K: int) -> dict:
+    """The launch a GEMM call of this shape gets on the current device: kernel
+    ("prefill" or "decode"), split-K factor, clusters, token tile, units and
+    units per cluster (the prefill kernel's; zero for the decode kernel)."""
+    out = (ctypes.c_int32 * 6)()
+    _check(library().qwp_gemm_plan(_PLAN_FORMATS[fmt], int(M), int(N), int(K), ctypes.cast(out, ctypes.c_void_p)),
+           "qwp_gemm_plan")
+    return {"kernel": {1: "prefill", 2: "decode"}[out[0]], "splits": out[1], "clusters": out[2],
+            "token_tile": out[3], "units": out[4], "units_per_cluster": out[5]}
+

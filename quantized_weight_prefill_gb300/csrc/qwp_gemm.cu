@@ -1032,31 +1032,31 @@ static Plan choose_plan(const int *slots, int64_t units, int nstages, int64_t nk
     return best;
 }
 
-// x is fp16 [M, K].  `after_prior` launches with programmatic stream
-// serialization so the kernel's set-up and weight prefetch overlap the grid just
-// before it (the x producer waits for that grid with griddepcontrol.wait).
+// Bytes of one weight stage (128 rows x 256 K) in format kFmt.
 template <int kFmt>
-static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, const void *x,
-                       float *y, int64_t M, int64_t N, int64_t K, int64_t group, cudaStream_t stream,
-                       uint64_t timeout_ns, bool after_prior) {
-    int rc = check_device();
-    if (rc) return rc;
+constexpr int weight_stage_bytes() {
+    return kFmt == FMT_Q4K   ? TILE_ROWS * Q4K_BLOCK_BYTES
+           : kFmt == FMT_Q6K ? TILE_ROWS * Q6K_BLOCK_BYTES
+                             : TILE_ROWS * CHUNK_ROW_BYTES * KB_PER_STAGE;
+}
+
+// Token tile, launch plan and unit count of an M x N x K product in format kFmt
+// on the current device (host only).
+template <int kFmt>
+static int plan_gemm(int64_t M, int64_t N, int64_t K, Plan &plan, int &bn, int64_t &units) {
     DeviceInfo *info = nullptr;
-    if ((rc = device_info<kFmt>(info))) return rc;
-    uint32_t *status = status_word();
-    if (!status) return QWP_ERR_CUDA;
+    const int rc = device_info<kFmt>(info);
+    if (rc) return rc;
     const int64_t row_tiles = (N + TILE_ROWS - 1) / TILE_ROWS;
     const int64_t nkb_total = K / CHUNK_K;
     const int nstages = static_cast<int>((nkb_total + KB_PER_STAGE - 1) / KB_PER_STAGE);
-    const int w_stage_bytes = kFmt == FMT_Q4K   ? TILE_ROWS * Q4K_BLOCK_BYTES
-                              : kFmt == FMT_Q6K ? TILE_ROWS * Q6K_BLOCK_BYTES
-                                                : TILE_ROWS * CHUNK_ROW_BYTES * KB_PER_STAGE;
+    const int w_stage_bytes = weight_stage_bytes<kFmt>();
     // Token tile: the widest (fewest tiles of <= 256 tokens) unless tiles of <= 128,
     // which allow split-K and two accumulators, give a cheaper plan (few units).
-    int bn = choose_bn(M, BN_MAX);
+    bn = choose_bn(M, BN_MAX);
     int64_t tok_tiles = (M + bn - 1) / bn;
     if (row_tiles * tok_tiles > 0x7fffffff) return QWP_ERR_UNSUPPORTED_SHAPE;
-    Plan plan = choose_plan(info->slots[kFmt], row_tiles * tok_tiles, nstages, nkb_total, bn, w_stage_bytes);
+    plan = choose_plan(info->slots[kFmt], row_tiles * tok_tiles, nstages, nkb_total, bn, w_stage_bytes);
     if (bn > static_cast<int>(ACC_STRIDE)) {
         const int bn2 = choose_bn(M, static_cast<int>(ACC_STRIDE));
         const int64_t tt2 = (M + bn2 - 1) / bn2;
@@ -1070,7 +1070,27 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
         }
     }
     if (plan.clusters <= 0) return QWP_ERR_UNSUPPORTED_SHAPE;
-    const int64_t units = row_tiles * tok_tiles;
+    units = row_tiles * tok_tiles;
+    return QWP_OK;
+}
+
+// x is fp16 [M, K].  `after_prior` launches with programmatic stream
+// serialization so the kernel's set-up and weight prefetch overlap the grid just
+// before it (the x producer waits for that grid with griddepcontrol.wait).
+template <int kFmt>
+static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, const void *x,
+                       float *y, int64_t M, int64_t N, int64_t K, int64_t group, cudaStream_t stream,
+                       uint64_t timeout_ns, bool after_prior) {
+    int rc = check_device();
+    if (rc) return rc;
+    uint32_t *status = status_word();
+    if (!status) return QWP_ERR_CUDA;
+    Plan plan;
+    int bn = 0;
+    int64_t units = 0;
+    if ((rc = plan_gemm<kFmt>(M, N, K, plan, bn, units))) return rc;
+    const int64_t row_tiles = (N + TILE_ROWS - 1) / TILE_ROWS;
+    const int nstages = static_cast<int>((K / CHUNK_K + KB_PER_STAGE - 1) / KB_PER_STAGE);
     CUtensorMap map;
     if ((rc = encode_x_map(&map, x, M, K, bn))) return rc;
 
@@ -1093,7 +1113,7 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     a.timeout_ns = timeout_ns;
     a.cb_shift = plan.cbs;
     a.x_stage_bytes = (bn * 128) << plan.cbs;
-    a.w_stage_bytes = w_stage_bytes;
+    a.w_stage_bytes = weight_stage_bytes<kFmt>();
     a.x_stages = plan.x_stages;
     a.w_stages = plan.w_stages;
     a.part_off = plan.part_off;
@@ -1297,4 +1317,32 @@ extern "C" int w4a16_gemm_bf16(const void *wq_tiled, const void *scales, const u
     if (!rc) rc = launch_gemm<FMT_W4A16>(wq_tiled, scales, zeros, x16, y, M, N, K, group, s, kDefaultTimeoutNs, true);
     if (cudaFreeAsync(x16, s) != cudaSuccess && !rc) rc = QWP_ERR_CUDA;
     return rc;
+}
+
+extern "C" int qwp_gemm_plan(int format, int64_t M, int64_t N, int64_t K, int32_t *plan_out) {
+    if (!plan_out || M < 1 || N < 1 || K < 1) return QWP_ERR_INVALID_ARG;
+    if (format != FMT_W4A16 && format != FMT_Q4K && format != FMT_Q6K) return QWP_ERR_INVALID_ARG;
+    if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30)) return QWP_ERR_UNSUPPORTED_SHAPE;
+    if (K % (format == FMT_W4A16 ? CHUNK_K : Q4K_BLOCK)) return QWP_ERR_UNSUPPORTED_SHAPE;
+    for (int i = 0; i < 6; ++i) plan_out[i] = 0;
+    if (decode_shaped(M, N, K)) {
+        plan_out[0] = 2;
+        return QWP_OK;
+    }
+    int rc = check_device();
+    if (rc) return rc;
+    Plan plan;
+    int bn = 0;
+    int64_t units = 0;
+    rc = format == FMT_Q4K   ? plan_gemm<FMT_Q4K>(M, N, K, plan, bn, units)
+         : format == FMT_Q6K ? plan_gemm<FMT_Q6K>(M, N, K, plan, bn, units)
+                             : plan_gemm<FMT_W4A16>(M, N, K, plan, bn, units);
+    if (rc) return rc;
+    plan_out[0] = 1;
+    plan_out[1] = plan.S;
+    plan_out[2] = plan.clusters;
+    plan_out[3] = bn;
+    plan_out[4] = static_cast<int32_t>(units);
+    plan_out[5] = static_cast<int32_t>((units + plan.clusters - 1) / plan.clusters);
+    return QWP_OK;
 }

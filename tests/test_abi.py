@@ -133,3 +133,22 @@ def test_decode_policy_round_trip_and_automatic_rule(lib):
     finally:
         qwp.set_decode_policy(prev)
 
+
+def test_gemm_plan_argument_checks(lib):
+    """qwp_gemm_plan rejects bad arguments before touching the device; decode-shaped
+    products are answered on the host."""
+    out = (ctypes.c_int32 * 6)()
+    p = ctypes.cast(out, ctypes.c_void_p)
+    assert lib.qwp_gemm_plan(1, 105, 24576, 4096, None) == INVALID
+    assert lib.qwp_gemm_plan(3, 105, 24576, 4096, p) == INVALID          # no such format
+    assert lib.qwp_gemm_plan(1, 0, 24576, 4096, p) == INVALID
+    assert lib.qwp_gemm_plan(1, 105, 24576, 4000, p) == SHAPE            # Q4_K: K % 256
+    assert lib.qwp_gemm_plan(2, 105, 24576, 4032, p) == SHAPE            # Q6_K: K % 256
+    assert lib.qwp_gemm_plan(0, 105, 24576, 4000, p) == SHAPE            # W4A16: K % 64
+    assert lib.qwp_gemm_plan(1, 105, 1 << 31, 4096, p) == SHAPE
+    prev = qwp.set_decode_policy(qwp.DECODE_ALWAYS)
+    try:
+        assert lib.qwp_gemm_plan(1, 1, 24576, 4096, p) == OK and list(out) == [2, 0, 0, 0, 0, 0]
+    finally:
+        qwp.set_decode_policy(prev)
+
