@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import subprocess
@@ -50,12 +51,22 @@ def layer_bytes(M):
 
 
 def kernel_source_hash() -> str:
-    h = hashlib.sha256()
+    """Hash of the sources the prefill kernel is compiled from: qwp_gemm.cu and
+    the local headers it includes, followed transitively."""
     csrc = os.path.join(ROOT, "quantized_weight_prefill_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode())
-            h.update(fh.read())
+    h = hashlib.sha256()
+    todo, seen = [os.path.join(csrc, "qwp_gemm.cu")], set()
+    while todo:
+        path = os.path.normpath(todo.pop(0))
+        if path in seen:
+            continue
+        seen.add(path)
+        with open(path, "rb") as fh:
+            text = fh.read()
+        h.update(os.path.relpath(path, ROOT).encode())
+        h.update(text)
+        for inc in re.findall(rb'#include "([^"]+)"', text):
+            todo.append(os.path.join(os.path.dirname(path), inc.decode()))
     return h.hexdigest()[:16]
 
 
