@@ -50,9 +50,10 @@ constexpr int DEC_THREADS = 32 * (DEC_CWARPS + 1);
 constexpr int DEC_X_BYTES = DEC_TOKENS * Q4K_BLOCK * 2;  // one super-block of x: 4 boxes of 8 x 128 B
 constexpr int DEC_PART_FLOATS = DEC_CWARPS * 32 * 4;     // one float4 per consumer lane
 
-// Ring depth per format (two CTAs per SM fit in shared memory).
+// Ring depth per format: Q4_K runs three CTAs per SM (3 slots of 23 KiB each),
+// Q6_K and W4A16 two (3 slots of 27 KiB, 4 of 20 KiB).
 template <int kFmt>
-__host__ __device__ constexpr int dec_stages() { return kFmt == DFMT_Q6K ? 3 : 4; }
+__host__ __device__ constexpr int dec_stages() { return kFmt == DFMT_W4A16 ? 4 : 3; }
 
 // Items the producer issues before the first one has landed.
 constexpr int DEC_PRE = 4;
@@ -99,7 +100,7 @@ __device__ __forceinline__ bool dec_wait(uint32_t bar, uint32_t parity, uint32_t
 enum : uint32_t { DWAIT_FULL = 0x21, DWAIT_READY, DWAIT_EMPTY, DWAIT_DRAIN };
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -264,7 +265,7 @@ __device__ __forceinline__ uint32_t item_owner(uint32_t i, uint32_t items, uint3
 }
 
 template <int kFmt>
-__global__ void __launch_bounds__(DEC_THREADS, 2)
+__global__ void __launch_bounds__(DEC_THREADS, kFmt == DFMT_Q4K ? 3 : 2)
     qwp_decode_kernel(const __grid_constant__ CUtensorMap tmap_x, const DecodeArgs args) {
     constexpr int NS = dec_stages<kFmt>();
     extern __shared__ uint8_t smem_raw[];
