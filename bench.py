@@ -504,67 +504,83 @@ def run_gpu(args):
         raise RuntimeError("kernel timeout during the per-launch timing pass")
     dom_ms = float(np.mean(dom_samples))
 
-    # ---- end to end: host buffers, copies inside the timed region.  Each step is
-    # one replay of a graph captured from the public API: the four x are copied
-    # from pinned host memory on one side stream, the four library calls run on the
-    # main stream, each as soon as its x has arrived, and each y is copied back to
-    # pinned host memory on another side stream as soon as its GEMM is done, so
-    # the copies of one projection overlap the GEMMs of the others.
+    # ---- end to end: host buffers, copies inside the timed region.  Steps run as
+    # a serving loop would: every step copies its four x from pinned host memory
+    # (side stream h2d_s), runs the four library calls on the main stream, each as
+    # soon as its x has arrived, and copies each y back to pinned host memory
+    # (side stream d2h_s) as soon as its GEMM is done.  Device x/y and host y are
+    # double-buffered, so step s+1's copies and GEMMs overlap step s's read-back;
+    # a buffer is reused only after the step two back has finished with it.  One
+    # CUDA graph holds E2E_SPAN steps (every weight copy at least once).
     x_host = [x.cpu().pin_memory() for x in xs]
-    y_host = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys]
-    x_dev = [torch.empty_like(x) for x in xs]
+    x_dev = [[torch.empty_like(x) for x in xs] for _ in range(2)]
+    y_dev = [[torch.empty_like(y) for y in ys] for _ in range(2)]
+    y_host = [[torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys] for _ in range(2)]
     h2d = sum(x.numel() * x.element_size() for x in x_host)
-    d2h = sum(y.numel() * y.element_size() for y in y_host)
+    d2h = sum(y.numel() * y.element_size() for y in y_host[0])
     h2d_s = torch.cuda.Stream(dev)
     d2h_s = torch.cuda.Stream(dev)
+    span = 4 * copies
 
-    def e2e_graph(c):
-        w = weights[c]
+    def e2e_graph():
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             cap = torch.cuda.current_stream(dev)
             h2d_s.wait_stream(cap)
             d2h_s.wait_stream(cap)
-            x_in = []
-            with torch.cuda.stream(h2d_s):
-                for i in range(len(LAYER)):
-                    x_dev[i].copy_(x_host[i], non_blocking=True)
-                    x_in.append(torch.cuda.Event())
-                    x_in[-1].record(h2d_s)
-            for i, (_, K, N) in enumerate(LAYER):
-                cap.wait_event(x_in[i])
-                qwp.q4k_gemm(w[i], x_dev[i], N, out=ys[i])
-                done = torch.cuda.Event()
-                done.record(cap)
-                d2h_s.wait_event(done)
-                with torch.cuda.stream(d2h_s):
-                    y_host[i].copy_(ys[i], non_blocking=True)
+            gemm_done, y_read = [], []
+            for j in range(span):
+                b, w = j % 2, weights[j % copies]
+                x_in = []
+                with torch.cuda.stream(h2d_s):
+                    for i in range(len(LAYER)):
+                        if j >= 2:
+                            h2d_s.wait_event(gemm_done[j - 2][i])  # x_dev[b][i] read by then
+                        x_dev[b][i].copy_(x_host[i], non_blocking=True)
+                        x_in.append(torch.cuda.Event())
+                        x_in[-1].record(h2d_s)
+                done, read = [], []
+                for i, (_, K, N) in enumerate(LAYER):
+                    cap.wait_event(x_in[i])
+                    if j >= 2:
+                        cap.wait_event(y_read[j - 2][i])  # y_dev[b][i] copied out by then
+                    qwp.q4k_gemm(w[i], x_dev[b][i], N, out=y_dev[b][i])
+                    done.append(torch.cuda.Event())
+                    done[-1].record(cap)
+                    d2h_s.wait_event(done[-1])
+                    with torch.cuda.stream(d2h_s):
+                        y_host[b][i].copy_(y_dev[b][i], non_blocking=True)
+                        read.append(torch.cuda.Event())
+                        read[-1].record(d2h_s)
+                gemm_done.append(done)
+                y_read.append(read)
             cap.wait_stream(h2d_s)
             cap.wait_stream(d2h_s)
         return g
 
-    e2e_graphs = [e2e_graph(c) for c in range(copies)]
-    for g in e2e_graphs:
-        g.replay()
+    e2e_g = e2e_graph()
+    e2e_g.replay()
     torch.cuda.synchronize()
-    e2e_steps = max(3, min(args.steps, 2000))
-    for s in range(args.warmup):
-        e2e_graphs[s % copies].replay()
+    replays = max(1, min(args.steps, 2000) // span)
+    e2e_steps = replays * span
+    for _ in range(max(1, args.warmup // span)):
+        e2e_g.replay()
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for s in range(e2e_steps):
-        e2e_graphs[s % copies].replay()
+    for _ in range(replays):
+        e2e_g.replay()
     e1.record(stream)
     torch.cuda.synchronize()
     if qwp.device_status() != 0:
         raise RuntimeError("kernel timeout during the end-to-end pass")
-    # the last step's results reached the host: spot-check them against the device
-    for i in range(len(LAYER)):
-        if not torch.equal(y_host[i], ys[i].cpu()):
-            raise RuntimeError("end-to-end copy of y does not match the device result")
+    # the last two steps' results reached the host: spot-check them against the device
+    for b in range(2):
+        for i in range(len(LAYER)):
+            if not torch.equal(y_host[b][i], y_dev[b][i].cpu()):
+                raise RuntimeError("end-to-end copy of y does not match the device result")
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     sampler.stop()
 
@@ -627,8 +643,9 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "e2e": {"value": world * M * e2e_steps / (e2e_ms * 1e-3), "unit": "tok/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "per step one CUDA graph of the public API calls: x from pinned host memory and y "
-                       "back to pinned host memory, copies on side streams overlapping the GEMMs"},
+                "how": "every step copies its x from pinned host memory and its y back to pinned host memory "
+                       "around the four public API calls (copies on side streams, double-buffered so a step's "
+                       f"read-back overlaps the next step's GEMMs); {span} steps per CUDA graph replay"},
         # per call: the bf16 -> fp16 activation conversion and the GEMM
         "gpu_launches": 2 * len(LAYER) * args.steps,
         "clocks": sampler.summary(),
