@@ -50,23 +50,29 @@ def layer_bytes(M):
     return sum(0.5625 * N * K + 2.0 * M * K + 4.0 * M * N for _, K, N in LAYER)
 
 
-def kernel_source_hash() -> str:
-    """Hash of the sources the prefill kernel is compiled from: qwp_gemm.cu and
-    the local headers it includes, followed transitively."""
+def kernel_source_files() -> list:
+    """The sources the prefill kernel is compiled from: qwp_gemm.cu and the local
+    headers it includes, followed transitively (paths relative to the repo)."""
     csrc = os.path.join(ROOT, "quantized_weight_prefill_gb300", "csrc")
-    h = hashlib.sha256()
-    todo, seen = [os.path.join(csrc, "qwp_gemm.cu")], set()
+    todo, seen = [os.path.join(csrc, "qwp_gemm.cu")], []
     while todo:
         path = os.path.normpath(todo.pop(0))
         if path in seen:
             continue
-        seen.add(path)
+        seen.append(path)
         with open(path, "rb") as fh:
-            text = fh.read()
-        h.update(os.path.relpath(path, ROOT).encode())
-        h.update(text)
-        for inc in re.findall(rb'#include "([^"]+)"', text):
-            todo.append(os.path.join(os.path.dirname(path), inc.decode()))
+            for inc in re.findall(rb'#include "([^"]+)"', fh.read()):
+                todo.append(os.path.join(os.path.dirname(path), inc.decode()))
+    return [os.path.relpath(p, ROOT) for p in seen]
+
+
+def kernel_source_hash() -> str:
+    """Hash of kernel_source_files(): a DRAM-traffic record stays valid while it holds."""
+    h = hashlib.sha256()
+    for rel in kernel_source_files():
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(rel.encode())
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 

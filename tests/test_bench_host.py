@@ -1,0 +1,46 @@
+"""Host-side helpers of bench.py, on the CPU: which sources key the stored DRAM
+traffic record, and that the record's algorithmic bytes match its workload."""
+import importlib.util
+import json
+import os
+import re
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_kernel_source_files_follow_includes():
+    files = _bench().kernel_source_files()
+    csrc = "quantized_weight_prefill_gb300/csrc/"
+    assert files[0] == csrc + "qwp_gemm.cu"
+    assert set(files) == {csrc + "qwp_gemm.cu", csrc + "qwp_decode.h", csrc + "qwp_format.cuh",
+                          csrc + "qwp_internal.h", csrc + "qwp_ptx.cuh", "include/qwp.h"}
+    # the decode kernel, the repack/dequant kernels and the no-alloc entry points
+    # are other translation units: changing them leaves the record valid
+    assert not any(f.endswith(("qwp_decode.cu", "qwp_aux.cu", "qwp_noalloc.cu")) for f in files)
+
+
+def test_kernel_source_hash_is_stable():
+    b = _bench()
+    h = b.kernel_source_hash()
+    assert re.fullmatch(r"[0-9a-f]{16}", h) and h == b.kernel_source_hash()
+
+
+def test_traffic_record_is_consistent():
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    M, N, K = (int(v) for v in re.fullmatch(r"M(\d+) N(\d+) K(\d+)", rec["workload"]).groups())
+    # the reported traffic is the captured DRAM reads + writes of one launch
+    assert rec["bytes_per_launch"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
+    # every packed weight byte (144 per 256 weights) and x (fp16) is read once, and
+    # not much more: re-reads would show here
+    weights_x = 144 * N * K // 256 + 2 * M * K
+    assert weights_x <= rec["dram_bytes_read"] <= 1.02 * weights_x
+    assert re.fullmatch(r"[0-9a-f]{16}", rec["kernel_hash"])
+    assert "--clock-control none" in rec["source"]
