@@ -16,11 +16,11 @@
  * prefill went from 42 to 208 tok/s", section "The fix: K-parallel batched
  * DMMV"): same weights, same operand rounding and the same error bound, bf16
  * activations converted inside the kernel, and G * 8 KiB + ceil(N/128) * 4
- * bytes of pool scratch (G <= 2 CTAs per SM) for the tiles its CTAs share.
+ * bytes of pool scratch (G <= 3 CTAs per SM) for the tiles its CTAs share.
  * Results are deterministic (shared tiles are summed in a fixed order).  By
  * default (QWP_DECODE_AUTO) it takes such products only where it measured
- * faster than the prefill kernel on GB300: M == 1 and N >= 65536; see
- * qwp_set_decode_policy.
+ * faster than the prefill kernel on GB300: N >= 65536 and M <= 2 (Q4_K, Q6_K)
+ * or M == 1 (W4A16); see qwp_set_decode_policy.
  * Every entry point returns QWP_OK (0) or a negative qwp_status; none throws.
  * Calls are thread-safe.
  *
@@ -261,8 +261,9 @@ QWP_API int qwp_device_status(void *stream);
 
 /*
  * Which decode-shaped products (see the top of this file) the GEMM entry points
- * run on the decode kernel, process-wide: QWP_DECODE_AUTO (the default: M == 1
- * and N >= 65536, where it measured faster), QWP_DECODE_NEVER (always the
+ * run on the decode kernel, process-wide: QWP_DECODE_AUTO (the default: N >=
+ * 65536 and M <= 2 for Q4_K and Q6_K, M == 1 for W4A16, where it measured
+ * faster), QWP_DECODE_NEVER (always the
  * prefill kernel) or QWP_DECODE_ALWAYS (every decode-shaped product).  Results
  * meet the same error bound either way.  Returns the previous policy (>= 0) or
  * QWP_ERR_INVALID_ARG.  Calls already issued keep the kernel they were given;
@@ -272,9 +273,10 @@ QWP_API int qwp_device_status(void *stream);
 enum qwp_decode_policy { QWP_DECODE_AUTO = 0, QWP_DECODE_NEVER = 1, QWP_DECODE_ALWAYS = 2 };
 QWP_API int qwp_set_decode_policy(int policy);
 
-/* 1 if a GEMM call of this shape would run the decode kernel under the current
- * policy, 0 if the prefill kernel (host-only; no device call). */
-QWP_API int qwp_decode_selected(int64_t M, int64_t N, int64_t K);
+/* 1 if a GEMM call of this weight format (0 W4A16, 1 Q4_K, 2 Q6_K) and shape
+ * would run the decode kernel under the current policy, 0 if the prefill kernel
+ * (host-only; no device call); QWP_ERR_INVALID_ARG for an unknown format. */
+QWP_API int qwp_decode_selected(int format, int64_t M, int64_t N, int64_t K);
 
 /*
  * The launch a GEMM call of this shape gets on the current device (host only:

@@ -80,7 +80,7 @@ def library() -> ctypes.CDLL:
         lib.w4a16_gemm_bf16.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p]
         lib.qwp_device_status.argtypes = [p]
         lib.qwp_set_decode_policy.argtypes = [ctypes.c_int]
-        lib.qwp_decode_selected.argtypes = [i64, i64, i64]
+        lib.qwp_decode_selected.argtypes = [ctypes.c_int, i64, i64, i64]
         lib.qwp_gemm_plan.argtypes = [ctypes.c_int, i64, i64, i64, p]
         for name in EXPORTED_SYMBOLS:
             if name != "qwp_status_string":
@@ -302,12 +302,16 @@ def set_decode_policy(policy: int) -> int:
     return rc
 
 
-def decode_selected(M: int, N: int, K: int) -> bool:
-    """Whether a GEMM call of this shape would run the decode kernel now."""
-    return bool(library().qwp_decode_selected(int(M), int(N), int(K)))
-
-
 _PLAN_FORMATS = {"w4a16": 0, "q4k": 1, "q6k": 2}
+
+
+def decode_selected(fmt: str, M: int, N: int, K: int) -> bool:
+    """Whether a GEMM call of this weight format ("q4k", "q6k", "w4a16") and shape
+    would run the decode kernel now."""
+    rc = library().qwp_decode_selected(_PLAN_FORMATS[fmt], int(M), int(N), int(K))
+    if rc < 0:
+        _check(rc, "qwp_decode_selected")
+    return bool(rc)
 
 
 def gemm_plan(fmt: str, M: int, N: int, K: int) -> dict:

@@ -692,11 +692,11 @@ static std::atomic<int> g_decode_policy{DECODE_POLICY_AUTO};
 
 int decode_policy() { return g_decode_policy.load(std::memory_order_relaxed); }
 
-bool decode_selected(int64_t M, int64_t N, int64_t K) {
+bool decode_selected(int fmt, int64_t M, int64_t N, int64_t K) {
     switch (decode_policy()) {
         case DECODE_POLICY_NEVER: return false;
         case DECODE_POLICY_ALWAYS: return decode_fits(M, N, K);
-        default: return decode_auto(M, N, K);
+        default: return decode_auto(fmt, M, N, K);
     }
 }
 
@@ -708,4 +708,7 @@ extern "C" int qwp_set_decode_policy(int policy) {
     return qwp::g_decode_policy.exchange(policy, std::memory_order_relaxed);
 }
 
-extern "C" int qwp_decode_selected(int64_t M, int64_t N, int64_t K) { return qwp::decode_selected(M, N, K) ? 1 : 0; }
+extern "C" int qwp_decode_selected(int format, int64_t M, int64_t N, int64_t K) {
+    if (format != qwp::DFMT_W4A16 && format != qwp::DFMT_Q4K && format != qwp::DFMT_Q6K) return QWP_ERR_INVALID_ARG;
+    return qwp::decode_selected(format, M, N, K) ? 1 : 0;
+}

@@ -32,19 +32,21 @@ enum : int { DECODE_POLICY_AUTO = 0, DECODE_POLICY_NEVER = 1, DECODE_POLICY_ALWA
 
 // The automatic choice, from both kernels timed on GB300 at 1 to 8 tokens (Q4_K,
 // Q6_K and W4A16, N from 2048 to 152064, K from 4096 to 12288): the decode kernel
-// is clearly faster only for vocabulary-sized matrices at one token (2% for Q4_K,
-// 7% for Q6_K at N = 152064); from N = 10240 to 24576 the two are within a few
-// percent either way, and the prefill kernel wins for narrower or K-heavy
-// matrices and from two or three tokens on.
-constexpr int64_t DECODE_AUTO_MAX_TOKENS = 1;
+// is clearly faster for vocabulary-sized matrices (N >= 65536) at one and two
+// tokens for Q4_K (5-8%) and Q6_K (4-7%), and at one token for W4A16 (a tie; two
+// tokens lose 4%); from N = 10240 to 24576 the two are within a few percent
+// either way, and the prefill kernel wins for narrower or K-heavy matrices and
+// from three tokens on.
 constexpr int64_t DECODE_AUTO_MIN_ROWS = 65536;
-inline bool decode_auto(int64_t M, int64_t N, int64_t K) {
-    return decode_fits(M, N, K) && M <= DECODE_AUTO_MAX_TOKENS && N >= DECODE_AUTO_MIN_ROWS;
+inline int64_t decode_auto_max_tokens(int fmt) { return fmt == DFMT_W4A16 ? 1 : 2; }
+inline bool decode_auto(int fmt, int64_t M, int64_t N, int64_t K) {
+    return decode_fits(M, N, K) && M <= decode_auto_max_tokens(fmt) && N >= DECODE_AUTO_MIN_ROWS;
 }
 
-// The current policy, and the choice it makes for an M x N x K product.
+// The current policy, and the choice it makes for an M x N x K product of
+// weight format fmt (DFMT_*).
 int decode_policy();
-bool decode_selected(int64_t M, int64_t N, int64_t K);
+bool decode_selected(int fmt, int64_t M, int64_t N, int64_t K);
 
 // Device scratch launch_decode needs for an N x K matrix of format `fmt` on the
 // current device (partial sums of tiles shared by two or more CTAs, and one

@@ -1194,7 +1194,7 @@ static int scratch_pool(cudaMemPool_t *out) {
 // Decode-shaped calls (at most 8 tokens, K a multiple of 256) go to the decode
 // kernel, which streams the same repacked weights without the tensor-memory
 // pipeline (and converts bf16 activations itself); its scratch comes from the pool.
-static bool decode_shaped(int64_t M, int64_t N, int64_t K) { return decode_selected(M, N, K); }
+static bool decode_shaped(int fmt, int64_t M, int64_t N, int64_t K) { return decode_selected(fmt, M, N, K); }
 
 static int run_decode(int fmt, const void *w, const void *scales, const uint8_t *zeros, const void *x, bool x_bf16,
                       float *y, int64_t M, int64_t N, int64_t K, int64_t group, cudaStream_t s) {
@@ -1219,7 +1219,7 @@ extern "C" int q4k_gemm_f16(const void *w_tiled, const void *x, float *y, int64_
     if (K % Q4K_BLOCK || K == 0) return K < 0 ? QWP_ERR_INVALID_ARG : QWP_ERR_UNSUPPORTED_SHAPE;
     int rc = gemm_shape_checks(w_tiled, x, y, M, N, K);
     if (rc || M == 0 || N == 0) return rc;
-    if (decode_shaped(M, N, K))
+    if (decode_shaped(DFMT_Q4K, M, N, K))
         return run_decode(DFMT_Q4K, w_tiled, nullptr, nullptr, x, false, y, M, N, K, 0,
                           static_cast<cudaStream_t>(stream));
     return launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0,
@@ -1233,7 +1233,7 @@ extern "C" int q4k_gemm(const void *w_tiled, const void *x, float *y, int64_t M,
     if (rc || M == 0 || N == 0) return rc;
     if ((rc = check_device())) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (decode_shaped(M, N, K)) return run_decode(DFMT_Q4K, w_tiled, nullptr, nullptr, x, true, y, M, N, K, 0, s);
+    if (decode_shaped(DFMT_Q4K, M, N, K)) return run_decode(DFMT_Q4K, w_tiled, nullptr, nullptr, x, true, y, M, N, K, 0, s);
     cudaMemPool_t pool;
     if ((rc = scratch_pool(&pool))) return rc;
     void *x16 = nullptr;
@@ -1252,7 +1252,7 @@ extern "C" int q6k_gemm_f16(const void *w_tiled, const void *x, float *y, int64_
     if (K % Q4K_BLOCK || K == 0) return K < 0 ? QWP_ERR_INVALID_ARG : QWP_ERR_UNSUPPORTED_SHAPE;
     int rc = gemm_shape_checks(w_tiled, x, y, M, N, K);
     if (rc || M == 0 || N == 0) return rc;
-    if (decode_shaped(M, N, K))
+    if (decode_shaped(DFMT_Q6K, M, N, K))
         return run_decode(DFMT_Q6K, w_tiled, nullptr, nullptr, x, false, y, M, N, K, 0,
                           static_cast<cudaStream_t>(stream));
     return launch_gemm<FMT_Q6K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0,
@@ -1266,7 +1266,7 @@ extern "C" int q6k_gemm(const void *w_tiled, const void *x, float *y, int64_t M,
     if (rc || M == 0 || N == 0) return rc;
     if ((rc = check_device())) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (decode_shaped(M, N, K)) return run_decode(DFMT_Q6K, w_tiled, nullptr, nullptr, x, true, y, M, N, K, 0, s);
+    if (decode_shaped(DFMT_Q6K, M, N, K)) return run_decode(DFMT_Q6K, w_tiled, nullptr, nullptr, x, true, y, M, N, K, 0, s);
     cudaMemPool_t pool;
     if ((rc = scratch_pool(&pool))) return rc;
     void *x16 = nullptr;
@@ -1288,7 +1288,7 @@ extern "C" int w4a16_gemm(const void *wq_tiled, const void *scales, const uint8_
     int rc = gemm_shape_checks(wq_tiled, x, y, M, N, K);
     if (rc || M == 0 || N == 0) return rc;
     if (!scales) return QWP_ERR_INVALID_ARG;
-    if (decode_shaped(M, N, K))
+    if (decode_shaped(DFMT_W4A16, M, N, K))
         return run_decode(DFMT_W4A16, wq_tiled, scales, zeros, x, false, y, M, N, K, group,
                           static_cast<cudaStream_t>(stream));
     return launch_gemm<FMT_W4A16>(wq_tiled, scales, zeros, x, y, M, N, K, group,
@@ -1305,7 +1305,7 @@ extern "C" int w4a16_gemm_bf16(const void *wq_tiled, const void *scales, const u
     if (!scales) return QWP_ERR_INVALID_ARG;
     if ((rc = check_device())) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (decode_shaped(M, N, K)) return run_decode(DFMT_W4A16, wq_tiled, scales, zeros, x, true, y, M, N, K, group, s);
+    if (decode_shaped(DFMT_W4A16, M, N, K)) return run_decode(DFMT_W4A16, wq_tiled, scales, zeros, x, true, y, M, N, K, group, s);
     cudaMemPool_t pool;
     if ((rc = scratch_pool(&pool))) return rc;
     void *x16 = nullptr;
@@ -1325,7 +1325,7 @@ extern "C" int qwp_gemm_plan(int format, int64_t M, int64_t N, int64_t K, int32_
     if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30)) return QWP_ERR_UNSUPPORTED_SHAPE;
     if (K % (format == FMT_W4A16 ? CHUNK_K : Q4K_BLOCK)) return QWP_ERR_UNSUPPORTED_SHAPE;
     for (int i = 0; i < 6; ++i) plan_out[i] = 0;
-    if (decode_shaped(M, N, K)) {
+    if (decode_shaped(format, M, N, K)) {
         plan_out[0] = 2;
         return QWP_OK;
     }

@@ -69,7 +69,7 @@ extern "C" int q4k_gemm_noalloc(const void *w_tiled, const void *x, float *y, in
     if ((rc = scratch_address(&x16, &dec))) return rc;
     // Decode-shaped calls: the decode kernel converts x itself and keeps its
     // partial sums in the fixed decode array.
-    if (decode_selected(M, N, K))
+    if (decode_selected(DFMT_Q4K, M, N, K))
         return launch_decode(DFMT_Q4K, w_tiled, nullptr, nullptr, x, true, y, M, N, K, 0, dec, kDecodeScratchBytes,
                              static_cast<cudaStream_t>(stream));
     // The conversion writes all M*K elements the GEMM reads, so nothing left

@@ -51,10 +51,10 @@ def _items(N, K):
 
 def test_decode_shapes_take_the_decode_path():
     assert all(1 <= M <= 8 and K % 256 == 0 and _items(N, K) >= 600 for M, N, K in SHAPES)
-    assert all(qwp.decode_selected(M, N, K) for M, N, K in SHAPES)
+    assert all(qwp.decode_selected("q4k", M, N, K) for M, N, K in SHAPES)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 65600, 512), (1, 66000, 768)])
+@pytest.mark.parametrize("M,N,K", [(1, 65600, 512), (1, 66000, 768), (2, 65600, 512)])
 def test_default_policy_both_kernels(M, N, K):
     """Under the default policy these shapes take the decode kernel; forced onto the
     prefill kernel they give results within the same bound."""
@@ -64,7 +64,7 @@ def test_default_policy_both_kernels(M, N, K):
     ref, mag = oracle.q4k_gemm(blocks, xb, N, K)
     for policy, decode in [(qwp.DECODE_AUTO, True), (qwp.DECODE_NEVER, False)]:
         qwp.set_decode_policy(policy)
-        assert qwp.decode_selected(M, N, K) == decode
+        assert qwp.decode_selected("q4k", M, N, K) == decode
         y = qwp.q4k_gemm(w, _bf16(xb), N).cpu().numpy()
         check_bound(y, ref, mag, f"policy {policy} M{M} N{N} K{K}")
 

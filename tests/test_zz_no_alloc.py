@@ -97,7 +97,7 @@ def test_noalloc_decode_shaped(policy, M, N, K):
     decode kernel forced (seven tokens)."""
     prev = qwp.set_decode_policy(policy)
     try:
-        assert qwp.decode_selected(M, N, K)
+        assert qwp.decode_selected("q4k", M, N, K)
         blocks = synth.q4k_weights(N, K, seed=906 + M)
         w = qwp.q4k_repack(torch.from_numpy(blocks.reshape(-1)).to(DEV), N, K)
         for call, seed in enumerate((907, 908)):
