@@ -66,13 +66,22 @@ def kernel_source_files() -> list:
     return [os.path.relpath(p, ROOT) for p in seen]
 
 
+def strip_c_comments(text: str) -> str:
+    """C/C++ source without its comments and with whitespace runs collapsed (string
+    and character literals kept as they are)."""
+    out = re.sub(r'"(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\'|//[^\n]*|/\*.*?\*/',
+                 lambda m: m.group(0) if m.group(0)[0] in "\"'" else " ", text, flags=re.S)
+    return re.sub(r"\s+", " ", out).strip()
+
+
 def kernel_source_hash() -> str:
-    """Hash of kernel_source_files(): a DRAM-traffic record stays valid while it holds."""
+    """Hash of kernel_source_files() with comments and layout ignored: a DRAM-traffic
+    record stays valid while the code it was captured from is unchanged."""
     h = hashlib.sha256()
     for rel in kernel_source_files():
-        with open(os.path.join(ROOT, rel), "rb") as fh:
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as fh:
             h.update(rel.encode())
-            h.update(fh.read())
+            h.update(strip_c_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -44,3 +44,11 @@ def test_traffic_record_is_consistent():
     assert weights_x <= rec["dram_bytes_read"] <= 1.02 * weights_x
     assert re.fullmatch(r"[0-9a-f]{16}", rec["kernel_hash"])
     assert "--clock-control none" in rec["source"]
+
+
+def test_kernel_hash_ignores_comments_only():
+    b = _bench()
+    code = 'int f(int a) { return a + 1; }  // one\n/* two */ const char *s = "x // y";\n'
+    assert b.strip_c_comments(code) == b.strip_c_comments("/* other */ " + code.replace("// one", "// three"))
+    assert b.strip_c_comments(code) != b.strip_c_comments(code.replace("a + 1", "a + 2"))
+    assert b.strip_c_comments(code) != b.strip_c_comments(code.replace('"x // y"', '"x // z"'))
