@@ -69,6 +69,32 @@ def test_default_policy_both_kernels(M, N, K):
         check_bound(y, ref, mag, f"policy {policy} M{M} N{N} K{K}")
 
 
+@pytest.mark.parametrize("fmt,M,decode", [("q6k", 1, True), ("q6k", 2, True), ("w4a16", 1, True),
+                                           ("w4a16", 2, False)])
+def test_default_policy_per_format(fmt, M, decode):
+    """The default choice per weight format on a wide matrix (N = 65600, K = 512):
+    Q6_K takes the decode kernel at one and two tokens, W4A16 at one token only;
+    under either kernel (default, then forced onto the prefill kernel) the result
+    meets the bound against the oracle."""
+    N, K, g = 65600, 512, 128
+    xb = synth.activations_bf16(M, K, seed=M + 17)
+    if fmt == "q6k":
+        blocks = synth.q6k_weights(N, K, seed=M * 59 + N)
+        w = qwp.q6k_repack(torch.from_numpy(blocks.reshape(-1)).to(DEV), N, K)
+        ref, mag = oracle.q6k_gemm(blocks, xb, N, K)
+        run = lambda: qwp.q6k_gemm(w, _bf16(xb), N)
+    else:
+        wq, s, z = synth.w4a16_weights(N, K, g, seed=M * 61 + N)
+        wt = qwp.w4a16_repack(torch.from_numpy(wq.view(np.int32)).to(DEV))
+        sd, zd = torch.from_numpy(s).to(DEV), torch.from_numpy(z).to(DEV)
+        ref, mag = oracle.w4a16_gemm_bf16(wq, s, z, xb, N, K, g)
+        run = lambda: qwp.w4a16_gemm_bf16(wt, sd, zd, _bf16(xb), N, g)
+    for policy, expect in [(qwp.DECODE_AUTO, decode), (qwp.DECODE_NEVER, False)]:
+        qwp.set_decode_policy(policy)
+        assert qwp.decode_selected(fmt, M, N, K) == expect
+        check_bound(run().cpu().numpy(), ref, mag, f"{fmt} policy {policy} M{M} N{N} K{K}")
+
+
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_decode_q4k_bf16(M, N, K):
     blocks = synth.q4k_weights(N, K, seed=M * 31 + N)
