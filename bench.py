@@ -312,92 +312,158 @@ def parse_gemm(spec):
     raise ValueError(f"bad --gemm spec {spec!r}: q4k:M:N:K, q6k:M:N:K or w4a16:M:N:K:group[:sym][:bf16]")
 
 
-def run_gemms(args, specs):
-    """One JSON line per GEMM shape: graph replays of the library call (Q4_K: bf16 x,
-    conversion included; W4A16: fp16 x, or bf16 x with ':bf16', no zero points with
-    ':sym'), one call per weight copy in the graph, the copies together larger than
-    2x L2, CUDA events around the timed replays."""
+def time_gemm(spec, steps, warmup, dev):
+    """Time one GEMM shape: graph replays of the library call (Q4_K, Q6_K: bf16 x;
+    W4A16: fp16 x, or bf16 x with ':bf16', no zero points with ':sym'), one call per
+    input copy in the graph (weights and x both rotate; the copies together are
+    larger than 2.5x L2, so every call streams its inputs from HBM), CUDA events on
+    the launching stream around the timed replays.  Returns the JSON record."""
     import torch
 
     import quantized_weight_prefill_gb300 as qwp
     import synth
 
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
     hbm, tc_burst, _, peak_kind = measured_peaks()
-    for spec in specs:
-        kind, M, N, K, g, flags = parse_gemm(spec)
-        if kind in ("q4k", "q6k"):
-            wbytes = N * K // 256 * (144 if kind == "q4k" else 210)
+    kind, M, N, K, g, flags = parse_gemm(spec)
+    if kind in ("q4k", "q6k"):
+        wbytes = N * K // 256 * (144 if kind == "q4k" else 210)
+    else:
+        wbytes = N * K // 2 + (N * K // g) * (2 if "sym" in flags else 3)
+    xbytes = 2 * M * K
+    copies = max(2, min(64, int(np.ceil(2.5 * l2 / (wbytes + xbytes)))))
+    ws, xs = [], []
+    bf16_x = kind in ("q4k", "q6k") or "bf16" in flags
+    for c in range(copies):
+        if kind == "q4k":
+            blocks = synth.q4k_weights(N, K, seed=100 + c)
+            ws.append((qwp.q4k_repack(torch.from_numpy(blocks.reshape(-1)).to(dev), N, K),))
+        elif kind == "q6k":
+            blocks = synth.q6k_weights(N, K, seed=100 + c)
+            ws.append((qwp.q6k_repack(torch.from_numpy(blocks.reshape(-1)).to(dev), N, K),))
         else:
-            wbytes = N * K // 2 + (N * K // g) * (2 if "sym" in flags else 3)
-        copies = max(2, min(64, int(np.ceil(2.5 * l2 / wbytes))))
-        ws = []
+            wq, sc, z = synth.w4a16_weights(N, K, g, seed=100 + c)
+            ws.append((qwp.w4a16_repack(torch.from_numpy(wq.view(np.int32)).to(dev)),
+                       torch.from_numpy(sc).to(dev), None if "sym" in flags else torch.from_numpy(z).to(dev)))
+        if bf16_x:
+            xs.append(torch.from_numpy(synth.activations_bf16(M, K, seed=7 + c).view(np.int16)).to(dev)
+                      .view(torch.bfloat16))
+        else:
+            xs.append(torch.from_numpy(synth.activations_f16(M, K, seed=7 + c)).to(dev))
+    y = torch.empty(M, N, dtype=torch.float32, device=dev)
+
+    def call(c):
+        if kind == "q4k":
+            qwp.q4k_gemm(ws[c][0], xs[c], N, out=y)
+        elif kind == "q6k":
+            qwp.q6k_gemm(ws[c][0], xs[c], N, out=y)
+        else:
+            gemm = qwp.w4a16_gemm_bf16 if "bf16" in flags else qwp.w4a16_gemm
+            gemm(ws[c][0], ws[c][1], ws[c][2], xs[c], N, g, out=y)
+
+    for s in range(warmup):
+        call(s % copies)
+    torch.cuda.synchronize()
+    # One graph holds a call per input copy, back to back, so that the host's
+    # graph-launch rate does not pace short GEMMs; it is replayed until at least
+    # `steps` calls have run.
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
         for c in range(copies):
-            if kind == "q4k":
-                blocks = synth.q4k_weights(N, K, seed=100 + c)
-                ws.append((qwp.q4k_repack(torch.from_numpy(blocks.reshape(-1)).to(dev), N, K),))
-            elif kind == "q6k":
-                blocks = synth.q6k_weights(N, K, seed=100 + c)
-                ws.append((qwp.q6k_repack(torch.from_numpy(blocks.reshape(-1)).to(dev), N, K),))
-            else:
-                wq, sc, z = synth.w4a16_weights(N, K, g, seed=100 + c)
-                ws.append((qwp.w4a16_repack(torch.from_numpy(wq.view(np.int32)).to(dev)),
-                           torch.from_numpy(sc).to(dev), None if "sym" in flags else torch.from_numpy(z).to(dev)))
-        if kind in ("q4k", "q6k") or "bf16" in flags:
-            x = torch.from_numpy(synth.activations_bf16(M, K, seed=7).view(np.int16)).to(dev).view(torch.bfloat16)
-        else:
-            x = torch.from_numpy(synth.activations_f16(M, K, seed=7)).to(dev)
-        y = torch.empty(M, N, dtype=torch.float32, device=dev)
-
-        def call(c):
-            if kind == "q4k":
-                qwp.q4k_gemm(ws[c][0], x, N, out=y)
-            elif kind == "q6k":
-                qwp.q6k_gemm(ws[c][0], x, N, out=y)
-            else:
-                gemm = qwp.w4a16_gemm_bf16 if "bf16" in flags else qwp.w4a16_gemm
-                gemm(ws[c][0], ws[c][1], ws[c][2], x, N, g, out=y)
-
-        for s in range(args.warmup):
-            call(s % copies)
-        torch.cuda.synchronize()
-        # One graph holds a call per weight copy, back to back, so that the host's
-        # graph-launch rate does not pace short GEMMs; it is replayed until at least
-        # `steps` calls have run.
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr):
-            for c in range(copies):
-                call(c)
+            call(c)
+    gr.replay()
+    torch.cuda.synchronize()
+    reps = max(1, -(-steps // copies))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
         gr.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if qwp.device_status() != 0:
+        raise RuntimeError(f"kernel timeout in {spec}")
+    t = e0.elapsed_time(e1) * 1e-3 / (reps * copies)
+    flops = 2.0 * M * N * K
+    byts = wbytes + xbytes + 4.0 * M * N
+    t_tc, t_hbm = flops / (tc_burst * 1e12), byts / (hbm * 1e9)
+    plan = qwp.gemm_plan(kind if kind != "w4a16" else "w4a16", M, N, K)
+    rec = {
+        "gemm": spec, "us": t * 1e6, "tflops": flops / t / 1e12,
+        "pct_bf16_peak": 100.0 * flops / t / 1e12 / tc_burst,
+        "gbs": byts / t / 1e9, "bound": "tensor" if t_tc >= t_hbm else "hbm",
+        "roofline_us": max(t_tc, t_hbm) * 1e6, "roofline_frac": max(t_tc, t_hbm) / t,
+        "peak_source": peak_kind, "calls_timed": reps * copies, "input_copies": copies,
+        "launches_per_call": 2 if bf16_x and plan.get("kernel") == "prefill" else 1,
+        "plan": plan,
+    }
+    del ws, xs, gr
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_gemms(args, specs):
+    """One JSON line per GEMM shape (see time_gemm)."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    for spec in specs:
+        print(json.dumps(time_gemm(spec, args.steps, args.warmup, dev)), flush=True)
+    return 0
+
+
+# The north-star targets, timed inside the default run: the M>=2048 tensor-core
+# target on the largest projection, and the two HBM-bound targets (M<=32, skinny N).
+TARGETS = (("gate_up_m2048", "q4k:2048:24576:4096", "tensor >= 0.60 of bf16 dense peak"),
+           ("q4k_m32_n2048_k2048", "q4k:32:2048:2048", "HBM roofline >= 0.70"),
+           ("skinny_n32_m4096_k4096", "q4k:4096:32:4096", "HBM roofline >= 0.70"))
+
+# Load-time repacks timed on their own: the layer's four Q4_K projections and the
+# two W4A16 shapes.
+REPACKS = (("q4k", "qkv", 4096, 6144), ("q4k", "o", 4096, 4096), ("q4k", "gate_up", 4096, 24576),
+           ("q4k", "down", 12288, 4096), ("w4a16", "w4a16_4096x12288", 4096, 12288),
+           ("w4a16", "w4a16_12288x4096", 12288, 4096))
+
+
+def time_repacks(dev, reps=20):
+    """Each load-time repack alone: CUDA events around `reps` back-to-back repacks of
+    one matrix (inputs of tens of MB: the first repack reads from HBM, later ones may
+    partly hit L2; the figure is the mean).  Bytes = packed bytes read + written."""
+    import torch
+
+    import quantized_weight_prefill_gb300 as qwp
+    import synth
+
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for fmt, name, K, N in REPACKS:
+        if fmt == "q4k":
+            src = torch.from_numpy(synth.q4k_weights(N, K, seed=300).reshape(-1)).to(dev)
+            nbytes = src.numel()
+            fn = lambda: qwp.q4k_repack(src, N, K)  # noqa: E731
+        else:
+            wq, _, _ = synth.w4a16_weights(N, K, 128, seed=300)
+            src = torch.from_numpy(wq.view(np.int32)).to(dev)
+            nbytes = src.numel() * 4
+            fn = lambda: qwp.w4a16_repack(src)  # noqa: E731
+        for _ in range(3):
+            fn()
         torch.cuda.synchronize()
-        reps = max(1, -(-args.steps // copies))
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(reps):
-            gr.replay()
+            fn()
         e1.record(stream)
         torch.cuda.synchronize()
-        if qwp.device_status() != 0:
-            raise RuntimeError(f"kernel timeout in {spec}")
-        t = e0.elapsed_time(e1) * 1e-3 / (reps * copies)
-        flops = 2.0 * M * N * K
-        xbytes = 2.0 * M * K
-        byts = wbytes + xbytes + 4.0 * M * N
-        t_roof = max(flops / (tc_burst * 1e12), byts / (hbm * 1e9))
-        print(json.dumps({
-            "gemm": spec, "us": t * 1e6, "tflops": flops / t / 1e12,
-            "pct_bf16_peak": 100.0 * flops / t / 1e12 / tc_burst,
-            "gbs": byts / t / 1e9, "bound": "tensor" if flops / (tc_burst * 1e12) >= byts / (hbm * 1e9) else "hbm",
-            "roofline_frac": t_roof / t, "peak_source": peak_kind, "calls_timed": reps * copies,
-            "weight_copies": copies, "launches_per_call": 2 if kind in ("q4k", "q6k") or "bf16" in flags else 1,
-        }), flush=True)
-        del ws, gr
-        torch.cuda.empty_cache()
-    return 0
+        ms = e0.elapsed_time(e1) / reps
+        out[name] = {"format": fmt, "N": N, "K": K, "bytes": nbytes, "ms": ms,
+                     "gbs": 2.0 * nbytes / (ms * 1e-3) / 1e9}
+        del src
+    torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------------------- GPU leg
@@ -602,6 +668,16 @@ def run_gpu(args):
     if rank != 0:
         return 0
 
+    # The benchmark spec's target shapes and the load-time repacks, each timed on its own
+    # after the layer (rank 0).
+    targets = {}
+    if not args.no_targets:
+        for name, spec, goal in TARGETS:
+            rec = time_gemm(spec, 200, args.warmup, dev)
+            rec["target"] = goal
+            targets[name] = rec
+    repack = time_repacks(dev)
+
     hbm, tc_burst, tc_sust, peak_kind = measured_peaks()
     ms_step = ms_total / args.steps
     value = world * M * args.steps / (ms_total * 1e-3)
@@ -634,7 +710,7 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "fp16 operands (bf16 input), fp32 accumulate",
         "data": "synthetic",
         "config": {
             "workload": layer_workload(),
@@ -655,6 +731,8 @@ def run_gpu(args):
             "ms_per_launch": dom_ms,
             "launch_timing": "CUDA events recorded inside the layer graphs around the dominant GEMM (conversion included), second timed pass after the steps",
         },
+        "targets": targets,
+        "repack": repack,
         "cpu_baseline": cpu,
         "e2e": {"value": world * M * e2e_steps / (e2e_ms * 1e-3), "unit": "tok/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -679,6 +757,7 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=REF_BUDGET_S,
                     help="reference arm: host seconds that warm-up and steps together aim at")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-targets", action="store_true", help="skip the per-GEMM target shapes after the layer")
     ap.add_argument("--gemm", action="append", default=[],
                     help="time single GEMMs instead of the layer: q4k:M:N:K, q6k:M:N:K or w4a16:M:N:K:group[:sym][:bf16]")
     ap.add_argument("--sweep", action="store_true", help="time every GEMM shape of the workloads")

@@ -23,7 +23,9 @@
  * faster than the prefill kernel on GB300: N >= 65536 and M <= 2 (Q4_K, Q6_K)
  * or M == 1 (W4A16); see qwp_set_decode_policy.
  * Every entry point returns QWP_OK (0) or a negative qwp_status; none throws.
- * Calls are thread-safe.
+ * Calls are thread-safe, with one exception: q4k_gemm_noalloc keeps its scratch
+ * in fixed arrays that all its calls on a device share, so its calls must not
+ * overlap on the GPU (see there).
  *
  * The method (web pages, by title and section):
  *  - "The dequant scratch round-trip is ZINC's last RDNA4 prefill tax",
@@ -66,7 +68,7 @@ typedef enum {
     QWP_ERR_DEVICE = -5,           /* the current device is not an sm_103 GPU            */
     QWP_ERR_TIMEOUT = -6,          /* a kernel's bounded wait expired (qwp_device_status) */
     QWP_ERR_RANGE = -7,            /* an activation overflowed fp16 (qwp_device_status)   */
-    QWP_ERR_SCRATCH_LIMIT = -8     /* M*K beyond QWP_NOALLOC_MAX_X_ELEMS (q4k_gemm_noalloc) */
+    QWP_ERR_SCRATCH_LIMIT = -8     /* q4k_gemm_noalloc: M*K beyond QWP_NOALLOC_MAX_X_ELEMS */
 } qwp_status;
 
 /* Human-readable name of a status code (static string). */
@@ -102,10 +104,13 @@ QWP_API int q4k_dequant(const void *w_tiled_dev, float *w_out_dev, int64_t N, in
 
 /*
  * y_dev[M][N] (fp32) = x_dev[M][K] (fp16) . W^T, W the repacked Q4_K matrix.
- * Each weight is unpacked on chip to an fp16 tensor-core operand: q*sc exactly
- * (from the 0x6400|n form of the nibble), then d*(q*sc) - RN(dmin*m) rounded
- * once to fp16 (requires |d|*sc*15 < 65504, true of any practical block);
- * fp32 accumulation in tensor memory.  K % 256 == 0; M, N >= 0 (M == 0 or
+ * Each weight is unpacked on chip to an fp16 tensor-core operand that is the
+ * fp16 rounding of the exact weight d*sc*q - dmin*m: q*sc exactly (from the
+ * 0x6400|n form of the nibble), d*(q*sc) - dmin*m in fp32 with an exact product
+ * and an exact dmin*m, then one rounding to fp16 (relative error at most
+ * 2^-11 * (1 + 2^-13); weights in fp16's subnormal range are exact, since every
+ * weight is a multiple of 2^-24; requires |w| <= 65504, true of any practical
+ * block); fp32 accumulation in tensor memory.  K % 256 == 0; M, N >= 0 (M == 0 or
  * N == 0 is a no-op); x_dev, w_tiled_dev and y_dev 16-byte aligned; x rows
  * contiguous (row stride K).  Allocates nothing, except the decode kernel's
  * scratch for decode-shaped calls.
@@ -142,7 +147,11 @@ QWP_API int q4k_gemm(const void *w_tiled_dev, const void *x_dev, float *y_dev,
  * and that every GPU loading the library's device code holds until the process
  * exits.  M*K beyond that size returns QWP_ERR_SCRATCH_LIMIT before any work.
  * Decode-shaped calls keep their partial sums in a second fixed array (4 MiB)
- * instead and read x directly (no fp16 copy).
+ * instead and read x directly (no fp16 copy); a decode-shaped call whose
+ * partial sums would not fit there (G * 8 KiB + ceil(N/128) * 4 bytes above
+ * 4 MiB, i.e. N beyond about 16 million rows) runs the prefill kernel through
+ * the first array instead, so QWP_ERR_SCRATCH_LIMIT means M*K above the limit
+ * and nothing else.
  * The first call on each device looks up the array's address on that device
  * (and loads the library's device code there if it is not loaded yet); make
  * that first call before any stream capture begins.  Every call on a device
@@ -191,10 +200,11 @@ QWP_API int q6k_dequant(const void *w_tiled_dev, float *w_out_dev, int64_t N, in
 
 /*
  * y_dev[M][N] (fp32) = x_dev[M][K] (fp16) . W^T, W the repacked Q6_K matrix.
- * Each weight is unpacked on chip to an fp16 tensor-core operand: (q - 32)
- * exactly, times RN(d*scale) rounded once more to fp16 (two fp16 roundings,
- * relative error at most 2^-10 for normal results); fp32 accumulation in
- * tensor memory.  Same shape, alignment and no-allocation rules as q4k_gemm_f16.
+ * Each weight is unpacked on chip to an fp16 tensor-core operand that is the
+ * fp16 rounding of the exact weight d*scale*(q - 32): d*(q - 32) exactly in
+ * fp32, times the scale exactly (at most 24 significant bits), then one
+ * rounding to fp16 (relative error at most 2^-11; subnormal weights exact);
+ * fp32 accumulation in tensor memory.  Same shape, alignment and no-allocation rules as q4k_gemm_f16.
  */
 QWP_API int q6k_gemm_f16(const void *w_tiled_dev, const void *x_dev, float *y_dev,
                          int64_t M, int64_t N, int64_t K, void *stream);

@@ -181,7 +181,7 @@ struct DecSub {
     uint4 wv;
     Q4kSubH ks;        // Q4_K
     uint2 hv;          // Q6_K high words of the two 16-wide halves
-    __half2 ds0, ds1;  // Q6_K RN(d * scale) of the halves
+    Q6kSub ds0, ds1;   // Q6_K constants of the halves
     __half2 s2, mz;    // W4A16 scale, 1024 + zero point
 
     template <int kWin>
@@ -190,20 +190,13 @@ struct DecSub {
         wv = *reinterpret_cast<const uint4 *>(wst + w + kWin * wstride);
         if (kFmt == DFMT_Q4K) {
             const uint4 h = *reinterpret_cast<const uint4 *>(wst + hdr);
-            const __half2 scm = __hsub2(as_half2(q4k_scmin_lane<kWin>(h, sh)), as_half2(0x64006400u));
-            ks.sc2 = __low2half2(scm);
-            ks.csc2 = __hmul2(ks.sc2, as_half2(0xE400E400u));     // x (-1024)
-            ks.sc16_2 = __hmul2(ks.sc2, as_half2(0x2C002C00u));   // x (1/16)
-            ks.csc16_2 = __hmul2(ks.sc2, as_half2(0xD400D400u));  // x (-64)
-            ks.d2 = as_half2(__byte_perm(h.x, 0u, 0x1010));
-            ks.nml2 = __hmul2(__high2half2(scm), as_half2(__byte_perm(h.x, 0u, 0x3232) ^ 0x80008000u));
+            ks = q4k_sub_consts(h.x, __hsub2(as_half2(q4k_scmin_lane<kWin>(h, sh)), as_half2(0x64006400u)));
         } else if (kFmt == DFMT_Q6K) {
             const uint32_t dbits = *reinterpret_cast<const uint16_t *>(wst + hdr);
             const uint32_t sc2 = *reinterpret_cast<const uint16_t *>(wst + sc + 8 * kWin);
             hv = *reinterpret_cast<const uint2 *>(wst + hi + kWin * hstride);
-            const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
-            ds0 = __float2half2_rn(d * static_cast<float>(static_cast<int8_t>(sc2 & 0xFFu)));
-            ds1 = __float2half2_rn(d * static_cast<float>(static_cast<int8_t>(sc2 >> 8)));
+            ds0 = q6k_sub(dbits, static_cast<int8_t>(sc2 & 0xFFu));
+            ds1 = q6k_sub(dbits, static_cast<int8_t>(sc2 >> 8));
         } else {
             const int64_t gi = n * args.groups_per_row + gidx;
             s2 = __half2half2(args.scales[gi]);

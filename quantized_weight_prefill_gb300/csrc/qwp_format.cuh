@@ -172,44 +172,66 @@ __device__ __forceinline__ void q4k_word_f32(uint32_t word, float dl, float ml, 
     }
 }
 
-// Per-sub-block fp16 constants of the GEMM's unpack.
+// Per-sub-block constants of the GEMM's unpack.
 struct Q4kSubH {
-    __half2 sc2;     // (sc, sc)
-    __half2 csc2;    // (-1024*sc, -1024*sc), exact
-    __half2 sc16_2;  // (sc/16, sc/16), exact
-    __half2 csc16_2; // (-64*sc, -64*sc), exact
-    __half2 d2;      // (d, d)
-    __half2 nml2;    // (-RN(dmin*m), -RN(dmin*m))
+    __half2 sc2;      // (sc, sc)
+    __half2 csc2;     // (-1024*sc, -1024*sc), exact
+    __half2 sc16_2;   // (sc/16, sc/16), exact
+    __half2 csc16_2;  // (-64*sc, -64*sc), exact
+    unsigned short d; // fp16 bits of d
+    float nml;        // -(dmin*m), exact in fp32 (at most 17 significant bits)
 };
 
-__device__ __forceinline__ Q4kSubH q4k_sub_f16(uint4 h, int j) {
+// The constants of one sub-block from the block's first header word (fp16 d in
+// bits 0-15, fp16 dmin in bits 16-31) and its exact (sc, m) pair.
+__device__ __forceinline__ Q4kSubH q4k_sub_consts(uint32_t hx, __half2 scm) {
     Q4kSubH k;
-    const __half2 scm = q4k_scmin(h, j);
     k.sc2 = __low2half2(scm);
     k.csc2 = __hmul2(k.sc2, as_half2(0xE400E400u));     // x (-1024)
     k.sc16_2 = __hmul2(k.sc2, as_half2(0x2C002C00u));   // x (1/16)
     k.csc16_2 = __hmul2(k.sc2, as_half2(0xD400D400u));  // x (-64)
-    k.d2 = as_half2(__byte_perm(h.x, 0u, 0x1010));
-    const __half2 ndmin2 = as_half2(__byte_perm(h.x, 0u, 0x3232) ^ 0x80008000u);
-    k.nml2 = __hmul2(__high2half2(scm), ndmin2);
+    k.d = static_cast<unsigned short>(hx & 0xFFFFu);
+    k.nml = -(__half2float(__ushort_as_half(static_cast<unsigned short>(hx >> 16))) * __high2float(scm));
     return k;
 }
 
-// The 8 weights of one word as fp16x2 MMA operands.  (1024+q)*sc - 1024*sc is
-// q*sc exactly (at most 945, inside fp16's 11-bit integer range; the fma does not
-// round its product), and d*(q*sc) - RN(dmin*m) is rounded once to fp16.  Pairs 1
-// and 3 are read in place from bits 4..7 of each half, as 1024 + 16q, which saves
-// their shifts: (1024+16q)*(sc/16) - 64*sc is the same exact q*sc.
+__device__ __forceinline__ Q4kSubH q4k_sub_f16(uint4 h, int j) { return q4k_sub_consts(h.x, q4k_scmin(h, j)); }
+
+// Both halves of an exact fp16 pair (a0, a1) through a*b + c, each with the
+// product formed exactly and the sum rounded once to fp32 (the mixed-precision
+// fma of sm_100 and later), then packed into fp16x2 with one more rounding.
+__device__ __forceinline__ uint32_t fma_pair_f16_f32_f16(uint32_t a, unsigned short b, float c) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 a0, a1;\n\t.reg .f32 lo, hi;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\t"
+        "fma.rn.f32.f16 lo, a0, %2, %3;\n\t"
+        "fma.rn.f32.f16 hi, a1, %2, %3;\n\t"
+        "cvt.rn.f16x2.f32 %0, hi, lo;\n\t}"
+        : "=r"(r)
+        : "r"(a), "h"(b), "f"(c));
+    return r;
+}
+
+// The 8 weights of one word as fp16x2 MMA operands, each the fp16 rounding of the
+// exact d*sc*q - dmin*m.  (1024+q)*sc - 1024*sc is q*sc exactly (at most 945,
+// inside fp16's 11-bit integer range; the fp16 fma does not round its product).
+// Then d*(q*sc) - dmin*m is formed in fp32: the product (at most 21 significant
+// bits) is exact inside the fma and dmin*m is exact, so one fp32 rounding at most
+// (none unless the two terms are more than 24 bits apart), then one rounding to
+// fp16: the operand's relative error is at most 2^-11 * (1 + 2^-13), and since the
+// exact weight is a multiple of 2^-24, weights in fp16's subnormal range are exact.
+// Pairs 1 and 3 are read in place from bits 4..7 of each half, as 1024 + 16q,
+// which saves their shifts: (1024+16q)*(sc/16) - 64*sc is the same exact q*sc.
 __device__ __forceinline__ void q4k_word_f16x2(uint32_t word, const Q4kSubH &k, uint32_t (&p)[4]) {
     const uint32_t w8 = word >> 8;
     const __half2 q0 = __hfma2(as_half2((word & 0x000F000Fu) | 0x64006400u), k.sc2, k.csc2);
     const __half2 q1 = __hfma2(as_half2((word & 0x00F000F0u) | 0x64006400u), k.sc16_2, k.csc16_2);
     const __half2 q2 = __hfma2(as_half2((w8 & 0x000F000Fu) | 0x64006400u), k.sc2, k.csc2);
     const __half2 q3 = __hfma2(as_half2((w8 & 0x00F000F0u) | 0x64006400u), k.sc16_2, k.csc16_2);
-    p[0] = as_u32(__hfma2(q0, k.d2, k.nml2));
-    p[1] = as_u32(__hfma2(q1, k.d2, k.nml2));
-    p[2] = as_u32(__hfma2(q2, k.d2, k.nml2));
-    p[3] = as_u32(__hfma2(q3, k.d2, k.nml2));
+    p[0] = fma_pair_f16_f32_f16(as_u32(q0), k.d, k.nml);
+    p[1] = fma_pair_f16_f32_f16(as_u32(q1), k.d, k.nml);
+    p[2] = fma_pair_f16_f32_f16(as_u32(q2), k.d, k.nml);
+    p[3] = fma_pair_f16_f32_f16(as_u32(q3), k.d, k.nml);
 }
 
 // ---------------------------------------------------------------- Q6_K unpack
@@ -228,22 +250,50 @@ __device__ __forceinline__ __half2 q6k_centered(uint32_t magic) {
     return __hsub2(as_half2(magic), as_half2(0x64206420u));
 }
 
-// The 8 weights of low word `lo` as fp16x2 MMA operands RN(RN(d*sc) * (q - 32)).
-template <int kSet>
-__device__ __forceinline__ void q6k_word_f16x2(uint32_t lo, uint32_t hi, __half2 ds2, uint32_t (&p)[4]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) p[i] = as_u32(__hmul2(q6k_centered(q6k_pair_magic<kSet>(lo, hi, i)), ds2));
+// Per-16-weight constants of the Q6_K unpack: fp16 d, -1056*d (exact in fp32) and
+// the int8 scale as fp32.
+struct Q6kSub {
+    unsigned short d;
+    float nd1056;
+    float sc;
+};
+
+__device__ __forceinline__ Q6kSub q6k_sub(uint32_t dbits, int sc) {
+    Q6kSub k;
+    k.d = static_cast<unsigned short>(dbits & 0xFFFFu);
+    k.nd1056 = -1056.f * __half2float(__ushort_as_half(k.d));
+    k.sc = static_cast<float>(sc);
+    return k;
 }
 
-// RN(d * sc_u) for the four sub-blocks u of one 64-wide chunk, as fp16x2 (d is the
-// block's fp16 bits, sc4 its four int8 scales).  d * sc is exact in fp32.
-__device__ __forceinline__ void q6k_chunk_scales(uint32_t dbits, uint32_t sc4, __half2 (&ds)[4]) {
-    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
+// The 8 weights of low word `lo` as fp16x2 MMA operands, each the fp16 rounding of
+// the exact d*sc*(q - 32): (1024+q)*d - 1056*d is d*(q - 32) exactly in fp32 (the
+// mixed-precision fma forms the product exactly; the result has at most 17
+// significant bits), times sc exactly (at most 24 bits), then one rounding to fp16.
+template <int kSet>
+__device__ __forceinline__ void q6k_word_f16x2(uint32_t lo, uint32_t hi, const Q6kSub &k, uint32_t (&p)[4]) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int sc = static_cast<int8_t>(static_cast<uint8_t>(sc4 >> (8 * u)));
-        ds[u] = __float2half2_rn(d * static_cast<float>(sc));
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t m = q6k_pair_magic<kSet>(lo, hi, i);
+        uint32_t r;
+        asm("{\n\t.reg .b16 a0, a1;\n\t.reg .f32 lo, hi;\n\t"
+            "mov.b32 {a0, a1}, %1;\n\t"
+            "fma.rn.f32.f16 lo, a0, %2, %3;\n\t"
+            "fma.rn.f32.f16 hi, a1, %2, %3;\n\t"
+            "mul.rn.f32 lo, lo, %4;\n\t"
+            "mul.rn.f32 hi, hi, %4;\n\t"
+            "cvt.rn.f16x2.f32 %0, hi, lo;\n\t}"
+            : "=r"(r)
+            : "r"(m), "h"(k.d), "f"(k.nd1056), "f"(k.sc));
+        p[i] = r;
     }
+}
+
+// The constants of the four 16-weight scale groups u of one 64-wide chunk (d is the
+// block's fp16 bits, sc4 its four int8 scales).
+__device__ __forceinline__ void q6k_chunk_scales(uint32_t dbits, uint32_t sc4, Q6kSub (&ks)[4]) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ks[u] = q6k_sub(dbits, static_cast<int8_t>(static_cast<uint8_t>(sc4 >> (8 * u))));
 }
 
 // ---------------------------------------------------------------- W4A16 unpack

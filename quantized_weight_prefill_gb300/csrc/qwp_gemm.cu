@@ -209,19 +209,19 @@ __device__ __forceinline__ void unpack_quarter(uint4 wv, const Q4kSubH &ks, __ha
 
 // Q6_K: low words 4q..4q+3 of a chunk (wv) with their high words h0 (sub-block
 // 2q) and h1 (sub-block 2q+1) into regs[off .. off+15].
-__device__ __forceinline__ void unpack_q6k_quarter(uint4 wv, uint32_t h0, uint32_t h1, __half2 ds0, __half2 ds1,
-                                                   uint32_t (&regs)[32], int off) {
+__device__ __forceinline__ void unpack_q6k_quarter(uint4 wv, uint32_t h0, uint32_t h1, const Q6kSub &k0,
+                                                   const Q6kSub &k1, uint32_t (&regs)[32], int off) {
     uint32_t p[4];
-    q6k_word_f16x2<0>(wv.x, h0, ds0, p);
+    q6k_word_f16x2<0>(wv.x, h0, k0, p);
 #pragma unroll
     for (int e = 0; e < 4; ++e) regs[off + e] = p[e];
-    q6k_word_f16x2<1>(wv.y, h0, ds0, p);
+    q6k_word_f16x2<1>(wv.y, h0, k0, p);
 #pragma unroll
     for (int e = 0; e < 4; ++e) regs[off + 4 + e] = p[e];
-    q6k_word_f16x2<0>(wv.z, h1, ds1, p);
+    q6k_word_f16x2<0>(wv.z, h1, k1, p);
 #pragma unroll
     for (int e = 0; e < 4; ++e) regs[off + 8 + e] = p[e];
-    q6k_word_f16x2<1>(wv.w, h1, ds1, p);
+    q6k_word_f16x2<1>(wv.w, h1, k1, p);
 #pragma unroll
     for (int e = 0; e < 4; ++e) regs[off + 12 + e] = p[e];
 }
@@ -491,9 +491,9 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
             Q4kSubH k0, k1;
             __half2 s2 = __float2half2_rn(0.f), mz = w4_magic_zero(0);
             uint4 hv = make_uint4(0, 0, 0, 0);  // Q6_K: high-bit words of this block
-            __half2 ds[4];                      // Q6_K: RN(d*sc) of its four sub-blocks
+            Q6kSub ds[4];                       // Q6_K: constants of its four 16-weight scale groups
             if (kQ6K)
-                for (int u = 0; u < 4; ++u) ds[u] = __float2half2_rn(0.f);
+                for (int u = 0; u < 4; ++u) ds[u] = q6k_sub(0u, 0);
             if (has_block) {
                 if (kQ6K) {
                     if (valid) {
@@ -1152,6 +1152,11 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
         return QWP_ERR_CUDA;
     }
     return QWP_OK;
+}
+
+int launch_q4k_prefill(const void *w, const void *x16, float *y, int64_t M, int64_t N, int64_t K,
+                       cudaStream_t stream, bool after_prior) {
+    return launch_gemm<FMT_Q4K>(w, nullptr, nullptr, x16, y, M, N, K, 0, stream, kDefaultTimeoutNs, after_prior);
 }
 
 }  // namespace qwp

@@ -30,6 +30,12 @@ constexpr uint32_t kStatusRangeBit = 0x10000u;
 // `stream`; the launch allows a programmatic dependent launch to follow.
 int launch_bf16_to_f16(const void *x, void *out, int64_t n, cudaStream_t stream);
 
+// The prefill (tcgen05) kernel on fp16 x for a Q4_K product, whatever the decode
+// policy says (x, w, y checked by the caller).  after_prior: launched with
+// programmatic stream serialization behind the grid just before it on `stream`.
+int launch_q4k_prefill(const void *w, const void *x16, float *y, int64_t M, int64_t N, int64_t K,
+                       cudaStream_t stream, bool after_prior);
+
 // Default bound on any single mbarrier wait inside a kernel.
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 

@@ -68,12 +68,15 @@ extern "C" int q4k_gemm_noalloc(const void *w_tiled, const void *x, float *y, in
     void *x16 = nullptr, *dec = nullptr;
     if ((rc = scratch_address(&x16, &dec))) return rc;
     // Decode-shaped calls: the decode kernel converts x itself and keeps its
-    // partial sums in the fixed decode array.
-    if (decode_selected(DFMT_Q4K, M, N, K))
+    // partial sums in the fixed decode array, when they fit there (for very wide
+    // matrices they may not: those run the prefill kernel below instead, whose
+    // fp16 copy of x always fits once M*K has passed the check above).
+    const size_t dec_need = decode_selected(DFMT_Q4K, M, N, K) ? decode_scratch_bytes(DFMT_Q4K, N, K) : 0;
+    if (dec_need && dec_need <= kDecodeScratchBytes)
         return launch_decode(DFMT_Q4K, w_tiled, nullptr, nullptr, x, true, y, M, N, K, 0, dec, kDecodeScratchBytes,
                              static_cast<cudaStream_t>(stream));
     // The conversion writes all M*K elements the GEMM reads, so nothing left
     // in the array by an earlier call is ever read.
     if ((rc = launch_bf16_to_f16(x, x16, M * K, static_cast<cudaStream_t>(stream)))) return rc;
-    return q4k_gemm_f16(w_tiled, x16, y, M, N, K, stream);
+    return launch_q4k_prefill(w_tiled, x16, y, M, N, K, static_cast<cudaStream_t>(stream), true);
 }

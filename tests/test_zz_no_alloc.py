@@ -1,11 +1,12 @@
 """q4k_gemm_noalloc (the Q4_K GEMM whose activation scratch is a fixed array in
-the library) against q4k_gemm (pool scratch), through the C ABI.
+the library) against the CPU oracle and against q4k_gemm (pool scratch), through
+the C ABI.
 
-Two calls in a row with different activations and token counts must each match
-q4k_gemm within the GEMM tolerance, so a stale copy of x left in the array by
-the first call cannot pass; M*K at the limit runs, one token row beyond it is
-rejected before any work.  Collected last so that it also runs after every other
-test in the same process.
+Two calls in a row with different activations and token counts must each meet
+the GEMM tolerance against the oracle and against q4k_gemm, so a stale copy of x
+left in the array by the first call cannot pass; M*K at the limit runs, one
+token row beyond it is rejected before any work.  Collected last so that it also
+runs after every other test in the same process.
 """
 import ctypes
 
@@ -24,13 +25,6 @@ SCRATCH_LIMIT = -8
 
 def _bf16_on_gpu(xb):
     return torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).to(DEV).view(torch.bfloat16)
-
-
-def _magnitude(blocks, xb, N, K):
-    """sum_k |x[m,k] * w[n,k]| from the oracle's dequantized weights (the tolerance's scale)."""
-    w = oracle.q4k_dequant(blocks.reshape(N, -1), N, K)
-    x = oracle.bf16_to_f64(xb).reshape(-1, K)
-    return np.abs(x) @ np.abs(w).T
 
 
 def test_noalloc_rejects_beyond_the_limit_before_any_cuda_call():
@@ -57,8 +51,10 @@ def test_noalloc_matches_q4k_gemm_on_two_calls_in_a_row():
         qwp.q4k_gemm_noalloc(w, x, N, out=y)
         torch.cuda.synchronize()
         assert qwp.device_status() == 0
-        check_bound(y.cpu().numpy(), y_ref.cpu().numpy().astype(np.float64), _magnitude(blocks, xb, N, K),
-                    f"q4k_gemm_noalloc call {call + 1} (M={M})")
+        ref, mag = oracle.q4k_gemm(blocks, xb, N, K)
+        check_bound(y.cpu().numpy(), ref, mag, f"q4k_gemm_noalloc call {call + 1} (M={M}) against the oracle")
+        check_bound(y.cpu().numpy(), y_ref.cpu().numpy().astype(np.float64), mag,
+                    f"q4k_gemm_noalloc call {call + 1} (M={M}) against q4k_gemm")
 
 
 @pytest.mark.gpu
@@ -75,8 +71,10 @@ def test_noalloc_at_the_limit_and_one_row_beyond():
     torch.cuda.synchronize()
     assert qwp.device_status() == 0
     rows = np.r_[0:16, M - 16:M]
-    check_bound(y[rows].cpu().numpy(), y_ref[rows].cpu().numpy().astype(np.float64),
-                _magnitude(blocks, xb[rows], N, K), "q4k_gemm_noalloc at M*K = limit")
+    ref, mag = oracle.q4k_gemm(blocks, xb[rows], N, K)
+    check_bound(y[rows].cpu().numpy(), ref, mag, "q4k_gemm_noalloc at M*K = limit, against the oracle")
+    check_bound(y[rows].cpu().numpy(), y_ref[rows].cpu().numpy().astype(np.float64), mag,
+                "q4k_gemm_noalloc at M*K = limit, against q4k_gemm")
     assert torch.isfinite(y).all()
 
     x_big = torch.zeros(M + 1, K, dtype=torch.bfloat16, device=DEV)
