@@ -303,6 +303,19 @@ QWP_API int qwp_decode_selected(int format, int64_t M, int64_t N, int64_t K);
  */
 QWP_API int qwp_gemm_plan(int format, int64_t M, int64_t N, int64_t K, int32_t *plan_out);
 
+/*
+ * The bound on each wait of the prefill kernel's main loop (ns, process-wide,
+ * for calls launched afterwards; default 2 s; kept in SM clock cycles at 2.1
+ * per ns, so it lasts longer at SM clocks below 2.1 GHz): a wait that runs out
+ * records QWP_ERR_TIMEOUT for qwp_device_status, the kernel's CTAs wait (with
+ * the default bound) for their own copies and MMAs in flight, meet their
+ * cluster peers at a cluster barrier, release their tensor memory and exit;
+ * later launches skip their work until the status is read.  A short bound makes
+ * that path run on purpose (a test hook).  0 or more than 60 s:
+ * QWP_ERR_INVALID_ARG.
+ */
+QWP_API int qwp_set_wait_timeout_ns(uint64_t ns);
+
 #ifdef __cplusplus
 }
 #endif

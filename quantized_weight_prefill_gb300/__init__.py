@@ -22,7 +22,7 @@ __all__ = [
     "q6k_repacked_bytes", "q6k_repack", "q6k_dequant", "q6k_gemm", "q6k_gemm_f16",
     "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_bf16",
     "device_status", "set_decode_policy", "decode_selected", "DECODE_AUTO", "DECODE_NEVER", "DECODE_ALWAYS",
-    "gemm_plan",
+    "gemm_plan", "set_wait_timeout_ns", "DEFAULT_WAIT_TIMEOUT_NS",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -32,6 +32,7 @@ EXPORTED_SYMBOLS = (
     "q4k_gemm_noalloc", "q6k_repacked_bytes", "q6k_repack", "q6k_dequant", "q6k_gemm", "q6k_gemm_f16",
     "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_bf16",
     "qwp_device_status", "qwp_set_decode_policy", "qwp_decode_selected", "qwp_gemm_plan",
+    "qwp_set_wait_timeout_ns",
 )
 
 # Decode-kernel dispatch policies (enum qwp_decode_policy in the header).
@@ -82,6 +83,7 @@ def library() -> ctypes.CDLL:
         lib.qwp_set_decode_policy.argtypes = [ctypes.c_int]
         lib.qwp_decode_selected.argtypes = [ctypes.c_int, i64, i64, i64]
         lib.qwp_gemm_plan.argtypes = [ctypes.c_int, i64, i64, i64, p]
+        lib.qwp_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
         for name in EXPORTED_SYMBOLS:
             if name != "qwp_status_string":
                 getattr(lib, name).restype = ctypes.c_int
@@ -324,3 +326,12 @@ def gemm_plan(fmt: str, M: int, N: int, K: int) -> dict:
     return {"kernel": {1: "prefill", 2: "decode"}[out[0]], "splits": out[1], "clusters": out[2],
             "token_tile": out[3], "units": out[4], "units_per_cluster": out[5]}
 
+
+# The prefill kernel's default bound on a main-loop wait (qwp_set_wait_timeout_ns).
+DEFAULT_WAIT_TIMEOUT_NS = 2_000_000_000
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    """Set the bound on the prefill kernel's main-loop waits (process-wide); calls
+    launched afterwards use it."""
+    _check(library().qwp_set_wait_timeout_ns(int(ns)), "qwp_set_wait_timeout_ns")

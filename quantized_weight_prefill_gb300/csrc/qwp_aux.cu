@@ -253,8 +253,10 @@ __global__ void w4_dequant_kernel(const uint8_t *__restrict__ w, const __half *_
 // that would round to infinity set the range flag in the status word.  Lets the
 // dependent GEMM launch start (programmatic dependent launch) right away.
 __global__ void bf16_to_f16_kernel(const uint4 *__restrict__ in, uint4 *__restrict__ out, int64_t n8,
-                                   uint32_t *status) {
+                                   uint32_t *status, uint32_t *zero, int nzero) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0u;
     bool overflow = false;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -273,15 +275,19 @@ __global__ void bf16_to_f16_kernel(const uint4 *__restrict__ in, uint4 *__restri
     if (overflow) atomicOr(status, kStatusRangeBit);
 }
 
-int launch_bf16_to_f16(const void *x, void *out, int64_t n, cudaStream_t stream) {
+int launch_bf16_to_f16(const void *x, void *out, int64_t n, cudaStream_t stream, uint32_t *zero, int nzero) {
     uint32_t *status = status_word();
     if (!status) return QWP_ERR_CUDA;
     const int64_t n8 = n / 8;
     const int64_t blocks = std::min<int64_t>((n8 + 255) / 256, 152 * 8);
     bf16_to_f16_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, stream>>>(
-        static_cast<const uint4 *>(x), static_cast<uint4 *>(out), n8, status);
+        static_cast<const uint4 *>(x), static_cast<uint4 *>(out), n8, status, zero, zero ? nzero : 0);
     return launch_status();
 }
+
+static std::atomic<uint64_t> g_wait_timeout_ns{kDefaultTimeoutNs};
+
+uint64_t wait_timeout_ns() { return g_wait_timeout_ns.load(std::memory_order_relaxed); }
 
 static unsigned grid_for(int64_t threads, int block) {
     return static_cast<unsigned>((threads + block - 1) / block);
@@ -411,6 +417,12 @@ extern "C" int w4a16_dequant(const void *wq_tiled, const void *scales, const uin
         static_cast<const uint8_t *>(wq_tiled), static_cast<const __half *>(scales), zeros, w_out, N,
         K, group);
     return launch_status();
+}
+
+extern "C" int qwp_set_wait_timeout_ns(uint64_t ns) {
+    if (ns == 0 || ns > 60000000000ull) return QWP_ERR_INVALID_ARG;
+    g_wait_timeout_ns.store(ns, std::memory_order_relaxed);
+    return QWP_OK;
 }
 
 extern "C" int qwp_device_status(void *stream) {

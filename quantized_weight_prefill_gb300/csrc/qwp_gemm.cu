@@ -112,7 +112,8 @@ struct GemmArgs {
     int acc_bufs;           // 2 when two accumulators fit (bn <= 128), else 1
     int part_off;           // shared-memory offset of the split-K partial buffer
     int part_overlay;       // 1: one unit per CTA, the partial buffer overlays the idle rings
-    uint64_t timeout_ns;
+    uint64_t timeout_cycles;  // bound on a main-loop wait, in SM clock cycles
+    uint64_t drain_cycles;    // bound on a wait for the CTA's own work in flight
 };
 
 // Status codes recorded on a timeout: which wait gave up.
@@ -124,14 +125,19 @@ enum : uint32_t {
 struct Ctl {
     uint32_t *abort;  // shared-memory flag
     uint32_t *status;
-    uint64_t timeout_ns;
+    uint64_t timeout_cycles;  // main-loop waits
+    uint64_t drain_cycles;    // waits for the CTA's own work in flight
 };
 
 // Bounded wait on phase `parity` of `bar`.  False if it timed out or the CTA is
 // aborting (this CTA or, through the status word, any other); a timeout
 // records `where` in the status word.  The loop mostly sits in try_wait (which
-// suspends the thread in hardware); the clock and the global status word are
-// looked at only every 64 polls.
+// suspends the thread in hardware, often until the phase completes, so a wait
+// takes few polls).  The bound is kept in SM clock cycles (clock64, a cheap
+// register read, looked at after every unsuccessful poll); the global status
+// word is read every 64 polls.  Waits that do not honour an abort (a CTA
+// waiting for its own copies and MMAs in flight before it exits) always allow
+// the default bound.
 // kLazy waits sleep between polls (roles off the critical path, which should
 // not take issue slots from the warps that are on it).
 template <bool kCluster = false, bool kLazy = false>
@@ -139,21 +145,21 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
                                          uint32_t where, bool honour_abort = true) {
     auto poll = [&] { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
     if (poll()) return true;
-    const uint64_t t0 = global_timer_ns();
+    const uint64_t t0 = clock64();
+    const uint64_t limit = honour_abort ? ctl.timeout_cycles : ctl.drain_cycles;
     for (uint32_t it = 1;; ++it) {
         if (kLazy) __nanosleep(256);
         if (poll()) return true;
         if (honour_abort && *reinterpret_cast<volatile uint32_t *>(ctl.abort)) return false;
-        if ((it & 63u) == 0) {
-            if (honour_abort && (*reinterpret_cast<volatile uint32_t *>(ctl.status) & kStatusTimeoutMask)) {
-                *reinterpret_cast<volatile uint32_t *>(ctl.abort) = 1u;  // another CTA failed
-                return false;
-            }
-            if (global_timer_ns() - t0 > ctl.timeout_ns) {
-                *reinterpret_cast<volatile uint32_t *>(ctl.abort) = 1u;
-                atomicCAS(ctl.status, 0u, 0x100u | where);
-                return false;
-            }
+        if (static_cast<uint64_t>(clock64()) - t0 > limit) {
+            *reinterpret_cast<volatile uint32_t *>(ctl.abort) = 1u;
+            atomicCAS(ctl.status, 0u, 0x100u | where);
+            return false;
+        }
+        if ((it & 63u) == 0 && honour_abort &&
+            (*reinterpret_cast<volatile uint32_t *>(ctl.status) & kStatusTimeoutMask)) {
+            *reinterpret_cast<volatile uint32_t *>(ctl.abort) = 1u;  // another CTA failed
+            return false;
         }
     }
 }
@@ -281,7 +287,7 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
     const uint32_t acc_empty = acc_full + 16, part_full = acc_empty + 16, part_free = part_full + 8;
     const uint32_t part_last = part_free + 8, drain = part_last + 8, rings_idle = drain + 8;
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + OFF_MISC);  // [0] tmem base, [1] abort
-    const Ctl ctl{misc + 1, args.status, args.timeout_ns};
+    const Ctl ctl{misc + 1, args.status, args.timeout_cycles, args.drain_cycles};
 
     // Copy of weight stage s (K blocks kb_begin + 4s ..) of row tile `tile` into ring slot ws.
     auto load_weight_stage = [&](int tile, int s, int ws) {
@@ -351,6 +357,9 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
     // last unit is reduced between two cluster barriers instead.)
     const bool split_mbar = S > 1 && !args.part_overlay;
     if (split_mbar) cluster_arrive_relaxed();
+    // This thread has arrived on the cluster barrier above and not yet waited on it
+    // (the epilogue warps wait at their start, the others at the last unit).
+    bool cluster_wait_due = split_mbar && warp < FIRST_EPI_WARP;
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const bool skip = misc[1] != 0;
@@ -794,7 +803,8 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
             const int last_off = split_mbar ? 0 : args.part_off;  // this unit's partial buffer
             const uint32_t part = smem_u32(smem + last_off);
             if (split_mbar) {
-                if (warp < FIRST_EPI_WARP) cluster_wait();  // (the epilogue warps waited already)
+                if (cluster_wait_due) cluster_wait();  // (the epilogue warps waited already)
+                cluster_wait_due = false;
             } else {
                 cluster_sync();
             }
@@ -868,9 +878,19 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
             }
         }
     }
+    // With split-K, no CTA of the cluster leaves before every peer is done with
+    // its shared memory: on the normal path every remote write or arrival aimed
+    // at a CTA is one that a thread there waited for, but after a timeout those
+    // waits are skipped, so a full cluster barrier (release / acquire) closes
+    // every path.  Every thread of every CTA reaches it: all waits before it are
+    // bounded.
+    if (S > 1) {
+        __syncwarp();
+        if (cluster_wait_due) cluster_wait();
+        cluster_sync();
+    }
     // Every read of tensor memory (epilogue and transform warps) is done before it
-    // is released.  (Peers touch this CTA's shared memory no more by now: every
-    // remote write or arrival aimed at it is one that a thread here waited for.)
+    // is released.
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
@@ -1077,10 +1097,15 @@ static int plan_gemm(int64_t M, int64_t N, int64_t K, Plan &plan, int &bn, int64
 // x is fp16 [M, K].  `after_prior` launches with programmatic stream
 // serialization so the kernel's set-up and weight prefetch overlap the grid just
 // before it (the x producer waits for that grid with griddepcontrol.wait).
+// A wait bound in SM clock cycles: at 2.1 cycles per ns (above GB300's highest SM
+// clock, 2.07 GHz) a bound never ends sooner than its time in ns; at a lower
+// clock it lasts proportionally longer.
+static uint64_t ns_to_cycles(uint64_t ns) { return ns * 21 / 10 + 1; }
+
 template <int kFmt>
 static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, const void *x,
                        float *y, int64_t M, int64_t N, int64_t K, int64_t group, cudaStream_t stream,
-                       uint64_t timeout_ns, bool after_prior) {
+                       bool after_prior) {
     int rc = check_device();
     if (rc) return rc;
     uint32_t *status = status_word();
@@ -1110,7 +1135,8 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     for (int sh = 0; sh < 31; ++sh)
         if ((1 << sh) == a.kb_per_group) a.kbg_shift = sh;
     a.bn = bn;
-    a.timeout_ns = timeout_ns;
+    a.timeout_cycles = ns_to_cycles(wait_timeout_ns());
+    a.drain_cycles = ns_to_cycles(kDefaultTimeoutNs);
     a.cb_shift = plan.cbs;
     a.x_stage_bytes = (bn * 128) << plan.cbs;
     a.w_stage_bytes = weight_stage_bytes<kFmt>();
@@ -1154,9 +1180,12 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     return QWP_OK;
 }
 
-int launch_q4k_prefill(const void *w, const void *x16, float *y, int64_t M, int64_t N, int64_t K,
-                       cudaStream_t stream, bool after_prior) {
-    return launch_gemm<FMT_Q4K>(w, nullptr, nullptr, x16, y, M, N, K, 0, stream, kDefaultTimeoutNs, after_prior);
+int launch_q4k_prefill_fixed(const void *w, const void *x, void *x16, float *y, int64_t M, int64_t N, int64_t K,
+                             cudaStream_t stream) {
+    int rc = check_device();
+    if (rc) return rc;
+    if ((rc = launch_bf16_to_f16(x, x16, M * K, stream))) return rc;
+    return launch_gemm<FMT_Q4K>(w, nullptr, nullptr, x16, y, M, N, K, 0, stream, true);
 }
 
 }  // namespace qwp
@@ -1228,7 +1257,7 @@ extern "C" int q4k_gemm_f16(const void *w_tiled, const void *x, float *y, int64_
         return run_decode(DFMT_Q4K, w_tiled, nullptr, nullptr, x, false, y, M, N, K, 0,
                           static_cast<cudaStream_t>(stream));
     return launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0,
-                             static_cast<cudaStream_t>(stream), kDefaultTimeoutNs, false);
+                             static_cast<cudaStream_t>(stream), false);
 }
 
 extern "C" int q4k_gemm(const void *w_tiled, const void *x, float *y, int64_t M, int64_t N,
@@ -1247,7 +1276,7 @@ extern "C" int q4k_gemm(const void *w_tiled, const void *x, float *y, int64_t M,
         return QWP_ERR_CUDA;
     }
     rc = launch_bf16_to_f16(x, x16, M * K, s);
-    if (!rc) rc = launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x16, y, M, N, K, 0, s, kDefaultTimeoutNs, true);
+    if (!rc) rc = launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x16, y, M, N, K, 0, s, true);
     if (cudaFreeAsync(x16, s) != cudaSuccess && !rc) rc = QWP_ERR_CUDA;
     return rc;
 }
@@ -1261,7 +1290,7 @@ extern "C" int q6k_gemm_f16(const void *w_tiled, const void *x, float *y, int64_
         return run_decode(DFMT_Q6K, w_tiled, nullptr, nullptr, x, false, y, M, N, K, 0,
                           static_cast<cudaStream_t>(stream));
     return launch_gemm<FMT_Q6K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0,
-                                static_cast<cudaStream_t>(stream), kDefaultTimeoutNs, false);
+                                static_cast<cudaStream_t>(stream), false);
 }
 
 extern "C" int q6k_gemm(const void *w_tiled, const void *x, float *y, int64_t M, int64_t N,
@@ -1280,7 +1309,7 @@ extern "C" int q6k_gemm(const void *w_tiled, const void *x, float *y, int64_t M,
         return QWP_ERR_CUDA;
     }
     rc = launch_bf16_to_f16(x, x16, M * K, s);
-    if (!rc) rc = launch_gemm<FMT_Q6K>(w_tiled, nullptr, nullptr, x16, y, M, N, K, 0, s, kDefaultTimeoutNs, true);
+    if (!rc) rc = launch_gemm<FMT_Q6K>(w_tiled, nullptr, nullptr, x16, y, M, N, K, 0, s, true);
     if (cudaFreeAsync(x16, s) != cudaSuccess && !rc) rc = QWP_ERR_CUDA;
     return rc;
 }
@@ -1297,7 +1326,7 @@ extern "C" int w4a16_gemm(const void *wq_tiled, const void *scales, const uint8_
         return run_decode(DFMT_W4A16, wq_tiled, scales, zeros, x, false, y, M, N, K, group,
                           static_cast<cudaStream_t>(stream));
     return launch_gemm<FMT_W4A16>(wq_tiled, scales, zeros, x, y, M, N, K, group,
-                              static_cast<cudaStream_t>(stream), kDefaultTimeoutNs, false);
+                              static_cast<cudaStream_t>(stream), false);
 }
 
 extern "C" int w4a16_gemm_bf16(const void *wq_tiled, const void *scales, const uint8_t *zeros,
@@ -1319,7 +1348,7 @@ extern "C" int w4a16_gemm_bf16(const void *wq_tiled, const void *scales, const u
         return QWP_ERR_CUDA;
     }
     rc = launch_bf16_to_f16(x, x16, M * K, s);
-    if (!rc) rc = launch_gemm<FMT_W4A16>(wq_tiled, scales, zeros, x16, y, M, N, K, group, s, kDefaultTimeoutNs, true);
+    if (!rc) rc = launch_gemm<FMT_W4A16>(wq_tiled, scales, zeros, x16, y, M, N, K, group, s, true);
     if (cudaFreeAsync(x16, s) != cudaSuccess && !rc) rc = QWP_ERR_CUDA;
     return rc;
 }

@@ -27,16 +27,24 @@ constexpr uint32_t kStatusTimeoutMask = 0xFFFFu;
 constexpr uint32_t kStatusRangeBit = 0x10000u;
 
 // Converts n bf16 values (n % 8 == 0, both pointers 16-byte aligned) to fp16 on
-// `stream`; the launch allows a programmatic dependent launch to follow.
-int launch_bf16_to_f16(const void *x, void *out, int64_t n, cudaStream_t stream);
+// `stream`, and zeroes `nzero` 32-bit words at `zero` (may be null); the launch
+// allows a programmatic dependent launch to follow.
+int launch_bf16_to_f16(const void *x, void *out, int64_t n, cudaStream_t stream, uint32_t *zero = nullptr,
+                       int nzero = 0);
 
-// The prefill (tcgen05) kernel on fp16 x for a Q4_K product, whatever the decode
-// policy says (x, w, y checked by the caller).  after_prior: launched with
-// programmatic stream serialization behind the grid just before it on `stream`.
-int launch_q4k_prefill(const void *w, const void *x16, float *y, int64_t M, int64_t N, int64_t K,
-                       cudaStream_t stream, bool after_prior);
+// The prefill (tcgen05) kernel for a Q4_K product with bf16 x, whatever the decode
+// policy says, converting x into the caller's array x16 (M*K fp16 values) and
+// never splitting units between CTAs, so that it allocates nothing (x, w, y
+// checked by the caller).
+int launch_q4k_prefill_fixed(const void *w, const void *x, void *x16, float *y, int64_t M, int64_t N, int64_t K,
+                             cudaStream_t stream);
 
-// Default bound on any single mbarrier wait inside a kernel.
+// Default bound on any single mbarrier wait inside a kernel; the waits for a
+// CTA's own copies and MMAs in flight before it exits always use it.
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
+
+// The bound on the prefill kernel's main-loop waits (qwp_set_wait_timeout_ns;
+// kDefaultTimeoutNs unless changed).
+uint64_t wait_timeout_ns();
 
 }  // namespace qwp

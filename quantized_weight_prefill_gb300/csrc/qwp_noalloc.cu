@@ -76,7 +76,7 @@ extern "C" int q4k_gemm_noalloc(const void *w_tiled, const void *x, float *y, in
         return launch_decode(DFMT_Q4K, w_tiled, nullptr, nullptr, x, true, y, M, N, K, 0, dec, kDecodeScratchBytes,
                              static_cast<cudaStream_t>(stream));
     // The conversion writes all M*K elements the GEMM reads, so nothing left
-    // in the array by an earlier call is ever read.
-    if ((rc = launch_bf16_to_f16(x, x16, M * K, static_cast<cudaStream_t>(stream)))) return rc;
-    return launch_q4k_prefill(w_tiled, x16, y, M, N, K, static_cast<cudaStream_t>(stream), true);
+    // in the array by an earlier call is ever read; units are never split
+    // between CTAs here, so the GEMM needs no workspace.
+    return launch_q4k_prefill_fixed(w_tiled, x, x16, y, M, N, K, static_cast<cudaStream_t>(stream));
 }

@@ -160,3 +160,9 @@ def test_gemm_plan_argument_checks(lib):
     finally:
         qwp.set_decode_policy(prev)
 
+
+def test_wait_limit_argument_checks(lib):
+    """qwp_set_wait_timeout_ns is host-only: it rejects 0 and more than 60 s."""
+    assert lib.qwp_set_wait_timeout_ns(0) == INVALID
+    assert lib.qwp_set_wait_timeout_ns(61_000_000_000) == INVALID
+    assert lib.qwp_set_wait_timeout_ns(qwp.DEFAULT_WAIT_TIMEOUT_NS) == OK
