@@ -22,6 +22,16 @@
  * default (QWP_DECODE_AUTO) it takes such products only where it measured
  * faster than the prefill kernel on GB300: N >= 65536 and M <= 2 (Q4_K, Q6_K)
  * or M == 1 (W4A16); see qwp_set_decode_policy.
+ * Skinny-N calls.  A Q4_K product with at most 64 weight rows (N <= 64) and at
+ * least 256 tokens runs a third kernel ("Skinny bf16 GEMM prefill_gemm_skinny.cu",
+ * sparkinfer PR #511, Summary table): tokens are the tensor core's M side and
+ * the activations are its operand as they are (bf16 or fp16, never converted),
+ * K is split over a thread-block cluster and summed through distributed shared
+ * memory in a fixed order.  With fp16 x the weights are the same single-rounded
+ * fp16 operand as above; with bf16 x each weight is the pair hi = bf16(w32),
+ * lo = bf16(w32 - hi) of its fp32 value w32, both multiplied with x and summed
+ * in the accumulator (relative weight error at most 2^-18 + 2^-24, so no range
+ * limit on x and no QWP_ERR_RANGE).  It allocates nothing.
  * Every entry point returns QWP_OK (0) or a negative qwp_status; none throws.
  * Calls are thread-safe, with one exception: q4k_gemm_noalloc keeps its scratch
  * in fixed arrays that all its calls on a device share, so its calls must not
@@ -113,7 +123,8 @@ QWP_API int q4k_dequant(const void *w_tiled_dev, float *w_out_dev, int64_t N, in
  * block); fp32 accumulation in tensor memory.  K % 256 == 0; M, N >= 0 (M == 0 or
  * N == 0 is a no-op); x_dev, w_tiled_dev and y_dev 16-byte aligned; x rows
  * contiguous (row stride K).  Allocates nothing, except the decode kernel's
- * scratch for decode-shaped calls.
+ * scratch for decode-shaped calls.  Skinny-N calls (above) take the skinny-N
+ * kernel.
  */
 QWP_API int q4k_gemm_f16(const void *w_tiled_dev, const void *x_dev, float *y_dev,
                          int64_t M, int64_t N, int64_t K, void *stream);
@@ -125,7 +136,8 @@ QWP_API int q4k_gemm_f16(const void *w_tiled_dev, const void *x_dev, float *y_de
  * M*K*2 bytes of scratch taken from a library-owned, stream-ordered memory pool
  * on the current device and released in stream order after the GEMM; then
  * q4k_gemm_f16 runs, launched so that its set-up overlaps the conversion.
- * Same shape and alignment rules as q4k_gemm_f16.
+ * Skinny-N calls (above) take x as bf16 in the skinny-N kernel: no conversion,
+ * no scratch, no range limit.  Same shape and alignment rules as q4k_gemm_f16.
  */
 QWP_API int q4k_gemm(const void *w_tiled_dev, const void *x_dev, float *y_dev,
                      int64_t M, int64_t N, int64_t K, void *stream);
@@ -293,7 +305,9 @@ QWP_API int qwp_decode_selected(int format, int64_t M, int64_t N, int64_t K);
  * The launch a GEMM call of this shape gets on the current device (host only:
  * it reads the device's properties but launches nothing).  `format`: 0 W4A16,
  * 1 Q4_K, 2 Q6_K.  plan_out[6] receives: [0] the kernel (1 the prefill kernel,
- * 2 the decode kernel, which leaves [1..5] at 0); [1] the split-K factor S (the
+ * 2 the decode kernel, which leaves [1..5] at 0, 3 the skinny-N kernel, which
+ * reports its split and clusters (token tiles of 128) the same way and 1 unit
+ * per cluster); [1] the split-K factor S (the
  * cluster size); [2] the clusters launched; [3] the token tile (tokens per
  * unit); [4] the units (128-row tiles x token tiles); [5] the units per cluster
  * at most.  Returns QWP_OK, QWP_ERR_INVALID_ARG (NULL plan_out, a size below 1,

@@ -318,12 +318,13 @@ def decode_selected(fmt: str, M: int, N: int, K: int) -> bool:
 
 def gemm_plan(fmt: str, M: int, N: int, K: int) -> dict:
     """The launch a GEMM call of this shape gets on the current device: kernel
-    ("prefill" or "decode"), split-K factor, clusters, token tile, units and
-    units per cluster (the prefill kernel's; zero for the decode kernel)."""
+    ("prefill", "decode" or "skinny"), split-K factor, clusters, token tile, units
+    and units per cluster (zero for the decode kernel; the skinny-N kernel reports
+    its cluster size, token tiles, 128, token tiles and 1)."""
     out = (ctypes.c_int32 * 6)()
     _check(library().qwp_gemm_plan(_PLAN_FORMATS[fmt], int(M), int(N), int(K), ctypes.cast(out, ctypes.c_void_p)),
            "qwp_gemm_plan")
-    return {"kernel": {1: "prefill", 2: "decode"}[out[0]], "splits": out[1], "clusters": out[2],
+    return {"kernel": {1: "prefill", 2: "decode", 3: "skinny"}[out[0]], "splits": out[1], "clusters": out[2],
             "token_tile": out[3], "units": out[4], "units_per_cluster": out[5]}
 
 

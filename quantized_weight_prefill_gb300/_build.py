@@ -15,7 +15,7 @@ from concurrent.futures import ThreadPoolExecutor
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
-SOURCES = ["qwp_gemm.cu", "qwp_decode.cu", "qwp_aux.cu", "qwp_noalloc.cu"]
+SOURCES = ["qwp_gemm.cu", "qwp_decode.cu", "qwp_skinny.cu", "qwp_aux.cu", "qwp_noalloc.cu"]
 LIB = os.path.join(HERE, "libqwp.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden",

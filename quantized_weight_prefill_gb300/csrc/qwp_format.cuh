@@ -222,16 +222,52 @@ __device__ __forceinline__ uint32_t fma_pair_f16_f32_f16(uint32_t a, unsigned sh
 // exact weight is a multiple of 2^-24, weights in fp16's subnormal range are exact.
 // Pairs 1 and 3 are read in place from bits 4..7 of each half, as 1024 + 16q,
 // which saves their shifts: (1024+16q)*(sc/16) - 64*sc is the same exact q*sc.
-__device__ __forceinline__ void q4k_word_f16x2(uint32_t word, const Q4kSubH &k, uint32_t (&p)[4]) {
+// The exact q*sc of the 8 weights of one word as 4 fp16 pairs (K order).
+__device__ __forceinline__ void q4k_word_qsc(uint32_t word, const Q4kSubH &k, uint32_t (&q)[4]) {
     const uint32_t w8 = word >> 8;
-    const __half2 q0 = __hfma2(as_half2((word & 0x000F000Fu) | 0x64006400u), k.sc2, k.csc2);
-    const __half2 q1 = __hfma2(as_half2((word & 0x00F000F0u) | 0x64006400u), k.sc16_2, k.csc16_2);
-    const __half2 q2 = __hfma2(as_half2((w8 & 0x000F000Fu) | 0x64006400u), k.sc2, k.csc2);
-    const __half2 q3 = __hfma2(as_half2((w8 & 0x00F000F0u) | 0x64006400u), k.sc16_2, k.csc16_2);
-    p[0] = fma_pair_f16_f32_f16(as_u32(q0), k.d, k.nml);
-    p[1] = fma_pair_f16_f32_f16(as_u32(q1), k.d, k.nml);
-    p[2] = fma_pair_f16_f32_f16(as_u32(q2), k.d, k.nml);
-    p[3] = fma_pair_f16_f32_f16(as_u32(q3), k.d, k.nml);
+    q[0] = as_u32(__hfma2(as_half2((word & 0x000F000Fu) | 0x64006400u), k.sc2, k.csc2));
+    q[1] = as_u32(__hfma2(as_half2((word & 0x00F000F0u) | 0x64006400u), k.sc16_2, k.csc16_2));
+    q[2] = as_u32(__hfma2(as_half2((w8 & 0x000F000Fu) | 0x64006400u), k.sc2, k.csc2));
+    q[3] = as_u32(__hfma2(as_half2((w8 & 0x00F000F0u) | 0x64006400u), k.sc16_2, k.csc16_2));
+}
+
+__device__ __forceinline__ void q4k_word_f16x2(uint32_t word, const Q4kSubH &k, uint32_t (&p)[4]) {
+    uint32_t q[4];
+    q4k_word_qsc(word, k, q);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = fma_pair_f16_f32_f16(q[i], k.d, k.nml);
+}
+
+// The 8 weights of one word as pairs of bf16 operands whose sum carries about 16
+// significant bits: w32 = RN32(d*(q*sc) - dmin*m) as above (no rounding to
+// fp16), hi = RN_bf16(w32), lo = RN_bf16(w32 - hi) (the difference is exact in
+// fp32); |w - (hi + lo)| <= (2^-18 + 2^-24)|w|.  For a bf16 x tile, whose
+// values the tensor core then multiplies exactly.
+__device__ __forceinline__ void q4k_word_bf16_hilo(uint32_t word, const Q4kSubH &k, uint32_t (&hi)[4],
+                                                   uint32_t (&lo)[4]) {
+    uint32_t q[4];
+    q4k_word_qsc(word, k, q);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t h, l;
+        asm("{\n\t.reg .b16 a0, a1;\n\t.reg .f32 w0, w1, h0, h1;\n\t.reg .b32 hb;\n\t"
+            "mov.b32 {a0, a1}, %2;\n\t"
+            "fma.rn.f32.f16 w0, a0, %3, %4;\n\t"
+            "fma.rn.f32.f16 w1, a1, %3, %4;\n\t"
+            "cvt.rn.bf16x2.f32 hb, w1, w0;\n\t"
+            "shl.b32 %0, hb, 16;\n\t"
+            "mov.b32 h0, %0;\n\t"
+            "and.b32 %0, hb, 0xFFFF0000;\n\t"
+            "mov.b32 h1, %0;\n\t"
+            "sub.rn.f32 w0, w0, h0;\n\t"
+            "sub.rn.f32 w1, w1, h1;\n\t"
+            "cvt.rn.bf16x2.f32 %1, w1, w0;\n\t"
+            "mov.b32 %0, hb;\n\t}"
+            : "=&r"(h), "=r"(l)
+            : "r"(q[i]), "h"(k.d), "f"(k.nml));
+        hi[i] = h;
+        lo[i] = l;
+    }
 }
 
 // ---------------------------------------------------------------- Q6_K unpack

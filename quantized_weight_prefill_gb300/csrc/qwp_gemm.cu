@@ -50,6 +50,7 @@
 #include "qwp_format.cuh"
 #include "qwp_internal.h"
 #include "qwp_ptx.cuh"
+#include "qwp_sync.cuh"
 
 namespace qwp {
 
@@ -122,57 +123,6 @@ enum : uint32_t {
     WAIT_ACC_FULL, WAIT_DRAIN, WAIT_ACC_EMPTY, WAIT_PART
 };
 
-struct Ctl {
-    uint32_t *abort;  // shared-memory flag
-    uint32_t *status;
-    uint64_t timeout_cycles;  // main-loop waits
-    uint64_t drain_cycles;    // waits for the CTA's own work in flight
-};
-
-// Bounded wait on phase `parity` of `bar`.  False if it timed out or the CTA is
-// aborting (this CTA or, through the status word, any other); a timeout
-// records `where` in the status word.  The loop mostly sits in try_wait (which
-// suspends the thread in hardware, often until the phase completes, so a wait
-// takes few polls).  The bound is kept in SM clock cycles (clock64, a cheap
-// register read, looked at after every unsuccessful poll); the global status
-// word is read every 64 polls.  Waits that do not honour an abort (a CTA
-// waiting for its own copies and MMAs in flight before it exits) always allow
-// the default bound.
-// kLazy waits sleep between polls (roles off the critical path, which should
-// not take issue slots from the warps that are on it).
-template <bool kCluster = false, bool kLazy = false>
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl &ctl,
-                                         uint32_t where, bool honour_abort = true) {
-    auto poll = [&] { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-    if (poll()) return true;
-    const uint64_t t0 = clock64();
-    const uint64_t limit = honour_abort ? ctl.timeout_cycles : ctl.drain_cycles;
-    for (uint32_t it = 1;; ++it) {
-        if (kLazy) __nanosleep(256);
-        if (poll()) return true;
-        if (honour_abort && *reinterpret_cast<volatile uint32_t *>(ctl.abort)) return false;
-        if (static_cast<uint64_t>(clock64()) - t0 > limit) {
-            *reinterpret_cast<volatile uint32_t *>(ctl.abort) = 1u;
-            atomicCAS(ctl.status, 0u, 0x100u | where);
-            return false;
-        }
-        if ((it & 63u) == 0 && honour_abort &&
-            (*reinterpret_cast<volatile uint32_t *>(ctl.status) & kStatusTimeoutMask)) {
-            *reinterpret_cast<volatile uint32_t *>(ctl.abort) = 1u;  // another CTA failed
-            return false;
-        }
-    }
-}
-
-// A wait on a barrier that peers of the cluster arrive on (acquire at cluster
-// scope), by the epilogue warps (lazy).
-__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, const Ctl &ctl, uint32_t where) {
-    return wait_bar<true, true>(bar, parity, ctl, where);
-}
-
-__device__ __forceinline__ bool aborted(const Ctl &ctl) {
-    return *reinterpret_cast<volatile uint32_t *>(ctl.abort) != 0;
-}
 
 // One commit group: CB 64-wide K blocks of 4 MMAs (K = 16 each).  A block c sits at
 // tensor-memory column acol + 32c, its x tile at B-descriptor low word
@@ -879,12 +829,14 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
         }
     }
     // With split-K, no CTA of the cluster leaves before every peer is done with
-    // its shared memory: on the normal path every remote write or arrival aimed
-    // at a CTA is one that a thread there waited for, but after a timeout those
-    // waits are skipped, so a full cluster barrier (release / acquire) closes
-    // every path.  Every thread of every CTA reaches it: all waits before it are
-    // bounded.
-    if (S > 1) {
+    // its shared memory.  With one unit per CTA every thread passes two full
+    // cluster barriers on every path and the remote stores happen between them.
+    // With a partial buffer of its own, on the normal path every remote write or
+    // arrival aimed at a CTA is one that a thread there waited for, but after a
+    // timeout those waits are skipped, so a full cluster barrier (release /
+    // acquire) closes every path.  Every thread of every CTA reaches it: all
+    // waits before it are bounded.
+    if (split_mbar) {
         __syncwarp();
         if (cluster_wait_due) cluster_wait();
         cluster_sync();
@@ -1097,11 +1049,6 @@ static int plan_gemm(int64_t M, int64_t N, int64_t K, Plan &plan, int &bn, int64
 // x is fp16 [M, K].  `after_prior` launches with programmatic stream
 // serialization so the kernel's set-up and weight prefetch overlap the grid just
 // before it (the x producer waits for that grid with griddepcontrol.wait).
-// A wait bound in SM clock cycles: at 2.1 cycles per ns (above GB300's highest SM
-// clock, 2.07 GHz) a bound never ends sooner than its time in ns; at a lower
-// clock it lasts proportionally longer.
-static uint64_t ns_to_cycles(uint64_t ns) { return ns * 21 / 10 + 1; }
-
 template <int kFmt>
 static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, const void *x,
                        float *y, int64_t M, int64_t N, int64_t K, int64_t group, cudaStream_t stream,
@@ -1256,6 +1203,8 @@ extern "C" int q4k_gemm_f16(const void *w_tiled, const void *x, float *y, int64_
     if (decode_shaped(DFMT_Q4K, M, N, K))
         return run_decode(DFMT_Q4K, w_tiled, nullptr, nullptr, x, false, y, M, N, K, 0,
                           static_cast<cudaStream_t>(stream));
+    if (skinny_selected(DFMT_Q4K, M, N, K))
+        return launch_skinny(w_tiled, x, false, y, M, N, K, static_cast<cudaStream_t>(stream));
     return launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0,
                              static_cast<cudaStream_t>(stream), false);
 }
@@ -1268,6 +1217,7 @@ extern "C" int q4k_gemm(const void *w_tiled, const void *x, float *y, int64_t M,
     if ((rc = check_device())) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (decode_shaped(DFMT_Q4K, M, N, K)) return run_decode(DFMT_Q4K, w_tiled, nullptr, nullptr, x, true, y, M, N, K, 0, s);
+    if (skinny_selected(DFMT_Q4K, M, N, K)) return launch_skinny(w_tiled, x, true, y, M, N, K, s);
     cudaMemPool_t pool;
     if ((rc = scratch_pool(&pool))) return rc;
     void *x16 = nullptr;
@@ -1365,6 +1315,21 @@ extern "C" int qwp_gemm_plan(int format, int64_t M, int64_t N, int64_t K, int32_
     }
     int rc = check_device();
     if (rc) return rc;
+    if (skinny_selected(format, M, N, K)) {
+        int dev = 0, sms = 0, S = 1;
+        int64_t tiles = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return QWP_ERR_CUDA;
+        if ((rc = skinny_plan(M, K, sms, S, tiles))) return rc;
+        plan_out[0] = 3;
+        plan_out[1] = S;
+        plan_out[2] = static_cast<int32_t>(tiles);
+        plan_out[3] = 128;
+        plan_out[4] = static_cast<int32_t>(tiles);
+        plan_out[5] = 1;
+        return QWP_OK;
+    }
     Plan plan;
     int bn = 0;
     int64_t units = 0;

@@ -39,6 +39,16 @@ int launch_bf16_to_f16(const void *x, void *out, int64_t n, cudaStream_t stream,
 int launch_q4k_prefill_fixed(const void *w, const void *x, void *x16, float *y, int64_t M, int64_t N, int64_t K,
                              cudaStream_t stream);
 
+// The skinny-N kernel (qwp_skinny.cu): Q4_K products with at most 64 weight rows
+// and at least SKINNY_MIN_TOKENS tokens.  x is bf16 (converted in shared memory)
+// or fp16; allocates nothing.
+constexpr int64_t SKINNY_MIN_TOKENS = 256;
+bool skinny_selected(int fmt, int64_t M, int64_t N, int64_t K);
+// Its launch: `splits` CTAs per cluster along K, `tiles` token tiles of 128.
+int skinny_plan(int64_t M, int64_t K, int sms, int &splits, int64_t &tiles);
+int launch_skinny(const void *w, const void *x, bool x_bf16, float *y, int64_t M, int64_t N, int64_t K,
+                  cudaStream_t stream);
+
 // Default bound on any single mbarrier wait inside a kernel; the waits for a
 // CTA's own copies and MMAs in flight before it exits always use it.
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s

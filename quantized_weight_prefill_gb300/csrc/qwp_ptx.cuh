@@ -142,6 +142,36 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint3
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] . B[smem]^T, kind::f16 (fp32 accumulate), both operands
+// given by shared-memory matrix descriptors; whether D accumulates is fixed at
+// compile time.
+template <bool kAccumulate>
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "n"(kAccumulate ? 1 : 0)
+        : "memory");
+}
+
+// Shared-memory writes of this thread made by ordinary stores become visible to
+// the async proxy (tensor-core operand reads) once the writer has passed this.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 16 bytes from the shared memory of a CTA of the cluster (a shared::cluster
+// address from mapa).
+__device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // True in exactly one lane of the (converged) warp.  Issuing the MMAs under this
 // rather than under `lane == 0` measured 10-15% faster for the whole GEMM at small N.
 __device__ __forceinline__ bool elect_one() {
@@ -264,6 +294,13 @@ __device__ __forceinline__ void fence_acq_rel_cluster() {
 
 __device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// 16 bytes to the shared memory of a CTA of the cluster (16-byte aligned address).
+__device__ __forceinline__ void st_shared_cluster_f32x4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                                        uint32_t d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
 }
 
 }  // namespace qwp

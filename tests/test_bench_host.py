@@ -20,7 +20,7 @@ def test_kernel_source_files_follow_includes():
     csrc = "quantized_weight_prefill_gb300/csrc/"
     assert files[0] == csrc + "qwp_gemm.cu"
     assert set(files) == {csrc + "qwp_gemm.cu", csrc + "qwp_decode.h", csrc + "qwp_format.cuh",
-                          csrc + "qwp_internal.h", csrc + "qwp_ptx.cuh", "include/qwp.h"}
+                          csrc + "qwp_internal.h", csrc + "qwp_ptx.cuh", csrc + "qwp_sync.cuh", "include/qwp.h"}
     # the decode kernel, the repack/dequant kernels and the no-alloc entry points
     # are other translation units: changing them leaves the record valid
     assert not any(f.endswith(("qwp_decode.cu", "qwp_aux.cu", "qwp_noalloc.cu")) for f in files)
