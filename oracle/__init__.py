@@ -14,6 +14,9 @@ Functions (each follows the passage cited in ``qwp_oracle.c``):
   w4a16_dequant               interleaved int4 words + fp16 scales + zeros -> fp64
   gemm                        y = x @ w.T and a = |x| @ |w|.T, both fp64, naive loops
   q4k_gemm / q6k_gemm / w4a16_gemm   decode + dequant + gemm in one call
+  q4k_terms                   the two exact terms a = d*sc*q, b = dmin*m of each Q4_K weight
+  q8_quantize / q8_dequant    activation quantization to 8-bit codes per block of 32
+  q4k_q8_gemm                 the Q4_K product with quantized activations, and its bound
 
 Parity pins: see ``tests/test_oracle_pins.py``.  The exact GGML bit layout of
 the 6-bit scale/min packing is not printed on the source pages and is
@@ -59,6 +62,8 @@ def _load():
         lib.oracle_q6k_dequant.argtypes = [p, i64, i64, p]
         lib.oracle_w4a16_dequant.argtypes = [p, p, p, i64, i64, i64, p]
         lib.oracle_gemm.argtypes = [p, p, i64, i64, i64, p, p]
+        lib.oracle_q4k_terms.argtypes = [p, i64, i64, p, p]
+        lib.oracle_q8_quantize.argtypes = [p, i64, i64, p, p, p]
         lib.oracle_num_threads.argtypes = []
         _lib = lib
     return _lib
@@ -192,3 +197,47 @@ def w4a16_gemm_bf16(wq, scales, zeros, x_bf16, N: int, K: int, group: int, with_
     w = w4a16_dequant(wq, scales, zeros, N, K, group)
     x = bf16_to_f64(np.asarray(x_bf16).view(np.uint16))
     return gemm(x.reshape(-1, K), w, with_abs)
+
+
+def q4k_terms(blocks: np.ndarray, N: int, K: int):
+    """The exact terms (a, b), both fp64 [N, K], of every Q4_K weight w = a - b:
+    a = d * sc_j * q and b = dmin * m_j."""
+    blk = np.ascontiguousarray(np.asarray(blocks, dtype=np.uint8).reshape(-1))
+    if blk.size != N * (K // 256) * 144 or K % 256:
+        raise ValueError("Q4_K buffer size does not match N, K")
+    a = np.empty((N, K), np.float64)
+    b = np.empty((N, K), np.float64)
+    _check(_load().oracle_q4k_terms(_ptr(blk), N, K, _ptr(a), _ptr(b)), "q4k_terms")
+    return a, b
+
+
+def q8_quantize(x_bf16_bits: np.ndarray, K: int):
+    """bf16 activations [M, K] -> (q int8 [M, K], d float32 [M, K/32], s int32 [M, K/32]):
+    per block of 32, d = amax/127, q = round(x * (1/d)) half away from zero, s = sum q,
+    all in fp32 (see qwp_oracle.c)."""
+    src = np.ascontiguousarray(np.asarray(x_bf16_bits).astype(np.uint16, copy=False).reshape(-1, K))
+    M = src.shape[0]
+    q = np.empty((M, K), np.int8)
+    d = np.empty((M, K // 32), np.float32)
+    s = np.empty((M, K // 32), np.int32)
+    _check(_load().oracle_q8_quantize(_ptr(src), M, K, _ptr(q), _ptr(d), _ptr(s)), "q8_quantize")
+    return q, d, s
+
+
+def q8_dequant(q: np.ndarray, d: np.ndarray) -> np.ndarray:
+    """The value each code stands for, d * q, in fp64 (exact)."""
+    q = np.asarray(q, dtype=np.int8)
+    M, K = q.shape
+    return q.astype(np.float64) * np.repeat(np.asarray(d, dtype=np.float64).reshape(M, K // 32), 32, axis=1)
+
+
+def q4k_q8_gemm(blocks: np.ndarray, q: np.ndarray, d: np.ndarray, N: int, K: int):
+    """Plain definition of the Q4_K product with quantized activations, fp64:
+    y[m, n] = sum_k W[n, k] * d[m, k/32] * q[m, k]; with it the bound magnitude
+    sum_k (|a[n, k]| + |b[n, k]|) * |d * q| over the weights' two terms."""
+    xh = q8_dequant(q, d)
+    w = q4k_dequant(blocks, N, K)
+    y = gemm(xh, w, with_abs=False)
+    a, b = q4k_terms(blocks, N, K)
+    mag2 = gemm(np.abs(xh), np.abs(a) + np.abs(b), with_abs=False)
+    return y, mag2

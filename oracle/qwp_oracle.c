@@ -42,6 +42,12 @@
  *    unpinned): 256 weights in 210 bytes -- ql[128] (low four bits), qh[64]
  *    (high two bits), int8 scales[16] (one per 16 weights), fp16 d last;
  *    w = d * scale * (q - 32) with q the 6-bit code.
+ *  - "The dequant scratch round-trip is ZINC's last RDNA4 prefill tax",
+ *    section "What removing it was worth": the DP4a path quantizes the
+ *    activations first (Q8_1: 8-bit codes per block of 32 with a scale) and
+ *    multiplies them, still packed, with the 4-bit weights.  The pages give no
+ *    rounding rule; the one taken here (GGML's Q8_1 rule, with the scale kept
+ *    in fp32 and an exact integer block sum) is in oracle_q8_quantize.
  */
 #include <math.h>
 #include <stdint.h>
@@ -239,6 +245,84 @@ int oracle_w4a16_dequant(const uint32_t *wq, const uint16_t *scales, const uint8
         }
     }
     return status;
+}
+
+/*
+ * The two terms of every Q4_K weight, w = a - b with a = d * sc_j * q and
+ * b = dmin * m_j (both exact in double), for the error bound of products whose
+ * arithmetic keeps the terms apart.  Same layout and checks as oracle_q4k_dequant.
+ */
+int oracle_q4k_terms(const uint8_t *blocks, int64_t N, int64_t K, double *a, double *b)
+{
+    if (N < 0 || K < 0 || K % 256 != 0)
+        return ORACLE_ERR_SHAPE;
+    const int64_t nb = K / 256;
+    int status = ORACLE_OK;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t blk_i = 0; blk_i < nb; ++blk_i) {
+            const uint8_t *blk = blocks + (n * nb + blk_i) * 144;
+            double d = oracle_half_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
+            double dmin = oracle_half_to_double((uint16_t)(blk[2] | (blk[3] << 8)));
+            if (!isfinite(d) || !isfinite(dmin)) {
+                status = ORACLE_ERR_NONFINITE;
+                continue;
+            }
+            for (int e = 0; e < 256; ++e) {
+                int c = e / 64, hi = (e % 64) / 32, l = e % 32;
+                int sc, m;
+                oracle_q4k_scale_min(blk + 4, 2 * c + hi, &sc, &m);
+                int qv = hi ? (blk[16 + 32 * c + l] >> 4) : (blk[16 + 32 * c + l] & 15);
+                a[n * K + blk_i * 256 + e] = d * sc * qv;
+                b[n * K + blk_i * 256 + e] = dmin * m;
+            }
+        }
+    }
+    return status;
+}
+
+/*
+ * Activation quantization: each token row of x ([M][K] bfloat16 bits) is cut
+ * into blocks of 32 along K.  Block j of row m gets
+ *     d = RN32(amax / 127),  amax = the largest |x| of the block (exact in fp32),
+ *     q = round-half-away-from-zero(RN32(x * RN32(1 / d)))  (q = 0 when d == 0),
+ *     s = the sum of the block's 32 codes (exact),
+ * every step in IEEE single precision, as written (GGML's Q8_1 rule; the scale
+ * is kept in fp32 rather than rounded to fp16, and the sum as an integer).
+ * q[M][K] int8, d[M][K/32] fp32, s[M][K/32] int32.  A non-finite x is rejected.
+ */
+int oracle_q8_quantize(const uint16_t *x, int64_t M, int64_t K, int8_t *q, float *d, int32_t *s)
+{
+    if (M < 0 || K < 0 || K % 32 != 0)
+        return ORACLE_ERR_SHAPE;
+    for (int64_t i = 0; i < M * K; ++i)
+        if (!isfinite(oracle_bf16_to_double(x[i])))
+            return ORACLE_ERR_NONFINITE;
+    const int64_t nbk = K / 32;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t j = 0; j < nbk; ++j) {
+            const uint16_t *xb = x + m * K + 32 * j;
+            float v[32];
+            float amax = 0.0f;
+            for (int l = 0; l < 32; ++l) {
+                v[l] = (float)oracle_bf16_to_double(xb[l]);  /* exact: bfloat16 is a subset of fp32 */
+                if (fabsf(v[l]) > amax)
+                    amax = fabsf(v[l]);
+            }
+            const float dj = amax / 127.0f;
+            const float id = dj != 0.0f ? 1.0f / dj : 0.0f;
+            int32_t sum = 0;
+            for (int l = 0; l < 32; ++l) {
+                const float t = v[l] * id;
+                const int qi = (int)roundf(t);
+                q[m * K + 32 * j + l] = (int8_t)qi;
+                sum += qi;
+            }
+            d[m * nbk + j] = dj;
+            s[m * nbk + j] = sum;
+        }
+    }
+    return ORACLE_OK;
 }
 
 /*

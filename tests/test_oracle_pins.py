@@ -409,3 +409,109 @@ def test_synth_value_ranges():
     d6 = q6[:, 208:210].copy().view("<u2").view(np.float16).astype(np.float64)
     assert d6.min() >= 1e-5 * (1 - 2 ** -10) and d6.max() <= 8e-5 * (1 + 2 ** -11)
     assert (d6 < 2.0 ** -14).any() and (d6 >= 2.0 ** -14).any()  # subnormal and normal fp16 d
+
+
+# ---------------------------------------------------------------- activation quantization
+
+
+def _q8_cases():
+    with open(os.path.join(GOLDEN, "q8_handbuilt.json")) as f:
+        return json.load(f)["cases"]
+
+
+def _bf16_bits(values):
+    """Exact bfloat16 bits of values that bfloat16 represents exactly."""
+    f = np.asarray(values, np.float32)
+    bits = (f.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal((bits.astype(np.uint32) << 16).view(np.float32), f), "not a bfloat16 value"
+    return bits
+
+
+@pytest.mark.parametrize("case", _q8_cases(), ids=lambda c: c["name"])
+def test_q8_handbuilt_blocks(case):
+    """Blocks worked out by hand (tests/golden/q8_handbuilt.json), also as the
+    second block of a row and with the row mirrored (q(-x) = -q(x))."""
+    x = _bf16_bits(_rle(case["x"]))
+    expect_q = _rle(case["q"]).astype(np.int64)
+    row = np.concatenate([_bf16_bits(np.full(32, 3.0)), x])
+    q, d, s = oracle.q8_quantize(row.reshape(1, 64), 64)
+    assert np.array_equal(q[0, 32:].astype(np.int64), expect_q)
+    assert d[0, 1] == np.float32(case["d"]) and s[0, 1] == case["s"]
+    q2, d2, s2 = oracle.q8_quantize((x ^ np.uint16(0x8000)).reshape(1, 32), 32)
+    assert np.array_equal(q2[0].astype(np.int64), -expect_q) and d2[0, 0] == np.float32(case["d"])
+    assert s2[0, 0] == -case["s"]
+
+
+def test_q8_invariants_on_wide_range_values():
+    """Every block: |q| <= 127, the largest |q| is 127 (unless the block is zero),
+    s = sum q, and d * q is within d/2 (plus fp32 rounding) of x."""
+    rng = np.random.default_rng(5)
+    M, K = 6, 1024
+    mant = rng.integers(0, 128, size=(M, K))
+    expo = rng.integers(100, 150, size=(M, K))  # 2^-27 .. 2^22
+    sign = rng.integers(0, 2, size=(M, K))
+    bits = ((sign << 15) | (expo << 7) | mant).astype(np.uint16)
+    bits[2, 64:96] = 0  # one zero block
+    q, d, s = oracle.q8_quantize(bits, K)
+    x = oracle.bf16_to_f64(bits)
+    qb = q.reshape(M, K // 32, 32).astype(np.int64)
+    assert np.abs(qb).max() <= 127
+    amax = np.abs(x.reshape(M, K // 32, 32)).max(axis=2)
+    assert np.array_equal(np.abs(qb).max(axis=2) == 127, amax > 0)
+    assert np.array_equal(qb.sum(axis=2), s.astype(np.int64))
+    err = np.abs(x - oracle.q8_dequant(q, d))
+    half = np.repeat(d.astype(np.float64), 32, axis=1) / 2
+    assert np.all(err <= half * (1 + 2.0 ** -20))
+    assert np.all(np.abs(d.astype(np.float64) * 127 - amax) <= amax * 2.0 ** -23)
+
+
+def test_q8_rejects_nonfinite_and_bad_shape():
+    bits = np.zeros((1, 32), np.uint16)
+    bits[0, 3] = 0x7F80  # +inf
+    with pytest.raises(ValueError):
+        oracle.q8_quantize(bits, 32)
+    with pytest.raises(ValueError):
+        oracle.q8_quantize(np.zeros((1, 48), np.uint16), 48)
+
+
+@pytest.mark.parametrize("case", _q4k_cases(), ids=lambda c: c["name"])
+def test_q4k_terms_handbuilt(case):
+    """w = a - b with a = d*sc*q and b = dmin*m: the hand-built blocks with dmin = 0
+    have b = 0 and a = w, those with d = 0 have a = 0 and b = -w."""
+    blocks = np.stack([_q4k_block(b) for b in case["blocks"]]).reshape(case["N"], -1)
+    a, b = oracle.q4k_terms(blocks, case["N"], case["K"])
+    w = np.concatenate([_rle(e) for e in case["expect"]]).reshape(case["N"], case["K"])
+    assert np.array_equal(a - b, w)
+    spec = case["blocks"][0]
+    if int(spec["dmin"], 16) == 0:
+        assert not b.any() and np.array_equal(a, w)
+    if int(spec["d"], 16) == 0:
+        assert not a.any() and np.array_equal(b, -w)
+
+
+def test_q4k_terms_worked_example():
+    """d = 2^-10, dmin = 2^-9, sc_0 = 3, m_0 = 5, q(element 0) = 7: a = 21/1024 and
+    b = 10/1024 for element 0; a = 0, b = 10/1024 for the rest of sub-block 0."""
+    case = next(c for c in _q4k_cases() if c["name"] == "worked_example_power_of_two_scales")
+    a, b = oracle.q4k_terms(_q4k_block(case["blocks"][0]).reshape(1, -1), 1, 256)
+    assert a[0, 0] == 21 / 1024 and b[0, 0] == 10 / 1024
+    assert not a[0, 1:32].any() and np.all(b[0, 1:32] == 10 / 1024) and not b[0, 32:].any()
+
+
+def test_q4k_q8_gemm_equals_unquantized_product_on_the_code_grid():
+    """Activations already on the code grid (each block's largest |x| is 127/64 and
+    every x a multiple of 1/64) quantize exactly, so the product with quantized
+    activations is the unquantized oracle product, bit for bit; the bound magnitude
+    over the two weight terms is at least the one over the weights."""
+    rng = np.random.default_rng(9)
+    M, N, K = 3, 7, 512
+    codes = rng.integers(-127, 128, size=(M, K))
+    codes[:, ::32] = 127 * np.where(rng.integers(0, 2, size=(M, K // 32)) > 0, 1, -1)
+    bits = _bf16_bits(codes / 64.0).reshape(M, K)
+    blocks = synth.q4k_weights(N, K, seed=10)
+    q, d, s = oracle.q8_quantize(bits, K)
+    assert np.array_equal(q.astype(np.int64), codes) and np.all(d == np.float32(1 / 64))
+    y, mag2 = oracle.q4k_q8_gemm(blocks, q, d, N, K)
+    y0, mag = oracle.q4k_gemm(blocks, bits, N, K)
+    assert np.array_equal(y, y0)
+    assert np.all(mag2 >= mag)
