@@ -303,18 +303,20 @@ SWEEP = (["q4k:32:2048:2048"]
 def parse_gemm(spec):
     parts = spec.split(":")
     kind = parts[0]
-    if kind in ("q4k", "q6k") and len(parts) == 4:
+    if kind in ("q4k", "q6k", "q4kq8") and len(parts) == 4:
         M, N, K = map(int, parts[1:])
         return kind, M, N, K, 0, set()
     if kind == "w4a16" and len(parts) >= 5 and set(parts[5:]) <= {"sym", "bf16"}:
         M, N, K, g = map(int, parts[1:5])
         return kind, M, N, K, g, set(parts[5:])
-    raise ValueError(f"bad --gemm spec {spec!r}: q4k:M:N:K, q6k:M:N:K or w4a16:M:N:K:group[:sym][:bf16]")
+    raise ValueError(f"bad --gemm spec {spec!r}: q4k:M:N:K, q6k:M:N:K, q4kq8:M:N:K or "
+                     "w4a16:M:N:K:group[:sym][:bf16]")
 
 
 def time_gemm(spec, steps, warmup, dev):
     """Time one GEMM shape: graph replays of the library call (Q4_K, Q6_K: bf16 x;
-    W4A16: fp16 x, or bf16 x with ':bf16', no zero points with ':sym'), one call per
+    W4A16: fp16 x, or bf16 x with ':bf16', no zero points with ':sym'; q4kq8: the
+    activation quantization of bf16 x and the Q4_K product with it), one call per
     input copy in the graph (weights and x both rotate; the copies together are
     larger than 2.5x L2, so every call streams its inputs from HBM), CUDA events on
     the launching stream around the timed replays.  Returns the JSON record."""
@@ -327,16 +329,17 @@ def time_gemm(spec, steps, warmup, dev):
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
     hbm, tc_burst, _, peak_kind = measured_peaks()
     kind, M, N, K, g, flags = parse_gemm(spec)
-    if kind in ("q4k", "q6k"):
-        wbytes = N * K // 256 * (144 if kind == "q4k" else 210)
+    if kind in ("q4k", "q6k", "q4kq8"):
+        wbytes = N * K // 256 * (210 if kind == "q6k" else 144)
     else:
         wbytes = N * K // 2 + (N * K // g) * (2 if "sym" in flags else 3)
     xbytes = 2 * M * K
     copies = max(2, min(64, int(np.ceil(2.5 * l2 / (wbytes + xbytes)))))
     ws, xs = [], []
-    bf16_x = kind in ("q4k", "q6k") or "bf16" in flags
+    bf16_x = kind in ("q4k", "q6k", "q4kq8") or "bf16" in flags
+    xqs = []
     for c in range(copies):
-        if kind == "q4k":
+        if kind in ("q4k", "q4kq8"):
             blocks = synth.q4k_weights(N, K, seed=100 + c)
             ws.append((qwp.q4k_repack(torch.from_numpy(blocks.reshape(-1)).to(dev), N, K),))
         elif kind == "q6k":
@@ -351,11 +354,16 @@ def time_gemm(spec, steps, warmup, dev):
                       .view(torch.bfloat16))
         else:
             xs.append(torch.from_numpy(synth.activations_f16(M, K, seed=7 + c)).to(dev))
+        if kind == "q4kq8":
+            xqs.append(torch.empty(qwp.q8_activation_bytes(M, K), dtype=torch.uint8, device=dev))
     y = torch.empty(M, N, dtype=torch.float32, device=dev)
 
     def call(c):
         if kind == "q4k":
             qwp.q4k_gemm(ws[c][0], xs[c], N, out=y)
+        elif kind == "q4kq8":
+            qwp.q8_quantize(xs[c], out=xqs[c])
+            qwp.q4k_q8_gemm(ws[c][0], xqs[c], M, N, K, out=y)
         elif kind == "q6k":
             qwp.q6k_gemm(ws[c][0], xs[c], N, out=y)
         else:
@@ -388,17 +396,17 @@ def time_gemm(spec, steps, warmup, dev):
     flops = 2.0 * M * N * K
     byts = wbytes + xbytes + 4.0 * M * N
     t_tc, t_hbm = flops / (tc_burst * 1e12), byts / (hbm * 1e9)
-    plan = qwp.gemm_plan(kind if kind != "w4a16" else "w4a16", M, N, K)
+    plan = {"kernel": "decode (8-bit activations)"} if kind == "q4kq8" else qwp.gemm_plan(kind, M, N, K)
     rec = {
         "gemm": spec, "us": t * 1e6, "tflops": flops / t / 1e12,
         "pct_bf16_peak": 100.0 * flops / t / 1e12 / tc_burst,
         "gbs": byts / t / 1e9, "bound": "tensor" if t_tc >= t_hbm else "hbm",
         "roofline_us": max(t_tc, t_hbm) * 1e6, "roofline_frac": max(t_tc, t_hbm) / t,
         "peak_source": peak_kind, "calls_timed": reps * copies, "input_copies": copies,
-        "launches_per_call": 2 if bf16_x and plan.get("kernel") == "prefill" else 1,
+        "launches_per_call": 2 if kind == "q4kq8" or (bf16_x and plan.get("kernel") == "prefill") else 1,
         "plan": plan,
     }
-    del ws, xs, gr
+    del ws, xs, xqs, gr
     torch.cuda.empty_cache()
     return rec
 
@@ -418,7 +426,9 @@ def run_gemms(args, specs):
 # target on the largest projection, and the two HBM-bound targets (M<=32, skinny N).
 TARGETS = (("gate_up_m2048", "q4k:2048:24576:4096", "tensor >= 0.60 of bf16 dense peak"),
            ("q4k_m32_n2048_k2048", "q4k:32:2048:2048", "HBM roofline >= 0.70"),
-           ("skinny_n32_m4096_k4096", "q4k:4096:32:4096", "HBM roofline >= 0.70"))
+           ("skinny_n32_m4096_k4096", "q4k:4096:32:4096", "HBM roofline >= 0.70"),
+           ("decode_m1_n152064_k4096", "q4k:1:152064:4096", "HBM roofline >= 0.70"),
+           ("decode_q8_m1_n152064_k4096", "q4kq8:1:152064:4096", "HBM roofline >= 0.70 (8-bit activations)"))
 
 # Load-time repacks timed on their own: the layer's four Q4_K projections and the
 # two W4A16 shapes.

@@ -177,6 +177,56 @@ QWP_API int q4k_gemm_noalloc(const void *w_tiled_dev, const void *x_dev, float *
                              int64_t M, int64_t N, int64_t K, void *stream);
 
 /*
+ * Quantized activations: the activation side of the DP4a path ("The dequant
+ * scratch round-trip is ZINC's last RDNA4 prefill tax", section "What removing
+ * it was worth": Q8_1 activations, quantized first, then multiplied still packed
+ * with the 4-bit weights).  Each token row of x is cut into blocks of 32 along K;
+ * block j gets d = amax/127 (amax its largest |x|), and every value the code
+ * q = round-half-away-from-zero(x * (1/d)) (0 when d == 0), each operation
+ * correctly rounded in fp32 (GGML's Q8_1 rule; d is kept in fp32, not fp16, and
+ * the block sum s of the codes exactly).  The pages give the idea, not the
+ * rounding rule: this is the reading taken.
+ *
+ * Buffer layout (device, 16-byte aligned, opaque to callers except for its
+ * size): tokens in groups of 8, the last group padded with zero tokens; group g
+ * and super-block b (256 values along K) form one 2560-byte record at
+ * (g*K/256 + b)*2560, token t of the group at t*320 inside it: 256 int8 codes
+ * (each run of 8 elements e0..e7 stored as e0 e4 e1 e5 e2 e6 e3 e7, the byte order
+ * of the repacked Q4_K nibbles), then the 8 fp32 scales d and the 8 code sums s
+ * (fp32, exact) of its 32-value blocks.
+ */
+
+/* Bytes of the quantized activations of M tokens: ceil(M/8) * (K/256) * 2560.  K % 256 == 0. */
+QWP_API int q8_activation_bytes(int64_t M, int64_t K, size_t *out_bytes);
+
+/*
+ * Quantize x_bf16_dev[M][K] (bf16, rows contiguous) into xq_dev (at least
+ * q8_activation_bytes).  K % 256 == 0; both pointers 16-byte aligned.  One
+ * kernel, no allocation.  A non-finite activation sets the range flag that
+ * qwp_device_status reports as QWP_ERR_RANGE (its codes are then undefined).
+ */
+QWP_API int q8_quantize(const void *x_bf16_dev, void *xq_dev, int64_t M, int64_t K, void *stream);
+
+/*
+ * y_dev[M][N] (fp32) = sum over k of W[n][k] * d[m][k/32] * q[m][k]: the Q4_K
+ * product with the quantized activations xq_dev (from q8_quantize with the same
+ * M and K), for decode-shaped calls, 1 <= M <= 8.  Per row, 32-value block and
+ * token, the 32 products of 4-bit weight codes and 8-bit activation codes are
+ * summed exactly in integers (dp4a), then combined in fp32 as
+ * d_x * (d*sc * dot - dmin*m * s): the result is the product of the weights with
+ * the dequantized activations d*q up to fp32 rounding, at most
+ * (K/32 + 4) * 2^-24 * sum_k (|d*sc*q_w| + |dmin*m|) * |d_x*q_x| per element.
+ * The quantization itself changes x by at most d/2 per value (half a code),
+ * which this entry point does not undo: it trades that for reading one byte per
+ * activation and one integer instruction per 4 weights.  Runs on the decode
+ * kernel (stream-K over 128-row tiles and 256-wide super-blocks); takes its
+ * scratch (partials of shared tiles) from the library's stream-ordered pool.
+ * K % 256 == 0; pointers 16-byte aligned; M > 8 returns QWP_ERR_UNSUPPORTED_SHAPE.
+ */
+QWP_API int q4k_q8_gemm(const void *w_tiled_dev, const void *xq_dev, float *y_dev,
+                        int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
  * Q6_K (GGML blocks of 256 weights along K, 210 bytes each: ql[128] low four
  * bits of the 6-bit codes, qh[64] high two bits, int8 scales[16] (one per 16
  * weights), fp16 d last; w = d * scale * (q - 32)).  Source: "How ZINC's RDNA4
@@ -277,7 +327,8 @@ QWP_API int w4a16_gemm_bf16(const void *wq_tiled_dev, const void *scales_dev, co
  * bounded wait on an mbarrier expired (the kernel then released its tensor
  * memory and exited; its output is invalid; while a timeout is recorded, every
  * GEMM launch on that device exits at once without writing y); QWP_ERR_RANGE
- * if q4k_gemm met an activation beyond the fp16 range (y then holds inf/nan);
+ * if an entry point converting bf16 activations to fp16 met one beyond the
+ * fp16 range (y then holds inf/nan), or q8_quantize met a non-finite one;
  * or QWP_ERR_CUDA.  Reading the word here clears it.
  */
 QWP_API int qwp_device_status(void *stream);

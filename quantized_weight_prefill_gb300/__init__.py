@@ -32,7 +32,7 @@ EXPORTED_SYMBOLS = (
     "q4k_gemm_noalloc", "q6k_repacked_bytes", "q6k_repack", "q6k_dequant", "q6k_gemm", "q6k_gemm_f16",
     "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_bf16",
     "qwp_device_status", "qwp_set_decode_policy", "qwp_decode_selected", "qwp_gemm_plan",
-    "qwp_set_wait_timeout_ns",
+    "qwp_set_wait_timeout_ns", "q8_activation_bytes", "q8_quantize", "q4k_q8_gemm",
 )
 
 # Decode-kernel dispatch policies (enum qwp_decode_policy in the header).
@@ -84,6 +84,9 @@ def library() -> ctypes.CDLL:
         lib.qwp_decode_selected.argtypes = [ctypes.c_int, i64, i64, i64]
         lib.qwp_gemm_plan.argtypes = [ctypes.c_int, i64, i64, i64, p]
         lib.qwp_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+        lib.q8_activation_bytes.argtypes = [i64, i64, sz]
+        lib.q8_quantize.argtypes = [p, p, i64, i64, p]
+        lib.q4k_q8_gemm.argtypes = [p, p, p, i64, i64, i64, p]
         for name in EXPORTED_SYMBOLS:
             if name != "qwp_status_string":
                 getattr(lib, name).restype = ctypes.c_int
@@ -183,6 +186,42 @@ def q4k_gemm_noalloc(w_tiled: torch.Tensor, x: torch.Tensor, N: int, out: torch.
         raise ValueError("out must be [M, N]")
     _check(library().q4k_gemm_noalloc(_ptr(w_tiled), _ptr(x), _ptr(out), M, N, K, _stream(x)),
            "q4k_gemm_noalloc")
+    return out
+
+
+def q8_activation_bytes(M: int, K: int) -> int:
+    out = ctypes.c_size_t()
+    _check(library().q8_activation_bytes(M, K, ctypes.byref(out)), "q8_activation_bytes")
+    return out.value
+
+
+def q8_quantize(x: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """bf16 activations [M, K] -> the quantized-activation records (uint8,
+    q8_activation_bytes(M, K) bytes): 8-bit codes per block of 32, fp32 scales."""
+    _dev(x, torch.bfloat16, "x")
+    M, K = x.shape
+    nbytes = q8_activation_bytes(M, K)
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+    _dev(out, torch.uint8, "out")
+    if out.numel() < nbytes:
+        raise ValueError("out is smaller than q8_activation_bytes(M, K)")
+    _check(library().q8_quantize(_ptr(x), _ptr(out), M, K, _stream(x)), "q8_quantize")
+    return out
+
+
+def q4k_q8_gemm(w_tiled: torch.Tensor, xq: torch.Tensor, M: int, N: int, K: int,
+                out: torch.Tensor | None = None) -> torch.Tensor:
+    """y[M, N] (fp32) = the Q4_K product with quantized activations xq (from
+    q8_quantize of an [M, K] x), 1 <= M <= 8."""
+    _dev(w_tiled, torch.uint8, "w_tiled")
+    _dev(xq, torch.uint8, "xq")
+    if xq.numel() < q8_activation_bytes(M, K):
+        raise ValueError("xq is smaller than q8_activation_bytes(M, K)")
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.float32, device=xq.device)
+    _dev(out, torch.float32, "out")
+    _check(library().q4k_q8_gemm(_ptr(w_tiled), _ptr(xq), _ptr(out), M, N, K, _stream(xq)), "q4k_q8_gemm")
     return out
 
 

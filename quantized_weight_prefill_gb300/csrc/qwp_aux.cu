@@ -285,6 +285,65 @@ int launch_bf16_to_f16(const void *x, void *out, int64_t n, cudaStream_t stream,
     return launch_status();
 }
 
+// Activation quantization to the record order of qwp_format.cuh: one warp per
+// (token, super-block), lane l taking elements 8l..8l+7 (block l/4 of 32).  Per
+// block: d = amax/127, q = round-half-away-from-zero(x * (1/d)) (0 when d == 0),
+// each step correctly rounded in fp32 (GGML's Q8_1 rule with the scale kept in
+// fp32), s = sum of the codes.  Tokens past M (padding of the last group) are
+// written as zeros.  A non-finite x sets the range bit of the status word.
+__global__ void q8_quantize_kernel(const uint4 *__restrict__ x, uint8_t *__restrict__ out, int M, int K,
+                                   int64_t warps, uint32_t *status) {
+    const int64_t wi = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (wi >= warps) return;  // surplus warps of the last block leave whole (wi is warp-uniform)
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const int nsb = K / Q4K_BLOCK;
+    const int64_t m = wi / nsb;  // token (padded count)
+    const int b = static_cast<int>(wi - m * nsb);
+    float v[8];
+    bool bad = false;
+    if (m < M) {
+        const uint4 raw = x[(m * K + static_cast<int64_t>(b) * Q4K_BLOCK) / 8 + lane];
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        bad |= !isfinite(v[i]);
+        amax = fmaxf(amax, fabsf(v[i]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float d = __fdiv_rn(amax, 127.f);
+    const float id = d != 0.f ? __fdiv_rn(1.f, d) : 0.f;
+    int q[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        q[i] = static_cast<int>(roundf(__fmul_rn(v[i], id)));
+        sum += q[i];
+    }
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    // e0 e4 e1 e5 | e2 e6 e3 e7
+    const uint32_t lo = (q[0] & 0xFF) | ((q[4] & 0xFF) << 8) | ((q[1] & 0xFF) << 16) | (static_cast<uint32_t>(q[5]) << 24);
+    const uint32_t hi = (q[2] & 0xFF) | ((q[6] & 0xFF) << 8) | ((q[3] & 0xFF) << 16) | (static_cast<uint32_t>(q[7]) << 24);
+    const int64_t g = m / Q8_GROUP_TOKENS;
+    uint8_t *rec = out + (g * nsb + b) * Q8_RECORD_BYTES + (m % Q8_GROUP_TOKENS) * Q8_TOKEN_BYTES;
+    *reinterpret_cast<uint2 *>(rec + 8 * lane) = make_uint2(lo, hi);
+    if ((lane & 3) == 0) {
+        reinterpret_cast<float *>(rec + 256)[lane >> 2] = d;
+        reinterpret_cast<float *>(rec + 288)[lane >> 2] = static_cast<float>(sum);
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(status, kStatusRangeBit);
+}
+
 static std::atomic<uint64_t> g_wait_timeout_ns{kDefaultTimeoutNs};
 
 uint64_t wait_timeout_ns() { return g_wait_timeout_ns.load(std::memory_order_relaxed); }
@@ -416,6 +475,32 @@ extern "C" int w4a16_dequant(const void *wq_tiled, const void *scales, const uin
     w4_dequant_kernel<<<grid_for(threads, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint8_t *>(wq_tiled), static_cast<const __half *>(scales), zeros, w_out, N,
         K, group);
+    return launch_status();
+}
+
+extern "C" int q8_activation_bytes(int64_t M, int64_t K, size_t *out_bytes) {
+    if (M < 0 || K < 0 || !out_bytes) return QWP_ERR_INVALID_ARG;
+    if (K % Q4K_BLOCK) return QWP_ERR_UNSUPPORTED_SHAPE;
+    *out_bytes = static_cast<size_t>((M + Q8_GROUP_TOKENS - 1) / Q8_GROUP_TOKENS) * (K / Q4K_BLOCK) * Q8_RECORD_BYTES;
+    return QWP_OK;
+}
+
+extern "C" int q8_quantize(const void *x_bf16, void *xq, int64_t M, int64_t K, void *stream) {
+    if (M < 0 || K < 0) return QWP_ERR_INVALID_ARG;
+    if (K % Q4K_BLOCK) return QWP_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || K == 0) return QWP_OK;
+    if (!x_bf16 || !xq) return QWP_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(xq)) return QWP_ERR_MISALIGNED;
+    if (M > (int64_t(1) << 31) - 8 || K > (int64_t(1) << 30)) return QWP_ERR_UNSUPPORTED_SHAPE;
+    int rc = check_device();
+    if (rc) return rc;
+    uint32_t *status = status_word();
+    if (!status) return QWP_ERR_CUDA;
+    const int64_t mpad = (M + Q8_GROUP_TOKENS - 1) / Q8_GROUP_TOKENS * Q8_GROUP_TOKENS;
+    const int64_t warps = mpad * (K / Q4K_BLOCK);
+    q8_quantize_kernel<<<grid_for(warps * 32, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4 *>(x_bf16), static_cast<uint8_t *>(xq), static_cast<int>(M), static_cast<int>(K),
+        warps, status);
     return launch_status();
 }
 

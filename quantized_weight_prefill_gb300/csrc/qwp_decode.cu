@@ -35,6 +35,7 @@
 // weights, as in the prefill transform) and reads 64 contiguous bytes of its
 // token's activations.
 #include <algorithm>
+#include <cstring>
 #include <atomic>
 #include <mutex>
 
@@ -55,6 +56,11 @@ constexpr int DEC_PART_FLOATS = DEC_CWARPS * 32 * 4;     // one float4 per consu
 template <int kFmt>
 __host__ __device__ constexpr int dec_stages() { return kFmt == DFMT_W4A16 ? 4 : 3; }
 
+// The weight format a kernel instance streams (the quantized-activation product
+// reads Q4_K weights).
+template <int kFmt>
+__host__ __device__ constexpr int dec_wfmt() { return kFmt == DFMT_Q4K_Q8 ? DFMT_Q4K : kFmt; }
+
 // Items the producer issues before the first one has landed.
 constexpr int DEC_PRE = 4;
 
@@ -66,6 +72,7 @@ struct DecodeArgs {
     const uint8_t *w;
     const __half *scales;   // W4A16
     const uint8_t *zeros;   // W4A16, or null (symmetric)
+    const uint8_t *xq;      // DFMT_Q4K_Q8: the quantized-activation records of the token group
     float *y;
     uint32_t *status;
     float *part;            // [grid][2][DEC_PART_FLOATS]: partials of shared tiles
@@ -250,6 +257,59 @@ __device__ __forceinline__ void dec_window(const uint8_t *wst, const uint8_t *xs
     dec_half<1>(qa, qb, xw, xo, acc);
 }
 
+// Quantized activations: one item's share of a lane -- row rr of the tile (R rows,
+// rr clamped into it) and sub-blocks 4*half .. 4*half+3 of the super-block.  Per
+// sub-block j and token t, dot = the 32 products of the 4-bit weight codes with
+// token t's 8-bit codes (8 dp4a: the low and the high nibbles of each weight word
+// against the two words of the matching 8 codes), and
+//     acc[t] += d_t,j * (d*sc_j * dot - dmin*m_j * s_t,j),
+// which is sum_k w_k * d_t,j * q_t,k over the sub-block (w = d*sc*q - dmin*m).
+// d*sc_j and dmin*m_j are exact in fp32; the integer dot is exact.
+__device__ __forceinline__ void q8_item(const uint8_t *wst, const uint8_t *xst, int R, int rr, int half, int M,
+                                        float (&acc)[8]) {
+    const uint4 h = *reinterpret_cast<const uint4 *>(wst + Q4K_HEADER_BYTES * rr);
+    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x & 0xFFFFu)));
+    const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x >> 16)));
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+        const int j = 4 * half + jj;
+        const uint4 wv = *reinterpret_cast<const uint4 *>(wst + Q4K_HEADER_BYTES * R + CHUNK_ROW_BYTES * R * (j >> 1) +
+                                                          ((j & 1) * R + rr) * 16);
+        const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+        int lo[4], hi[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            lo[v] = static_cast<int>(w[v] & 0x0F0F0F0Fu);         // elements 8v + (0, 4, 1, 5)
+            hi[v] = static_cast<int>((w[v] >> 4) & 0x0F0F0F0Fu);  // elements 8v + (2, 6, 3, 7)
+        }
+        // The 6-bit scale and min of sub-block jj (half 0) or jj + 4 (half 1).
+        const uint32_t sh = 8u * jj;
+        const uint32_t b_lo = h.y >> sh, b_mid = h.z >> sh, b_hi = h.w >> sh;
+        const uint32_t sc = half ? ((b_hi & 15u) | ((b_lo >> 2) & 0x30u)) : (b_lo & 63u);
+        const uint32_t mn = half ? (((b_hi >> 4) & 15u) | ((b_mid >> 2) & 0x30u)) : (b_mid & 63u);
+        const float dsc = d * static_cast<float>(sc), dm = dmin * static_cast<float>(mn);
+#pragma unroll
+        for (int t = 0; t < DEC_TOKENS; ++t) {
+            if (t < M) {
+                const uint8_t *xt = xst + t * Q8_TOKEN_BYTES;
+                const uint4 x0 = *reinterpret_cast<const uint4 *>(xt + 32 * j);
+                const uint4 x1 = *reinterpret_cast<const uint4 *>(xt + 32 * j + 16);
+                const float dx = reinterpret_cast<const float *>(xt + 256)[j];
+                const float sx = reinterpret_cast<const float *>(xt + 288)[j];
+                int dot = __dp4a(lo[0], static_cast<int>(x0.x), 0);
+                dot = __dp4a(hi[0], static_cast<int>(x0.y), dot);
+                dot = __dp4a(lo[1], static_cast<int>(x0.z), dot);
+                dot = __dp4a(hi[1], static_cast<int>(x0.w), dot);
+                dot = __dp4a(lo[2], static_cast<int>(x1.x), dot);
+                dot = __dp4a(hi[2], static_cast<int>(x1.y), dot);
+                dot = __dp4a(lo[3], static_cast<int>(x1.z), dot);
+                dot = __dp4a(hi[3], static_cast<int>(x1.w), dot);
+                acc[t] = fmaf(dx, fmaf(dsc, static_cast<float>(dot), -(dm * sx)), acc[t]);
+            }
+        }
+    }
+}
+
 // First item of CTA c's range, and the CTA whose range holds item i.
 // (items * G < 2^32: 32-bit arithmetic.)
 __device__ __forceinline__ uint32_t range_begin(uint32_t c, uint32_t items, uint32_t G) { return c * items / G; }
@@ -258,9 +318,10 @@ __device__ __forceinline__ uint32_t item_owner(uint32_t i, uint32_t items, uint3
 }
 
 template <int kFmt>
-__global__ void __launch_bounds__(DEC_THREADS, kFmt == DFMT_Q4K ? 3 : 2)
+__global__ void __launch_bounds__(DEC_THREADS, dec_wfmt<kFmt>() == DFMT_Q4K ? 3 : 2)
     qwp_decode_kernel(const __grid_constant__ CUtensorMap tmap_x, const DecodeArgs args) {
     constexpr int NS = dec_stages<kFmt>();
+    constexpr bool kQ8 = kFmt == DFMT_Q4K_Q8;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -286,7 +347,7 @@ __global__ void __launch_bounds__(DEC_THREADS, kFmt == DFMT_Q4K ? 3 : 2)
     const uint8_t *p_src = nullptr;
     auto p_setup_tile = [&]() {
         const int R = tile_rows(args.N, p_tile);
-        if (kFmt == DFMT_Q4K) {
+        if (dec_wfmt<kFmt>() == DFMT_Q4K) {
             p_bytes = static_cast<uint32_t>(R) * Q4K_BLOCK_BYTES;
             p_src = args.w + q4k_group_offset(args.K, p_tile, R, p_sb);
         } else if (kFmt == DFMT_Q6K) {
@@ -301,11 +362,19 @@ __global__ void __launch_bounds__(DEC_THREADS, kFmt == DFMT_Q4K ? 3 : 2)
     // Lane 0 of the producer warp: item beg + st (= the next one) into slot st % NS.
     auto issue_next = [&](int st) {
         const int s = st % NS;
-        mbar_arrive_expect_tx(full + 8 * s, p_bytes + DEC_X_BYTES);
-        bulk_copy_g2s(smem_u32(slot_w(s)), p_src, p_bytes, full + 8 * s);
-        const int k0 = static_cast<int>(p_sb) * Q4K_BLOCK;
-        for (int b = 0; b < 4; ++b)
-            tma_load_2d(smem_u32(slot_x(s) + 1024 * b), &tmap_x, k0 + 64 * b, 0, full + 8 * s);
+        if (kQ8) {
+            // The super-block's quantized-activation record: one contiguous copy.
+            mbar_arrive_expect_tx(full + 8 * s, p_bytes + Q8_RECORD_BYTES);
+            bulk_copy_g2s(smem_u32(slot_w(s)), p_src, p_bytes, full + 8 * s);
+            bulk_copy_g2s(smem_u32(slot_x(s)), args.xq + static_cast<int64_t>(p_sb) * Q8_RECORD_BYTES, Q8_RECORD_BYTES,
+                          full + 8 * s);
+        } else {
+            mbar_arrive_expect_tx(full + 8 * s, p_bytes + DEC_X_BYTES);
+            bulk_copy_g2s(smem_u32(slot_w(s)), p_src, p_bytes, full + 8 * s);
+            const int k0 = static_cast<int>(p_sb) * Q4K_BLOCK;
+            for (int b = 0; b < 4; ++b)
+                tma_load_2d(smem_u32(slot_x(s) + 1024 * b), &tmap_x, k0 + 64 * b, 0, full + 8 * s);
+        }
         if (++p_sb == nsb) {
             p_sb = 0;
             ++p_tile;
@@ -400,18 +469,25 @@ __global__ void __launch_bounds__(DEC_THREADS, kFmt == DFMT_Q4K ? 3 : 2)
     // ---------------------------------------------------------------- consumers
     const int g = static_cast<int>(lane >> 2), t = static_cast<int>(lane & 3);
     const int r0 = 16 * static_cast<int>(warp) + g, r1 = r0 + 8;
+    // Quantized activations: lane l takes row 16*warp + l%16 of the tile and half
+    // l/16 of each super-block's sub-blocks; at the end of a tile the two halves
+    // are added and lane l keeps tokens 4*(l/16) .. +3 of the row.
+    const int qrow = 16 * static_cast<int>(warp) + static_cast<int>(lane & 15), qhalf = static_cast<int>(lane >> 4);
     const uint32_t wait_bar = args.x_bf16 ? ready : full;
     const uint32_t first_tile = beg / nsb;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc8[DEC_TOKENS] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     bool fine = ok;  // every item so far was consumed
 
-    // Writes (sum of) this CTA's values of tile `tile` to y, rows r0/r1, tokens 2t, 2t+1.
+    // Writes (sum of) this CTA's values of tile `tile` to y: rows r0/r1, tokens 2t,
+    // 2t+1 (the MMA fragment), or row qrow, tokens 4*qhalf .. +3.
     auto store = [&](uint32_t tile, const float (&v)[4]) {
         const int R = tile_rows(args.N, tile);
         const int64_t nb = tile * TILE_ROWS;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const int row = r0 + 8 * (e >> 1), tok = 2 * t + (e & 1);
+            const int row = kQ8 ? qrow : r0 + 8 * (e >> 1);
+            const int tok = kQ8 ? 4 * qhalf + e : 2 * t + (e & 1);
             if (row < R && tok < args.M) args.y[static_cast<int64_t>(tok) * args.N + nb + row] = v[e];
         }
     };
@@ -481,25 +557,41 @@ __global__ void __launch_bounds__(DEC_THREADS, kFmt == DFMT_Q4K ? 3 : 2)
                                                     args.x_bf16 ? DWAIT_READY : DWAIT_FULL));
         }
         if (fine) {
-            if (tile != rows_tile) {
-                rows.set(tile_rows(args.N, tile), r0, r1, t, tile);
-                rows_tile = tile;
-            }
             const uint8_t *wst = slot_w(s);
             const uint8_t *xst = slot_x(s);
-            // W4A16: the quantisation group of the lane's sub-block in each window.
-            int g0 = 0, g1 = 0;
-            if (kFmt == DFMT_W4A16) {
-                const int kb = static_cast<int>(sb) * (Q4K_BLOCK / CHUNK_K) + (t >> 1);  // 64-wide block of window 0
-                g0 = (kb * CHUNK_K) / args.group;
-                g1 = ((kb + 2) * CHUNK_K) / args.group;
+            if constexpr (kQ8) {
+                const int R = tile_rows(args.N, tile);
+                q8_item(wst, xst, R, min(qrow, R - 1), qhalf, args.M, acc8);
+            } else {
+                if (tile != rows_tile) {
+                    rows.set(tile_rows(args.N, tile), r0, r1, t, tile);
+                    rows_tile = tile;
+                }
+                // W4A16: the quantisation group of the lane's sub-block in each window.
+                int g0 = 0, g1 = 0;
+                if (kFmt == DFMT_W4A16) {
+                    const int kb = static_cast<int>(sb) * (Q4K_BLOCK / CHUNK_K) + (t >> 1);  // 64-wide block of window 0
+                    g0 = (kb * CHUNK_K) / args.group;
+                    g1 = ((kb + 2) * CHUNK_K) / args.group;
+                }
+                dec_window<0>(wst, xst, rows, xo, sh, g0, args, acc);
+                dec_window<1>(wst, xst, rows, xo, sh, g1, args, acc);
             }
-            dec_window<0>(wst, xst, rows, xo, sh, g0, args, acc);
-            dec_window<1>(wst, xst, rows, xo, sh, g1, args, acc);
             __syncwarp();
             if (lane == 0) mbar_arrive(empty + 8 * s);
         }
         if (sb == nsb - 1 || st == n_items - 1) {
+            if constexpr (kQ8) {
+                // Lanes l and l ^ 16 hold the two halves of the same row.
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float mine = qhalf ? acc8[4 + e] : acc8[e], theirs_keep = qhalf ? acc8[e] : acc8[4 + e];
+                    // Each lane sends the partner the tokens the partner keeps.
+                    acc[e] = mine + __shfl_xor_sync(0xffffffffu, theirs_keep, 16);
+                }
+#pragma unroll
+                for (int e = 0; e < DEC_TOKENS; ++e) acc8[e] = 0.f;
+            }
             flush(tile);
             acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
         }
@@ -536,7 +628,7 @@ static EncodeTiledFn dec_encode_fn() {
 }
 
 static int weight_stage_bytes(int fmt) {
-    return fmt == DFMT_Q4K ? TILE_ROWS * Q4K_BLOCK_BYTES
+    return fmt == DFMT_Q4K || fmt == DFMT_Q4K_Q8 ? TILE_ROWS * Q4K_BLOCK_BYTES
          : fmt == DFMT_Q6K ? TILE_ROWS * Q6K_BLOCK_BYTES
                            : TILE_ROWS * CHUNK_ROW_BYTES * 4;
 }
@@ -607,24 +699,28 @@ static int launch_decode_fmt(const void *w, const void *scales, const uint8_t *z
         return QWP_ERR_CUDA;
     }
 
-    EncodeTiledFn fn = dec_encode_fn();
-    if (!fn) return QWP_ERR_CUDA;
     CUtensorMap map;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    cuuint32_t box[2] = {64, DEC_TOKENS};
-    cuuint32_t estr[2] = {1, 1};
-    if (fn(&map, x_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-           const_cast<void *>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return QWP_ERR_CUDA;
+    memset(&map, 0, sizeof(map));  // unused by the quantized-activation product (x comes by bulk copy)
+    if (kFmt != DFMT_Q4K_Q8) {
+        EncodeTiledFn fn = dec_encode_fn();
+        if (!fn) return QWP_ERR_CUDA;
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+        cuuint32_t box[2] = {64, DEC_TOKENS};
+        cuuint32_t estr[2] = {1, 1};
+        if (fn(&map, x_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+               const_cast<void *>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return QWP_ERR_CUDA;
+    }
 
     const DecLayout L = dec_layout<kFmt>();
     DecodeArgs a;
     a.w = static_cast<const uint8_t *>(w);
     a.scales = static_cast<const __half *>(scales);
     a.zeros = zeros;
+    a.xq = kFmt == DFMT_Q4K_Q8 ? static_cast<const uint8_t *>(x) : nullptr;
     a.y = y;
     a.status = status;
     a.part = static_cast<float *>(scratch);
@@ -638,7 +734,7 @@ static int launch_decode_fmt(const void *w, const void *scales, const uint8_t *z
     a.nsb = static_cast<int>(K / Q4K_BLOCK);
     a.stage_stride = L.stage_stride;
     a.bar_off = L.bar_off;
-    a.x_bf16 = x_bf16 ? 1 : 0;
+    a.x_bf16 = x_bf16 && kFmt != DFMT_Q4K_Q8 ? 1 : 0;
     a.timeout_ns = kDefaultTimeoutNs;
 
     qwp_decode_kernel<kFmt><<<static_cast<unsigned>(G), DEC_THREADS, L.smem, stream>>>(map, a);
@@ -658,6 +754,7 @@ size_t decode_scratch_bytes(int fmt, int64_t N, int64_t K) {
         case DFMT_Q4K: return scratch_need<DFMT_Q4K>(N, K);
         case DFMT_Q6K: return scratch_need<DFMT_Q6K>(N, K);
         case DFMT_W4A16: return scratch_need<DFMT_W4A16>(N, K);
+        case DFMT_Q4K_Q8: return scratch_need<DFMT_Q4K_Q8>(N, K);
         default: return 0;
     }
 }
@@ -677,6 +774,9 @@ int launch_decode(int fmt, const void *w, const void *scales, const uint8_t *zer
         case DFMT_W4A16:
             return launch_decode_fmt<DFMT_W4A16>(w, scales, zeros, x, x_bf16, y, M, N, K, group, scratch,
                                                  scratch_bytes, stream);
+        case DFMT_Q4K_Q8:
+            return launch_decode_fmt<DFMT_Q4K_Q8>(w, scales, zeros, x, false, y, M, N, K, group, scratch,
+                                                  scratch_bytes, stream);
         default: return QWP_ERR_INVALID_ARG;
     }
 }

@@ -5,8 +5,10 @@
 
 namespace qwp {
 
-// Weight formats of launch_decode (same numbering as the prefill kernel's).
-enum : int { DFMT_W4A16 = 0, DFMT_Q4K = 1, DFMT_Q6K = 2 };
+// Weight formats of launch_decode (same numbering as the prefill kernel's), and
+// DFMT_Q4K_Q8: Q4_K weights with 8-bit quantized activations (record order of
+// qwp_format.cuh), multiplied with integer dot products.
+enum : int { DFMT_W4A16 = 0, DFMT_Q4K = 1, DFMT_Q6K = 2, DFMT_Q4K_Q8 = 3 };
 
 // The largest token count the decode kernel takes (one MMA's N).
 constexpr int64_t DECODE_MAX_TOKENS = 8;
@@ -55,7 +57,8 @@ size_t decode_scratch_bytes(int fmt, int64_t N, int64_t K);
 
 // y[M][N] = x[M][K] . W^T for 1 <= M <= 8 and K % 256 == 0, W repacked in format
 // `fmt`; x fp16, or bf16 when x_bf16 (converted in shared memory; an fp16
-// overflow sets the range bit of the status word).  `scratch` (16-byte aligned,
+// overflow sets the range bit of the status word); for DFMT_Q4K_Q8, x is the
+// quantized-activation records of the first token group (x_bf16 ignored).  `scratch` (16-byte aligned,
 // at least decode_scratch_bytes) is used in stream order; its counters are
 // cleared on `stream` before the kernel.  Allocates nothing.
 int launch_decode(int fmt, const void *w, const void *scales, const uint8_t *zeros, const void *x, bool x_bf16,

@@ -38,6 +38,19 @@
 //                  pair's low nibbles once the low word is shifted right by 4p.
 // 210 bytes per 256 weights as in GGML (plus the row padding of the last tile).
 //
+// Quantized activations (the 8-bit codes of the DP4a-style product), record
+// order.  Tokens are taken in groups of 8 (the last group padded with zero
+// tokens); token group g and super-block b (256 values along K) form one record
+// of 8 * Q8_TOKEN_BYTES bytes at (g * K/256 + b) * Q8_RECORD_BYTES, token t of
+// the group at t * Q8_TOKEN_BYTES inside it:
+//   bytes 0..255   the 256 int8 codes; each run of 8 elements e0..e7 is stored
+//                  as e0 e4 e1 e5 e2 e6 e3 e7, so that its two 32-bit words line
+//                  up byte for byte with the low and the high nibbles of the
+//                  repacked Q4_K word of the same 8 elements;
+//   bytes 256..287 the 8 fp32 scales d of the record's 32-value blocks;
+//   bytes 288..319 the 8 code sums of those blocks, as fp32 (exact: |s| <= 4064).
+// A record is one contiguous bulk copy.
+//
 // W4A16, repacked order.  Same 128-row tiles; tile t starts at 128*t * K/2.
 // Inside, K-block j (64 weights along K) of all R rows is a plane of 32*R bytes
 // at j*32*R, laid out [h][row i][16 bytes] as above, word v being the original
@@ -60,6 +73,9 @@ constexpr int Q6K_BLOCK_BYTES = 210;
 constexpr int Q6K_SCALE_PLANE = 2;   // x Rp: byte offset of the scale plane
 constexpr int Q6K_LOW_PLANE = 18;    // x Rp: first low plane
 constexpr int Q6K_HIGH_PLANE = 146;  // x Rp: first high plane
+constexpr int Q8_GROUP_TOKENS = 8;   // tokens per quantized-activation record
+constexpr int Q8_TOKEN_BYTES = 320;  // one token's 256 codes, 8 scales, 8 sums
+constexpr int Q8_RECORD_BYTES = Q8_GROUP_TOKENS * Q8_TOKEN_BYTES;
 
 __host__ __device__ __forceinline__ int tile_rows(int64_t N, int64_t tile) {
     int64_t r = N - tile * TILE_ROWS;

@@ -285,13 +285,14 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
         mbar_init(part_last, NUM_XFORM_WARPS * S);  // the last unit: every transform warp of every rank
         mbar_init(rings_idle, S);                   // the last unit: one arrival per rank
         mbar_init(drain, 1);
-        // A failure recorded earlier (and not yet read by qwp_device_status) makes
-        // every later launch skip its work instead of waiting out its own timeouts
-        // (the weight copies started below are still waited for).
-        misc[1] = (*reinterpret_cast<volatile uint32_t *>(args.status) & kStatusTimeoutMask) ? 1u : 0u;
         fence_mbar_init();
         prefetch_tensormap(&tmap_x);
         for (int s = 0; s < w_pre; ++s) load_weight_stage(unit_tile(units0), s, s);
+        // A failure recorded earlier (and not yet read by qwp_device_status) makes
+        // every later launch skip its work instead of waiting out its own timeouts
+        // (the weight copies started above are still waited for).  Read after the
+        // copies are issued, so that its latency is not in front of theirs.
+        misc[1] = (*reinterpret_cast<volatile uint32_t *>(args.status) & kStatusTimeoutMask) ? 1u : 0u;
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(misc), TMEM_COLS);
@@ -1229,6 +1230,16 @@ extern "C" int q4k_gemm(const void *w_tiled, const void *x, float *y, int64_t M,
     if (!rc) rc = launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x16, y, M, N, K, 0, s, true);
     if (cudaFreeAsync(x16, s) != cudaSuccess && !rc) rc = QWP_ERR_CUDA;
     return rc;
+}
+
+extern "C" int q4k_q8_gemm(const void *w_tiled, const void *xq, float *y, int64_t M, int64_t N, int64_t K,
+                           void *stream) {
+    if (K % Q4K_BLOCK || K == 0) return K < 0 ? QWP_ERR_INVALID_ARG : QWP_ERR_UNSUPPORTED_SHAPE;
+    int rc = gemm_shape_checks(w_tiled, xq, y, M, N, K);
+    if (rc || M == 0 || N == 0) return rc;
+    if (M > DECODE_MAX_TOKENS) return QWP_ERR_UNSUPPORTED_SHAPE;
+    return run_decode(DFMT_Q4K_Q8, w_tiled, nullptr, nullptr, xq, false, y, M, N, K, 0,
+                      static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int q6k_gemm_f16(const void *w_tiled, const void *x, float *y, int64_t M, int64_t N,

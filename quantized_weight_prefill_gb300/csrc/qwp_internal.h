@@ -40,8 +40,8 @@ int launch_q4k_prefill_fixed(const void *w, const void *x, void *x16, float *y, 
                              cudaStream_t stream);
 
 // The skinny-N kernel (qwp_skinny.cu): Q4_K products with at most 64 weight rows
-// and at least SKINNY_MIN_TOKENS tokens.  x is bf16 (converted in shared memory)
-// or fp16; allocates nothing.
+// and at least SKINNY_MIN_TOKENS tokens.  x is bf16 or fp16, read as it is by the
+// tensor core; allocates nothing.
 constexpr int64_t SKINNY_MIN_TOKENS = 256;
 bool skinny_selected(int fmt, int64_t M, int64_t N, int64_t K);
 // Its launch: `splits` CTAs per cluster along K, `tiles` token tiles of 128.

@@ -173,3 +173,29 @@ def check_bound(y_gpu: np.ndarray, y_ref: np.ndarray, mag: np.ndarray, what: str
     assert np.isfinite(y_gpu).all(), f"{what}: non-finite output"
     return ratio
 
+
+
+# --- documented quantized-activation record layout (numpy restatement) -----------
+
+Q8_PERM = np.array([0, 4, 1, 5, 2, 6, 3, 7])  # stored byte i of a run of 8 holds element Q8_PERM[i]
+
+
+def q8_records_reference(q: np.ndarray, d: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """The record buffer for codes q [M, K] int8, scales d [M, K/32] fp32 and sums
+    s [M, K/32]: tokens in groups of 8 (zero-padded), one 2560-byte record per
+    (group, 256-wide super-block), 320 bytes per token: the 256 codes with each run
+    of 8 stored in the order e0 e4 e1 e5 e2 e6 e3 e7, 8 fp32 scales, 8 fp32 sums."""
+    M, K = q.shape
+    G, nsb = -(-M // 8), K // 256
+    codes = np.zeros((G * 8, K), np.int8)
+    codes[:M] = q
+    dd = np.zeros((G * 8, K // 32), np.float32)
+    dd[:M] = d
+    ss = np.zeros((G * 8, K // 32), np.float32)
+    ss[:M] = s
+    runs = codes.reshape(G * 8, K // 8, 8)[:, :, Q8_PERM].reshape(G, 8, nsb, 256)
+    rec = np.zeros((G, nsb, 8, 320), np.uint8)
+    rec[..., :256] = runs.transpose(0, 2, 1, 3).view(np.uint8)
+    rec[..., 256:288] = dd.reshape(G, 8, nsb, 8).transpose(0, 2, 1, 3).view(np.uint8).reshape(G, nsb, 8, 32)
+    rec[..., 288:320] = ss.reshape(G, 8, nsb, 8).transpose(0, 2, 1, 3).view(np.uint8).reshape(G, nsb, 8, 32)
+    return rec.reshape(-1)

@@ -48,6 +48,15 @@ def test_status_strings(lib):
         assert lib.qwp_status_string(code).decode() == name
 
 
+def test_q8_activation_bytes(lib):
+    assert qwp.q8_activation_bytes(1, 4096) == 16 * 2560
+    assert qwp.q8_activation_bytes(8, 256) == 2560
+    assert qwp.q8_activation_bytes(9, 512) == 2 * 2 * 2560
+    assert qwp.q8_activation_bytes(0, 512) == 0
+    assert lib.q8_activation_bytes(4, 100, ctypes.byref(ctypes.c_size_t())) == SHAPE
+    assert lib.q8_activation_bytes(-1, 256, ctypes.byref(ctypes.c_size_t())) == INVALID
+
+
 def test_repacked_bytes(lib):
     assert qwp.q4k_repacked_bytes(4096, 4096) == 4096 * 16 * 144
     assert qwp.q4k_repacked_bytes(3, 512) == 3 * 2 * 144
@@ -103,6 +112,17 @@ def test_gemm_argument_checks_before_any_cuda_call(lib):
     assert lib.q4k_dequant(a16, a16, 4, 300, None) == SHAPE
     assert lib.w4a16_repack(a16, a16, 4, 96, None) == SHAPE
     assert lib.w4a16_dequant(a16, a16, a16, a16, 4, 256, 96, None) == INVALID
+    # quantized activations
+    assert lib.q8_quantize(a16, a16, 4, 100, None) == SHAPE
+    assert lib.q8_quantize(a16, a16, -1, 256, None) == INVALID
+    assert lib.q8_quantize(None, a16, 4, 256, None) == INVALID
+    assert lib.q8_quantize(a16, _p(0x2008), 4, 256, None) == MISALIGNED
+    assert lib.q8_quantize(None, None, 0, 256, None) == OK
+    assert lib.q4k_q8_gemm(a16, a16, a16, 9, 8, 256, None) == SHAPE    # more than 8 tokens
+    assert lib.q4k_q8_gemm(a16, a16, a16, 8, 8, 100, None) == SHAPE
+    assert lib.q4k_q8_gemm(None, a16, a16, 8, 8, 256, None) == INVALID
+    assert lib.q4k_q8_gemm(a16, _p(0x1008), a16, 8, 8, 256, None) == MISALIGNED
+    assert lib.q4k_q8_gemm(None, None, None, 0, 8, 256, None) == OK
 
 
 def test_decode_policy_round_trip_and_automatic_rule(lib):
