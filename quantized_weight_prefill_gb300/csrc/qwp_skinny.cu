@@ -45,9 +45,9 @@ namespace {
 
 constexpr int SK_TOKENS = 128;                 // tokens per CTA (MMA M)
 constexpr int SK_MAX_N = 64;                   // weight rows (MMA N, padded to 16)
-constexpr int SK_MAX_XS = 8;                   // x ring slots (each XB 64-wide K blocks)
-constexpr int SK_X_BLOCK = SK_TOKENS * 128;    // 128 tokens x 64 16-bit values = 16 KiB
-constexpr int SK_XB_PREF = 2;                  // K blocks per x copy, where the ring keeps 4 blocks
+constexpr int SK_MAX_XS = 8;                   // x ring: one 64-wide K block per slot
+constexpr int SK_MIN_XS = 3;
+constexpr int SK_X_SLOT = SK_TOKENS * 128;     // 128 tokens x 64 16-bit values = 16 KiB
 constexpr int SK_BS = 2;                       // B ring: one 256-wide stage per slot
 constexpr int SK_WS = 2;                       // packed weight stages
 constexpr int SK_W_SLOT = SK_MAX_N * Q4K_BLOCK_BYTES;
@@ -58,35 +58,30 @@ constexpr int SK_THREADS = 32 * (SK_XFORM0 + SK_NXFORM);
 constexpr uint32_t SK_TMEM_COLS = 64;
 
 // The shared-memory layout (offsets from the 1 KiB-aligned base): the x ring of
-// `xs` slots of xb K blocks each (one TMA copy: xb consecutive 16 KiB tiles), the
-// B ring (a slot is one 256-wide stage: 4 blocks of n_pad rows x 128 bytes, twice
-// that for bf16 x, whose lo tiles follow the hi tiles), the packed weight ring,
-// the barriers and two words (tensor-memory base, abort flag).
+// `xs` slots, the B ring (a slot is one 256-wide stage: 4 blocks of n_pad rows x
+// 128 bytes, twice that for bf16 x, whose lo tiles follow the hi tiles), the
+// packed weight ring, the barriers and two words (tensor-memory base, abort flag).
 struct SkLayout {
     int xs, b_slot, off_b, off_w, off_bar, off_misc;
 };
-__host__ __device__ constexpr SkLayout sk_layout(int n_pad, bool bf16, int xb) {
+__host__ __device__ constexpr SkLayout sk_layout(int n_pad, bool bf16) {
     SkLayout l{};
     l.b_slot = (bf16 ? 2 : 1) * 4 * n_pad * 128;
     const int rest = SK_BS * l.b_slot + SK_WS * SK_W_SLOT + 8 * SK_NUM_BARS + 16 + 1024;  // + base alignment slack
-    l.xs = (SK_SMEM - rest) / (xb * SK_X_BLOCK);
+    l.xs = (SK_SMEM - rest) / SK_X_SLOT;
     if (l.xs > SK_MAX_XS) l.xs = SK_MAX_XS;
-    l.off_b = l.xs * xb * SK_X_BLOCK;
+    l.off_b = l.xs * SK_X_SLOT;
     l.off_w = l.off_b + SK_BS * l.b_slot;
     l.off_bar = l.off_w + SK_WS * SK_W_SLOT;
     l.off_misc = l.off_bar + 8 * SK_NUM_BARS;
     return l;
 }
-// Blocks per x copy: SK_XB_PREF where the ring then still holds 4 blocks, else 1.
-__host__ __device__ constexpr int sk_xb(int n_pad, bool bf16) {
-    return sk_layout(n_pad, bf16, SK_XB_PREF).xs * SK_XB_PREF >= 4 ? SK_XB_PREF : 1;
-}
-static_assert(sk_layout(SK_MAX_N, true, 1).xs >= 3, "the x ring keeps at least three blocks");
-static_assert(sk_layout(SK_MAX_N, true, 1).off_misc + 16 + 1024 <= SK_SMEM, "shared memory budget");
+static_assert(sk_layout(SK_MAX_N, true).xs >= SK_MIN_XS, "the x ring keeps at least three slots");
+static_assert(sk_layout(SK_MAX_N, true).off_misc + 16 + 1024 <= SK_SMEM, "shared memory budget");
 static_assert(SK_SMEM <= 232448, "opt-in shared memory per CTA");
-// The partial tile of one CTA overlays its x ring (at least 3 blocks): [128
-// tokens][n_pad + 4] fp32 (the 4 extra floats per row spread the rows over the banks).
-static_assert(SK_TOKENS * (SK_MAX_N + 4) * 4 <= 3 * SK_X_BLOCK, "partial tile fits the x ring");
+// The partial tile of one CTA overlays its x ring: [128 tokens][n_pad + 4] fp32
+// (the 4 extra floats per row spread the rows over the banks).
+static_assert(SK_TOKENS * (SK_MAX_N + 4) * 4 <= SK_MIN_XS * SK_X_SLOT, "partial tile fits the x ring");
 
 struct SkinnyArgs {
     const uint8_t *w;     // repacked Q4_K (one tile of R = N rows)
@@ -97,7 +92,6 @@ struct SkinnyArgs {
     int splits;           // S (cluster size along x)
     int stages;           // 256-wide stages per CTA (K / 256 / S)
     int x_bf16;           // 1: x and the weight operands are bf16 (hi + lo), else fp16
-    int xb;               // 64-wide K blocks per x copy (1, 2 or 4; divides 4)
     uint64_t timeout_cycles, drain_cycles;
 };
 
@@ -109,15 +103,6 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
     return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// One x copy: K blocks kb .. kb + xb - 1 of tokens m0 .. m0 + 127 (a 2-D map over
-// [M][K] when xb == 1, else a 3-D map over [K/64][M][64]).
-__device__ __forceinline__ void sk_load_x(uint32_t dst, const CUtensorMap *map, int m0, int kb, int xb, uint32_t bar) {
-    if (xb == 1)
-        tma_load_2d(dst, map, kb * CHUNK_K, m0, bar);
-    else
-        tma_load_3d(dst, map, 0, m0, kb, bar);
-}
-
 __global__ void __launch_bounds__(SK_THREADS, 1)
     qwp_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const SkinnyArgs args) {
     extern __shared__ uint8_t smem_raw[];
@@ -125,16 +110,13 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
                                                 ~static_cast<uintptr_t>(1023));
     const uint32_t warp = warp_id(), lane = lane_id();
     const bool bf16 = args.x_bf16 != 0;
-    const int XB = args.xb;
-    const SkLayout L = sk_layout(args.n_pad, bf16, XB);
+    const SkLayout L = sk_layout(args.n_pad, bf16);
     const int XS = L.xs;
-    const uint32_t x_slot = static_cast<uint32_t>(XB) * SK_X_BLOCK;
     const int S = args.splits;
     const int rank = static_cast<int>(blockIdx.x);  // cluster rank along K
     const int m0 = static_cast<int>(blockIdx.y) * SK_TOKENS;
     const int st0 = rank * args.stages;              // first 256-wide stage of this CTA
     const int nblk = 4 * args.stages;                // 64-wide K blocks of this CTA
-    const int nxs = nblk / XB;                       // x copies of this CTA
     const int R = args.N;                            // weight rows (one tile)
     const uint32_t b_tile = static_cast<uint32_t>(args.n_pad) * 128u;  // one block of B (hi, or the fp16 tile)
 
@@ -145,7 +127,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     const uint32_t acc_full = b_empty + 8 * SK_BS, drain = acc_full + 8;
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + L.off_misc);  // [0] tensor memory, [1] abort
     const Ctl ctl{misc + 1, args.status, args.timeout_cycles, args.drain_cycles};
-    const int x_pre = min(XS, nxs), w_pre = min(SK_WS, args.stages);  // copies started at set-up
+    const int x_pre = min(XS, nblk), w_pre = min(SK_WS, args.stages);  // copies started at set-up
     const uint32_t w_bytes = static_cast<uint32_t>(R) * Q4K_BLOCK_BYTES;
 
     if (threadIdx.x == 0) {
@@ -168,8 +150,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         // The first x tiles and weight stages start before the block-wide barrier
         // (their slots are empty); this thread is also the x producer.
         for (int j = 0; j < x_pre; ++j) {
-            mbar_arrive_expect_tx(x_full + 8 * j, x_slot);
-            sk_load_x(smem_u32(smem + j * x_slot), &tmap_x, m0, 4 * st0 + j * XB, XB, x_full + 8 * j);
+            mbar_arrive_expect_tx(x_full + 8 * j, SK_X_SLOT);
+            tma_load_2d(smem_u32(smem + j * SK_X_SLOT), &tmap_x, (4 * st0 + j) * CHUNK_K, m0, x_full + 8 * j);
         }
         for (int i = 0; i < w_pre; ++i) {
             mbar_arrive_expect_tx(w_full + 8 * i, w_bytes);
@@ -198,11 +180,11 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
             for (int j = 0; j < x_pre; ++j) wait_bar(x_full + 8 * j, 0, ctl, SW_DRAIN, false);
         if (lane == 0 && !skip) {
             int j = x_pre, xs = x_pre % XS;
-            uint32_t ph = x_pre == XS ? 1u : 0u;  // the pass over the ring that copy j starts
-            for (; j < nxs; ++j) {
+            uint32_t ph = x_pre == XS ? 1u : 0u;  // the pass over the ring that block j starts
+            for (; j < nblk; ++j) {
                 if (j >= XS && !wait_bar(x_empty + 8 * xs, ph ^ 1, ctl, SW_X_EMPTY)) break;
-                mbar_arrive_expect_tx(x_full + 8 * xs, x_slot);
-                sk_load_x(smem_u32(smem + xs * x_slot), &tmap_x, m0, 4 * st0 + j * XB, XB, x_full + 8 * xs);
+                mbar_arrive_expect_tx(x_full + 8 * xs, SK_X_SLOT);
+                tma_load_2d(smem_u32(smem + xs * SK_X_SLOT), &tmap_x, (4 * st0 + j) * CHUNK_K, m0, x_full + 8 * xs);
                 if (++xs == XS) {
                     xs = 0;
                     ph ^= 1;
@@ -242,12 +224,9 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
                 const int bs = i % SK_BS;
                 if (!(ok = __all_sync(0xffffffffu, wait_bar(b_full + 8 * bs, (i / SK_BS) & 1, ctl, SW_B_FULL)))) break;
                 for (int blk = 0; blk < 4; ++blk) {
-                    const int xsub = blk % XB;  // block within the x copy
-                    if (xsub == 0) {
-                        if (!(ok = __all_sync(0xffffffffu, wait_bar(x_full + 8 * xs, xph, ctl, SW_X_FULL)))) break;
-                        tc_fence_after();
-                    }
-                    const uint64_t a_desc = smem_desc_sw128(smem_u32(smem + xs * x_slot) + xsub * SK_X_BLOCK);
+                    if (!(ok = __all_sync(0xffffffffu, wait_bar(x_full + 8 * xs, xph, ctl, SW_X_FULL)))) break;
+                    tc_fence_after();
+                    const uint64_t a_desc = smem_desc_sw128(smem_u32(smem + xs * SK_X_SLOT));
                     const uint32_t b_addr = smem_u32(smem + L.off_b + bs * L.b_slot) + blk * b_tile;
                     const uint64_t b_desc = smem_desc_sw128(b_addr);
                     const uint64_t l_desc = smem_desc_sw128(b_addr + lo_off);
@@ -262,10 +241,10 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
                             mma_ss<true>(tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc);
                             if (bf16) mma_ss<true>(tmem, a_desc + 2u * kk, l_desc + 2u * kk, idesc);
                         }
-                        if (xsub == XB - 1) mma_commit(x_empty + 8 * xs);
+                        mma_commit(x_empty + 8 * xs);
                     }
                     __syncwarp();
-                    if (xsub == XB - 1 && ++xs == XS) {
+                    if (++xs == XS) {
                         xs = 0;
                         xph ^= 1;
                     }
@@ -489,22 +468,13 @@ int launch_skinny(const void *w, const void *x, bool x_bf16, float *y, int64_t M
     if ((rc = skinny_plan(M, K, sms, S, tiles))) return rc;
     SkEncodeTiledFn fn = sk_encode_fn();
     if (!fn) return QWP_ERR_CUDA;
-    const int n_pad = static_cast<int>((N + 15) / 16 * 16);
-    const int xb = sk_xb(n_pad, x_bf16);
-    // xb == 1: x as [M][K], one 128-token x 64-value tile per copy.  xb > 1: x
-    // viewed as [K/64 blocks][M rows][64 values], one copy bringing xb consecutive
-    // tiles (each row's xb * 128 bytes contiguous in HBM).
     CUtensorMap map;
-    const cuuint32_t rank = xb == 1 ? 2 : 3;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(CHUNK_K), static_cast<cuuint64_t>(M),
-                          static_cast<cuuint64_t>(K / CHUNK_K)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(CHUNK_K) * 2};
-    if (xb == 1) dims[0] = static_cast<cuuint64_t>(K);
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(CHUNK_K), static_cast<cuuint32_t>(SK_TOKENS),
-                         static_cast<cuuint32_t>(xb)};
-    cuuint32_t estr[3] = {1, 1, 1};
-    if (fn(&map, x_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank,
-           const_cast<void *>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(CHUNK_K), static_cast<cuuint32_t>(SK_TOKENS)};
+    cuuint32_t estr[2] = {1, 1};
+    if (fn(&map, x_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(x),
+           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return QWP_ERR_CUDA;
     SkinnyArgs a;
@@ -514,11 +484,10 @@ int launch_skinny(const void *w, const void *x, bool x_bf16, float *y, int64_t M
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
-    a.n_pad = n_pad;
+    a.n_pad = static_cast<int>((N + 15) / 16 * 16);
     a.splits = S;
     a.stages = static_cast<int>(K / Q4K_BLOCK / S);
     a.x_bf16 = x_bf16 ? 1 : 0;
-    a.xb = xb;
     a.timeout_cycles = ns_to_cycles(wait_timeout_ns());
     a.drain_cycles = ns_to_cycles(kDefaultTimeoutNs);
     cudaLaunchConfig_t cfg = {};
