@@ -5,6 +5,7 @@
 
 #include "qwp_format.cuh"
 #include "qwp_internal.h"
+#include "qwp_ptx.cuh"
 
 namespace qwp {
 
@@ -251,10 +252,12 @@ __global__ void w4_dequant_kernel(const uint8_t *__restrict__ w, const __half *_
 // magnitude in [2^-14, 65504] converts exactly (8 significant bits fit fp16's
 // 11); smaller values become fp16 subnormals (absolute error <= 2^-25); values
 // that would round to infinity set the range flag in the status word.  Lets the
-// dependent GEMM launch start (programmatic dependent launch) right away.
+// dependent GEMM launch start (programmatic dependent launch) right away, and
+// waits for the grids before it (which may write x or still read `out`).
 __global__ void bf16_to_f16_kernel(const uint4 *__restrict__ in, uint4 *__restrict__ out, int64_t n8,
                                    uint32_t *status, uint32_t *zero, int nzero) {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_launch_dependents();
+    pdl_wait();
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0u;
     bool overflow = false;
@@ -280,9 +283,8 @@ int launch_bf16_to_f16(const void *x, void *out, int64_t n, cudaStream_t stream,
     if (!status) return QWP_ERR_CUDA;
     const int64_t n8 = n / 8;
     const int64_t blocks = std::min<int64_t>((n8 + 255) / 256, 152 * 8);
-    bf16_to_f16_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, stream>>>(
-        static_cast<const uint4 *>(x), static_cast<uint4 *>(out), n8, status, zero, zero ? nzero : 0);
-    return launch_status();
+    return launch_pdl(bf16_to_f16_kernel, static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, stream,
+                      static_cast<const uint4 *>(x), static_cast<uint4 *>(out), n8, status, zero, zero ? nzero : 0);
 }
 
 // Activation quantization to the record order of qwp_format.cuh: one warp per
@@ -293,6 +295,8 @@ int launch_bf16_to_f16(const void *x, void *out, int64_t n, cudaStream_t stream,
 // written as zeros.  A non-finite x sets the range bit of the status word.
 __global__ void q8_quantize_kernel(const uint4 *__restrict__ x, uint8_t *__restrict__ out, int M, int K,
                                    int64_t warps, uint32_t *status) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t wi = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (wi >= warps) return;  // surplus warps of the last block leave whole (wi is warp-uniform)
     const int lane = static_cast<int>(threadIdx.x & 31);
@@ -498,10 +502,9 @@ extern "C" int q8_quantize(const void *x_bf16, void *xq, int64_t M, int64_t K, v
     if (!status) return QWP_ERR_CUDA;
     const int64_t mpad = (M + Q8_GROUP_TOKENS - 1) / Q8_GROUP_TOKENS * Q8_GROUP_TOKENS;
     const int64_t warps = mpad * (K / Q4K_BLOCK);
-    q8_quantize_kernel<<<grid_for(warps * 32, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4 *>(x_bf16), static_cast<uint8_t *>(xq), static_cast<int>(M), static_cast<int>(K),
-        warps, status);
-    return launch_status();
+    return launch_pdl(q8_quantize_kernel, grid_for(warps * 32, 256), 256, static_cast<cudaStream_t>(stream),
+                      static_cast<const uint4 *>(x_bf16), static_cast<uint8_t *>(xq), static_cast<int>(M),
+                      static_cast<int>(K), warps, status);
 }
 
 extern "C" int qwp_set_wait_timeout_ns(uint64_t ns) {

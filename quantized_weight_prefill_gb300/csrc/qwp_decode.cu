@@ -389,6 +389,7 @@ __global__ void __launch_bounds__(DEC_THREADS, dec_wfmt<kFmt>() == DFMT_Q4K ? 3 
     // launch makes this one skip its work; the copies started are still waited for).
     constexpr int PTHREAD = 32 * DEC_CWARPS;
     int issued = 0;
+    pdl_launch_dependents();
     if (threadIdx.x == PTHREAD) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(full + 8 * s, 1);
@@ -399,14 +400,16 @@ __global__ void __launch_bounds__(DEC_THREADS, dec_wfmt<kFmt>() == DFMT_Q4K ? 3 
         p_tile = beg / nsb;
         p_sb = beg - p_tile * nsb;
         if (n_items > 0) p_setup_tile();
-        // x may come from the grid launched just before (programmatic dependent launch).
-        asm volatile("griddepcontrol.wait;" ::: "memory");
+        // x and the weights may come from the grids launched just before.
+        pdl_wait();
         const int pre = min(min(NS, DEC_PRE), n_items);
         for (int st = 0; st < pre; ++st) issue_next(st);
         issued = pre;
     }
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
+        pdl_wait();  // (every other thread is ordered after the waits by the barrier below)
         *abort = (*reinterpret_cast<volatile uint32_t *>(args.status) & kStatusTimeoutMask) ? 1u : 0u;
+    }
     __syncthreads();
     bool ok = *reinterpret_cast<volatile uint32_t *>(abort) == 0;
 
@@ -737,8 +740,21 @@ static int launch_decode_fmt(const void *w, const void *scales, const uint8_t *z
     a.x_bf16 = x_bf16 && kFmt != DFMT_Q4K_Q8 ? 1 : 0;
     a.timeout_ns = kDefaultTimeoutNs;
 
-    qwp_decode_kernel<kFmt><<<static_cast<unsigned>(G), DEC_THREADS, L.smem, stream>>>(map, a);
-    return launch_status();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(G), 1, 1);
+    cfg.blockDim = dim3(DEC_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(L.smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, qwp_decode_kernel<kFmt>, map, a) != cudaSuccess) {
+        cudaGetLastError();
+        return QWP_ERR_CUDA;
+    }
+    return QWP_OK;
 }
 
 template <int kFmt>

@@ -263,6 +263,7 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
     // The weight producer's thread sets up the barriers and starts the first weight
     // copies of its first unit before the block-wide barrier (their slots are empty).
     const int w_pre = units0 < nunits ? min(WS, nstage) : 0;
+    pdl_launch_dependents();
     if (threadIdx.x == 64) {
         for (int s = 0; s < X_MAX_STAGES; ++s) mbar_init(x_full + 8 * s, 1);
         for (int s = 0; s < A_STAGES; ++s) mbar_init(mma_done + 8 * s, 1);
@@ -287,6 +288,10 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
         mbar_init(drain, 1);
         fence_mbar_init();
         prefetch_tensormap(&tmap_x);
+        // The weights may come from a repack launched just before, the status word
+        // from any earlier kernel; every other thread is ordered after this wait by
+        // the block-wide barrier below.
+        pdl_wait();
         for (int s = 0; s < w_pre; ++s) load_weight_stage(unit_tile(units0), s, s);
         // A failure recorded earlier (and not yet read by qwp_device_status) makes
         // every later launch skip its work instead of waiting out its own timeouts
@@ -319,9 +324,7 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
     if (warp == 0) {
         // ------------------------------------------------------------ x producer
         if (lane == 0 && !skip) {
-            // x may be written by the grid launched just before this one (the
-            // activation conversion); nothing else here depends on it.
-            asm volatile("griddepcontrol.wait;" ::: "memory");
+            pdl_wait();  // x may come from the grid launched just before (ordered already; explicit here)
             int issued = 0;     // groups issued over all units
             int xs = 0;         // ring slot (running counters: no division in the loop)
             int dk = 0;         // mma_done slot of group `issued - XS`, and its phase
@@ -748,25 +751,70 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
                 }
                 tc_fence_before();
             }
-        } else {
+        } else if (!split_mbar) {
+            // One unit per CTA: every CTA's rings are idle now (its MMAs are done and
+            // all its warps passed the barrier above), so each writes its partial
+            // tile into its own rings, [token][row]; after a cluster barrier (release
+            // / acquire) rank q sums its tokens over the ranks' shared memory in rank
+            // order and writes y; a last barrier keeps every CTA's shared memory alive
+            // until its peers have read it (a thread arrives after storing the sums
+            // of everything it read, so that arrival needs no release).
             const uint32_t rank = cluster_ctarank();
             const int per = (args.bn + S - 1) / S;
-            const int last_off = split_mbar ? 0 : args.part_off;  // this unit's partial buffer
-            const uint32_t part = smem_u32(smem + last_off);
-            if (split_mbar) {
-                if (cluster_wait_due) cluster_wait();  // (the epilogue warps waited already)
-                cluster_wait_due = false;
-            } else {
-                cluster_sync();
-            }
-            if (xf) {
-                bool push_ok = acc_ok;
-                if (split_mbar) {
-                    // This CTA's MMAs are done (or failed): its rings are idle.
-                    if (warp == FIRST_XFORM_WARP && lane == 0)
-                        for (int q = 0; q < S; ++q) mbar_arrive_remote(map_shared_rank(rings_idle, q));
-                    push_ok = __all_sync(0xffffffffu, wait_bar<true, false>(rings_idle, 0, ctl, WAIT_PART)) && push_ok;
+            float *own = reinterpret_cast<float *>(smem);
+            if (xf && acc_ok && !aborted(ctl)) {
+                tc_fence_after();
+                for (int ci = grp; ci < args.bn / 16; ci += NUM_XFORM_WARPS / 4) {
+                    uint32_t v[16];
+                    tmem_ld_x16(dcol + 16u * ci, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) own[(16 * ci + t) * TILE_ROWS + row] = __uint_as_float(v[t]);
                 }
+                tc_fence_before();
+            }
+            __syncwarp();
+            cluster_sync();
+            const int t0 = min(args.bn, static_cast<int>(rank) * per);
+            const int t1 = min(args.bn, t0 + per);
+            if (!aborted(ctl)) {
+                const uint32_t own_addr = smem_u32(own);
+                const int items = (t1 - t0) * (TILE_ROWS / 4);
+                for (int itm = threadIdx.x; itm < items; itm += NUM_THREADS) {
+                    const int tt = t0 + itm / (TILE_ROWS / 4);
+                    const int r4 = 4 * (itm % (TILE_ROWS / 4));
+                    const uint32_t off = static_cast<uint32_t>((tt * TILE_ROWS + r4) * 4);
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int q = 0; q < S; ++q) {
+                        const float4 pv = ld_shared_cluster_f4(map_shared_rank(own_addr + off, static_cast<uint32_t>(q)));
+                        acc.x += pv.x; acc.y += pv.y; acc.z += pv.z; acc.w += pv.w;
+                    }
+                    const int m = m0 + tt;
+                    if (m < args.M) {
+                        float *yr = args.y + static_cast<int64_t>(m) * args.N + static_cast<int64_t>(tile) * TILE_ROWS;
+                        const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (r4 + e < R) __stcs(yr + r4 + e, a4[e]);
+                    }
+                }
+            }
+            __syncwarp();
+            cluster_arrive_relaxed();
+            cluster_wait();
+        } else {
+            // Several units per CTA, the last one through the partial buffers at the
+            // start of the owners' rings (see above).
+            const uint32_t rank = cluster_ctarank();
+            const int per = (args.bn + S - 1) / S;
+            const uint32_t part = smem_u32(smem);
+            if (cluster_wait_due) cluster_wait();  // (the epilogue warps waited already)
+            cluster_wait_due = false;
+            if (xf) {
+                // This CTA's MMAs are done (or failed): its rings are idle.
+                if (warp == FIRST_XFORM_WARP && lane == 0)
+                    for (int q = 0; q < S; ++q) mbar_arrive_remote(map_shared_rank(rings_idle, q));
+                const bool push_ok = __all_sync(0xffffffffu, wait_bar<true, false>(rings_idle, 0, ctl, WAIT_PART)) && acc_ok;
                 if (push_ok && !aborted(ctl)) {
                     tc_fence_after();
                     for (int ci = grp; ci < args.bn / 16; ci += NUM_XFORM_WARPS / 4) {
@@ -789,27 +837,20 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
                 }
                 // Arrive even after a failure (the status word already says so), so
                 // that the owners need not wait out their own timeouts.
-                if (split_mbar) {
-                    fence_acq_rel_cluster();
-                    __syncwarp();
-                    if (lane == 0)
-                        for (int q = 0; q < S; ++q) mbar_arrive_remote(map_shared_rank(part_last, q));
-                }
+                fence_acq_rel_cluster();
+                __syncwarp();
+                if (lane == 0)
+                    for (int q = 0; q < S; ++q) mbar_arrive_remote(map_shared_rank(part_last, q));
             }
-            // With split_mbar the epilogue warps take no part: they may still be busy.
-            const bool summer = !split_mbar || warp < FIRST_EPI_WARP;
-            bool all_in = true;
-            if (split_mbar)
-                all_in = summer && __all_sync(0xffffffffu, wait_bar<true, false>(part_last, 0, ctl, WAIT_PART));
-            else
-                cluster_sync();
+            // The epilogue warps take no part: they may still be busy.
+            const bool summer = warp < FIRST_EPI_WARP;
+            const bool all_in = summer && __all_sync(0xffffffffu, wait_bar<true, false>(part_last, 0, ctl, WAIT_PART));
             const int t0 = min(args.bn, static_cast<int>(rank) * per);
             const int t1 = min(args.bn, t0 + per);
             if (summer && all_in && !aborted(ctl)) {
-                const float *pbuf = reinterpret_cast<const float *>(smem + last_off);
+                const float *pbuf = reinterpret_cast<const float *>(smem);
                 const int items = (t1 - t0) * (TILE_ROWS / 4);
-                const int nsum = split_mbar ? FIRST_EPI_WARP * 32 : NUM_THREADS;
-                for (int itm = threadIdx.x; itm < items; itm += nsum) {
+                for (int itm = threadIdx.x; itm < items; itm += FIRST_EPI_WARP * 32) {
                     const int tt = itm / (TILE_ROWS / 4);
                     const int r4 = 4 * (itm % (TILE_ROWS / 4));
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1047,13 +1088,11 @@ static int plan_gemm(int64_t M, int64_t N, int64_t K, Plan &plan, int &bn, int64
     return QWP_OK;
 }
 
-// x is fp16 [M, K].  `after_prior` launches with programmatic stream
-// serialization so the kernel's set-up and weight prefetch overlap the grid just
-// before it (the x producer waits for that grid with griddepcontrol.wait).
+// x is fp16 [M, K].  Launched with programmatic stream serialization: the
+// kernel's set-up overlaps the end of the grid before it (see pdl_wait).
 template <int kFmt>
 static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, const void *x,
-                       float *y, int64_t M, int64_t N, int64_t K, int64_t group, cudaStream_t stream,
-                       bool after_prior) {
+                       float *y, int64_t M, int64_t N, int64_t K, int64_t group, cudaStream_t stream) {
     int rc = check_device();
     if (rc) return rc;
     uint32_t *status = status_word();
@@ -1112,11 +1151,9 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
         attrs[nattr].val.clusterDim.z = plan.S;
         ++nattr;
     }
-    if (after_prior) {
-        attrs[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attrs[nattr].val.programmaticStreamSerializationAllowed = 1;
-        ++nattr;
-    }
+    attrs[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[nattr].val.programmaticStreamSerializationAllowed = 1;
+    ++nattr;
     cfg.attrs = attrs;
     cfg.numAttrs = nattr;
     const cudaError_t le = a.acc_bufs == 2 ? cudaLaunchKernelEx(&cfg, qwp_gemm_kernel<kFmt, true>, map, a)
@@ -1133,7 +1170,7 @@ int launch_q4k_prefill_fixed(const void *w, const void *x, void *x16, float *y, 
     int rc = check_device();
     if (rc) return rc;
     if ((rc = launch_bf16_to_f16(x, x16, M * K, stream))) return rc;
-    return launch_gemm<FMT_Q4K>(w, nullptr, nullptr, x16, y, M, N, K, 0, stream, true);
+    return launch_gemm<FMT_Q4K>(w, nullptr, nullptr, x16, y, M, N, K, 0, stream);
 }
 
 }  // namespace qwp
@@ -1207,7 +1244,7 @@ extern "C" int q4k_gemm_f16(const void *w_tiled, const void *x, float *y, int64_
     if (skinny_selected(DFMT_Q4K, M, N, K))
         return launch_skinny(w_tiled, x, false, y, M, N, K, static_cast<cudaStream_t>(stream));
     return launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0,
-                             static_cast<cudaStream_t>(stream), false);
+                             static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int q4k_gemm(const void *w_tiled, const void *x, float *y, int64_t M, int64_t N,
@@ -1227,7 +1264,7 @@ extern "C" int q4k_gemm(const void *w_tiled, const void *x, float *y, int64_t M,
         return QWP_ERR_CUDA;
     }
     rc = launch_bf16_to_f16(x, x16, M * K, s);
-    if (!rc) rc = launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x16, y, M, N, K, 0, s, true);
+    if (!rc) rc = launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x16, y, M, N, K, 0, s);
     if (cudaFreeAsync(x16, s) != cudaSuccess && !rc) rc = QWP_ERR_CUDA;
     return rc;
 }
@@ -1251,7 +1288,7 @@ extern "C" int q6k_gemm_f16(const void *w_tiled, const void *x, float *y, int64_
         return run_decode(DFMT_Q6K, w_tiled, nullptr, nullptr, x, false, y, M, N, K, 0,
                           static_cast<cudaStream_t>(stream));
     return launch_gemm<FMT_Q6K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0,
-                                static_cast<cudaStream_t>(stream), false);
+                                static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int q6k_gemm(const void *w_tiled, const void *x, float *y, int64_t M, int64_t N,
@@ -1270,7 +1307,7 @@ extern "C" int q6k_gemm(const void *w_tiled, const void *x, float *y, int64_t M,
         return QWP_ERR_CUDA;
     }
     rc = launch_bf16_to_f16(x, x16, M * K, s);
-    if (!rc) rc = launch_gemm<FMT_Q6K>(w_tiled, nullptr, nullptr, x16, y, M, N, K, 0, s, true);
+    if (!rc) rc = launch_gemm<FMT_Q6K>(w_tiled, nullptr, nullptr, x16, y, M, N, K, 0, s);
     if (cudaFreeAsync(x16, s) != cudaSuccess && !rc) rc = QWP_ERR_CUDA;
     return rc;
 }
@@ -1287,7 +1324,7 @@ extern "C" int w4a16_gemm(const void *wq_tiled, const void *scales, const uint8_
         return run_decode(DFMT_W4A16, wq_tiled, scales, zeros, x, false, y, M, N, K, group,
                           static_cast<cudaStream_t>(stream));
     return launch_gemm<FMT_W4A16>(wq_tiled, scales, zeros, x, y, M, N, K, group,
-                              static_cast<cudaStream_t>(stream), false);
+                              static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int w4a16_gemm_bf16(const void *wq_tiled, const void *scales, const uint8_t *zeros,
@@ -1309,7 +1346,7 @@ extern "C" int w4a16_gemm_bf16(const void *wq_tiled, const void *scales, const u
         return QWP_ERR_CUDA;
     }
     rc = launch_bf16_to_f16(x, x16, M * K, s);
-    if (!rc) rc = launch_gemm<FMT_W4A16>(wq_tiled, scales, zeros, x16, y, M, N, K, group, s, true);
+    if (!rc) rc = launch_gemm<FMT_W4A16>(wq_tiled, scales, zeros, x16, y, M, N, K, group, s);
     if (cudaFreeAsync(x16, s) != cudaSuccess && !rc) rc = QWP_ERR_CUDA;
     return rc;
 }

@@ -21,6 +21,26 @@ inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? QWP_OK : QWP_ERR_CUDA;
 }
 
+// Launches `kernel` with programmatic stream serialization (the kernel calls
+// pdl_wait before touching memory that earlier grids write or read).
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(block, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) != cudaSuccess) {
+        cudaGetLastError();
+        return QWP_ERR_CUDA;
+    }
+    return QWP_OK;
+}
+
 // Status word bits: a timeout records 0x100 | (which wait) in the low 16 bits;
 // an activation outside the fp16 range sets kStatusRangeBit.
 constexpr uint32_t kStatusTimeoutMask = 0xFFFFu;

@@ -19,6 +19,17 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
 
+// Programmatic dependent launch.  Every kernel of the library lets the grid
+// launched after it on the stream start as soon as all of its CTAs are running
+// (that grid's CTAs then take SMs as they free up and do their set-up), and
+// waits for the grids it depends on -- pdl_wait returns once they have completed
+// and their memory is visible -- before its first access to global memory that
+// another kernel may write or read.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t warp_id() {
     return __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
 }

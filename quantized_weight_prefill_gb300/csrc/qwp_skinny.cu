@@ -130,6 +130,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     const int x_pre = min(XS, nblk), w_pre = min(SK_WS, args.stages);  // copies started at set-up
     const uint32_t w_bytes = static_cast<uint32_t>(R) * Q4K_BLOCK_BYTES;
 
+    pdl_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < XS; ++s) {
             mbar_init(x_full + 8 * s, 1);
@@ -147,6 +148,9 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         mbar_init(drain, 1);
         fence_mbar_init();
         prefetch_tensormap(&tmap_x);
+        // x, the weights and the status word may come from the grids launched just
+        // before; every other thread is ordered after this wait by the barrier below.
+        pdl_wait();
         // The first x tiles and weight stages start before the block-wide barrier
         // (their slots are empty); this thread is also the x producer.
         for (int j = 0; j < x_pre; ++j) {
@@ -495,13 +499,15 @@ int launch_skinny(const void *w, const void *x, bool x_bf16, float *y, int64_t M
     cfg.blockDim = dim3(SK_THREADS, 1, 1);
     cfg.dynamicSmemBytes = SK_SMEM;
     cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = static_cast<unsigned>(S);
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, qwp_skinny_kernel, map, a) != cudaSuccess) {
         cudaGetLastError();
         return QWP_ERR_CUDA;
