@@ -9,6 +9,9 @@
  * stream-ordered pool, released in stream order after the call: the fp16 copy
  * of x taken by q4k_gemm, q6k_gemm and w4a16_gemm_bf16, and, for decode-shaped
  * calls of any GEMM entry point (see below), the decode kernel's partial sums.
+ * Every kernel of the library is launched with programmatic stream
+ * serialization and waits for the grids before it (griddepcontrol.wait) before
+ * touching memory they may write or read.
  *
  * Decode-shaped calls.  A GEMM with 1 <= M <= 8 tokens, K % 256 == 0 and at
  * least 600 (128-row tile, 256-wide super-block) items (ceil(N/128) * K/256)

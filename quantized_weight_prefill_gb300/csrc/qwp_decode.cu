@@ -52,9 +52,10 @@ constexpr int DEC_X_BYTES = DEC_TOKENS * Q4K_BLOCK * 2;  // one super-block of x
 constexpr int DEC_PART_FLOATS = DEC_CWARPS * 32 * 4;     // one float4 per consumer lane
 
 // Ring depth per format: Q4_K runs three CTAs per SM (3 slots of 23 KiB each),
-// Q6_K and W4A16 two (3 slots of 27 KiB, 4 of 20 KiB).
+// Q6_K and W4A16 two (3 slots of 27 KiB, 4 of 20 KiB), the 8-bit-activation
+// product two (4 slots of 23 KiB).
 template <int kFmt>
-__host__ __device__ constexpr int dec_stages() { return kFmt == DFMT_W4A16 ? 4 : 3; }
+__host__ __device__ constexpr int dec_stages() { return kFmt == DFMT_W4A16 || kFmt == DFMT_Q4K_Q8 ? 4 : 3; }
 
 // The weight format a kernel instance streams (the quantized-activation product
 // reads Q4_K weights).
@@ -258,55 +259,81 @@ __device__ __forceinline__ void dec_window(const uint8_t *wst, const uint8_t *xs
 }
 
 // Quantized activations: one item's share of a lane -- row rr of the tile (R rows,
-// rr clamped into it) and sub-blocks 4*half .. 4*half+3 of the super-block.  Per
-// sub-block j and token t, dot = the 32 products of the 4-bit weight codes with
-// token t's 8-bit codes (8 dp4a: the low and the high nibbles of each weight word
-// against the two words of the matching 8 codes), and
-//     acc[t] += d_t,j * (d*sc_j * dot - dmin*m_j * s_t,j),
+// rr clamped into it) and sub-blocks 4*half .. 4*half+3 of the super-block -- for
+// NT tokens.  Per sub-block j and token t the 32 products of the 4-bit weight codes
+// with token t's 8-bit codes are summed exactly with 8 dp4a, as S = 16 * dot: the
+// high nibbles are used in place (w & 0xF0F0F0F0, i.e. 16 * code) and the low ones
+// moved up by a multiply (the shift runs on the FMA pipe, the masks on the ALU
+// pipe), each against the matching word of codes of the record; then
+//     acc[t] += d_t,j * ((d*sc_j / 16) * S - dmin*m_j * s_t,j),
 // which is sum_k w_k * d_t,j * q_t,k over the sub-block (w = d*sc*q - dmin*m).
-// d*sc_j and dmin*m_j are exact in fp32; the integer dot is exact.
-__device__ __forceinline__ void q8_item(const uint8_t *wst, const uint8_t *xst, int R, int rr, int half, int M,
+// d*sc_j / 16 and dmin*m_j are exact in fp32; |S| < 2^20 converts exactly.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+template <int NT, int T0>
+__device__ __forceinline__ void q8_item(const uint8_t *wst, const uint8_t *xst, int R, int rr, int half,
                                         float (&acc)[8]) {
     const uint4 h = *reinterpret_cast<const uint4 *>(wst + Q4K_HEADER_BYTES * rr);
-    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x & 0xFFFFu)));
+    const float d16 = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x & 0xFFFFu))) * 0.0625f;
     const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x >> 16)));
+    // The row's words of sub-block 4*half (chunk 2*half, first half-plane); sub-block
+    // 4*half + jj sits jj/2 chunk planes (32*R bytes) and jj%2 half-planes (16*R) further.
+    const uint8_t *w0 = wst + Q4K_HEADER_BYTES * R + CHUNK_ROW_BYTES * R * (2 * half) + rr * 16;
+    const uint8_t *x0 = xst + T0 * Q8_TOKEN_BYTES + 128 * half;  // token T0's codes of sub-block 4*half
+    const float *dx0 = reinterpret_cast<const float *>(xst + T0 * Q8_TOKEN_BYTES + 256 + 16 * half);  // scale; sum +32 B
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
-        const int j = 4 * half + jj;
-        const uint4 wv = *reinterpret_cast<const uint4 *>(wst + Q4K_HEADER_BYTES * R + CHUNK_ROW_BYTES * R * (j >> 1) +
-                                                          ((j & 1) * R + rr) * 16);
+        const uint4 wv = *reinterpret_cast<const uint4 *>(w0 + (jj >> 1) * (CHUNK_ROW_BYTES * R) + (jj & 1) * (16 * R));
         const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-        int lo[4], hi[4];
+        uint32_t lo[4], hi[4];
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-            lo[v] = static_cast<int>(w[v] & 0x0F0F0F0Fu);         // elements 8v + (0, 4, 1, 5)
-            hi[v] = static_cast<int>((w[v] >> 4) & 0x0F0F0F0Fu);  // elements 8v + (2, 6, 3, 7)
+            lo[v] = (w[v] * 16u) & 0xF0F0F0F0u;  // 16 x elements 8v + (0, 4, 1, 5)
+            hi[v] = w[v] & 0xF0F0F0F0u;          // 16 x elements 8v + (2, 6, 3, 7)
         }
         // The 6-bit scale and min of sub-block jj (half 0) or jj + 4 (half 1).
         const uint32_t sh = 8u * jj;
         const uint32_t b_lo = h.y >> sh, b_mid = h.z >> sh, b_hi = h.w >> sh;
         const uint32_t sc = half ? ((b_hi & 15u) | ((b_lo >> 2) & 0x30u)) : (b_lo & 63u);
         const uint32_t mn = half ? (((b_hi >> 4) & 15u) | ((b_mid >> 2) & 0x30u)) : (b_mid & 63u);
-        const float dsc = d * static_cast<float>(sc), dm = dmin * static_cast<float>(mn);
+        const float dsc16 = d16 * static_cast<float>(sc), dm = dmin * static_cast<float>(mn);
 #pragma unroll
-        for (int t = 0; t < DEC_TOKENS; ++t) {
-            if (t < M) {
-                const uint8_t *xt = xst + t * Q8_TOKEN_BYTES;
-                const uint4 x0 = *reinterpret_cast<const uint4 *>(xt + 32 * j);
-                const uint4 x1 = *reinterpret_cast<const uint4 *>(xt + 32 * j + 16);
-                const float dx = reinterpret_cast<const float *>(xt + 256)[j];
-                const float sx = reinterpret_cast<const float *>(xt + 288)[j];
-                int dot = __dp4a(lo[0], static_cast<int>(x0.x), 0);
-                dot = __dp4a(hi[0], static_cast<int>(x0.y), dot);
-                dot = __dp4a(lo[1], static_cast<int>(x0.z), dot);
-                dot = __dp4a(hi[1], static_cast<int>(x0.w), dot);
-                dot = __dp4a(lo[2], static_cast<int>(x1.x), dot);
-                dot = __dp4a(hi[2], static_cast<int>(x1.y), dot);
-                dot = __dp4a(lo[3], static_cast<int>(x1.z), dot);
-                dot = __dp4a(hi[3], static_cast<int>(x1.w), dot);
-                acc[t] = fmaf(dx, fmaf(dsc, static_cast<float>(dot), -(dm * sx)), acc[t]);
-            }
+        for (int t = 0; t < NT; ++t) {
+            const uint8_t *xt = x0 + t * Q8_TOKEN_BYTES + 32 * jj;
+            const uint4 xa = *reinterpret_cast<const uint4 *>(xt);
+            const uint4 xb = *reinterpret_cast<const uint4 *>(xt + 16);
+            int s16 = dp4a_us(lo[0], xa.x, 0);
+            s16 = dp4a_us(hi[0], xa.y, s16);
+            s16 = dp4a_us(lo[1], xa.z, s16);
+            s16 = dp4a_us(hi[1], xa.w, s16);
+            s16 = dp4a_us(lo[2], xb.x, s16);
+            s16 = dp4a_us(hi[2], xb.y, s16);
+            s16 = dp4a_us(lo[3], xb.z, s16);
+            s16 = dp4a_us(hi[3], xb.w, s16);
+            const float dx = dx0[t * (Q8_TOKEN_BYTES / 4) + jj];
+            const float sx = dx0[t * (Q8_TOKEN_BYTES / 4) + 8 + jj];
+            acc[T0 + t] = fmaf(dx, fmaf(dsc16, static_cast<float>(s16), -(dm * sx)), acc[T0 + t]);
         }
+    }
+}
+
+// The token count as a compile-time 1, 2 or 4 per pass, 8 tokens in two passes
+// (the record's tokens past M are zero codes with zero scale and sum, so rounding
+// M up adds exact zeros to accumulators that are never stored; the weight words are
+// unpacked once per pass).  At two CTAs per SM (96 registers) no pass spills.
+__device__ __forceinline__ void q8_item_m(const uint8_t *wst, const uint8_t *xst, int R, int rr, int half, int M,
+                                          float (&acc)[8]) {
+    if (M == 1) {
+        q8_item<1, 0>(wst, xst, R, rr, half, acc);
+    } else if (M == 2) {
+        q8_item<2, 0>(wst, xst, R, rr, half, acc);
+    } else {
+        q8_item<4, 0>(wst, xst, R, rr, half, acc);
+        if (M > 4) q8_item<4, 4>(wst, xst, R, rr, half, acc);
     }
 }
 
@@ -318,7 +345,7 @@ __device__ __forceinline__ uint32_t item_owner(uint32_t i, uint32_t items, uint3
 }
 
 template <int kFmt>
-__global__ void __launch_bounds__(DEC_THREADS, dec_wfmt<kFmt>() == DFMT_Q4K ? 3 : 2)
+__global__ void __launch_bounds__(DEC_THREADS, kFmt == DFMT_Q4K ? 3 : 2)
     qwp_decode_kernel(const __grid_constant__ CUtensorMap tmap_x, const DecodeArgs args) {
     constexpr int NS = dec_stages<kFmt>();
     constexpr bool kQ8 = kFmt == DFMT_Q4K_Q8;
@@ -564,7 +591,7 @@ __global__ void __launch_bounds__(DEC_THREADS, dec_wfmt<kFmt>() == DFMT_Q4K ? 3 
             const uint8_t *xst = slot_x(s);
             if constexpr (kQ8) {
                 const int R = tile_rows(args.N, tile);
-                q8_item(wst, xst, R, min(qrow, R - 1), qhalf, args.M, acc8);
+                q8_item_m(wst, xst, R, min(qrow, R - 1), qhalf, args.M, acc8);
             } else {
                 if (tile != rows_tile) {
                     rows.set(tile_rows(args.N, tile), r0, r1, t, tile);
