@@ -74,6 +74,12 @@ constexpr int A_STAGES = 8;
 constexpr int BN_MAX = 256;
 constexpr int KB_PER_STAGE = 4;  // 64-wide K blocks per weight stage
 constexpr int MAX_SPLITS = 8;    // portable cluster size
+// bf16 x is converted in the kernel (no conversion kernel) for up to this many
+// tokens: the MMA warp converts the token row of each x slot right before its
+// MMAs, one 16-byte chunk per lane and group (at one token 6-16% faster than a
+// conversion kernel; at two tokens mixed; at eight, with eight chunks per lane on
+// the MMA warp's critical path, up to 44% slower).
+constexpr int CONVERT_MAX_M = 1;
 constexpr uint32_t ACC_COL = 0;
 constexpr uint32_t ACC_STRIDE = 128;  // second accumulator buffer (token tiles of <= 128)
 constexpr uint32_t A_COL = 256;
@@ -113,6 +119,7 @@ struct GemmArgs {
     int acc_bufs;           // 2 when two accumulators fit (bn <= 128), else 1
     int part_off;           // shared-memory offset of the split-K partial buffer
     int part_overlay;       // 1: one unit per CTA, the partial buffer overlays the idle rings
+    int x_convert;          // 1: x is bf16 (one token), converted to fp16 in shared memory by the MMA warp
     uint64_t timeout_cycles;  // bound on a main-loop wait, in SM clock cycles
     uint64_t drain_cycles;    // bound on a wait for the CTA's own work in flight
 };
@@ -388,6 +395,9 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
             const uint32_t x_lo0 = static_cast<uint32_t>(xdesc0), x_hi = static_cast<uint32_t>(xdesc0 >> 32);
             const uint32_t x_step = static_cast<uint32_t>(args.x_stage_bytes) >> 4;  // one x slot, descriptor units
             const uint32_t tile_desc = static_cast<uint32_t>(args.bn) * 128u >> 4;   // one x tile, descriptor units
+            const int conv_rows = min(args.bn, args.M);  // bf16 x: token rows of a tile (one token tile)
+            const int x_tile_bytes = args.bn * 128;
+            bool big = false;  // bf16 x: an activation beyond fp16's range
             int it = 0;
             for (int u = units0; ok && u < nunits; u += ustep, ++it) {
                 // The unit accumulates into buffer b once the epilogue has drained b.
@@ -401,6 +411,30 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
                     ok = __all_sync(0xffffffffu, wait_bar(x_full + 8 * xs, xph, ctl, WAIT_X_FULL) &&
                                                      wait_bar(a_full + 8 * gs, gph, ctl, WAIT_A_FULL));
                     if (!ok) break;
+                    if (args.x_convert) {
+                        // bf16 x of a few tokens: the token rows of the group's tiles (8
+                        // chunks of 8 consecutive K each; the swizzle moves whole chunks
+                        // within a row) to fp16 in place; the other rows are the copies'
+                        // zero fill, zero in fp16 too.
+                        uint8_t *slot = x_ring + xs * args.x_stage_bytes;
+                        for (int j = static_cast<int>(lane); j < (conv_rows * 8) << cbs; j += 32) {
+                            uint4 *chunk = reinterpret_cast<uint4 *>(slot + (j / (conv_rows * 8)) * x_tile_bytes) +
+                                           j % (conv_rows * 8);
+                            const uint4 v = *chunk;
+                            const uint32_t src[4] = {v.x, v.y, v.z, v.w};
+                            uint32_t dst[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float lo = __uint_as_float(src[e] << 16);
+                                const float hi = __uint_as_float(src[e] & 0xFFFF0000u);
+                                big |= !(fabsf(lo) < 65520.f) || !(fabsf(hi) < 65520.f);
+                                dst[e] = as_u32(__floats2half2_rn(lo, hi));
+                            }
+                            *chunk = make_uint4(dst[0], dst[1], dst[2], dst[3]);
+                        }
+                        fence_proxy_async_smem();  // read by the tensor core next
+                        __syncwarp();
+                    }
                     tc_fence_after();
                     const uint32_t b_lo = x_lo0 + x_step * static_cast<uint32_t>(xs);
                     const uint32_t acol = tmem + A_COL + (32u << cbs) * static_cast<uint32_t>(gs);
@@ -420,6 +454,7 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
                 if (ok && elect_one()) mma_commit(acc_full + 8 * b);
                 __syncwarp();
             }
+            if (__any_sync(0xffffffffu, big) && lane == 0) atomicOr(args.status, kStatusRangeBit);
             if (!ok && lane == 0) {
                 mma_commit(drain);
                 wait_bar(drain, 0, ctl, WAIT_DRAIN, false);
@@ -914,14 +949,14 @@ static EncodeTiledFn encode_fn() {
 }
 
 // x [M][K] 16-bit, box = 64 (K) x bn (rows), 128-byte swizzle, zero fill out of bounds.
-static int encode_x_map(CUtensorMap *map, const void *x, int64_t M, int64_t K, int bn) {
+static int encode_x_map(CUtensorMap *map, const void *x, int64_t M, int64_t K, int bn, bool bf16) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return QWP_ERR_CUDA;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(CHUNK_K), static_cast<cuuint32_t>(bn)};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                     const_cast<void *>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1088,11 +1123,13 @@ static int plan_gemm(int64_t M, int64_t N, int64_t K, Plan &plan, int &bn, int64
     return QWP_OK;
 }
 
-// x is fp16 [M, K].  Launched with programmatic stream serialization: the
-// kernel's set-up overlaps the end of the grid before it (see pdl_wait).
+// x is fp16 [M, K], or bf16 when x_bf16 (converted in shared memory by the MMA
+// warp; only for M <= CONVERT_MAX_M).  Launched with programmatic stream
+// serialization: the kernel's set-up overlaps the end of the grid before it.
 template <int kFmt>
 static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, const void *x,
-                       float *y, int64_t M, int64_t N, int64_t K, int64_t group, cudaStream_t stream) {
+                       float *y, int64_t M, int64_t N, int64_t K, int64_t group, cudaStream_t stream,
+                       bool x_bf16 = false) {
     int rc = check_device();
     if (rc) return rc;
     uint32_t *status = status_word();
@@ -1103,8 +1140,9 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     if ((rc = plan_gemm<kFmt>(M, N, K, plan, bn, units))) return rc;
     const int64_t row_tiles = (N + TILE_ROWS - 1) / TILE_ROWS;
     const int nstages = static_cast<int>((K / CHUNK_K + KB_PER_STAGE - 1) / KB_PER_STAGE);
+    if (x_bf16 && M > CONVERT_MAX_M) return QWP_ERR_UNSUPPORTED_SHAPE;
     CUtensorMap map;
-    if ((rc = encode_x_map(&map, x, M, K, bn))) return rc;
+    if ((rc = encode_x_map(&map, x, M, K, bn, x_bf16))) return rc;
 
     GemmArgs a;
     a.w = static_cast<const uint8_t *>(w);
@@ -1131,6 +1169,7 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     a.w_stages = plan.w_stages;
     a.part_off = plan.part_off;
     a.part_overlay = plan.overlay ? 1 : 0;
+    a.x_convert = x_bf16 ? 1 : 0;
     a.splits = plan.S;
     a.kb_per_split = ((nstages + plan.S - 1) / plan.S) * KB_PER_STAGE;
     a.n_units = static_cast<int>(units);
@@ -1169,6 +1208,7 @@ int launch_q4k_prefill_fixed(const void *w, const void *x, void *x16, float *y, 
                              cudaStream_t stream) {
     int rc = check_device();
     if (rc) return rc;
+    if (M <= CONVERT_MAX_M) return launch_gemm<FMT_Q4K>(w, nullptr, nullptr, x, y, M, N, K, 0, stream, true);
     if ((rc = launch_bf16_to_f16(x, x16, M * K, stream))) return rc;
     return launch_gemm<FMT_Q4K>(w, nullptr, nullptr, x16, y, M, N, K, 0, stream);
 }
@@ -1256,6 +1296,8 @@ extern "C" int q4k_gemm(const void *w_tiled, const void *x, float *y, int64_t M,
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (decode_shaped(DFMT_Q4K, M, N, K)) return run_decode(DFMT_Q4K, w_tiled, nullptr, nullptr, x, true, y, M, N, K, 0, s);
     if (skinny_selected(DFMT_Q4K, M, N, K)) return launch_skinny(w_tiled, x, true, y, M, N, K, s);
+    // One token: the kernel converts x itself (no conversion kernel, no scratch).
+    if (M <= CONVERT_MAX_M) return launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0, s, true);
     cudaMemPool_t pool;
     if ((rc = scratch_pool(&pool))) return rc;
     void *x16 = nullptr;
@@ -1299,6 +1341,8 @@ extern "C" int q6k_gemm(const void *w_tiled, const void *x, float *y, int64_t M,
     if ((rc = check_device())) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (decode_shaped(DFMT_Q6K, M, N, K)) return run_decode(DFMT_Q6K, w_tiled, nullptr, nullptr, x, true, y, M, N, K, 0, s);
+    // One token: the kernel converts x itself (no conversion kernel, no scratch).
+    if (M <= CONVERT_MAX_M) return launch_gemm<FMT_Q6K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0, s, true);
     cudaMemPool_t pool;
     if ((rc = scratch_pool(&pool))) return rc;
     void *x16 = nullptr;
@@ -1338,6 +1382,8 @@ extern "C" int w4a16_gemm_bf16(const void *wq_tiled, const void *scales, const u
     if ((rc = check_device())) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (decode_shaped(DFMT_W4A16, M, N, K)) return run_decode(DFMT_W4A16, wq_tiled, scales, zeros, x, true, y, M, N, K, group, s);
+    // One token: the kernel converts x itself (no conversion kernel, no scratch).
+    if (M <= CONVERT_MAX_M) return launch_gemm<FMT_W4A16>(wq_tiled, scales, zeros, x, y, M, N, K, group, s, true);
     cudaMemPool_t pool;
     if ((rc = scratch_pool(&pool))) return rc;
     void *x16 = nullptr;

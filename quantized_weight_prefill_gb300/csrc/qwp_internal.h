@@ -53,7 +53,8 @@ int launch_bf16_to_f16(const void *x, void *out, int64_t n, cudaStream_t stream,
                        int nzero = 0);
 
 // The prefill (tcgen05) kernel for a Q4_K product with bf16 x, whatever the decode
-// policy says, converting x into the caller's array x16 (M*K fp16 values) and
+// policy says, converting x into the caller's array x16 (M*K fp16 values; one
+// token: inside the GEMM kernel) and
 // never splitting units between CTAs, so that it allocates nothing (x, w, y
 // checked by the caller).
 int launch_q4k_prefill_fixed(const void *w, const void *x, void *x16, float *y, int64_t M, int64_t N, int64_t K,

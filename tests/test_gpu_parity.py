@@ -124,15 +124,38 @@ def test_q4k_gemm_f16_activations(M, N, K):
     check_bound(y, ref, mag, f"q4k f16 M{M} N{N} K{K}")
 
 
-def test_q4k_bf16_activation_beyond_fp16_range_is_reported():
-    """An activation that overflows fp16 is reported as QWP_ERR_RANGE, and the next call is clean."""
-    N, K, M = 128, 256, 8
+@pytest.mark.parametrize("M,N,K", [(1, 2048, 2048), (1, 40000, 1024), (1, 19456, 4096), (1, 700, 8192),
+                                   (2, 3000, 1024)])
+def test_q4k_small_m_converts_x_in_the_kernel(M, N, K):
+    """One token: bf16 x goes to the prefill kernel unconverted and its MMA warp
+    converts the token row of each x slot in shared memory (no conversion kernel),
+    also when a CTA runs several units (N = 40000) and with split-K; two tokens take
+    the conversion kernel."""
+    prev = qwp.set_decode_policy(qwp.DECODE_NEVER)
+    try:
+        assert qwp.gemm_plan("q4k", M, N, K)["kernel"] == "prefill"
+        blocks, w = _q4k_on_gpu(N, K, seed=M * 3 + N)
+        xb = synth.activations_bf16(M, K, seed=M + 9)
+        y = qwp.q4k_gemm(w, _bf16_on_gpu(xb), N).cpu().numpy()
+    finally:
+        qwp.set_decode_policy(prev)
+    ref, mag = oracle.q4k_gemm(blocks, xb, N, K)
+    check_bound(y, ref, mag, f"q4k small M{M} N{N} K{K} plan {qwp.gemm_plan('q4k', M, N, K)}")
+
+
+@pytest.mark.parametrize("M", [8, 1])
+def test_q4k_bf16_activation_beyond_fp16_range_is_reported(M):
+    """An activation that overflows fp16 is reported as QWP_ERR_RANGE, and the next
+    call is clean (8 tokens: the conversion kernel; 1 token: the GEMM kernel's own
+    conversion)."""
+    N, K = 128, 256
     blocks, w = _q4k_on_gpu(N, K, seed=31)
     xb = synth.activations_bf16(M, K, seed=32).copy()
-    xb[3, 17] = 0x4880  # bf16 262144.0, beyond fp16's largest finite value
+    r = min(3, M - 1)
+    xb[r, 17] = 0x4880  # bf16 262144.0, beyond fp16's largest finite value
     qwp.q4k_gemm(w, _bf16_on_gpu(xb), N)
     assert qwp.device_status() == -7
-    xb[3, 17] = 0x3F80  # 1.0
+    xb[r, 17] = 0x3F80  # 1.0
     y = qwp.q4k_gemm(w, _bf16_on_gpu(xb), N).cpu().numpy()
     assert qwp.device_status() == 0
     ref, mag = oracle.q4k_gemm(blocks, xb, N, K)
