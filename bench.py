@@ -306,17 +306,21 @@ def parse_gemm(spec):
     if kind in ("q4k", "q6k", "q4kq8") and len(parts) == 4:
         M, N, K = map(int, parts[1:])
         return kind, M, N, K, 0, set()
+    if kind == "q4kb" and len(parts) == 5:  # a strided batch: q4kb:B:M:N:K (B in the group slot)
+        B, M, N, K = map(int, parts[1:])
+        return kind, M, N, K, B, set()
     if kind == "w4a16" and len(parts) >= 5 and set(parts[5:]) <= {"sym", "bf16"}:
         M, N, K, g = map(int, parts[1:5])
         return kind, M, N, K, g, set(parts[5:])
-    raise ValueError(f"bad --gemm spec {spec!r}: q4k:M:N:K, q6k:M:N:K, q4kq8:M:N:K or "
+    raise ValueError(f"bad --gemm spec {spec!r}: q4k:M:N:K, q6k:M:N:K, q4kq8:M:N:K, q4kb:B:M:N:K or "
                      "w4a16:M:N:K:group[:sym][:bf16]")
 
 
 def time_gemm(spec, steps, warmup, dev):
     """Time one GEMM shape: graph replays of the library call (Q4_K, Q6_K: bf16 x;
     W4A16: fp16 x, or bf16 x with ':bf16', no zero points with ':sym'; q4kq8: the
-    activation quantization of bf16 x and the Q4_K product with it), one call per
+    activation quantization of bf16 x and the Q4_K product with it; q4kb: a strided
+    batch of B Q4_K products in one call, all counted), one call per
     input copy in the graph (weights and x both rotate; the copies together are
     larger than 2.5x L2, so every call streams its inputs from HBM), CUDA events on
     the launching stream around the timed replays.  Returns the JSON record."""
@@ -329,19 +333,23 @@ def time_gemm(spec, steps, warmup, dev):
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
     hbm, tc_burst, _, peak_kind = measured_peaks()
     kind, M, N, K, g, flags = parse_gemm(spec)
-    if kind in ("q4k", "q6k", "q4kq8"):
-        wbytes = N * K // 256 * (210 if kind == "q6k" else 144)
+    nb = g if kind == "q4kb" else 1  # problems per call
+    if kind in ("q4k", "q6k", "q4kq8", "q4kb"):
+        wbytes = nb * N * K // 256 * (210 if kind == "q6k" else 144)
     else:
         wbytes = N * K // 2 + (N * K // g) * (2 if "sym" in flags else 3)
-    xbytes = 2 * M * K
+    xbytes = 2 * M * K * nb
     copies = max(2, min(64, int(np.ceil(2.5 * l2 / (wbytes + xbytes)))))
     ws, xs = [], []
-    bf16_x = kind in ("q4k", "q6k", "q4kq8") or "bf16" in flags
+    bf16_x = kind in ("q4k", "q6k", "q4kq8", "q4kb") or "bf16" in flags
     xqs = []
     for c in range(copies):
         if kind in ("q4k", "q4kq8"):
             blocks = synth.q4k_weights(N, K, seed=100 + c)
             ws.append((qwp.q4k_repack(torch.from_numpy(blocks.reshape(-1)).to(dev), N, K),))
+        elif kind == "q4kb":
+            ws.append((torch.cat([qwp.q4k_repack(torch.from_numpy(synth.q4k_weights(N, K, seed=100 + c * nb + p)
+                                                                  .reshape(-1)).to(dev), N, K) for p in range(nb)]),))
         elif kind == "q6k":
             blocks = synth.q6k_weights(N, K, seed=100 + c)
             ws.append((qwp.q6k_repack(torch.from_numpy(blocks.reshape(-1)).to(dev), N, K),))
@@ -349,14 +357,19 @@ def time_gemm(spec, steps, warmup, dev):
             wq, sc, z = synth.w4a16_weights(N, K, g, seed=100 + c)
             ws.append((qwp.w4a16_repack(torch.from_numpy(wq.view(np.int32)).to(dev)),
                        torch.from_numpy(sc).to(dev), None if "sym" in flags else torch.from_numpy(z).to(dev)))
-        if bf16_x:
+        if kind == "q4kb":
+            xs.append(torch.from_numpy(np.ascontiguousarray(np.stack([synth.activations_bf16(M, K, seed=7 + c * nb + p)
+                                                                      for p in range(nb)])).view(np.int16))
+                      .to(dev).view(torch.bfloat16))
+        elif bf16_x:
             xs.append(torch.from_numpy(synth.activations_bf16(M, K, seed=7 + c).view(np.int16)).to(dev)
                       .view(torch.bfloat16))
         else:
             xs.append(torch.from_numpy(synth.activations_f16(M, K, seed=7 + c)).to(dev))
         if kind == "q4kq8":
             xqs.append(torch.empty(qwp.q8_activation_bytes(M, K), dtype=torch.uint8, device=dev))
-    y = torch.empty(M, N, dtype=torch.float32, device=dev)
+    y = torch.empty(nb, M, N, dtype=torch.float32, device=dev) if kind == "q4kb" else \
+        torch.empty(M, N, dtype=torch.float32, device=dev)
 
     def call(c):
         if kind == "q4k":
@@ -364,6 +377,8 @@ def time_gemm(spec, steps, warmup, dev):
         elif kind == "q4kq8":
             qwp.q8_quantize(xs[c], out=xqs[c])
             qwp.q4k_q8_gemm(ws[c][0], xqs[c], M, N, K, out=y)
+        elif kind == "q4kb":
+            qwp.q4k_gemm_batched(ws[c][0], xs[c], N, out=y)
         elif kind == "q6k":
             qwp.q6k_gemm(ws[c][0], xs[c], N, out=y)
         else:
@@ -393,17 +408,18 @@ def time_gemm(spec, steps, warmup, dev):
     if qwp.device_status() != 0:
         raise RuntimeError(f"kernel timeout in {spec}")
     t = e0.elapsed_time(e1) * 1e-3 / (reps * copies)
-    flops = 2.0 * M * N * K
-    byts = wbytes + xbytes + 4.0 * M * N
+    flops = 2.0 * M * N * K * nb
+    byts = wbytes + xbytes + 4.0 * M * N * nb
     t_tc, t_hbm = flops / (tc_burst * 1e12), byts / (hbm * 1e9)
-    plan = {"kernel": "decode (8-bit activations)"} if kind == "q4kq8" else qwp.gemm_plan(kind, M, N, K)
+    plan = ({"kernel": "decode (8-bit activations)"} if kind == "q4kq8"
+            else {"kernel": "prefill (batch of %d)" % nb} if kind == "q4kb" else qwp.gemm_plan(kind, M, N, K))
     rec = {
         "gemm": spec, "us": t * 1e6, "tflops": flops / t / 1e12,
         "pct_bf16_peak": 100.0 * flops / t / 1e12 / tc_burst,
         "gbs": byts / t / 1e9, "bound": "tensor" if t_tc >= t_hbm else "hbm",
         "roofline_us": max(t_tc, t_hbm) * 1e6, "roofline_frac": max(t_tc, t_hbm) / t,
         "peak_source": peak_kind, "calls_timed": reps * copies, "input_copies": copies,
-        "launches_per_call": 2 if kind == "q4kq8" or (bf16_x and plan.get("kernel") == "prefill") else 1,
+        "launches_per_call": 2 if kind in ("q4kq8", "q4kb") or (bf16_x and plan.get("kernel") == "prefill") else 1,
         "plan": plan,
     }
     del ws, xs, xqs, gr

@@ -149,6 +149,26 @@ QWP_API int q4k_gemm(const void *w_tiled_dev, const void *x_dev, float *y_dev,
                      int64_t M, int64_t N, int64_t K, void *stream);
 
 /*
+ * A batch of independent Q4_K products of one shape in one launch (strided
+ * batch): for p = 0 .. batch-1, y_p[M][N] = x_p[M][K] . W_p^T with W_p the
+ * repacked matrix at w_tiled_dev + p * q4k_repacked_bytes(N, K), x_p at
+ * x_dev + p*M*K elements and y_p at y_dev + p*M*N floats.  The units (128-row
+ * tile x token tile) of all problems share one persistent grid, so a batch of
+ * small products pays the launch, the pipeline fill and the tail once (the way
+ * to approach the HBM roofline with GEMMs too small to fill the GPU alone, e.g.
+ * the experts of a mixture-of-experts layer).  Same operand rounding, error
+ * bound and rules as q4k_gemm (bf16 x, converted to fp16 into pool scratch
+ * first: batch*M*K*2 bytes) and q4k_gemm_f16 (fp16 x); always the prefill kernel.
+ * The three base pointers are 16-byte aligned (QWP_ERR_MISALIGNED otherwise);
+ * problem p's y, p*M*N floats on, need not be.  batch <= 65535, batch*M*K and
+ * batch*M*N <= 2^40 (QWP_ERR_UNSUPPORTED_SHAPE otherwise); batch == 0 is a no-op.
+ */
+QWP_API int q4k_gemm_batched(const void *w_tiled_dev, const void *x_dev, float *y_dev, int64_t batch,
+                             int64_t M, int64_t N, int64_t K, void *stream);
+QWP_API int q4k_gemm_batched_f16(const void *w_tiled_dev, const void *x_dev, float *y_dev, int64_t batch,
+                                 int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
  * The largest activation q4k_gemm_noalloc accepts: M*K <= 8,388,608 values
  * (for example M <= 2048 at K = 4096, M <= 682 at K = 12288).
  */

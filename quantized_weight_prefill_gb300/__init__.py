@@ -33,6 +33,7 @@ EXPORTED_SYMBOLS = (
     "w4a16_repacked_bytes", "w4a16_repack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_bf16",
     "qwp_device_status", "qwp_set_decode_policy", "qwp_decode_selected", "qwp_gemm_plan",
     "qwp_set_wait_timeout_ns", "q8_activation_bytes", "q8_quantize", "q4k_q8_gemm",
+    "q4k_gemm_batched", "q4k_gemm_batched_f16",
 )
 
 # Decode-kernel dispatch policies (enum qwp_decode_policy in the header).
@@ -87,6 +88,8 @@ def library() -> ctypes.CDLL:
         lib.q8_activation_bytes.argtypes = [i64, i64, sz]
         lib.q8_quantize.argtypes = [p, p, i64, i64, p]
         lib.q4k_q8_gemm.argtypes = [p, p, p, i64, i64, i64, p]
+        lib.q4k_gemm_batched.argtypes = [p, p, p, i64, i64, i64, i64, p]
+        lib.q4k_gemm_batched_f16.argtypes = [p, p, p, i64, i64, i64, i64, p]
         for name in EXPORTED_SYMBOLS:
             if name != "qwp_status_string":
                 getattr(lib, name).restype = ctypes.c_int
@@ -172,6 +175,27 @@ def q4k_gemm_f16(w_tiled: torch.Tensor, x: torch.Tensor, N: int, out: torch.Tens
         out = torch.empty(M, N, dtype=torch.float32, device=x.device)
     _dev(out, torch.float32, "out")
     _check(library().q4k_gemm_f16(_ptr(w_tiled), _ptr(x), _ptr(out), M, N, K, _stream(x)), "q4k_gemm_f16")
+    return out
+
+
+def q4k_gemm_batched(w_tiled: torch.Tensor, x: torch.Tensor, N: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """A strided batch of Q4_K products in one launch: x [B, M, K] (bf16 or fp16),
+    w_tiled the B repacked matrices back to back (B * q4k_repacked_bytes(N, K) bytes),
+    y [B, M, N] fp32."""
+    _dev(w_tiled, torch.uint8, "w_tiled")
+    if x.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("x must be bfloat16 or float16")
+    _dev(x, x.dtype, "x")
+    B, M, K = x.shape
+    if w_tiled.numel() != B * q4k_repacked_bytes(N, K):
+        raise ValueError("w_tiled must hold B repacked matrices of N x K")
+    if out is None:
+        out = torch.empty(B, M, N, dtype=torch.float32, device=x.device)
+    _dev(out, torch.float32, "out")
+    if tuple(out.shape) != (B, M, N):
+        raise ValueError("out must be [B, M, N]")
+    fn = library().q4k_gemm_batched if x.dtype == torch.bfloat16 else library().q4k_gemm_batched_f16
+    _check(fn(_ptr(w_tiled), _ptr(x), _ptr(out), B, M, N, K, _stream(x)), "q4k_gemm_batched")
     return out
 
 

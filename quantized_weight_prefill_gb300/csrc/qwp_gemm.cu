@@ -120,6 +120,9 @@ struct GemmArgs {
     int part_off;           // shared-memory offset of the split-K partial buffer
     int part_overlay;       // 1: one unit per CTA, the partial buffer overlays the idle rings
     int x_convert;          // 1: x is bf16 (one token), converted to fp16 in shared memory by the MMA warp
+    int batch;              // independent problems of one shape (1: a single GEMM)
+    int units_per_problem;  // row tiles x token tiles of one problem
+    int64_t w_batch_bytes;  // bytes from one problem's weights to the next's
     uint64_t timeout_cycles;  // bound on a main-loop wait, in SM clock cycles
     uint64_t drain_cycles;    // bound on a wait for the CTA's own work in flight
 };
@@ -221,8 +224,12 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
     // Row tile and token tile of unit u: consecutive units share a token tile, so
     // concurrently running CTAs read the same activation tile (one read, L2 hits);
     // the packed weights are the smaller stream per unit.
-    auto unit_tile = [&](int u) { return u % args.row_tiles; };
-    auto unit_m0 = [&](int u) { return (u / args.row_tiles) * args.bn; };
+    // Batched calls number the units problem-major; problem p's weights, x and y
+    // sit p strides further (x through the third coordinate of its tensor map).
+    auto unit_prob = [&](int u) { return args.batch > 1 ? u / args.units_per_problem : 0; };
+    auto unit_tile = [&](int u) { return (u - unit_prob(u) * args.units_per_problem) % args.row_tiles; };
+    auto unit_m0 = [&](int u) { return ((u - unit_prob(u) * args.units_per_problem) / args.row_tiles) * args.bn; };
+    auto unit_y = [&](int u) { return args.y + static_cast<int64_t>(unit_prob(u)) * args.M * args.N; };
 
     const uint32_t bar0 = smem_u32(smem + OFF_BAR);
     // The MMA issuer works in commit groups of CB = 2^cb_shift consecutive K blocks:
@@ -246,22 +253,24 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + OFF_MISC);  // [0] tmem base, [1] abort
     const Ctl ctl{misc + 1, args.status, args.timeout_cycles, args.drain_cycles};
 
-    // Copy of weight stage s (K blocks kb_begin + 4s ..) of row tile `tile` into ring slot ws.
-    auto load_weight_stage = [&](int tile, int s, int ws) {
+    // Copy of weight stage s (K blocks kb_begin + 4s ..) of unit u's row tile into ring slot ws.
+    auto load_weight_stage = [&](int u, int s, int ws) {
+        const int tile = unit_tile(u);
+        const uint8_t *wp = args.w + static_cast<int64_t>(unit_prob(u)) * args.w_batch_bytes;
         const int R = tile_rows(args.N, tile);
         const int kb0 = kb_begin + KB_PER_STAGE * s;
         const int nblk = min(KB_PER_STAGE, kb_end - kb0);
         const uint8_t *src;
         uint32_t bytes;
         if (kQ4K) {
-            src = args.w + q4k_group_offset(args.K, tile, R, kb0 / KB_PER_STAGE);
+            src = wp + q4k_group_offset(args.K, tile, R, kb0 / KB_PER_STAGE);
             bytes = static_cast<uint32_t>(R) * Q4K_BLOCK_BYTES;
         } else if (kQ6K) {
             const int Rp = q6k_padded_rows(R);
-            src = args.w + q6k_group_offset(args.K, tile, Rp, kb0 / KB_PER_STAGE);
+            src = wp + q6k_group_offset(args.K, tile, Rp, kb0 / KB_PER_STAGE);
             bytes = static_cast<uint32_t>(Rp) * Q6K_BLOCK_BYTES;
         } else {
-            src = args.w + w4_plane_offset(args.K, tile, R, kb0);
+            src = wp + w4_plane_offset(args.K, tile, R, kb0);
             bytes = static_cast<uint32_t>(R) * CHUNK_ROW_BYTES * nblk;
         }
         mbar_arrive_expect_tx(w_full + 8 * ws, bytes);
@@ -299,7 +308,7 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
         // from any earlier kernel; every other thread is ordered after this wait by
         // the block-wide barrier below.
         pdl_wait();
-        for (int s = 0; s < w_pre; ++s) load_weight_stage(unit_tile(units0), s, s);
+        for (int s = 0; s < w_pre; ++s) load_weight_stage(units0, s, s);
         // A failure recorded earlier (and not yet read by qwp_device_status) makes
         // every later launch skip its work instead of waiting out its own timeouts
         // (the weight copies started above are still waited for).  Read after the
@@ -339,16 +348,21 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
             bool ok = true;
             const uint32_t tile_bytes = static_cast<uint32_t>(args.bn) * 128u;
             for (int u = units0; ok && u < nunits; u += ustep) {
-                const int m0 = unit_m0(u);
+                const int m0 = unit_m0(u), xp = unit_prob(u);
                 for (int g = 0; g < ngroups; ++g) {
                     if (issued >= XS) {  // slot xs last held group issued - XS
                         if (!(ok = wait_bar(mma_done + 8 * dk, dph, ctl, WAIT_X_EMPTY))) break;
                         if (++dk == dslots) { dk = 0; dph ^= 1; }
                     }
                     mbar_arrive_expect_tx(x_full + 8 * xs, tile_bytes << cbs);
-                    for (int c = 0; c < (1 << cbs); ++c)
-                        tma_load_2d(smem_u32(x_ring + xs * args.x_stage_bytes + c * tile_bytes), &tmap_x,
-                                    (kb_begin + (g << cbs) + c) * CHUNK_K, m0, x_full + 8 * xs);
+                    for (int c = 0; c < (1 << cbs); ++c) {
+                        const uint32_t dst = smem_u32(x_ring + xs * args.x_stage_bytes + c * tile_bytes);
+                        const int kc = (kb_begin + (g << cbs) + c) * CHUNK_K;
+                        if (args.batch > 1)
+                            tma_load_3d(dst, &tmap_x, kc, m0, xp, x_full + 8 * xs);
+                        else
+                            tma_load_2d(dst, &tmap_x, kc, m0, x_full + 8 * xs);
+                    }
                     ++issued;
                     if (++xs == XS) xs = 0;
                 }
@@ -371,7 +385,7 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
                 for (int s = 0; s < nstage; ++s) {
                     if (issued >= w_pre) {
                         if (issued >= WS && !(ok = wait_bar(w_empty + 8 * ws, wph ^ 1, ctl, WAIT_W_EMPTY))) break;
-                        load_weight_stage(tile, s, ws);
+                        load_weight_stage(u, s, ws);
                     }
                     ++issued;
                     if (++ws == WS) { ws = 0; wph ^= 1; }
@@ -574,7 +588,7 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
             // left step by 32 tokens.  (Stepping a pointer rather than forming each
             // address from the token index keeps this loop cheap: it runs while the
             // MMAs wait for the accumulator, 8 stores per load.)
-            float *yc = args.y + (static_cast<int64_t>(m0) + 8 * grp) * N + static_cast<int64_t>(tile) * TILE_ROWS + r;
+            float *yc = unit_y(uu) + (static_cast<int64_t>(m0) + 8 * grp) * N + static_cast<int64_t>(tile) * TILE_ROWS + r;
             const int64_t chunk_step = 8 * (NUM_XFORM_WARPS / 4) * N;
             int left = args.M - m0 - 8 * grp;
             const bool row_ok = r < R;
@@ -662,7 +676,7 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
                     if (two) tmem_ld_x16(dcol + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
                     tmem_wait_ld();
                     if (row < R) {
-                        float *yc = args.y + static_cast<int64_t>(m0 + c0) * args.N + n;
+                        float *yc = unit_y(u) + static_cast<int64_t>(m0 + c0) * args.N + n;
                         const int nt = min(two ? 32 : 16, args.M - (m0 + c0));
 #pragma unroll
                         for (int t = 0; t < 32; ++t)
@@ -720,7 +734,7 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
                     }
                     const int m = m0 + t0 + tt;
                     if (m < args.M) {
-                        float *yr = args.y + static_cast<int64_t>(m) * args.N + static_cast<int64_t>(tile) * TILE_ROWS;
+                        float *yr = unit_y(u) + static_cast<int64_t>(m) * args.N + static_cast<int64_t>(tile) * TILE_ROWS;
                         const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
@@ -781,7 +795,7 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
 #pragma unroll
                         for (int t = 0; t < 16; ++t)
                             if (mb + t < args.M)
-                                __stcs(args.y + static_cast<int64_t>(mb + t) * args.N + n, __uint_as_float(v[t]));
+                                __stcs(unit_y(lu) + static_cast<int64_t>(mb + t) * args.N + n, __uint_as_float(v[t]));
                     }
                 }
                 tc_fence_before();
@@ -826,7 +840,7 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
                     }
                     const int m = m0 + tt;
                     if (m < args.M) {
-                        float *yr = args.y + static_cast<int64_t>(m) * args.N + static_cast<int64_t>(tile) * TILE_ROWS;
+                        float *yr = unit_y(lu) + static_cast<int64_t>(m) * args.N + static_cast<int64_t>(tile) * TILE_ROWS;
                         const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
@@ -895,7 +909,7 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
                     }
                     const int m = m0 + t0 + tt;
                     if (m < args.M) {
-                        float *yr = args.y + static_cast<int64_t>(m) * args.N + static_cast<int64_t>(tile) * TILE_ROWS;
+                        float *yr = unit_y(lu) + static_cast<int64_t>(m) * args.N + static_cast<int64_t>(tile) * TILE_ROWS;
                         const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
@@ -949,14 +963,16 @@ static EncodeTiledFn encode_fn() {
 }
 
 // x [M][K] 16-bit, box = 64 (K) x bn (rows), 128-byte swizzle, zero fill out of bounds.
-static int encode_x_map(CUtensorMap *map, const void *x, int64_t M, int64_t K, int bn, bool bf16) {
+// x as [batch][M][K] (rank 2 when batch == 1), box 64 K x bn tokens.
+static int encode_x_map(CUtensorMap *map, const void *x, int64_t M, int64_t K, int bn, bool bf16, int64_t batch) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return QWP_ERR_CUDA;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(CHUNK_K), static_cast<cuuint32_t>(bn)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(M) * K * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(CHUNK_K), static_cast<cuuint32_t>(bn), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    batch > 1 ? 3 : 2,
                     const_cast<void *>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1092,7 +1108,7 @@ constexpr int weight_stage_bytes() {
 // Token tile, launch plan and unit count of an M x N x K product in format kFmt
 // on the current device (host only).
 template <int kFmt>
-static int plan_gemm(int64_t M, int64_t N, int64_t K, Plan &plan, int &bn, int64_t &units) {
+static int plan_gemm(int64_t M, int64_t N, int64_t K, Plan &plan, int &bn, int64_t &units, int64_t batch = 1) {
     DeviceInfo *info = nullptr;
     const int rc = device_info<kFmt>(info);
     if (rc) return rc;
@@ -1104,13 +1120,13 @@ static int plan_gemm(int64_t M, int64_t N, int64_t K, Plan &plan, int &bn, int64
     // which allow split-K and two accumulators, give a cheaper plan (few units).
     bn = choose_bn(M, BN_MAX);
     int64_t tok_tiles = (M + bn - 1) / bn;
-    if (row_tiles * tok_tiles > 0x7fffffff) return QWP_ERR_UNSUPPORTED_SHAPE;
-    plan = choose_plan(info->slots[kFmt], row_tiles * tok_tiles, nstages, nkb_total, bn, w_stage_bytes);
+    if (batch * row_tiles * tok_tiles > 0x7fffffff) return QWP_ERR_UNSUPPORTED_SHAPE;
+    plan = choose_plan(info->slots[kFmt], batch * row_tiles * tok_tiles, nstages, nkb_total, bn, w_stage_bytes);
     if (bn > static_cast<int>(ACC_STRIDE)) {
         const int bn2 = choose_bn(M, static_cast<int>(ACC_STRIDE));
         const int64_t tt2 = (M + bn2 - 1) / bn2;
-        if (row_tiles * tt2 <= 0x7fffffff) {
-            const Plan p2 = choose_plan(info->slots[kFmt], row_tiles * tt2, nstages, nkb_total, bn2, w_stage_bytes);
+        if (batch * row_tiles * tt2 <= 0x7fffffff) {
+            const Plan p2 = choose_plan(info->slots[kFmt], batch * row_tiles * tt2, nstages, nkb_total, bn2, w_stage_bytes);
             if (p2.cost < plan.cost - 1e-9) {
                 plan = p2;
                 bn = bn2;
@@ -1119,7 +1135,7 @@ static int plan_gemm(int64_t M, int64_t N, int64_t K, Plan &plan, int &bn, int64
         }
     }
     if (plan.clusters <= 0) return QWP_ERR_UNSUPPORTED_SHAPE;
-    units = row_tiles * tok_tiles;
+    units = row_tiles * tok_tiles;  // of one problem
     return QWP_OK;
 }
 
@@ -1129,7 +1145,7 @@ static int plan_gemm(int64_t M, int64_t N, int64_t K, Plan &plan, int &bn, int64
 template <int kFmt>
 static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, const void *x,
                        float *y, int64_t M, int64_t N, int64_t K, int64_t group, cudaStream_t stream,
-                       bool x_bf16 = false) {
+                       bool x_bf16 = false, int64_t batch = 1, int64_t w_batch_bytes = 0) {
     int rc = check_device();
     if (rc) return rc;
     uint32_t *status = status_word();
@@ -1137,12 +1153,12 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     Plan plan;
     int bn = 0;
     int64_t units = 0;
-    if ((rc = plan_gemm<kFmt>(M, N, K, plan, bn, units))) return rc;
+    if ((rc = plan_gemm<kFmt>(M, N, K, plan, bn, units, batch))) return rc;
     const int64_t row_tiles = (N + TILE_ROWS - 1) / TILE_ROWS;
     const int nstages = static_cast<int>((K / CHUNK_K + KB_PER_STAGE - 1) / KB_PER_STAGE);
     if (x_bf16 && M > CONVERT_MAX_M) return QWP_ERR_UNSUPPORTED_SHAPE;
     CUtensorMap map;
-    if ((rc = encode_x_map(&map, x, M, K, bn, x_bf16))) return rc;
+    if ((rc = encode_x_map(&map, x, M, K, bn, x_bf16, batch))) return rc;
 
     GemmArgs a;
     a.w = static_cast<const uint8_t *>(w);
@@ -1172,7 +1188,10 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     a.x_convert = x_bf16 ? 1 : 0;
     a.splits = plan.S;
     a.kb_per_split = ((nstages + plan.S - 1) / plan.S) * KB_PER_STAGE;
-    a.n_units = static_cast<int>(units);
+    a.n_units = static_cast<int>(batch * units);
+    a.batch = static_cast<int>(batch);
+    a.units_per_problem = static_cast<int>(units);
+    a.w_batch_bytes = w_batch_bytes;
     a.row_tiles = static_cast<int>(row_tiles);
     a.acc_bufs = bn <= static_cast<int>(ACC_STRIDE) ? 2 : 1;
 
@@ -1309,6 +1328,45 @@ extern "C" int q4k_gemm(const void *w_tiled, const void *x, float *y, int64_t M,
     if (!rc) rc = launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x16, y, M, N, K, 0, s);
     if (cudaFreeAsync(x16, s) != cudaSuccess && !rc) rc = QWP_ERR_CUDA;
     return rc;
+}
+
+// A batch of independent Q4_K products of one shape in one launch: problem p's
+// repacked weights at w_tiled + p*q4k_repacked_bytes(N, K), its x at x + p*M*K and
+// its y at y + p*M*N; the units of all problems share the persistent grid.
+static int q4k_batched(const void *w_tiled, const void *x, bool x_bf16, float *y, int64_t batch, int64_t M,
+                       int64_t N, int64_t K, void *stream) {
+    if (batch < 0 || M < 0 || N < 0 || K < 0) return QWP_ERR_INVALID_ARG;
+    if (K % Q4K_BLOCK || K == 0) return QWP_ERR_UNSUPPORTED_SHAPE;
+    if (batch == 0) return QWP_OK;
+    int rc = gemm_shape_checks(w_tiled, x, y, M, N, K);
+    if (rc || M == 0 || N == 0) return rc;
+    if (batch > 65535 || batch * M * K > (int64_t(1) << 40) || batch * M * N > (int64_t(1) << 40))
+        return QWP_ERR_UNSUPPORTED_SHAPE;
+    if ((rc = check_device())) return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t wbytes = N * (K / Q4K_BLOCK) * Q4K_BLOCK_BYTES;
+    if (!x_bf16) return launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0, s, false, batch, wbytes);
+    cudaMemPool_t pool;
+    if ((rc = scratch_pool(&pool))) return rc;
+    void *x16 = nullptr;
+    if (cudaMallocFromPoolAsync(&x16, static_cast<size_t>(batch * M * K) * 2, pool, s) != cudaSuccess) {
+        cudaGetLastError();
+        return QWP_ERR_CUDA;
+    }
+    rc = launch_bf16_to_f16(x, x16, batch * M * K, s);
+    if (!rc) rc = launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x16, y, M, N, K, 0, s, false, batch, wbytes);
+    if (cudaFreeAsync(x16, s) != cudaSuccess && !rc) rc = QWP_ERR_CUDA;
+    return rc;
+}
+
+extern "C" int q4k_gemm_batched(const void *w_tiled, const void *x, float *y, int64_t batch, int64_t M, int64_t N,
+                                int64_t K, void *stream) {
+    return q4k_batched(w_tiled, x, true, y, batch, M, N, K, stream);
+}
+
+extern "C" int q4k_gemm_batched_f16(const void *w_tiled, const void *x, float *y, int64_t batch, int64_t M,
+                                    int64_t N, int64_t K, void *stream) {
+    return q4k_batched(w_tiled, x, false, y, batch, M, N, K, stream);
 }
 
 extern "C" int q4k_q8_gemm(const void *w_tiled, const void *xq, float *y, int64_t M, int64_t N, int64_t K,

@@ -123,6 +123,14 @@ def test_gemm_argument_checks_before_any_cuda_call(lib):
     assert lib.q4k_q8_gemm(None, a16, a16, 8, 8, 256, None) == INVALID
     assert lib.q4k_q8_gemm(a16, _p(0x1008), a16, 8, 8, 256, None) == MISALIGNED
     assert lib.q4k_q8_gemm(None, None, None, 0, 8, 256, None) == OK
+    # batched
+    assert lib.q4k_gemm_batched(a16, a16, a16, -1, 8, 8, 256, None) == INVALID
+    assert lib.q4k_gemm_batched(a16, a16, a16, 2, 8, 8, 100, None) == SHAPE
+    assert lib.q4k_gemm_batched(a16, a16, a16, 70000, 8, 8, 256, None) == SHAPE
+    assert lib.q4k_gemm_batched(None, a16, a16, 2, 8, 8, 256, None) == INVALID
+    assert lib.q4k_gemm_batched_f16(a16, _p(0x1008), a16, 2, 8, 8, 256, None) == MISALIGNED
+    assert lib.q4k_gemm_batched(None, None, None, 0, 8, 8, 256, None) == OK
+    assert lib.q4k_gemm_batched_f16(None, None, None, 3, 0, 8, 256, None) == OK
 
 
 def test_decode_policy_round_trip_and_automatic_rule(lib):
