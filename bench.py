@@ -442,6 +442,8 @@ def run_gemms(args, specs):
 # target on the largest projection, and the two HBM-bound targets (M<=32, skinny N).
 TARGETS = (("gate_up_m2048", "q4k:2048:24576:4096", "tensor >= 0.60 of bf16 dense peak"),
            ("q4k_m32_n2048_k2048", "q4k:32:2048:2048", "HBM roofline >= 0.70"),
+           ("q4k_m32_n2048_k2048_batch32", "q4kb:32:32:2048:2048",
+            "HBM roofline >= 0.70 (32 independent products of that shape in one launch)"),
            ("skinny_n32_m4096_k4096", "q4k:4096:32:4096", "HBM roofline >= 0.70"),
            ("decode_m1_n152064_k4096", "q4k:1:152064:4096", "HBM roofline >= 0.70"),
            ("decode_q8_m1_n152064_k4096", "q4kq8:1:152064:4096", "HBM roofline >= 0.70 (8-bit activations)"))
