@@ -85,6 +85,13 @@ constexpr uint32_t ACC_STRIDE = 128;  // second accumulator buffer (token tiles 
 constexpr uint32_t A_COL = 256;
 constexpr uint32_t TMEM_COLS = 512;
 
+// Split-K: tokens of a unit owned by each of S cluster ranks, a multiple of 4.
+// Partial sums travel between ranks as quads (4 consecutive tokens of one row,
+// 16 bytes): a partial buffer holds, per source rank q, the owner's `per` tokens
+// quad-major, float index ((q*per + t) / 4) * 4*TILE_ROWS + 4*row + t % 4, so a
+// warp's 32 rows write and read 512 contiguous bytes per quad.
+__host__ __device__ constexpr int split_per(int bn, int S) { return ((bn + S - 1) / S + 3) & ~3; }
+
 // Shared memory: a ring region (x slots, then weight stages, then, with split-K,
 // the buffer that receives the cluster's partial sums), then mbarriers and misc words.
 constexpr int RING_BYTES = 224 * 1024;
@@ -192,10 +199,45 @@ __device__ __forceinline__ void unpack_q6k_quarter(uint4 wv, uint32_t h0, uint32
     for (int e = 0; e < 4; ++e) regs[off + 12 + e] = p[e];
 }
 
+// Split-K: y for the quad (tokens m .. m+3, row `row` of row tile `tile`), tokens
+// at or beyond M and rows at or beyond R left out.  A warp's 32 consecutive rows
+// write 128 contiguous bytes per token.
+__device__ __forceinline__ void store_quad(float *y, float4 acc, int m, int tile, int row, int R, int M,
+                                           int64_t N) {
+    if (row >= R) return;
+    float *yc = y + static_cast<int64_t>(m) * N + static_cast<int64_t>(tile) * TILE_ROWS + row;
+    const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        if (m + e < M) __stcs(yc + e * N, a4[e]);
+}
+
+// Split-K: an owner's sum of its tokens [t0, t1) of the tile over the S source
+// regions of its partial buffer (quad-major, see split_per), in rank order, to y.
+// Threads first, first + stride, .. take (quad, row) items, rows fastest.
+__device__ __forceinline__ void reduce_quads(const float4 *pbuf, int S, int per, int t0, int t1, int first,
+                                             int stride, float *y, int m0, int tile, int R, int M, int64_t N) {
+    const int items = (t1 - t0) / 4 * TILE_ROWS;
+    for (int itm = first; itm < items; itm += stride) {
+        const int qd = itm / TILE_ROWS, rr = itm % TILE_ROWS;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < S; ++q) {
+            const float4 pv = pbuf[(q * (per / 4) + qd) * TILE_ROWS + rr];
+            acc.x += pv.x; acc.y += pv.y; acc.z += pv.z; acc.w += pv.w;
+        }
+        store_quad(y, acc, m0 + t0 + 4 * qd, tile, rr, R, M, N);
+    }
+}
+
 // kTwoAcc: token tiles of at most 128, two accumulators, split-K allowed, 23
 // warps; else one accumulator, no split-K and no epilogue warps (the two are
 // compiled apart, so that neither carries the other's code and registers).
-template <int kFmt, bool kTwoAcc>
+// kBatch: a strided batch of problems (x through a rank-3 tensor map); compiled
+// apart too, since the per-unit problem offsets cost single GEMMs ~1 us.
+// kMulti: a CTA may run several units (else at most one: no epilogue-warp loop
+// and no split-K buffer of its own are compiled in; the launches of one unit per
+// CTA measured up to 0.5 us slower with that code present).
+template <int kFmt, bool kTwoAcc, bool kBatch = false, bool kMulti = true>
 __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
     qwp_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmArgs args) {
     constexpr bool kQ4K = kFmt == FMT_Q4K;
@@ -226,7 +268,7 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
     // the packed weights are the smaller stream per unit.
     // Batched calls number the units problem-major; problem p's weights, x and y
     // sit p strides further (x through the third coordinate of its tensor map).
-    auto unit_prob = [&](int u) { return args.batch > 1 ? u / args.units_per_problem : 0; };
+    auto unit_prob = [&](int u) { return kBatch ? u / args.units_per_problem : 0; };
     auto unit_tile = [&](int u) { return (u - unit_prob(u) * args.units_per_problem) % args.row_tiles; };
     auto unit_m0 = [&](int u) { return ((u - unit_prob(u) * args.units_per_problem) / args.row_tiles) * args.bn; };
     auto unit_y = [&](int u) { return args.y + static_cast<int64_t>(unit_prob(u)) * args.M * args.N; };
@@ -327,7 +369,7 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
     // here and waits once, just before its first remote access (epilogue warps) or
     // at the last unit (the others).  (With the buffer overlaying the rings, the
     // last unit is reduced between two cluster barriers instead.)
-    const bool split_mbar = S > 1 && !args.part_overlay;
+    const bool split_mbar = kMulti && S > 1 && !args.part_overlay;
     if (split_mbar) cluster_arrive_relaxed();
     // This thread has arrived on the cluster barrier above and not yet waited on it
     // (the epilogue warps wait at their start, the others at the last unit).
@@ -358,7 +400,7 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
                     for (int c = 0; c < (1 << cbs); ++c) {
                         const uint32_t dst = smem_u32(x_ring + xs * args.x_stage_bytes + c * tile_bytes);
                         const int kc = (kb_begin + (g << cbs) + c) * CHUNK_K;
-                        if (args.batch > 1)
+                        if (kBatch)
                             tma_load_3d(dst, &tmap_x, kc, m0, xp, x_full + 8 * xs);
                         else
                             tma_load_2d(dst, &tmap_x, kc, m0, x_full + 8 * xs);
@@ -651,14 +693,14 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
         const int row = static_cast<int>(quarter * 32 + lane);
         const uint32_t lane_base = (quarter * 32u) << 16;
         const uint32_t rank = S > 1 ? cluster_ctarank() : 0u;
-        const int per = (args.bn + S - 1) / S;  // tokens owned by each cluster rank
+        const int per = split_per(args.bn, S);  // tokens owned by each cluster rank
         const uint32_t part = smem_u32(smem + args.part_off);
         // Two accumulators: these warps finish every unit but the CTA's last one
         // (which all transform warps finish together after the main loop).
         if (split_mbar) cluster_wait();
         bool ok = !skip && nbufs == 2;
         int it = 0;
-        for (int u = units0; ok && u + ustep < nunits; u += ustep, ++it) {
+        for (int u = units0; kMulti && ok && u + ustep < nunits; u += ustep, ++it) {
             const int tile = unit_tile(u), m0 = unit_m0(u);
             const int R = tile_rows(args.N, tile);
             const int b = nbufs == 2 ? (it & 1) : 0;
@@ -689,25 +731,29 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
             } else {
                 // Split-K through distributed shared memory.  Rank q owns tokens
                 // [q*per, q*per + per) of the tile.  Each CTA pushes its partial for
-                // every token into the owner's buffer [source rank][token][row] once the
-                // owners have consumed the previous unit (part_free), then tells the
-                // owners (part_full); each owner sums its tokens over the source ranks
-                // in rank order (deterministic) and writes y.
+                // every token, quad by quad, into the owner's buffer (source rank
+                // `rank`'s region, see split_per) once the owners have consumed the
+                // previous unit (part_free), then tells the owners (part_full); each
+                // owner sums its tokens over the source ranks in rank order
+                // (deterministic) and writes y.
                 if (it > 0 && !(ok = __all_sync(0xffffffffu, wait_bar_cluster(part_free, (it - 1) & 1, ctl, WAIT_PART))))
                     break;
+                int owner = 0, tt = 0;  // owner rank of the next quad, and its first token there
+                uint32_t dst = map_shared_rank(part, 0) +
+                               static_cast<uint32_t>(((static_cast<int>(rank) * per) / 4 * TILE_ROWS + row) * 16);
                 for (int c0 = 0; c0 < args.bn; c0 += 16) {
                     uint32_t v[16];
                     tmem_ld_x16(dcol + c0, v);
                     tmem_wait_ld();
-                    int owner = c0 / per, tt = c0 - owner * per;
-                    uint32_t dst = map_shared_rank(part, owner);
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        st_shared_cluster_f32(dst + static_cast<uint32_t>(((static_cast<int>(rank) * per + tt) * TILE_ROWS + row) * 4),
-                                              __uint_as_float(v[t]));
-                        if (++tt == per && t < 15) {
+                    for (int j = 0; j < 4; ++j) {
+                        st_shared_cluster_f32x4(dst, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        dst += TILE_ROWS * 16;
+                        if ((tt += 4) == per) {  // the next quad belongs to the next rank (if any)
                             tt = 0;
-                            dst = map_shared_rank(part, ++owner);
+                            if (++owner < S)
+                                dst = map_shared_rank(part, owner) +
+                                      static_cast<uint32_t>(((static_cast<int>(rank) * per) / 4 * TILE_ROWS + row) * 16);
                         }
                     }
                 }
@@ -721,26 +767,9 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
                 if (!(ok = __all_sync(0xffffffffu, wait_bar_cluster(part_full, it & 1, ctl, WAIT_PART)))) break;
                 const int t0 = min(args.bn, static_cast<int>(rank) * per);
                 const int t1 = min(args.bn, t0 + per);
-                const float *pbuf = reinterpret_cast<const float *>(smem + args.part_off);
-                const int items = (t1 - t0) * (TILE_ROWS / 4);
-                const int et = static_cast<int>((warp - FIRST_EPI_WARP) * 32 + lane);
-                for (int itm = et; itm < items; itm += NUM_EPI_WARPS * 32) {
-                    const int tt = itm / (TILE_ROWS / 4);
-                    const int r4 = 4 * (itm % (TILE_ROWS / 4));
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int q = 0; q < S; ++q) {
-                        const float4 pv = *reinterpret_cast<const float4 *>(pbuf + (q * per + tt) * TILE_ROWS + r4);
-                        acc.x += pv.x; acc.y += pv.y; acc.z += pv.z; acc.w += pv.w;
-                    }
-                    const int m = m0 + t0 + tt;
-                    if (m < args.M) {
-                        float *yr = unit_y(u) + static_cast<int64_t>(m) * args.N + static_cast<int64_t>(tile) * TILE_ROWS;
-                        const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (r4 + e < R) __stcs(yr + r4 + e, a4[e]);
-                    }
-                }
+                reduce_quads(reinterpret_cast<const float4 *>(smem + args.part_off), S, per, t0, t1,
+                             static_cast<int>((warp - FIRST_EPI_WARP) * 32 + lane), NUM_EPI_WARPS * 32,
+                             unit_y(u), m0, tile, R, args.M, args.N);
                 // The buffer may be refilled once every epilogue warp here has read it.
                 fence_acq_rel_cluster();
                 __syncwarp();
@@ -855,7 +884,7 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
             // Several units per CTA, the last one through the partial buffers at the
             // start of the owners' rings (see above).
             const uint32_t rank = cluster_ctarank();
-            const int per = (args.bn + S - 1) / S;
+            const int per = split_per(args.bn, S);
             const uint32_t part = smem_u32(smem);
             if (cluster_wait_due) cluster_wait();  // (the epilogue warps waited already)
             cluster_wait_due = false;
@@ -866,21 +895,18 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
                 const bool push_ok = __all_sync(0xffffffffu, wait_bar<true, false>(rings_idle, 0, ctl, WAIT_PART)) && acc_ok;
                 if (push_ok && !aborted(ctl)) {
                     tc_fence_after();
-                    for (int ci = grp; ci < args.bn / 16; ci += NUM_XFORM_WARPS / 4) {
-                        uint32_t v[16];
-                        tmem_ld_x16(dcol + 16u * ci, v);
+                    // Quad Q (tokens 4Q .. 4Q+3) goes to the rank owning it; this
+                    // warp's quads are grp, grp + 4, .. (16 tokens apart).
+                    int owner = (4 * grp) / per, tt = 4 * grp - owner * per;
+                    for (int Q = grp; Q < args.bn / 4; Q += NUM_XFORM_WARPS / 4) {
+                        uint32_t v[4];
+                        tmem_ld_x4(dcol + 4u * Q, v);
                         tmem_wait_ld();
-                        int owner = (16 * ci) / per, tt = 16 * ci - owner * per;
-                        uint32_t dst = map_shared_rank(part, owner);
-#pragma unroll
-                        for (int t = 0; t < 16; ++t) {
-                            st_shared_cluster_f32(dst + static_cast<uint32_t>(((static_cast<int>(rank) * per + tt) * TILE_ROWS + row) * 4),
-                                                  __uint_as_float(v[t]));
-                            if (++tt == per && t < 15) {
-                                tt = 0;
-                                dst = map_shared_rank(part, ++owner);
-                            }
-                        }
+                        st_shared_cluster_f32x4(
+                            map_shared_rank(part, owner) +
+                                static_cast<uint32_t>((((static_cast<int>(rank) * per + tt) / 4) * TILE_ROWS + row) * 16),
+                            v[0], v[1], v[2], v[3]);
+                        for (tt += 16; tt >= per && owner + 1 < S; tt -= per) ++owner;
                     }
                     tc_fence_before();
                 }
@@ -896,27 +922,9 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
             const bool all_in = summer && __all_sync(0xffffffffu, wait_bar<true, false>(part_last, 0, ctl, WAIT_PART));
             const int t0 = min(args.bn, static_cast<int>(rank) * per);
             const int t1 = min(args.bn, t0 + per);
-            if (summer && all_in && !aborted(ctl)) {
-                const float *pbuf = reinterpret_cast<const float *>(smem);
-                const int items = (t1 - t0) * (TILE_ROWS / 4);
-                for (int itm = threadIdx.x; itm < items; itm += FIRST_EPI_WARP * 32) {
-                    const int tt = itm / (TILE_ROWS / 4);
-                    const int r4 = 4 * (itm % (TILE_ROWS / 4));
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int q = 0; q < S; ++q) {
-                        const float4 pv = *reinterpret_cast<const float4 *>(pbuf + (q * per + tt) * TILE_ROWS + r4);
-                        acc.x += pv.x; acc.y += pv.y; acc.z += pv.z; acc.w += pv.w;
-                    }
-                    const int m = m0 + t0 + tt;
-                    if (m < args.M) {
-                        float *yr = unit_y(lu) + static_cast<int64_t>(m) * args.N + static_cast<int64_t>(tile) * TILE_ROWS;
-                        const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (r4 + e < R) __stcs(yr + r4 + e, a4[e]);
-                    }
-                }
-            }
+            if (summer && all_in && !aborted(ctl))
+                reduce_quads(reinterpret_cast<const float4 *>(smem), S, per, t0, t1, static_cast<int>(threadIdx.x),
+                             FIRST_EPI_WARP * 32, unit_y(lu), m0, tile, R, args.M, args.N);
         }
     }
     // With split-K, no CTA of the cluster leaves before every peer is done with
@@ -992,6 +1000,28 @@ struct DeviceInfo {
     bool ready[NUM_FMTS] = {};
 };
 
+// The kernel instances of one format and batch mode: lift their dynamic
+// shared-memory limit to SMEM_BYTES (non-zero on failure).
+template <int kFmt, bool kBatch>
+static int allow_smem() {
+    const auto lift = [](const void *k) {
+        return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess;
+    };
+    return lift(reinterpret_cast<const void *>(qwp_gemm_kernel<kFmt, true, kBatch, true>)) ||
+           lift(reinterpret_cast<const void *>(qwp_gemm_kernel<kFmt, true, kBatch, false>)) ||
+           lift(reinterpret_cast<const void *>(qwp_gemm_kernel<kFmt, false, kBatch, true>));
+}
+
+// Launch of the instance for a plan: two accumulators or one, several units per
+// CTA or at most one.
+template <int kFmt, bool kBatch>
+static cudaError_t launch_instance(const cudaLaunchConfig_t &cfg, const CUtensorMap &map, const GemmArgs &a,
+                                   bool multi) {
+    if (a.acc_bufs != 2) return cudaLaunchKernelEx(&cfg, qwp_gemm_kernel<kFmt, false, kBatch, true>, map, a);
+    return multi ? cudaLaunchKernelEx(&cfg, qwp_gemm_kernel<kFmt, true, kBatch, true>, map, a)
+                 : cudaLaunchKernelEx(&cfg, qwp_gemm_kernel<kFmt, true, kBatch, false>, map, a);
+}
+
 template <int kFmt>
 static int device_info(DeviceInfo *&out) {
     static DeviceInfo info[64];
@@ -1003,11 +1033,9 @@ static int device_info(DeviceInfo *&out) {
     if (!d.ready[kFmt]) {
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return QWP_ERR_CUDA;
-        if (cudaFuncSetAttribute(qwp_gemm_kernel<kFmt, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES) != cudaSuccess ||
-            cudaFuncSetAttribute(qwp_gemm_kernel<kFmt, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES) != cudaSuccess)
-            return QWP_ERR_CUDA;
+        if (allow_smem<kFmt, false>()) return QWP_ERR_CUDA;
+        if constexpr (kFmt == FMT_Q4K)  // the strided-batch kernels (same resources, same slots)
+            if (allow_smem<kFmt, true>()) return QWP_ERR_CUDA;
         d.slots[kFmt][1] = d.sms;
         for (int S = 2; S <= MAX_SPLITS; ++S) {
             cudaLaunchConfig_t cfg = {};
@@ -1050,8 +1078,7 @@ static bool layout(int bn, int S, int cbs, int w_stage_bytes, bool reserve, Plan
     const int x_stage = (bn * 128) << cbs;
     int avail = RING_BYTES;
     if (S > 1 && reserve) {
-        const int per = (bn + S - 1) / S;
-        const int part_bytes = S * per * TILE_ROWS * 4;
+        const int part_bytes = S * split_per(bn, S) * TILE_ROWS * 4;
         avail = (RING_BYTES - part_bytes) & ~1023;
     }
     // Keep room for 4 weight stages if the x ring still gets 2 slots, else for 2.
@@ -1214,8 +1241,15 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     ++nattr;
     cfg.attrs = attrs;
     cfg.numAttrs = nattr;
-    const cudaError_t le = a.acc_bufs == 2 ? cudaLaunchKernelEx(&cfg, qwp_gemm_kernel<kFmt, true>, map, a)
-                                           : cudaLaunchKernelEx(&cfg, qwp_gemm_kernel<kFmt, false>, map, a);
+    // Several units per CTA when the units outnumber the clusters.
+    const bool multi = static_cast<int64_t>(a.n_units) > static_cast<int64_t>(plan.clusters);
+    cudaError_t le;
+    if constexpr (kFmt == FMT_Q4K) {
+        le = batch > 1 ? launch_instance<kFmt, true>(cfg, map, a, multi) : launch_instance<kFmt, false>(cfg, map, a, multi);
+    } else {
+        if (batch > 1) return QWP_ERR_UNSUPPORTED_SHAPE;  // strided batches are Q4_K only
+        le = launch_instance<kFmt, false>(cfg, map, a, multi);
+    }
     if (le != cudaSuccess) {
         cudaGetLastError();
         return QWP_ERR_CUDA;

@@ -249,6 +249,14 @@ __device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t *r) {
                  : "memory");
 }
 
+// Each thread of the warp loads 4 consecutive 32-bit columns of its own lane.
+__device__ __forceinline__ void tmem_ld_x4(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr)
+                 : "memory");
+}
+
 // Each thread of the warp loads 8 consecutive 32-bit columns of its own lane.
 __device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, uint32_t (&r)[8]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
