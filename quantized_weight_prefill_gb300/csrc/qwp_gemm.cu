@@ -96,7 +96,7 @@ __host__ __device__ constexpr int split_per(int bn, int S) { return ((bn + S - 1
 // the buffer that receives the cluster's partial sums), then mbarriers and misc words.
 constexpr int RING_BYTES = 224 * 1024;
 constexpr int OFF_BAR = RING_BYTES;
-constexpr int NUM_BARS = X_MAX_STAGES + 2 * W_MAX_STAGES + 2 * A_STAGES + 4 + 5;
+constexpr int NUM_BARS = 2 * X_MAX_STAGES + 2 * W_MAX_STAGES + 2 * A_STAGES + 4 + 5;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -126,7 +126,8 @@ struct GemmArgs {
     int acc_bufs;           // 2 when two accumulators fit (bn <= 128), else 1
     int part_off;           // shared-memory offset of the split-K partial buffer
     int part_overlay;       // 1: one unit per CTA, the partial buffer overlays the idle rings
-    int x_convert;          // 1: x is bf16 (one token), converted to fp16 in shared memory by the MMA warp
+    int x_convert;          // x is bf16, converted to fp16 in shared memory: 1 by the MMA warp (one
+                            // token), 2 by the epilogue warps (one unit per CTA); 0: x is fp16
     int batch;              // independent problems of one shape (1: a single GEMM)
     int units_per_problem;  // row tiles x token tiles of one problem
     int64_t w_batch_bytes;  // bytes from one problem's weights to the next's
@@ -292,6 +293,7 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
     const uint32_t a_full = w_empty + 8 * W_MAX_STAGES, acc_full = a_full + 8 * A_STAGES;
     const uint32_t acc_empty = acc_full + 16, part_full = acc_empty + 16, part_free = part_full + 8;
     const uint32_t part_last = part_free + 8, drain = part_last + 8, rings_idle = drain + 8;
+    const uint32_t x_conv = rings_idle + 8;  // x slot converted to fp16 (x_convert == 2)
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + OFF_MISC);  // [0] tmem base, [1] abort
     const Ctl ctl{misc + 1, args.status, args.timeout_cycles, args.drain_cycles};
 
@@ -323,7 +325,10 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
     const int w_pre = units0 < nunits ? min(WS, nstage) : 0;
     pdl_launch_dependents();
     if (threadIdx.x == 64) {
-        for (int s = 0; s < X_MAX_STAGES; ++s) mbar_init(x_full + 8 * s, 1);
+        for (int s = 0; s < X_MAX_STAGES; ++s) {
+            mbar_init(x_full + 8 * s, 1);
+            mbar_init(x_conv + 8 * s, NUM_EPI_WARPS);
+        }
         for (int s = 0; s < A_STAGES; ++s) mbar_init(mma_done + 8 * s, 1);
         for (int s = 0; s < W_MAX_STAGES; ++s) {
             mbar_init(w_full + 8 * s, 1);
@@ -464,10 +469,11 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
                 tc_fence_after();
                 const uint32_t dcol = tmem + ACC_COL + ACC_STRIDE * static_cast<uint32_t>(b);
                 for (int g = 0; g < ngroups; ++g) {
-                    ok = __all_sync(0xffffffffu, wait_bar(x_full + 8 * xs, xph, ctl, WAIT_X_FULL) &&
+                    ok = __all_sync(0xffffffffu, wait_bar((!kMulti && args.x_convert == 2 ? x_conv : x_full) + 8 * xs, xph, ctl,
+                                                              WAIT_X_FULL) &&
                                                      wait_bar(a_full + 8 * gs, gph, ctl, WAIT_A_FULL));
                     if (!ok) break;
-                    if (args.x_convert) {
+                    if (args.x_convert == 1) {
                         // bf16 x of a few tokens: the token rows of the group's tiles (8
                         // chunks of 8 consecutive K each; the swizzle moves whole chunks
                         // within a row) to fp16 in place; the other rows are the copies'
@@ -695,6 +701,48 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
         const uint32_t rank = S > 1 ? cluster_ctarank() : 0u;
         const int per = split_per(args.bn, S);  // tokens owned by each cluster rank
         const uint32_t part = smem_u32(smem + args.part_off);
+        // One unit per CTA and bf16 x: until the accumulator is complete these warps
+        // have nothing else to do, so they convert every x slot to fp16 in place
+        // as it lands (round to nearest, the range bit of the status word set on an
+        // overflow, as the conversion kernel does), then hand it to the MMA warp.
+        // Only the token rows of a tile are converted; the other rows are the
+        // copies' zero fill, zero in fp16 too.
+        if constexpr (!kMulti) {
+            if (args.x_convert == 2 && !skip) {
+                const int et = static_cast<int>((warp - FIRST_EPI_WARP) * 32 + lane);
+                const int x_tile_bytes = args.bn * 128;
+                bool big = false, cok = true;
+                int xs = 0;
+                uint32_t xph = 0;
+                for (int u = units0; cok && u < nunits; u += ustep) {
+                    const int rows = min(args.bn, args.M - unit_m0(u));  // token rows of this unit's tiles
+                    const int chunks = (rows * 8) << cbs;                // 16-byte chunks of a slot's token rows
+                    for (int g = 0; g < ngroups; ++g) {
+                        if (!(cok = __all_sync(0xffffffffu, wait_bar(x_full + 8 * xs, xph, ctl, WAIT_X_FULL)))) break;
+                        uint8_t *slot = x_ring + xs * args.x_stage_bytes;
+                        for (int j = et; j < chunks; j += NUM_EPI_WARPS * 32) {
+                            uint4 *chunk = reinterpret_cast<uint4 *>(slot + (j / (rows * 8)) * x_tile_bytes) + j % (rows * 8);
+                            const uint4 v = *chunk;
+                            const uint32_t src[4] = {v.x, v.y, v.z, v.w};
+                            uint32_t dst[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float lo = __uint_as_float(src[e] << 16);
+                                const float hi = __uint_as_float(src[e] & 0xFFFF0000u);
+                                big |= !(fabsf(lo) < 65520.f) || !(fabsf(hi) < 65520.f);
+                                dst[e] = as_u32(__floats2half2_rn(lo, hi));
+                            }
+                            *chunk = make_uint4(dst[0], dst[1], dst[2], dst[3]);
+                        }
+                        fence_proxy_async_smem();  // read by the tensor core next
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(x_conv + 8 * xs);
+                        if (++xs == args.x_stages) { xs = 0; xph ^= 1; }
+                    }
+                }
+                if (__any_sync(0xffffffffu, big) && lane == 0) atomicOr(args.status, kStatusRangeBit);
+            }
+        }
         // Two accumulators: these warps finish every unit but the CTA's last one
         // (which all transform warps finish together after the main loop).
         if (split_mbar) cluster_wait();
@@ -1166,9 +1214,38 @@ static int plan_gemm(int64_t M, int64_t N, int64_t K, Plan &plan, int &bn, int64
     return QWP_OK;
 }
 
-// x is fp16 [M, K], or bf16 when x_bf16 (converted in shared memory by the MMA
-// warp; only for M <= CONVERT_MAX_M).  Launched with programmatic stream
-// serialization: the kernel's set-up overlaps the end of the grid before it.
+// How the prefill kernel converts bf16 x itself for a plan: 2 when every CTA
+// runs at most one unit with two accumulators (the epilogue warps are free until
+// the end) and its x is small, 1 for one token (the MMA warp), else 0 (the
+// caller converts x first).  Each CTA converts the x of its own unit and K range,
+// so CTAs that share a token tile convert it again; measured on GB300, up to
+// X_CONVERT_MAX_BYTES per CTA the launch saved over the conversion kernel (Q4_K
+// M=8 N4096 K4096 11.4 -> 10.0 us, M=32 N2048 K2048 8.4 -> 8.0 us), while 229 KB
+// per CTA (M=105, N4096, K4096, split-K 4) took 13.8 -> 21.5 us and 131 KB (a
+// batch of eight M=32 N2048 K2048 products) 17.5 -> 20.7 us.
+constexpr int64_t X_CONVERT_MAX_BYTES = 32 * 1024;
+static int x_convert_mode(const Plan &plan, int bn, int64_t units_all, int64_t M, int64_t K) {
+    const int64_t k_cta = (K / CHUNK_K + plan.S - 1) / plan.S * CHUNK_K;  // K of one split, at most
+    const int64_t bytes = std::min<int64_t>(bn, M) * k_cta * 2;
+    if (units_all <= plan.clusters && bn <= static_cast<int>(ACC_STRIDE) && bytes <= X_CONVERT_MAX_BYTES) return 2;
+    return M <= CONVERT_MAX_M ? 1 : 0;
+}
+
+// Whether a bf16-x product of this shape (one problem, or a strided batch) is
+// converted inside the prefill kernel (no conversion kernel, no scratch).
+template <int kFmt>
+static bool converts_in_kernel(int64_t M, int64_t N, int64_t K, int64_t batch = 1) {
+    Plan plan;
+    int bn = 0;
+    int64_t units = 0;
+    if (plan_gemm<kFmt>(M, N, K, plan, bn, units, batch)) return false;
+    return x_convert_mode(plan, bn, batch * units, M, K) != 0;
+}
+
+// x is fp16 [M, K], or bf16 when x_bf16 (converted in shared memory by the
+// kernel, see x_convert_mode; QWP_ERR_UNSUPPORTED_SHAPE if the plan allows
+// neither way).  Launched with programmatic stream serialization: the kernel's
+// set-up overlaps the end of the grid before it.
 template <int kFmt>
 static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, const void *x,
                        float *y, int64_t M, int64_t N, int64_t K, int64_t group, cudaStream_t stream,
@@ -1183,7 +1260,8 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     if ((rc = plan_gemm<kFmt>(M, N, K, plan, bn, units, batch))) return rc;
     const int64_t row_tiles = (N + TILE_ROWS - 1) / TILE_ROWS;
     const int nstages = static_cast<int>((K / CHUNK_K + KB_PER_STAGE - 1) / KB_PER_STAGE);
-    if (x_bf16 && M > CONVERT_MAX_M) return QWP_ERR_UNSUPPORTED_SHAPE;
+    const int conv = x_bf16 ? x_convert_mode(plan, bn, batch * units, M, K) : 0;
+    if (x_bf16 && !conv) return QWP_ERR_UNSUPPORTED_SHAPE;
     CUtensorMap map;
     if ((rc = encode_x_map(&map, x, M, K, bn, x_bf16, batch))) return rc;
 
@@ -1212,7 +1290,7 @@ static int launch_gemm(const void *w, const void *scales, const uint8_t *zeros, 
     a.w_stages = plan.w_stages;
     a.part_off = plan.part_off;
     a.part_overlay = plan.overlay ? 1 : 0;
-    a.x_convert = x_bf16 ? 1 : 0;
+    a.x_convert = conv;
     a.splits = plan.S;
     a.kb_per_split = ((nstages + plan.S - 1) / plan.S) * KB_PER_STAGE;
     a.n_units = static_cast<int>(batch * units);
@@ -1261,7 +1339,8 @@ int launch_q4k_prefill_fixed(const void *w, const void *x, void *x16, float *y, 
                              cudaStream_t stream) {
     int rc = check_device();
     if (rc) return rc;
-    if (M <= CONVERT_MAX_M) return launch_gemm<FMT_Q4K>(w, nullptr, nullptr, x, y, M, N, K, 0, stream, true);
+    if (converts_in_kernel<FMT_Q4K>(M, N, K))
+        return launch_gemm<FMT_Q4K>(w, nullptr, nullptr, x, y, M, N, K, 0, stream, true);
     if ((rc = launch_bf16_to_f16(x, x16, M * K, stream))) return rc;
     return launch_gemm<FMT_Q4K>(w, nullptr, nullptr, x16, y, M, N, K, 0, stream);
 }
@@ -1349,8 +1428,10 @@ extern "C" int q4k_gemm(const void *w_tiled, const void *x, float *y, int64_t M,
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (decode_shaped(DFMT_Q4K, M, N, K)) return run_decode(DFMT_Q4K, w_tiled, nullptr, nullptr, x, true, y, M, N, K, 0, s);
     if (skinny_selected(DFMT_Q4K, M, N, K)) return launch_skinny(w_tiled, x, true, y, M, N, K, s);
-    // One token: the kernel converts x itself (no conversion kernel, no scratch).
-    if (M <= CONVERT_MAX_M) return launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0, s, true);
+    // One unit per CTA, or one token: the kernel converts x itself (no conversion
+    // kernel, no scratch).
+    if (converts_in_kernel<FMT_Q4K>(M, N, K))
+        return launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0, s, true);
     cudaMemPool_t pool;
     if ((rc = scratch_pool(&pool))) return rc;
     void *x16 = nullptr;
@@ -1379,7 +1460,8 @@ static int q4k_batched(const void *w_tiled, const void *x, bool x_bf16, float *y
     if ((rc = check_device())) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t wbytes = N * (K / Q4K_BLOCK) * Q4K_BLOCK_BYTES;
-    if (!x_bf16) return launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0, s, false, batch, wbytes);
+    if (!x_bf16 || converts_in_kernel<FMT_Q4K>(M, N, K, batch))
+        return launch_gemm<FMT_Q4K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0, s, x_bf16, batch, wbytes);
     cudaMemPool_t pool;
     if ((rc = scratch_pool(&pool))) return rc;
     void *x16 = nullptr;
@@ -1433,8 +1515,10 @@ extern "C" int q6k_gemm(const void *w_tiled, const void *x, float *y, int64_t M,
     if ((rc = check_device())) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (decode_shaped(DFMT_Q6K, M, N, K)) return run_decode(DFMT_Q6K, w_tiled, nullptr, nullptr, x, true, y, M, N, K, 0, s);
-    // One token: the kernel converts x itself (no conversion kernel, no scratch).
-    if (M <= CONVERT_MAX_M) return launch_gemm<FMT_Q6K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0, s, true);
+    // One unit per CTA, or one token: the kernel converts x itself (no conversion
+    // kernel, no scratch).
+    if (converts_in_kernel<FMT_Q6K>(M, N, K))
+        return launch_gemm<FMT_Q6K>(w_tiled, nullptr, nullptr, x, y, M, N, K, 0, s, true);
     cudaMemPool_t pool;
     if ((rc = scratch_pool(&pool))) return rc;
     void *x16 = nullptr;
@@ -1474,8 +1558,10 @@ extern "C" int w4a16_gemm_bf16(const void *wq_tiled, const void *scales, const u
     if ((rc = check_device())) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (decode_shaped(DFMT_W4A16, M, N, K)) return run_decode(DFMT_W4A16, wq_tiled, scales, zeros, x, true, y, M, N, K, group, s);
-    // One token: the kernel converts x itself (no conversion kernel, no scratch).
-    if (M <= CONVERT_MAX_M) return launch_gemm<FMT_W4A16>(wq_tiled, scales, zeros, x, y, M, N, K, group, s, true);
+    // One unit per CTA, or one token: the kernel converts x itself (no conversion
+    // kernel, no scratch).
+    if (converts_in_kernel<FMT_W4A16>(M, N, K))
+        return launch_gemm<FMT_W4A16>(wq_tiled, scales, zeros, x, y, M, N, K, group, s, true);
     cudaMemPool_t pool;
     if ((rc = scratch_pool(&pool))) return rc;
     void *x16 = nullptr;

@@ -124,40 +124,60 @@ def test_q4k_gemm_f16_activations(M, N, K):
     check_bound(y, ref, mag, f"q4k f16 M{M} N{N} K{K}")
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 2048, 2048), (1, 40000, 1024), (1, 19456, 4096), (1, 700, 8192),
-                                   (2, 3000, 1024)])
-def test_q4k_small_m_converts_x_in_the_kernel(M, N, K):
-    """One token: bf16 x goes to the prefill kernel unconverted and its MMA warp
-    converts the token row of each x slot in shared memory (no conversion kernel),
-    also when a CTA runs several units (N = 40000) and with split-K; two tokens take
-    the conversion kernel."""
+def _x_conversion(M, N, K, fmt="q4k"):
+    """Where a bf16-x call of this shape on the prefill kernel converts x: "epilogue"
+    (every CTA runs at most one unit with two accumulators and converts at most
+    32 KB of x: the epilogue warps convert each x slot), "mma" (one token: the MMA
+    warp converts the token row), else "kernel" (a conversion kernel first)."""
+    p = qwp.gemm_plan(fmt, M, N, K)
+    assert p["kernel"] == "prefill"
+    k_cta = -(-(K // 64) // p["splits"]) * 64
+    if p["units_per_cluster"] == 1 and p["token_tile"] <= 128 and min(p["token_tile"], M) * k_cta * 2 <= 32768:
+        return "epilogue"
+    return "mma" if M == 1 else "kernel"
+
+
+@pytest.mark.parametrize("M,N,K,where", [(1, 2048, 2048, "epilogue"), (1, 40000, 1024, "mma"),
+                                         (1, 19456, 4096, "epilogue"), (1, 700, 8192, "epilogue"),
+                                         (2, 3000, 1024, "epilogue"), (32, 2048, 2048, "epilogue"),
+                                         (105, 4096, 4096, "kernel"), (16, 1000, 768, "epilogue"),
+                                         (8, 40000, 1024, "kernel"), (300, 40000, 256, "kernel")])
+def test_q4k_bf16_x_conversion_paths(M, N, K, where):
+    """bf16 x on the prefill kernel, each way of converting it to the fp16 MMA
+    operand: by the epilogue warps in shared memory (one unit per CTA, also with
+    split-K and ragged token rows), by the MMA warp (one token, CTAs with several
+    units), or by a conversion kernel first; every element within the bound."""
     prev = qwp.set_decode_policy(qwp.DECODE_NEVER)
     try:
-        assert qwp.gemm_plan("q4k", M, N, K)["kernel"] == "prefill"
+        assert _x_conversion(M, N, K) == where, qwp.gemm_plan("q4k", M, N, K)
         blocks, w = _q4k_on_gpu(N, K, seed=M * 3 + N)
         xb = synth.activations_bf16(M, K, seed=M + 9)
         y = qwp.q4k_gemm(w, _bf16_on_gpu(xb), N).cpu().numpy()
     finally:
         qwp.set_decode_policy(prev)
     ref, mag = oracle.q4k_gemm(blocks, xb, N, K)
-    check_bound(y, ref, mag, f"q4k small M{M} N{N} K{K} plan {qwp.gemm_plan('q4k', M, N, K)}")
+    check_bound(y, ref, mag, f"q4k bf16 M{M} N{N} K{K} ({where}) plan {qwp.gemm_plan('q4k', M, N, K)}")
 
 
-@pytest.mark.parametrize("M", [8, 1])
-def test_q4k_bf16_activation_beyond_fp16_range_is_reported(M):
-    """An activation that overflows fp16 is reported as QWP_ERR_RANGE, and the next
-    call is clean (8 tokens: the conversion kernel; 1 token: the GEMM kernel's own
-    conversion)."""
-    N, K = 128, 256
-    blocks, w = _q4k_on_gpu(N, K, seed=31)
-    xb = synth.activations_bf16(M, K, seed=32).copy()
-    r = min(3, M - 1)
-    xb[r, 17] = 0x4880  # bf16 262144.0, beyond fp16's largest finite value
-    qwp.q4k_gemm(w, _bf16_on_gpu(xb), N)
-    assert qwp.device_status() == -7
-    xb[r, 17] = 0x3F80  # 1.0
-    y = qwp.q4k_gemm(w, _bf16_on_gpu(xb), N).cpu().numpy()
-    assert qwp.device_status() == 0
+@pytest.mark.parametrize("M,N,K,where", [(8, 128, 256, "epilogue"), (1, 40000, 256, "mma"),
+                                         (8, 40000, 256, "kernel"), (32, 2048, 2048, "epilogue")])
+def test_q4k_bf16_activation_beyond_fp16_range_is_reported(M, N, K, where):
+    """An activation that overflows fp16 is reported as QWP_ERR_RANGE whichever way
+    x is converted, and the next call is clean."""
+    prev = qwp.set_decode_policy(qwp.DECODE_NEVER)
+    try:
+        assert _x_conversion(M, N, K) == where
+        blocks, w = _q4k_on_gpu(N, K, seed=31)
+        xb = synth.activations_bf16(M, K, seed=32).copy()
+        r = min(3, M - 1)
+        xb[r, K - 17] = 0x4880  # bf16 262144.0, beyond fp16's largest finite value
+        qwp.q4k_gemm(w, _bf16_on_gpu(xb), N)
+        assert qwp.device_status() == -7
+        xb[r, K - 17] = 0x3F80  # 1.0
+        y = qwp.q4k_gemm(w, _bf16_on_gpu(xb), N).cpu().numpy()
+        assert qwp.device_status() == 0
+    finally:
+        qwp.set_decode_policy(prev)
     ref, mag = oracle.q4k_gemm(blocks, xb, N, K)
     check_bound(y, ref, mag, "after a range error")
 
