@@ -138,10 +138,12 @@ QWP_API int q4k_gemm_f16(const void *w_tiled_dev, const void *x_dev, float *y_de
  * larger ones overflow, which qwp_device_status reports as QWP_ERR_RANGE) into
  * M*K*2 bytes of scratch taken from a library-owned, stream-ordered memory pool
  * on the current device and released in stream order after the GEMM; then
- * q4k_gemm_f16 runs, launched so that its set-up overlaps the conversion.  With
- * one token (M == 1) on the prefill kernel the GEMM kernel converts x itself, in
- * shared memory (same rounding and range report; no conversion kernel, no
- * scratch).  Skinny-N calls (above) take x as bf16 in the skinny-N kernel: no
+ * q4k_gemm_f16 runs, launched so that its set-up overlaps the conversion.  The
+ * prefill kernel converts x itself, in shared memory (same rounding and range
+ * report; no conversion kernel, no scratch), when each of its CTAs runs one
+ * work unit and converts at most 32 KB of x (for example M <= 32 at N = 2048,
+ * K = 2048; qwp_gemm_plan tells the plan), and for one token (M == 1).
+ * Skinny-N calls (above) take x as bf16 in the skinny-N kernel: no
  * conversion, no scratch, no range limit.  Same shape and alignment rules as
  * q4k_gemm_f16.
  */
@@ -183,8 +185,8 @@ QWP_API int q4k_gemm_batched_f16(const void *w_tiled_dev, const void *x_dev, flo
  * q4k_gemm (the same kernels run); the fp16 copy of x goes into a fixed array
  * of QWP_NOALLOC_MAX_X_ELEMS fp16 values (16 MiB) that is part of the library
  * and that every GPU loading the library's device code holds until the process
- * exits (one-token calls on the prefill kernel convert x inside the GEMM kernel
- * and do not use it).  M*K beyond that size returns QWP_ERR_SCRATCH_LIMIT before
+ * exits (calls whose prefill kernel converts x itself, as described for
+ * q4k_gemm, do not use it).  M*K beyond that size returns QWP_ERR_SCRATCH_LIMIT before
  * any work.
  * Decode-shaped calls keep their partial sums in a second fixed array (4 MiB)
  * instead and read x directly (no fp16 copy); a decode-shaped call whose
@@ -301,8 +303,8 @@ QWP_API int q6k_gemm_f16(const void *w_tiled_dev, const void *x_dev, float *y_de
 
 /*
  * The same product for bf16 activations, converted to fp16 exactly as q4k_gemm
- * does (pool scratch, or in the kernel for one token; same rules, same
- * QWP_ERR_RANGE report).
+ * does (pool scratch, or in the GEMM kernel under the same conditions; same
+ * rules, same QWP_ERR_RANGE report).
  */
 QWP_API int q6k_gemm(const void *w_tiled_dev, const void *x_dev, float *y_dev,
                      int64_t M, int64_t N, int64_t K, void *stream);
@@ -344,8 +346,8 @@ QWP_API int w4a16_gemm(const void *wq_tiled_dev, const void *scales_dev, const u
  * converted to fp16 into M*K*2 bytes of scratch from the library-owned,
  * stream-ordered pool (exact for |x| in [2^-14, 65504]; an overflow is reported
  * by qwp_device_status as QWP_ERR_RANGE), then w4a16_gemm runs, launched so that
- * its set-up overlaps the conversion; with one token the GEMM kernel converts x
- * itself.  Same rules as w4a16_gemm.
+ * its set-up overlaps the conversion; the GEMM kernel converts x itself under
+ * the conditions described for q4k_gemm.  Same rules as w4a16_gemm.
  */
 QWP_API int w4a16_gemm_bf16(const void *wq_tiled_dev, const void *scales_dev, const uint8_t *zeros_dev,
                     const void *x_dev, float *y_dev, int64_t M, int64_t N, int64_t K, int64_t group,
