@@ -615,18 +615,33 @@ def run_gpu(args):
 
     # ---- end to end: host buffers, copies inside the timed region.  Steps run as
     # a serving loop would: every step copies its four x from pinned host memory
-    # (side stream h2d_s), runs the four library calls on the main stream, each as
-    # soon as its x has arrived, and copies each y back to pinned host memory
-    # (side stream d2h_s) as soon as its GEMM is done.  Device x/y and host y are
-    # double-buffered, so step s+1's copies and GEMMs overlap step s's read-back;
-    # a buffer is reused only after the step two back has finished with it.  One
-    # CUDA graph holds E2E_SPAN steps (every weight copy at least once).
-    x_host = [x.cpu().pin_memory() for x in xs]
-    x_dev = [[torch.empty_like(x) for x in xs] for _ in range(2)]
-    y_dev = [[torch.empty_like(y) for y in ys] for _ in range(2)]
-    y_host = [[torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys] for _ in range(2)]
-    h2d = sum(x.numel() * x.element_size() for x in x_host)
-    d2h = sum(y.numel() * y.element_size() for y in y_host[0])
+    # (side stream h2d_s, one copy: the four x sit back to back in one buffer), runs
+    # the four library calls on the main stream once they have arrived, and copies
+    # the four y back to pinned host memory (side stream d2h_s, one copy) once the
+    # step's GEMMs are done.  Device x/y and host y are double-buffered, so step
+    # s+1's copies and GEMMs overlap step s's read-back; a buffer is reused only
+    # after the step two back has finished with it.  One CUDA graph holds E2E_SPAN
+    # steps (every weight copy at least once).
+    def packed(tensors, make):
+        """One buffer holding the tensors' shapes back to back, and views of it."""
+        total = sum(t.numel() for t in tensors)
+        buf = make(total, tensors[0].dtype)
+        views, off = [], 0
+        for t in tensors:
+            views.append(buf[off:off + t.numel()].view(t.shape))
+            off += t.numel()
+        return buf, views
+
+    pinned = lambda n, dt: torch.empty(n, dtype=dt).pin_memory()  # noqa: E731
+    on_dev = lambda n, dt: torch.empty(n, dtype=dt, device=dev)  # noqa: E731
+    x_host_buf, x_host = packed(xs, pinned)
+    for i, x in enumerate(xs):
+        x_host[i].copy_(x.cpu())
+    x_dev = [packed(xs, on_dev) for _ in range(2)]
+    y_dev = [packed(ys, on_dev) for _ in range(2)]
+    y_host = [packed(ys, pinned) for _ in range(2)]
+    h2d = x_host_buf.numel() * x_host_buf.element_size()
+    d2h = y_host[0][0].numel() * y_host[0][0].element_size()
     h2d_s = torch.cuda.Stream(dev)
     d2h_s = torch.cuda.Stream(dev)
     span = 4 * copies
@@ -640,27 +655,24 @@ def run_gpu(args):
             gemm_done, y_read = [], []
             for j in range(span):
                 b, w = j % 2, weights[j % copies]
-                x_in = []
                 with torch.cuda.stream(h2d_s):
-                    for i in range(len(LAYER)):
-                        if j >= 2:
-                            h2d_s.wait_event(gemm_done[j - 2][i])  # x_dev[b][i] read by then
-                        x_dev[b][i].copy_(x_host[i], non_blocking=True)
-                        x_in.append(torch.cuda.Event())
-                        x_in[-1].record(h2d_s)
-                done, read = [], []
-                for i, (_, K, N) in enumerate(LAYER):
-                    cap.wait_event(x_in[i])
                     if j >= 2:
-                        cap.wait_event(y_read[j - 2][i])  # y_dev[b][i] copied out by then
-                    qwp.q4k_gemm(w[i], x_dev[b][i], N, out=y_dev[b][i])
-                    done.append(torch.cuda.Event())
-                    done[-1].record(cap)
-                    d2h_s.wait_event(done[-1])
-                    with torch.cuda.stream(d2h_s):
-                        y_host[b][i].copy_(y_dev[b][i], non_blocking=True)
-                        read.append(torch.cuda.Event())
-                        read[-1].record(d2h_s)
+                        h2d_s.wait_event(gemm_done[j - 2])  # x_dev[b] read by then
+                    x_dev[b][0].copy_(x_host_buf, non_blocking=True)
+                    x_in = torch.cuda.Event()
+                    x_in.record(h2d_s)
+                cap.wait_event(x_in)
+                if j >= 2:
+                    cap.wait_event(y_read[j - 2])  # y_dev[b] copied out by then
+                for i, (_, K, N) in enumerate(LAYER):
+                    qwp.q4k_gemm(w[i], x_dev[b][1][i], N, out=y_dev[b][1][i])
+                done = torch.cuda.Event()
+                done.record(cap)
+                d2h_s.wait_event(done)
+                with torch.cuda.stream(d2h_s):
+                    y_host[b][0].copy_(y_dev[b][0], non_blocking=True)
+                    read = torch.cuda.Event()
+                    read.record(d2h_s)
                 gemm_done.append(done)
                 y_read.append(read)
             cap.wait_stream(h2d_s)
@@ -687,9 +699,8 @@ def run_gpu(args):
         raise RuntimeError("kernel timeout during the end-to-end pass")
     # the last two steps' results reached the host: spot-check them against the device
     for b in range(2):
-        for i in range(len(LAYER)):
-            if not torch.equal(y_host[b][i], y_dev[b][i].cpu()):
-                raise RuntimeError("end-to-end copy of y does not match the device result")
+        if not torch.equal(y_host[b][0], y_dev[b][0].cpu()):
+            raise RuntimeError("end-to-end copy of y does not match the device result")
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     sampler.stop()
 
@@ -764,9 +775,10 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "e2e": {"value": world * M * e2e_steps / (e2e_ms * 1e-3), "unit": "tok/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "every step copies its x from pinned host memory and its y back to pinned host memory "
-                       "around the four public API calls (copies on side streams, double-buffered so a step's "
-                       f"read-back overlaps the next step's GEMMs); {span} steps per CUDA graph replay"},
+                "how": "every step copies its four x from pinned host memory (one copy) and its four y back to "
+                       "pinned host memory (one copy) around the four public API calls (copies on side streams, "
+                       "double-buffered so a step's read-back overlaps the next step's GEMMs); "
+                       f"{span} steps per CUDA graph replay"},
         # per call: the bf16 -> fp16 activation conversion and the GEMM
         "gpu_launches": 2 * len(LAYER) * args.steps,
         "clocks": sampler.summary(),
