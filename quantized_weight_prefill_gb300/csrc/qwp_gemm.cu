@@ -910,11 +910,16 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
                     const int tt = t0 + itm / (TILE_ROWS / 4);
                     const int r4 = 4 * (itm % (TILE_ROWS / 4));
                     const uint32_t off = static_cast<uint32_t>((tt * TILE_ROWS + r4) * 4);
+                    // All S remote loads are issued before the first sum needs one
+                    // (a dependent load-add chain costs S round trips over the cluster).
+                    float4 pv[MAX_SPLITS];
+#pragma unroll
+                    for (int q = 0; q < MAX_SPLITS; ++q)
+                        if (q < S) pv[q] = ld_shared_cluster_f4(map_shared_rank(own_addr + off, static_cast<uint32_t>(q)));
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int q = 0; q < S; ++q) {
-                        const float4 pv = ld_shared_cluster_f4(map_shared_rank(own_addr + off, static_cast<uint32_t>(q)));
-                        acc.x += pv.x; acc.y += pv.y; acc.z += pv.z; acc.w += pv.w;
-                    }
+#pragma unroll
+                    for (int q = 0; q < MAX_SPLITS; ++q)
+                        if (q < S) { acc.x += pv[q].x; acc.y += pv[q].y; acc.z += pv[q].z; acc.w += pv[q].w; }
                     const int m = m0 + tt;
                     if (m < args.M) {
                         float *yr = unit_y(lu) + static_cast<int64_t>(m) * args.N + static_cast<int64_t>(tile) * TILE_ROWS;
