@@ -355,12 +355,14 @@ __global__ void __launch_bounds__(block_threads(kTwoAcc), 1)
         // from any earlier kernel; every other thread is ordered after this wait by
         // the block-wide barrier below.
         pdl_wait();
-        for (int s = 0; s < w_pre; ++s) load_weight_stage(units0, s, s);
         // A failure recorded earlier (and not yet read by qwp_device_status) makes
         // every later launch skip its work instead of waiting out its own timeouts
-        // (the weight copies started above are still waited for).  Read after the
-        // copies are issued, so that its latency is not in front of theirs.
-        misc[1] = (*reinterpret_cast<volatile uint32_t *>(args.status) & kStatusTimeoutMask) ? 1u : 0u;
+        // (the weight copies started below are still waited for).  The status load
+        // is issued before the copies and its value used after them, so that its
+        // latency overlaps theirs instead of adding to the set-up.
+        const uint32_t status_now = *reinterpret_cast<volatile uint32_t *>(args.status);
+        for (int s = 0; s < w_pre; ++s) load_weight_stage(units0, s, s);
+        misc[1] = (status_now & kStatusTimeoutMask) ? 1u : 0u;
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(misc), TMEM_COLS);

@@ -151,6 +151,11 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         // x, the weights and the status word may come from the grids launched just
         // before; every other thread is ordered after this wait by the barrier below.
         pdl_wait();
+        // A failure recorded earlier (and not yet read) makes this launch skip its
+        // work; the copies below are still waited for.  The status load is issued
+        // first and its value used only after the copies are issued, so that its
+        // latency (about 1 us once every CTA's copies are queued) overlaps theirs.
+        const uint32_t status_now = *reinterpret_cast<volatile uint32_t *>(args.status);
         // The first x tiles and weight stages start before the block-wide barrier
         // (their slots are empty); this thread is also the x producer.
         for (int j = 0; j < x_pre; ++j) {
@@ -162,10 +167,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
             bulk_copy_g2s(smem_u32(smem + L.off_w + i * SK_W_SLOT), args.w + q4k_group_offset(args.K, 0, R, st0 + i),
                           w_bytes, w_full + 8 * i);
         }
-        // A failure recorded earlier (and not yet read) makes this launch skip its
-        // work; the copies above are still waited for.  (Read after issuing them, so
-        // that its latency is not in front of theirs.)
-        misc[1] = (*reinterpret_cast<volatile uint32_t *>(args.status) & kStatusTimeoutMask) ? 1u : 0u;
+        misc[1] = (status_now & kStatusTimeoutMask) ? 1u : 0u;
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(misc), SK_TMEM_COLS);
