@@ -427,15 +427,17 @@ __global__ void __launch_bounds__(DEC_THREADS, kFmt == DFMT_Q4K ? 3 : 2)
         p_tile = beg / nsb;
         p_sb = beg - p_tile * nsb;
         if (n_items > 0) p_setup_tile();
-        // x and the weights may come from the grids launched just before.
+        // x, the weights and the status word may come from the grids launched just
+        // before (every other thread is ordered after this wait by the barrier below).
         pdl_wait();
+        // A failure recorded earlier makes this launch skip its work; the status load
+        // is issued before the first copies and its value used after them, so that
+        // its latency overlaps theirs.
+        const uint32_t status_now = *reinterpret_cast<volatile uint32_t *>(args.status);
         const int pre = min(min(NS, DEC_PRE), n_items);
         for (int st = 0; st < pre; ++st) issue_next(st);
         issued = pre;
-    }
-    if (threadIdx.x == 0) {
-        pdl_wait();  // (every other thread is ordered after the waits by the barrier below)
-        *abort = (*reinterpret_cast<volatile uint32_t *>(args.status) & kStatusTimeoutMask) ? 1u : 0u;
+        *abort = (status_now & kStatusTimeoutMask) ? 1u : 0u;
     }
     __syncthreads();
     bool ok = *reinterpret_cast<volatile uint32_t *>(abort) == 0;
