@@ -19,7 +19,7 @@
  * prefill went from 42 to 208 tok/s", section "The fix: K-parallel batched
  * DMMV"): same weights, same operand rounding and the same error bound, bf16
  * activations converted inside the kernel, and G * 8 KiB + ceil(N/128) * 4
- * bytes of pool scratch (G: the decode grid, at most 3 CTAs per SM) for the
+ * bytes of pool scratch (G: the decode grid, at most 2 CTAs per SM) for the
  * tiles its CTAs share.
  * Results are deterministic (shared tiles are summed in a fixed order).  By
  * default (QWP_DECODE_AUTO) it takes such products only where it measured
