@@ -538,8 +538,11 @@ def run_gpu(args):
             qwp.q4k_gemm(w[i], xs[i], N, out=ys[i])
 
     # warm up eagerly (library set-up happens outside any capture), then capture
-    # one graph per weight copy holding the whole layer.  The timed steps replay
-    # these plain graphs.  A second set, with timing-event nodes around the dominant
+    # one graph per weight copy holding the whole layer, and one graph holding
+    # 4 x copies consecutive layers (the weight copies in turn), as a model's
+    # layers run back to back.  The timed steps replay the multi-layer graph (each
+    # replay is 4 x copies steps) and single-layer graphs for any remainder.  A
+    # second set, with timing-event nodes around the dominant
     # GEMM, serves its per-launch time in a second timed pass: event nodes inside a
     # graph cost ~4 us each (they end the overlap of one launch with the next), so
     # they stay out of the steps that give the tok/s figure, and the per-launch time
@@ -570,15 +573,24 @@ def run_gpu(args):
             calls(c, range(dom + 1, len(LAYER)))
         ev_graphs.append(g)
         dom_events.append((e0, e1))
-    for g in graphs + ev_graphs:
+    span_layers = 4 * copies  # layers per multi-layer graph (the end-to-end graph holds as many steps)
+    multi = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(multi):
+        for j in range(span_layers):
+            calls(j % copies, range(len(LAYER)))
+    for g in graphs + ev_graphs + [multi]:
         g.replay()
     torch.cuda.synchronize()
 
-    def step(s):
-        graphs[s % copies].replay()
+    def run_steps(n):
+        # n steps: whole multi-layer replays, then single layers (weight copies keep
+        # rotating in order either way)
+        for _ in range(n // span_layers):
+            multi.replay()
+        for s in range(n % span_layers):
+            graphs[s % copies].replay()
 
-    for s in range(args.warmup):
-        step(s)
+    run_steps(max(args.warmup, span_layers))
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
@@ -590,8 +602,7 @@ def run_gpu(args):
     end = torch.cuda.Event(enable_timing=True)
     wall0 = time.time()
     start.record(stream)
-    for s in range(args.steps):
-        step(s)
+    run_steps(args.steps)
     end.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -755,7 +766,9 @@ def run_gpu(args):
             "workload": layer_workload(),
             "global_batch": M * world, "seq_len": M, "parallelism": f"replicas x{world}",
             "l2": f"weights rotate over {copies} copies ({copies * layer_w_bytes / 1e6:.0f} MB > 2x L2)",
-            "launch": "one CUDA graph of the four library calls per weight copy, replayed per step",
+            "launch": f"CUDA graphs of {4 * copies} consecutive layers (the four library calls each, the "
+                      f"{copies} weight copies in turn), as a model's layers run back to back; each replay is "
+                      f"{4 * copies} steps",
         },
         "layer_tflops": tflops_layer,
         "layer_pct_bf16_peak": 100.0 * tflops_layer / tc_burst,
