@@ -23,8 +23,9 @@
  * tiles its CTAs share.
  * Results are deterministic (shared tiles are summed in a fixed order).  By
  * default (QWP_DECODE_AUTO) it takes such products only where it measured
- * faster than the prefill kernel on GB300: N >= 65536 and M <= 2 (Q4_K, Q6_K)
- * or M == 1 (W4A16); see qwp_set_decode_policy.
+ * faster than the prefill kernel on GB300: M <= 2 and N >= 24576 for Q4_K, N >=
+ * 65536 for Q6_K, N >= 24576 at one token and N >= 65536 at two for W4A16; see
+ * qwp_set_decode_policy.
  * Skinny-N calls.  A Q4_K product with at most 64 weight rows (N <= 64) and at
  * least 256 tokens runs a third kernel ("Skinny bf16 GEMM prefill_gemm_skinny.cu",
  * sparkinfer PR #511, Summary table): tokens are the tensor core's M side and
@@ -367,9 +368,9 @@ QWP_API int qwp_device_status(void *stream);
 
 /*
  * Which decode-shaped products (see the top of this file) the GEMM entry points
- * run on the decode kernel, process-wide: QWP_DECODE_AUTO (the default: N >=
- * 65536 and M <= 2 for Q4_K and Q6_K, M == 1 for W4A16, where it measured
- * faster), QWP_DECODE_NEVER (always the
+ * run on the decode kernel, process-wide: QWP_DECODE_AUTO (the default: M <= 2
+ * and N >= 24576 for Q4_K, N >= 65536 for Q6_K, N >= 24576 at one token and N >=
+ * 65536 at two for W4A16, where it measured faster), QWP_DECODE_NEVER (always the
  * prefill kernel) or QWP_DECODE_ALWAYS (every decode-shaped product).  Results
  * meet the same error bound either way.  Returns the previous policy (>= 0) or
  * QWP_ERR_INVALID_ARG.  Calls already issued keep the kernel they were given;

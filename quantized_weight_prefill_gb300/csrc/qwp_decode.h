@@ -32,17 +32,23 @@ inline bool decode_fits(int64_t M, int64_t N, int64_t K) {
 // the prefill kernel, ALWAYS takes every product that decode_fits.
 enum : int { DECODE_POLICY_AUTO = 0, DECODE_POLICY_NEVER = 1, DECODE_POLICY_ALWAYS = 2 };
 
-// The automatic choice, from both kernels timed on GB300 at 1 to 8 tokens (Q4_K,
-// Q6_K and W4A16, N from 2048 to 152064, K from 4096 to 12288): the decode kernel
-// is clearly faster for vocabulary-sized matrices (N >= 65536) at one and two
-// tokens for Q4_K (5-8%) and Q6_K (4-7%), and at one token for W4A16 (a tie; two
-// tokens lose 4%); from N = 10240 to 24576 the two are within a few percent
-// either way, and the prefill kernel wins for narrower or K-heavy matrices and
-// from three tokens on.
-constexpr int64_t DECODE_AUTO_MIN_ROWS = 65536;
-inline int64_t decode_auto_max_tokens(int fmt) { return fmt == DFMT_W4A16 ? 1 : 2; }
+// The automatic choice, from both kernels timed on GB300 (Q4_K, Q6_K and W4A16,
+// N from 2048 to 152064, K from 4096 to 12288, 1 to 8 tokens; last with the
+// decode kernel at two CTAs per SM): the decode kernel is faster at one and two
+// tokens from N = 24576 for Q4_K (M1 N24576 32.8 against 34.1 us, M2 33.2
+// against 35.3, M1 N65536 65.7 against 71.9) and for W4A16 at one token (31.6
+// against 33.4), at two tokens for W4A16 from N = 65536 (65.6 against 71.0), and
+// for Q6_K from N = 65536 (a tie at 24576); the prefill kernel wins for narrower
+// or K-heavy matrices (N <= 12288, or K = 12288 at N = 4096) and from three
+// tokens on (M3 N152064 a tie, M4 +2.5%).
+inline int64_t decode_auto_min_rows(int fmt, int64_t M) {
+    if (fmt == DFMT_Q6K) return 65536;
+    if (fmt == DFMT_W4A16 && M > 1) return 65536;
+    return 24576;
+}
+constexpr int64_t DECODE_AUTO_MAX_TOKENS = 2;
 inline bool decode_auto(int fmt, int64_t M, int64_t N, int64_t K) {
-    return decode_fits(M, N, K) && M <= decode_auto_max_tokens(fmt) && N >= DECODE_AUTO_MIN_ROWS;
+    return decode_fits(M, N, K) && M <= DECODE_AUTO_MAX_TOKENS && N >= decode_auto_min_rows(fmt, M);
 }
 
 // The current policy, and the choice it makes for an M x N x K product of

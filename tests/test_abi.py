@@ -135,24 +135,25 @@ def test_gemm_argument_checks_before_any_cuda_call(lib):
 
 def test_decode_policy_round_trip_and_automatic_rule(lib):
     """The dispatch between the decode and the prefill kernel is host logic: the
-    automatic rule (N >= 65536 and at most two tokens for Q4_K and Q6_K, one for
-    W4A16, plus what the decode kernel needs: K % 256 == 0 and >= 600 tile
-    items), the two forced policies, and the rejection of an unknown policy or
-    format."""
+    automatic rule (at most two tokens; N >= 24576 for Q4_K, N >= 65536 for Q6_K,
+    N >= 24576 at one token and N >= 65536 at two for W4A16; plus what the decode
+    kernel needs: K % 256 == 0 and >= 600 tile items), the two forced policies,
+    and the rejection of an unknown policy or format."""
     sel = qwp.decode_selected
     prev = qwp.set_decode_policy(qwp.DECODE_AUTO)
     try:
         for f in ("q4k", "q6k", "w4a16"):
-            assert sel(f, 1, 152064, 4096) and sel(f, 1, 65536, 4096)
+            assert sel(f, 1, 152064, 4096) and sel(f, 1, 65536, 4096) and sel(f, 2, 65536, 4096)
             assert sel(f, 1, 65600, 512)                 # 513 x 2 = 1026 items
             assert not sel(f, 3, 152064, 4096)           # three tokens: the prefill kernel
-            assert not sel(f, 1, 65408, 4096)            # 511 row tiles
-            assert not sel(f, 1, 24576, 4096)
+            assert not sel(f, 1, 12288, 4096)            # narrow
             assert not sel(f, 1, 152064, 4000)           # K % 256 != 0
             assert not sel(f, 1, 65536, 256)             # 512 x 1 = 512 items
             assert not sel(f, 0, 152064, 4096)
-        assert sel("q4k", 2, 152064, 4096) and sel("q6k", 2, 65536, 4096)
-        assert not sel("w4a16", 2, 152064, 4096)         # W4A16: one token only
+        assert sel("q4k", 1, 24576, 4096) and sel("q4k", 2, 24576, 4096)
+        assert not sel("q4k", 1, 24448, 4096)            # 191 row tiles
+        assert not sel("q6k", 1, 24576, 4096) and not sel("q6k", 1, 65408, 4096)
+        assert sel("w4a16", 1, 24576, 4096) and not sel("w4a16", 2, 24576, 4096)
         assert lib.qwp_decode_selected(3, 1, 152064, 4096) == INVALID
         assert lib.qwp_decode_selected(-1, 1, 152064, 4096) == INVALID
         assert qwp.set_decode_policy(qwp.DECODE_ALWAYS) == qwp.DECODE_AUTO

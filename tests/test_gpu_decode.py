@@ -69,14 +69,17 @@ def test_default_policy_both_kernels(M, N, K):
         check_bound(y, ref, mag, f"policy {policy} M{M} N{N} K{K}")
 
 
-@pytest.mark.parametrize("fmt,M,decode", [("q6k", 1, True), ("q6k", 2, True), ("w4a16", 1, True),
-                                           ("w4a16", 2, False)])
-def test_default_policy_per_format(fmt, M, decode):
-    """The default choice per weight format on a wide matrix (N = 65600, K = 512):
-    Q6_K takes the decode kernel at one and two tokens, W4A16 at one token only;
-    under either kernel (default, then forced onto the prefill kernel) the result
-    meets the bound against the oracle."""
-    N, K, g = 65600, 512, 128
+@pytest.mark.parametrize("fmt,M,N,decode", [("q6k", 1, 65600, True), ("q6k", 2, 65600, True),
+                                             ("q6k", 1, 24640, False), ("w4a16", 1, 65600, True),
+                                             ("w4a16", 2, 65600, True), ("w4a16", 1, 24640, True),
+                                             ("w4a16", 2, 24640, False)])
+def test_default_policy_per_format(fmt, M, N, decode):
+    """The default choice per weight format on wide matrices (K = 512 or 1536, so
+    that both take at least 600 tile items): Q6_K takes the decode kernel from N =
+    65536, W4A16 from N = 24576 at one token and from 65536 at two; under either
+    kernel (default, then forced onto the prefill kernel) the result meets the
+    bound against the oracle."""
+    K, g = (512 if N > 65536 else 1536), 128
     xb = synth.activations_bf16(M, K, seed=M + 17)
     if fmt == "q6k":
         blocks = synth.q6k_weights(N, K, seed=M * 59 + N)
