@@ -141,6 +141,7 @@ def _x_conversion(M, N, K, fmt="q4k"):
                                          (1, 19456, 4096, "epilogue"), (1, 700, 8192, "epilogue"),
                                          (2, 3000, 1024, "epilogue"), (32, 2048, 2048, "epilogue"),
                                          (105, 4096, 4096, "kernel"), (16, 1000, 768, "epilogue"),
+                                         (13, 700, 8192, "epilogue"), (24, 1000, 1536, "epilogue"),
                                          (8, 40000, 1024, "kernel"), (300, 40000, 256, "kernel")])
 def test_q4k_bf16_x_conversion_paths(M, N, K, where):
     """bf16 x on the prefill kernel, each way of converting it to the fp16 MMA
