@@ -48,10 +48,13 @@ constexpr int SK_MAX_N = 64;                   // weight rows (MMA N, padded to 
 constexpr int SK_MAX_XS = 8;                   // x ring: one 64-wide K block per slot
 constexpr int SK_MIN_XS = 3;
 constexpr int SK_X_SLOT = SK_TOKENS * 128;     // 128 tokens x 64 16-bit values = 16 KiB
-constexpr int SK_BS = 2;                       // B ring: one 256-wide stage per slot
-constexpr int SK_WS = 2;                       // packed weight stages
 constexpr int SK_W_SLOT = SK_MAX_N * Q4K_BLOCK_BYTES;
-constexpr int SK_NUM_BARS = 2 * SK_MAX_XS + 2 * SK_WS + 2 * SK_BS + 2;
+constexpr int SK_SHORT_STAGES = 4;             // K range of a "short" CTA, in 256-wide stages
+// B ring (one 256-wide stage per slot) and packed-weight ring depths: two each,
+// or, for a CTA whose K range is at most SK_SHORT_STAGES stages, all of them.
+__host__ __device__ constexpr int sk_rings(bool short_k) { return short_k ? SK_SHORT_STAGES : 2; }
+constexpr int SK_MAX_RING = SK_SHORT_STAGES;
+constexpr int SK_NUM_BARS = 2 * SK_MAX_XS + 4 * SK_MAX_RING + 2;
 constexpr int SK_SMEM = 227 * 1024;            // requested; the layout below fits inside
 constexpr int SK_XFORM0 = 3, SK_NXFORM = 4;    // transform / epilogue warps
 constexpr int SK_THREADS = 32 * (SK_XFORM0 + SK_NXFORM);
@@ -62,22 +65,29 @@ constexpr uint32_t SK_TMEM_COLS = 64;
 // 128 bytes, twice that for bf16 x, whose lo tiles follow the hi tiles), the
 // packed weight ring, the barriers and two words (tensor-memory base, abort flag).
 struct SkLayout {
-    int xs, b_slot, off_b, off_w, off_bar, off_misc;
+    int xs, b_slot, w_slot, off_b, off_w, off_bar, off_misc;
 };
-__host__ __device__ constexpr SkLayout sk_layout(int n_pad, bool bf16) {
+__host__ __device__ constexpr SkLayout sk_layout(int n_pad, bool bf16, int rows, bool short_k) {
     SkLayout l{};
     l.b_slot = (bf16 ? 2 : 1) * 4 * n_pad * 128;
-    const int rest = SK_BS * l.b_slot + SK_WS * SK_W_SLOT + 8 * SK_NUM_BARS + 16 + 1024;  // + base alignment slack
+    l.w_slot = short_k ? (rows * Q4K_BLOCK_BYTES + 15) & ~15 : SK_W_SLOT;
+    const int R = sk_rings(short_k);
+    const int rest = R * l.b_slot + R * l.w_slot + 8 * SK_NUM_BARS + 16 + 1024;  // + base alignment slack
     l.xs = (SK_SMEM - rest) / SK_X_SLOT;
     if (l.xs > SK_MAX_XS) l.xs = SK_MAX_XS;
     l.off_b = l.xs * SK_X_SLOT;
-    l.off_w = l.off_b + SK_BS * l.b_slot;
-    l.off_bar = l.off_w + SK_WS * SK_W_SLOT;
+    l.off_w = l.off_b + R * l.b_slot;
+    l.off_bar = l.off_w + R * l.w_slot;
     l.off_misc = l.off_bar + 8 * SK_NUM_BARS;
     return l;
 }
-static_assert(sk_layout(SK_MAX_N, true).xs >= SK_MIN_XS, "the x ring keeps at least three slots");
-static_assert(sk_layout(SK_MAX_N, true).off_misc + 16 + 1024 <= SK_SMEM, "shared memory budget");
+static_assert(sk_layout(SK_MAX_N, true, SK_MAX_N, false).xs >= SK_MIN_XS, "the x ring keeps at least three slots");
+static_assert(sk_layout(SK_MAX_N, true, SK_MAX_N, false).off_misc + 16 + 1024 <= SK_SMEM, "shared memory budget");
+// Whether a launch takes the short-K rings: its CTAs' K range is at most
+// SK_SHORT_STAGES stages and the layout still leaves four x slots.
+__host__ __device__ constexpr bool sk_short(int n_pad, bool bf16, int rows, int stages) {
+    return stages <= SK_SHORT_STAGES && sk_layout(n_pad, bf16, rows, true).xs >= 4;
+}
 static_assert(SK_SMEM <= 232448, "opt-in shared memory per CTA");
 // The partial tile of one CTA overlays its x ring: [128 tokens][n_pad + 4] fp32
 // (the 4 extra floats per row spread the rows over the banks).
@@ -103,6 +113,10 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
     return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// kShort: the rings of sk_rings(true) (see sk_short); compiled apart, so that the
+// ring indexing stays constant in both (with run-time depths the longer shapes
+// measured 2-5% slower).
+template <bool kShort>
 __global__ void __launch_bounds__(SK_THREADS, 1)
     qwp_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const SkinnyArgs args) {
     extern __shared__ uint8_t smem_raw[];
@@ -110,7 +124,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
                                                 ~static_cast<uintptr_t>(1023));
     const uint32_t warp = warp_id(), lane = lane_id();
     const bool bf16 = args.x_bf16 != 0;
-    const SkLayout L = sk_layout(args.n_pad, bf16);
+    const SkLayout L = sk_layout(args.n_pad, bf16, args.N, kShort);
+    constexpr int BS = sk_rings(kShort), WS = sk_rings(kShort);
     const int XS = L.xs;
     const int S = args.splits;
     const int rank = static_cast<int>(blockIdx.x);  // cluster rank along K
@@ -122,12 +137,12 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
 
     const uint32_t bar0 = smem_u32(smem + L.off_bar);
     const uint32_t x_full = bar0, x_empty = x_full + 8 * SK_MAX_XS;
-    const uint32_t w_full = x_empty + 8 * SK_MAX_XS, w_empty = w_full + 8 * SK_WS;
-    const uint32_t b_full = w_empty + 8 * SK_WS, b_empty = b_full + 8 * SK_BS;
-    const uint32_t acc_full = b_empty + 8 * SK_BS, drain = acc_full + 8;
+    const uint32_t w_full = x_empty + 8 * SK_MAX_XS, w_empty = w_full + 8 * SK_MAX_RING;
+    const uint32_t b_full = w_empty + 8 * SK_MAX_RING, b_empty = b_full + 8 * SK_MAX_RING;
+    const uint32_t acc_full = b_empty + 8 * SK_MAX_RING, drain = acc_full + 8;
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + L.off_misc);  // [0] tensor memory, [1] abort
     const Ctl ctl{misc + 1, args.status, args.timeout_cycles, args.drain_cycles};
-    const int x_pre = min(XS, nblk), w_pre = min(SK_WS, args.stages);  // copies started at set-up
+    const int x_pre = min(XS, nblk), w_pre = min(WS, args.stages);  // copies started at set-up
     const uint32_t w_bytes = static_cast<uint32_t>(R) * Q4K_BLOCK_BYTES;
 
     pdl_launch_dependents();
@@ -136,11 +151,11 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
             mbar_init(x_full + 8 * s, 1);
             mbar_init(x_empty + 8 * s, 1);
         }
-        for (int s = 0; s < SK_WS; ++s) {
+        for (int s = 0; s < WS; ++s) {
             mbar_init(w_full + 8 * s, 1);
             mbar_init(w_empty + 8 * s, SK_NXFORM);
         }
-        for (int s = 0; s < SK_BS; ++s) {
+        for (int s = 0; s < BS; ++s) {
             mbar_init(b_full + 8 * s, SK_NXFORM);
             mbar_init(b_empty + 8 * s, 1);
         }
@@ -164,7 +179,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         }
         for (int i = 0; i < w_pre; ++i) {
             mbar_arrive_expect_tx(w_full + 8 * i, w_bytes);
-            bulk_copy_g2s(smem_u32(smem + L.off_w + i * SK_W_SLOT), args.w + q4k_group_offset(args.K, 0, R, st0 + i),
+            bulk_copy_g2s(smem_u32(smem + L.off_w + i * L.w_slot), args.w + q4k_group_offset(args.K, 0, R, st0 + i),
                           w_bytes, w_full + 8 * i);
         }
         misc[1] = (status_now & kStatusTimeoutMask) ? 1u : 0u;
@@ -206,14 +221,14 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         if (lane == 0 && !skip) {
             int i = w_pre;
             for (; i < args.stages; ++i) {
-                const int ws = i % SK_WS;
-                if (i >= SK_WS && !wait_bar(w_empty + 8 * ws, ((i / SK_WS) & 1) ^ 1, ctl, SW_W_EMPTY)) break;
+                const int ws = i % WS;
+                if (i >= WS && !wait_bar(w_empty + 8 * ws, ((i / WS) & 1) ^ 1, ctl, SW_W_EMPTY)) break;
                 mbar_arrive_expect_tx(w_full + 8 * ws, w_bytes);
-                bulk_copy_g2s(smem_u32(smem + L.off_w + ws * SK_W_SLOT), args.w + q4k_group_offset(args.K, 0, R, st0 + i),
+                bulk_copy_g2s(smem_u32(smem + L.off_w + ws * L.w_slot), args.w + q4k_group_offset(args.K, 0, R, st0 + i),
                               w_bytes, w_full + 8 * ws);
             }
-            for (int g = max(0, i - SK_WS); g < i; ++g)
-                wait_bar(w_full + 8 * (g % SK_WS), (g / SK_WS) & 1, ctl, SW_DRAIN, false);
+            for (int g = max(0, i - WS); g < i; ++g)
+                wait_bar(w_full + 8 * (g % WS), (g / WS) & 1, ctl, SW_DRAIN, false);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -227,8 +242,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
             int xs = 0;
             uint32_t xph = 0;
             for (int i = 0; ok && i < args.stages; ++i) {
-                const int bs = i % SK_BS;
-                if (!(ok = __all_sync(0xffffffffu, wait_bar(b_full + 8 * bs, (i / SK_BS) & 1, ctl, SW_B_FULL)))) break;
+                const int bs = i % BS;
+                if (!(ok = __all_sync(0xffffffffu, wait_bar(b_full + 8 * bs, (i / BS) & 1, ctl, SW_B_FULL)))) break;
                 for (int blk = 0; blk < 4; ++blk) {
                     if (!(ok = __all_sync(0xffffffffu, wait_bar(x_full + 8 * xs, xph, ctl, SW_X_FULL)))) break;
                     tc_fence_after();
@@ -275,12 +290,12 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         const int groups = (args.n_pad + 31) / 32;
         bool ok = !skip;
         for (int i = 0; ok && i < args.stages; ++i) {
-            const int ws = i % SK_WS, bs = i % SK_BS;
-            if (!(ok = __all_sync(0xffffffffu, wait_bar(w_full + 8 * ws, (i / SK_WS) & 1, ctl, SW_W_FULL)))) break;
-            if (i >= SK_BS &&
-                !(ok = __all_sync(0xffffffffu, wait_bar(b_empty + 8 * bs, ((i / SK_BS) & 1) ^ 1, ctl, SW_B_EMPTY))))
+            const int ws = i % WS, bs = i % BS;
+            if (!(ok = __all_sync(0xffffffffu, wait_bar(w_full + 8 * ws, (i / WS) & 1, ctl, SW_W_FULL)))) break;
+            if (i >= BS &&
+                !(ok = __all_sync(0xffffffffu, wait_bar(b_empty + 8 * bs, ((i / BS) & 1) ^ 1, ctl, SW_B_EMPTY))))
                 break;
-            const uint8_t *wst = smem + L.off_w + ws * SK_W_SLOT;
+            const uint8_t *wst = smem + L.off_w + ws * L.w_slot;
             uint8_t *bst = smem + L.off_b + bs * L.b_slot;
             for (int pr = xw; pr < 4 * groups; pr += SK_NXFORM) {
                 const int g = pr >> 2, blk = pr & 3;
@@ -434,9 +449,14 @@ static int sk_device_sms(int &sms) {
     if (!cache[dev]) {
         int n = 0;
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return QWP_ERR_CUDA;
-        if (cudaFuncSetAttribute(qwp_skinny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM) !=
+        if (cudaFuncSetAttribute(qwp_skinny_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM) !=
                 cudaSuccess ||
-            cudaFuncSetAttribute(qwp_skinny_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
+            cudaFuncSetAttribute(qwp_skinny_kernel<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(qwp_skinny_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(qwp_skinny_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
+                cudaSuccess)
             return QWP_ERR_CUDA;
         cache[dev] = n;
     }
@@ -510,7 +530,9 @@ int launch_skinny(const void *w, const void *x, bool x_bf16, float *y, int64_t M
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, qwp_skinny_kernel, map, a) != cudaSuccess) {
+    const bool short_k = sk_short(a.n_pad, x_bf16, a.N, a.stages);
+    if (cudaLaunchKernelEx(&cfg, short_k ? qwp_skinny_kernel<true> : qwp_skinny_kernel<false>, map, a) !=
+        cudaSuccess) {
         cudaGetLastError();
         return QWP_ERR_CUDA;
     }
