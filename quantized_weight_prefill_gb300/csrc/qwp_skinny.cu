@@ -439,7 +439,11 @@ static SkEncodeTiledFn sk_encode_fn() {
     return fn;
 }
 
-// The SM count (cached per device) and the kernel's shared-memory attribute.
+// The SM count and the clusters of S = 1, 2, 4, 8 CTAs that can be resident at
+// once (cached per device), and the kernel's shared-memory attribute.  (Clusters
+// of 8 fill only 15 x 8 of GB300's 152 SMs at this footprint, clusters of 4 36 x
+// 4: a grid of more clusters than that runs in two waves.)
+static int sk_cluster_cache[64][9];
 static int sk_device_sms(int &sms) {
     static int cache[64];
     static std::mutex mu;
@@ -458,10 +462,37 @@ static int sk_device_sms(int &sms) {
             cudaFuncSetAttribute(qwp_skinny_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
                 cudaSuccess)
             return QWP_ERR_CUDA;
+        for (int S = 1; S <= 8; S *= 2) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(S), 64, 1);
+            cfg.blockDim = dim3(SK_THREADS, 1, 1);
+            cfg.dynamicSmemBytes = SK_SMEM;
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = static_cast<unsigned>(S);
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, qwp_skinny_kernel<false>, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                clusters = n / S;  // the plain SM-count rule
+            }
+            sk_cluster_cache[dev][S] = clusters;
+        }
         cache[dev] = n;
     }
     sms = cache[dev];
     return QWP_OK;
+}
+
+// Resident clusters of S CTAs on the current device (after sk_device_sms).
+static int sk_cluster_slots(int S, int sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || S < 1 || S > 8) return sms / (S < 1 ? 1 : S);
+    const int c = sk_cluster_cache[dev][S];
+    return c > 0 ? c : sms / S;
 }
 
 }  // namespace
@@ -474,10 +505,12 @@ bool skinny_selected(int fmt, int64_t M, int64_t N, int64_t K) {
 int skinny_plan(int64_t M, int64_t K, int sms, int &splits, int64_t &tiles) {
     tiles = (M + SK_TOKENS - 1) / SK_TOKENS;
     const int64_t nst = K / Q4K_BLOCK;
+    int dummy = 0;
+    if (sk_device_sms(dummy)) return QWP_ERR_CUDA;
     // The most ranks (a power of two up to 8 that divides the stages) with all
-    // CTAs resident at once; at least one.
+    // clusters resident at once; at least one.
     splits = 1;
-    while (splits < 8 && nst % (2 * splits) == 0 && tiles * 2 * splits <= sms) splits *= 2;
+    while (splits < 8 && nst % (2 * splits) == 0 && tiles <= sk_cluster_slots(2 * splits, sms)) splits *= 2;
     return tiles <= 65535 ? QWP_OK : QWP_ERR_UNSUPPORTED_SHAPE;
 }
 
