@@ -161,7 +161,8 @@ QWP_API int q4k_gemm(const void *w_tiled_dev, const void *x_dev, float *y_dev,
  * to approach the HBM roofline with GEMMs too small to fill the GPU alone, e.g.
  * the experts of a mixture-of-experts layer).  Same operand rounding, error
  * bound and rules as q4k_gemm (bf16 x, converted to fp16 into pool scratch
- * first: batch*M*K*2 bytes) and q4k_gemm_f16 (fp16 x); always the prefill kernel.
+ * first, batch*M*K*2 bytes, or by the kernel itself under the conditions
+ * described for q4k_gemm) and q4k_gemm_f16 (fp16 x); always the prefill kernel.
  * The three base pointers are 16-byte aligned (QWP_ERR_MISALIGNED otherwise);
  * problem p's y, p*M*N floats on, need not be.  batch <= 65535, batch*M*K and
  * batch*M*N <= 2^40 (QWP_ERR_UNSUPPORTED_SHAPE otherwise); batch == 0 is a no-op.
