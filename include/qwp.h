@@ -142,8 +142,9 @@ QWP_API int q4k_gemm_f16(const void *w_tiled_dev, const void *x_dev, float *y_de
  * q4k_gemm_f16 runs, launched so that its set-up overlaps the conversion.  The
  * prefill kernel converts x itself, in shared memory (same rounding and range
  * report; no conversion kernel, no scratch), when each of its CTAs runs one
- * work unit and converts at most 32 KB of x (for example M <= 32 at N = 2048,
- * K = 2048; qwp_gemm_plan tells the plan), and for one token (M == 1).
+ * work unit and converts at most 32 KB of x, or 64 KB of at most 16 token rows
+ * (for example M <= 32 at N = 2048, K = 2048; qwp_gemm_plan tells the plan), and
+ * for one token (M == 1).
  * Skinny-N calls (above) take x as bf16 in the skinny-N kernel: no
  * conversion, no scratch, no range limit.  Same shape and alignment rules as
  * q4k_gemm_f16.

@@ -1226,15 +1226,18 @@ static int plan_gemm(int64_t M, int64_t N, int64_t K, Plan &plan, int &bn, int64
 // the end) and its x is small, 1 for one token (the MMA warp), else 0 (the
 // caller converts x first).  Each CTA converts the x of its own unit and K range,
 // so CTAs that share a token tile convert it again; measured on GB300, up to
-// X_CONVERT_MAX_BYTES per CTA the launch saved over the conversion kernel (Q4_K
-// M=8 N4096 K4096 11.4 -> 10.0 us, M=32 N2048 K2048 8.4 -> 8.0 us), while 229 KB
-// per CTA (M=105, N4096, K4096, split-K 4) took 13.8 -> 21.5 us and 131 KB (a
-// batch of eight M=32 N2048 K2048 products) 17.5 -> 20.7 us.
-constexpr int64_t X_CONVERT_MAX_BYTES = 32 * 1024;
+// 32 KB per CTA (64 KB with at most 16 token rows) the launch saved over the
+// conversion kernel (Q4_K M=8 N4096 K4096 11.4 -> 10.0 us, M=32 N2048 K2048 8.4
+// -> 8.0 us, M=8 N4096 K12288 20.3 -> 19.3 us, M=16 N6144 K4096 15.4 -> 15.0
+// us), while 64 KB of 32 rows (M=32 N4096 K4096) took 11.4 -> 11.8 us, 229 KB
+// (M=105, N4096, K4096, split-K 4) 13.8 -> 21.5 us and 131 KB (a batch of eight
+// M=32 N2048 K2048 products) 17.5 -> 20.7 us.
 static int x_convert_mode(const Plan &plan, int bn, int64_t units_all, int64_t M, int64_t K) {
     const int64_t k_cta = (K / CHUNK_K + plan.S - 1) / plan.S * CHUNK_K;  // K of one split, at most
-    const int64_t bytes = std::min<int64_t>(bn, M) * k_cta * 2;
-    if (units_all <= plan.clusters && bn <= static_cast<int>(ACC_STRIDE) && bytes <= X_CONVERT_MAX_BYTES) return 2;
+    const int64_t rows = std::min<int64_t>(bn, M);
+    const int64_t bytes = rows * k_cta * 2;
+    const bool small = bytes <= 32 * 1024 || (rows <= 16 && bytes <= 64 * 1024);
+    if (units_all <= plan.clusters && bn <= static_cast<int>(ACC_STRIDE) && small) return 2;
     return M <= CONVERT_MAX_M ? 1 : 0;
 }
 

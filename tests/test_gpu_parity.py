@@ -127,12 +127,15 @@ def test_q4k_gemm_f16_activations(M, N, K):
 def _x_conversion(M, N, K, fmt="q4k"):
     """Where a bf16-x call of this shape on the prefill kernel converts x: "epilogue"
     (every CTA runs at most one unit with two accumulators and converts at most
-    32 KB of x: the epilogue warps convert each x slot), "mma" (one token: the MMA
-    warp converts the token row), else "kernel" (a conversion kernel first)."""
+    32 KB of x, or 64 KB of at most 16 token rows: the epilogue warps convert each
+    x slot), "mma" (one token: the MMA warp converts the token row), else "kernel"
+    (a conversion kernel first)."""
     p = qwp.gemm_plan(fmt, M, N, K)
     assert p["kernel"] == "prefill"
     k_cta = -(-(K // 64) // p["splits"]) * 64
-    if p["units_per_cluster"] == 1 and p["token_tile"] <= 128 and min(p["token_tile"], M) * k_cta * 2 <= 32768:
+    rows = min(p["token_tile"], M)
+    small = rows * k_cta * 2 <= 32768 or (rows <= 16 and rows * k_cta * 2 <= 65536)
+    if p["units_per_cluster"] == 1 and p["token_tile"] <= 128 and small:
         return "epilogue"
     return "mma" if M == 1 else "kernel"
 
@@ -142,6 +145,7 @@ def _x_conversion(M, N, K, fmt="q4k"):
                                          (2, 3000, 1024, "epilogue"), (32, 2048, 2048, "epilogue"),
                                          (105, 4096, 4096, "kernel"), (16, 1000, 768, "epilogue"),
                                          (13, 700, 8192, "epilogue"), (24, 1000, 1536, "epilogue"),
+                                         (8, 4096, 12288, "epilogue"), (32, 4096, 4096, "kernel"),
                                          (8, 40000, 1024, "kernel"), (300, 40000, 256, "kernel")])
 def test_q4k_bf16_x_conversion_paths(M, N, K, where):
     """bf16 x on the prefill kernel, each way of converting it to the fp16 MMA
