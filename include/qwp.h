@@ -33,9 +33,11 @@
  * K is split over a thread-block cluster and summed through distributed shared
  * memory in a fixed order.  With fp16 x the weights are the same single-rounded
  * fp16 operand as above; with bf16 x each weight is the pair hi = bf16(w32),
- * lo = bf16(w32 - hi) of its fp32 value w32, both multiplied with x and summed
- * in the accumulator (relative weight error at most 2^-18 + 2^-24, so no range
- * limit on x and no QWP_ERR_RANGE).  It allocates nothing.
+ * lo = bf16(w32 - hi) of its fp32 value w32, both multiplied with x (x.hi and
+ * x.lo accumulated apart in fp32 and added at the end; relative weight error at
+ * most 2^-18 + 2^-24, so no range limit on x and no QWP_ERR_RANGE).  Token
+ * tiles of up to 128 tokens are cut so that the clusters fill the GPU in whole
+ * waves.  It allocates nothing.
  * Every entry point returns QWP_OK (0) or a negative qwp_status; none throws.
  * Calls are thread-safe, with one exception: q4k_gemm_noalloc keeps its scratch
  * in fixed arrays that all its calls on a device share, so its calls must not
@@ -392,8 +394,8 @@ QWP_API int qwp_decode_selected(int format, int64_t M, int64_t N, int64_t K);
  * it reads the device's properties but launches nothing).  `format`: 0 W4A16,
  * 1 Q4_K, 2 Q6_K.  plan_out[6] receives: [0] the kernel (1 the prefill kernel,
  * 2 the decode kernel, which leaves [1..5] at 0, 3 the skinny-N kernel, which
- * reports its split and clusters (token tiles of 128) the same way and 1 unit
- * per cluster); [1] the split-K factor S (the
+ * reports its split, clusters and token tile (at most 128 tokens; the plan of
+ * bf16 activations) the same way and 1 unit per cluster); [1] the split-K factor S (the
  * cluster size); [2] the clusters launched; [3] the token tile (tokens per
  * unit); [4] the units (128-row tiles x token tiles); [5] the units per cluster
  * at most.  Returns QWP_OK, QWP_ERR_INVALID_ARG (NULL plan_out, a size below 1,

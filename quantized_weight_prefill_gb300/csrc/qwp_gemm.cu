@@ -1598,16 +1598,16 @@ extern "C" int qwp_gemm_plan(int format, int64_t M, int64_t N, int64_t K, int32_
     int rc = check_device();
     if (rc) return rc;
     if (skinny_selected(format, M, N, K)) {
-        int dev = 0, sms = 0, S = 1;
+        int dev = 0, sms = 0, S = 1, tm = 0;
         int64_t tiles = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return QWP_ERR_CUDA;
-        if ((rc = skinny_plan(M, K, sms, S, tiles))) return rc;
+        if ((rc = skinny_plan(M, K, true, sms, S, tiles, tm))) return rc;  // the bf16-x entry point's plan
         plan_out[0] = 3;
         plan_out[1] = S;
         plan_out[2] = static_cast<int32_t>(tiles);
-        plan_out[3] = 128;
+        plan_out[3] = tm;
         plan_out[4] = static_cast<int32_t>(tiles);
         plan_out[5] = 1;
         return QWP_OK;

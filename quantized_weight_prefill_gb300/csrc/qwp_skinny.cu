@@ -4,22 +4,27 @@
 // 128 x 128 tile wastes three quarters of it and leaves most SMs idle.  Here the
 // activations are the stream that matters (M*K*2 bytes against N*K*0.5625 of
 // weights), so the roles of the general kernel are turned around:
-//   * tokens are the MMA's M side: a 128-token x tile (one 64-wide K block) is
-//     the A operand, loaded by TMA into shared memory (128-byte swizzle) and
-//     given to the tensor core as it is, bf16 or fp16: every activation is read
-//     once, by the one CTA that uses it, and never converted;
+//   * tokens are the MMA's M side: an x tile of up to 128 tokens (one 64-wide K
+//     block) is the A operand, loaded by TMA into shared memory (128-byte
+//     swizzle) and given to the tensor core as it is, bf16 or fp16: every
+//     activation is read once, by the one CTA that uses it, and never converted.
+//     The tile height is chosen per launch so that the grid fills the GPU in
+//     whole waves (the MMA still covers 128 rows; rows past the tile are not
+//     loaded and their results are never stored);
 //   * the weights are the B operand (N padded to 16..64 rows): the packed Q4_K
 //     stages are bulk-copied into shared memory and unpacked by the transform
 //     warps into a ring of swizzled K-major tiles.  For fp16 x that is one fp16
 //     tile per 64-wide K block, the single-rounding operand of the general
 //     kernel.  For bf16 x (kind::f16 wants A and B of one type) it is two bf16
 //     tiles, hi and lo, whose sum carries the weight to about 16 significant
-//     bits, and two MMAs per K step: the weight side is only N/128 of the work;
-//   * the fp32 accumulator D[128 tokens x N] lives in tensor memory;
+//     bits, stacked as one operand of 2N rows: one MMA per K step (its time is
+//     set by the 128 token rows, not by N at these widths) accumulates x.hi and
+//     x.lo side by side, and the epilogue adds the two;
+//   * the fp32 accumulator D[128 tokens x N (2N)] lives in tensor memory;
 //   * K is split S ways across a thread-block cluster (grid S x token tiles, S a
 //     power of two dividing the 256-wide stages); each CTA writes its partial
 //     tile into its own (idle) x ring, and after a cluster barrier each rank sums
-//     a 128/S-row slice over the ranks, in rank order (deterministic), reading
+//     a 1/S slice of the tile's rows over the ranks, in rank order (deterministic), reading
 //     its peers' shared memory, and writes y; a second cluster barrier keeps
 //     every CTA alive until its peers have read it.
 // One launch, no device memory of its own.  Roles:
@@ -43,7 +48,7 @@
 namespace qwp {
 namespace {
 
-constexpr int SK_TOKENS = 128;                 // tokens per CTA (MMA M)
+constexpr int SK_TOKENS = 128;                 // MMA M: the most tokens per CTA
 constexpr int SK_MAX_N = 64;                   // weight rows (MMA N, padded to 16)
 constexpr int SK_MAX_XS = 8;                   // x ring: one 64-wide K block per slot
 constexpr int SK_MIN_XS = 3;
@@ -58,11 +63,11 @@ constexpr int SK_NUM_BARS = 2 * SK_MAX_XS + 4 * SK_MAX_RING + 2;
 constexpr int SK_SMEM = 227 * 1024;            // requested; the layout below fits inside
 constexpr int SK_XFORM0 = 3, SK_NXFORM = 4;    // transform / epilogue warps
 constexpr int SK_THREADS = 32 * (SK_XFORM0 + SK_NXFORM);
-constexpr uint32_t SK_TMEM_COLS = 64;
+constexpr uint32_t SK_TMEM_COLS = 2 * SK_MAX_N;  // bf16 x: the hi and the lo sums
 
 // The shared-memory layout (offsets from the 1 KiB-aligned base): the x ring of
 // `xs` slots, the B ring (a slot is one 256-wide stage: 4 blocks of n_pad rows x
-// 128 bytes, twice that for bf16 x, whose lo tiles follow the hi tiles), the
+// 128 bytes, for bf16 x of 2 n_pad rows: the hi rows, then the lo rows), the
 // packed weight ring, the barriers and two words (tensor-memory base, abort flag).
 struct SkLayout {
     int xs, b_slot, w_slot, off_b, off_w, off_bar, off_misc;
@@ -99,6 +104,7 @@ struct SkinnyArgs {
     uint32_t *status;
     int M, N, K;
     int n_pad;            // N rounded up to 16
+    int tm;               // tokens per CTA (token tile height, 1..SK_TOKENS)
     int splits;           // S (cluster size along x)
     int stages;           // 256-wide stages per CTA (K / 256 / S)
     int x_bf16;           // 1: x and the weight operands are bf16 (hi + lo), else fp16
@@ -129,11 +135,13 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     const int XS = L.xs;
     const int S = args.splits;
     const int rank = static_cast<int>(blockIdx.x);  // cluster rank along K
-    const int m0 = static_cast<int>(blockIdx.y) * SK_TOKENS;
+    const int tm = args.tm;
+    const int m0 = static_cast<int>(blockIdx.y) * tm;
     const int st0 = rank * args.stages;              // first 256-wide stage of this CTA
     const int nblk = 4 * args.stages;                // 64-wide K blocks of this CTA
     const int R = args.N;                            // weight rows (one tile)
-    const uint32_t b_tile = static_cast<uint32_t>(args.n_pad) * 128u;  // one block of B (hi, or the fp16 tile)
+    const uint32_t b_tile = static_cast<uint32_t>(args.n_pad) * 128u;  // n_pad rows of B (hi, lo, or fp16)
+    const uint32_t b_blk = (bf16 ? 2u : 1u) * b_tile;                     // one 64-wide K block of B
 
     const uint32_t bar0 = smem_u32(smem + L.off_bar);
     const uint32_t x_full = bar0, x_empty = x_full + 8 * SK_MAX_XS;
@@ -144,6 +152,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     const Ctl ctl{misc + 1, args.status, args.timeout_cycles, args.drain_cycles};
     const int x_pre = min(XS, nblk), w_pre = min(WS, args.stages);  // copies started at set-up
     const uint32_t w_bytes = static_cast<uint32_t>(R) * Q4K_BLOCK_BYTES;
+    const uint32_t x_bytes = static_cast<uint32_t>(tm) * 128u;  // one TMA box: tm rows of 64 values
 
     pdl_launch_dependents();
     if (threadIdx.x == 0) {
@@ -174,7 +183,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         // The first x tiles and weight stages start before the block-wide barrier
         // (their slots are empty); this thread is also the x producer.
         for (int j = 0; j < x_pre; ++j) {
-            mbar_arrive_expect_tx(x_full + 8 * j, SK_X_SLOT);
+            mbar_arrive_expect_tx(x_full + 8 * j, x_bytes);
             tma_load_2d(smem_u32(smem + j * SK_X_SLOT), &tmap_x, (4 * st0 + j) * CHUNK_K, m0, x_full + 8 * j);
         }
         for (int i = 0; i < w_pre; ++i) {
@@ -204,7 +213,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
             uint32_t ph = x_pre == XS ? 1u : 0u;  // the pass over the ring that block j starts
             for (; j < nblk; ++j) {
                 if (j >= XS && !wait_bar(x_empty + 8 * xs, ph ^ 1, ctl, SW_X_EMPTY)) break;
-                mbar_arrive_expect_tx(x_full + 8 * xs, SK_X_SLOT);
+                mbar_arrive_expect_tx(x_full + 8 * xs, x_bytes);
                 tma_load_2d(smem_u32(smem + xs * SK_X_SLOT), &tmap_x, (4 * st0 + j) * CHUNK_K, m0, x_full + 8 * xs);
                 if (++xs == XS) {
                     xs = 0;
@@ -233,11 +242,11 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // Per 64-wide K block: 4 K steps of 16; both operands advance 32 bytes (2
-        // descriptor units) per step.  bf16 x: each step is two MMAs, with the hi
-        // and the lo weight tiles, into the same accumulator.
+        // descriptor units) per step.  bf16 x: the B operand is the hi and the lo
+        // rows together (MMA N = 2 n_pad).
         if (!skip) {
-            const uint32_t idesc = make_idesc_f16(bf16, SK_TOKENS, static_cast<uint32_t>(args.n_pad));
-            const uint32_t lo_off = bf16 ? 4u * b_tile : 0u;
+            const uint32_t idesc =
+                make_idesc_f16(bf16, SK_TOKENS, static_cast<uint32_t>((bf16 ? 2 : 1) * args.n_pad));
             bool ok = true;
             int xs = 0;
             uint32_t xph = 0;
@@ -248,20 +257,15 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
                     if (!(ok = __all_sync(0xffffffffu, wait_bar(x_full + 8 * xs, xph, ctl, SW_X_FULL)))) break;
                     tc_fence_after();
                     const uint64_t a_desc = smem_desc_sw128(smem_u32(smem + xs * SK_X_SLOT));
-                    const uint32_t b_addr = smem_u32(smem + L.off_b + bs * L.b_slot) + blk * b_tile;
-                    const uint64_t b_desc = smem_desc_sw128(b_addr);
-                    const uint64_t l_desc = smem_desc_sw128(b_addr + lo_off);
+                    const uint64_t b_desc =
+                        smem_desc_sw128(smem_u32(smem + L.off_b + bs * L.b_slot) + blk * b_blk);
                     if (elect_one()) {
                         if (i == 0 && blk == 0)
                             mma_ss<false>(tmem, a_desc, b_desc, idesc);
                         else
                             mma_ss<true>(tmem, a_desc, b_desc, idesc);
-                        if (bf16) mma_ss<true>(tmem, a_desc, l_desc, idesc);
 #pragma unroll
-                        for (int kk = 1; kk < 4; ++kk) {
-                            mma_ss<true>(tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc);
-                            if (bf16) mma_ss<true>(tmem, a_desc + 2u * kk, l_desc + 2u * kk, idesc);
-                        }
+                        for (int kk = 1; kk < 4; ++kk) mma_ss<true>(tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc);
                         mma_commit(x_empty + 8 * xs);
                     }
                     __syncwarp();
@@ -310,9 +314,9 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
                 }
                 const Q4kSubH k0 = q4k_sub_f16(hdr, 2 * blk), k1 = q4k_sub_f16(hdr, 2 * blk + 1);
                 const uint32_t w[8] = {wv0.x, wv0.y, wv0.z, wv0.w, wv1.x, wv1.y, wv1.z, wv1.w};
-                uint8_t *bt = bst + blk * b_tile;
+                uint8_t *bt = bst + blk * b_blk;
                 if (bf16) {
-                    uint8_t *lt = bt + 4 * b_tile;
+                    uint8_t *lt = bt + b_tile;  // row n_pad + r: the swizzle of row r (n_pad % 8 == 0)
 #pragma unroll
                     for (int v = 0; v < 8; ++v) {  // word v holds elements 8v..8v+7: 16-byte chunk v of the row
                         uint32_t h[4], l[4];
@@ -343,7 +347,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     }
 
     // The accumulator: warps 3..6 (lane quarters 3, 0, 1, 2) hold token rows
-    // 32q .. 32q+31 of the tile, n_pad columns each.  S == 1: straight to y.  S > 1:
+    // 32q .. 32q+31 of the tile, n_pad columns each (bf16 x: the hi sums, then
+    // n_pad columns of lo sums, added here).  S == 1: straight to y.  S > 1:
     // into this CTA's x ring, [row][n_pad + 4], for the cluster's reduction (every
     // x tile has been consumed once the accumulator is complete).
     const int pstride = args.n_pad + 4;
@@ -355,9 +360,17 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
             for (int c0 = 0; c0 < args.n_pad; c0 += 16) {
                 uint32_t v[16];
                 tmem_ld_x16(tmem + ((q * 32u) << 16) + static_cast<uint32_t>(c0), v);
-                tmem_wait_ld();
+                if (bf16) {
+                    uint32_t u[16];
+                    tmem_ld_x16(tmem + ((q * 32u) << 16) + static_cast<uint32_t>(args.n_pad + c0), u);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(u[e]));
+                } else {
+                    tmem_wait_ld();
+                }
                 if (S == 1) {
-                    if (m < args.M) {
+                    if (row < tm && m < args.M) {
                         float *yr = args.y + static_cast<int64_t>(m) * args.N + c0;
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
@@ -376,8 +389,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     }
     if (S > 1) {
         // Every rank's partial tile is in its shared memory (or the rank failed and
-        // the status word says so); rank r sums rows [r*128/S, (r+1)*128/S) over the
-        // ranks in rank order and writes them.  The second barrier keeps each CTA's
+        // the status word says so); rank r sums rows [r*rows, (r+1)*rows) of the
+        // tile (rows = ceil(tm/S) <= 128/S) over the ranks in rank order and writes them.  The second barrier keeps each CTA's
         // shared memory alive until its peers have read it: a thread arrives after
         // its sums (which consumed every value it loaded from a peer) are stored, so
         // it needs no release, and not waiting for the y stores to complete keeps
@@ -385,10 +398,11 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         __syncwarp();
         cluster_sync();
         if (!skip && !aborted(ctl)) {
-            const int rows = SK_TOKENS / S, groups = args.n_pad / 4;
+            const int rows = (tm + S - 1) / S, groups = args.n_pad / 4;
             const uint32_t local = smem_u32(pbuf);
             for (int it = static_cast<int>(threadIdx.x); it < rows * groups; it += SK_THREADS) {
                 const int row = rank * rows + it / groups, c = 4 * (it % groups);
+                if (row >= tm) break;  // rows grow with it
                 const uint32_t off = static_cast<uint32_t>((row * pstride + c) * 4);
                 float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
                 for (int r2 = 0; r2 < S; ++r2) {
@@ -502,15 +516,36 @@ bool skinny_selected(int fmt, int64_t M, int64_t N, int64_t K) {
            M <= (int64_t(1) << 30);
 }
 
-int skinny_plan(int64_t M, int64_t K, int sms, int &splits, int64_t &tiles) {
-    tiles = (M + SK_TOKENS - 1) / SK_TOKENS;
+// Launch plan: S CTAs per cluster along K (a power of two up to 8 dividing the
+// 256-wide stages) and token tiles of tm <= 128 rows, cut so that the clusters run
+// in whole waves of resident clusters.  Per CTA and 64-wide K block the time is
+// the larger of its x stream (tm rows of 128 bytes) and its MMAs (128 rows
+// whatever tm is: two per K step for bf16 x), plus a fixed cost per wave and one
+// for the cluster reduction; the cheapest plan wins.  In units of the stream
+// time of one 128-byte row at the full-GPU rate (~3 ns on GB300): the MMAs of a
+// block cost 77 rows (bf16 x) or 39 (fp16 x), a wave or a reduction ~2 us.
+int skinny_plan(int64_t M, int64_t K, bool x_bf16, int sms, int &splits, int64_t &tiles, int &tm) {
     const int64_t nst = K / Q4K_BLOCK;
     int dummy = 0;
     if (sk_device_sms(dummy)) return QWP_ERR_CUDA;
-    // The most ranks (a power of two up to 8 that divides the stages) with all
-    // clusters resident at once; at least one.
-    splits = 1;
-    while (splits < 8 && nst % (2 * splits) == 0 && tiles <= sk_cluster_slots(2 * splits, sms)) splits *= 2;
+    const int64_t mma_rows = x_bf16 ? 77 : 39, fixed = 625;
+    double best = 1e300;
+    splits = 0;
+    for (int S = 1; S <= 8 && nst % S == 0; S *= 2) {
+        const int64_t slots = sk_cluster_slots(S, sms);
+        if (slots < 1) continue;
+        const int64_t waves = (M + SK_TOKENS * slots - 1) / (SK_TOKENS * slots);
+        const int64_t h = (M + waves * slots - 1) / (waves * slots);  // <= SK_TOKENS
+        const int64_t blocks = 4 * (nst / S);
+        const double cost = static_cast<double>(waves) * (blocks * std::max(h, mma_rows) + fixed) + (S > 1 ? fixed : 0);
+        if (cost < best) {
+            best = cost;
+            splits = S;
+            tm = static_cast<int>(h);
+        }
+    }
+    if (splits == 0) return QWP_ERR_CUDA;
+    tiles = (M + tm - 1) / tm;
     return tiles <= 65535 ? QWP_OK : QWP_ERR_UNSUPPORTED_SHAPE;
 }
 
@@ -522,15 +557,15 @@ int launch_skinny(const void *w, const void *x, bool x_bf16, float *y, int64_t M
     if (!status) return QWP_ERR_CUDA;
     int sms = 0;
     if ((rc = sk_device_sms(sms))) return rc;
-    int S = 1;
+    int S = 1, tm = SK_TOKENS;
     int64_t tiles = 0;
-    if ((rc = skinny_plan(M, K, sms, S, tiles))) return rc;
+    if ((rc = skinny_plan(M, K, x_bf16, sms, S, tiles, tm))) return rc;
     SkEncodeTiledFn fn = sk_encode_fn();
     if (!fn) return QWP_ERR_CUDA;
     CUtensorMap map;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(CHUNK_K), static_cast<cuuint32_t>(SK_TOKENS)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(CHUNK_K), static_cast<cuuint32_t>(tm)};
     cuuint32_t estr[2] = {1, 1};
     if (fn(&map, x_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(x),
            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -544,6 +579,7 @@ int launch_skinny(const void *w, const void *x, bool x_bf16, float *y, int64_t M
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
     a.n_pad = static_cast<int>((N + 15) / 16 * 16);
+    a.tm = tm;
     a.splits = S;
     a.stages = static_cast<int>(K / Q4K_BLOCK / S);
     a.x_bf16 = x_bf16 ? 1 : 0;

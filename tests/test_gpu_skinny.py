@@ -1,8 +1,9 @@
 """The skinny-N kernel (Q4_K, N <= 64 weight rows, M >= 256 tokens) against the oracle.
 
 Through the C ABI: bf16 and fp16 activations, weight counts from 1 to 64 (MMA N
-padded to 16, 32, 48, 64), ragged token tiles, K split over clusters of 1, 2, 4
-and 8 CTAs, the workload's stress shape (M=4096, N=32, K=4096; sampled token
+padded to 16, 32, 48, 64), token tiles of 2 to 128 rows (cut to fill whole
+waves) with a ragged last tile, K split over clusters of 1, 2, 4 and 8 CTAs
+(reduction slices that do not divide the tile), the workload's stress shape (M=4096, N=32, K=4096; sampled token
 rows), blocks whose terms cancel, bitwise reproducibility, the no-alloc entry
 point and bf16 activations beyond fp16's range (taken as they are).  Every element must
 meet |y - y_oracle| <= 1e-3 * sum|x*w| + 1e-5.
@@ -37,7 +38,7 @@ def _setup(M, N, K, seed):
 
 # (M, N, K): N over 1..64, ragged M, K giving every cluster size 1, 2, 4, 8.
 SHAPES = [(256, 32, 4096), (300, 1, 256), (1000, 7, 512), (513, 16, 1024), (777, 33, 2048),
-          (4096, 64, 4096), (2048, 48, 12288), (20000, 32, 512), (640, 17, 8192)]
+          (4096, 64, 4096), (2048, 48, 12288), (20000, 32, 512), (640, 17, 8192), (5000, 5, 2048)]
 
 
 def test_shapes_take_the_skinny_kernel_with_every_split():
@@ -45,7 +46,9 @@ def test_shapes_take_the_skinny_kernel_with_every_split():
     for M, N, K in SHAPES:
         p = qwp.gemm_plan("q4k", M, N, K)
         assert p["kernel"] == "skinny", (M, N, K, p)
-        assert p["clusters"] == -(-M // 128) and (K // 256) % p["splits"] == 0
+        tm = p["token_tile"]
+        assert 1 <= tm <= 128 and p["clusters"] == -(-M // tm) and (K // 256) % p["splits"] == 0
+        assert (p["clusters"] - 1) * tm < M  # no empty tile
         splits.add(p["splits"])
     assert {1, 2, 4, 8} <= splits, sorted(splits)
     assert qwp.gemm_plan("q4k", 255, 32, 4096)["kernel"] == "prefill"
@@ -63,7 +66,7 @@ def test_skinny_bf16_against_oracle(M, N, K):
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32)), "not bitwise reproducible"
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 32, 4096), (777, 33, 2048)])
+@pytest.mark.parametrize("M,N,K", [(256, 32, 4096), (777, 33, 2048), (1000, 7, 512), (4096, 32, 4096)])
 def test_skinny_f16_against_oracle(M, N, K):
     blocks = synth.q4k_weights(N, K, seed=M + 5)
     w = qwp.q4k_repack(torch.from_numpy(blocks.reshape(-1)).to(DEV), N, K)
