@@ -51,8 +51,10 @@ namespace {
 constexpr int SK_TOKENS = 128;                 // MMA M: the most tokens per CTA
 constexpr int SK_MAX_N = 64;                   // weight rows (MMA N, padded to 16)
 constexpr int SK_MAX_XS = 8;                   // x ring: one 64-wide K block per slot
+constexpr int SK_X_PRE = 2;                    // x tiles requested before the block-wide barrier
 constexpr int SK_MIN_XS = 3;
-constexpr int SK_X_SLOT = SK_TOKENS * 128;     // 128 tokens x 64 16-bit values = 16 KiB
+// An x slot: tm rows of 64 16-bit values (128 bytes), in whole 1 KiB swizzle atoms.
+__host__ __device__ constexpr int sk_x_slot(int tm) { return (tm * 128 + 1023) & ~1023; }
 constexpr int SK_W_SLOT = SK_MAX_N * Q4K_BLOCK_BYTES;
 constexpr int SK_SHORT_STAGES = 4;             // K range of a "short" CTA, in 256-wide stages
 // B ring (one 256-wide stage per slot) and packed-weight ring depths: two each,
@@ -66,37 +68,43 @@ constexpr int SK_THREADS = 32 * (SK_XFORM0 + SK_NXFORM);
 constexpr uint32_t SK_TMEM_COLS = 2 * SK_MAX_N;  // bf16 x: the hi and the lo sums
 
 // The shared-memory layout (offsets from the 1 KiB-aligned base): the x ring of
-// `xs` slots, the B ring (a slot is one 256-wide stage: 4 blocks of n_pad rows x
-// 128 bytes, for bf16 x of 2 n_pad rows: the hi rows, then the lo rows), the
+// `xs` slots of x_slot bytes (as many as fit, up to SK_MAX_XS), the B ring (a
+// slot is one 256-wide stage: 4 blocks of n_pad rows x 128 bytes, for bf16 x of
+// 2 n_pad rows: the hi rows, then the lo rows), the
 // packed weight ring, the barriers and two words (tensor-memory base, abort flag).
 struct SkLayout {
     int xs, b_slot, w_slot, off_b, off_w, off_bar, off_misc;
 };
-__host__ __device__ constexpr SkLayout sk_layout(int n_pad, bool bf16, int rows, bool short_k) {
+__host__ __device__ constexpr SkLayout sk_layout(int n_pad, bool bf16, int rows, bool short_k, int x_slot) {
     SkLayout l{};
     l.b_slot = (bf16 ? 2 : 1) * 4 * n_pad * 128;
     l.w_slot = short_k ? (rows * Q4K_BLOCK_BYTES + 15) & ~15 : SK_W_SLOT;
     const int R = sk_rings(short_k);
     const int rest = R * l.b_slot + R * l.w_slot + 8 * SK_NUM_BARS + 16 + 1024;  // + base alignment slack
-    l.xs = (SK_SMEM - rest) / SK_X_SLOT;
+    l.xs = (SK_SMEM - rest) / x_slot;
     if (l.xs > SK_MAX_XS) l.xs = SK_MAX_XS;
-    l.off_b = l.xs * SK_X_SLOT;
+    l.off_b = l.xs * x_slot;
     l.off_w = l.off_b + R * l.b_slot;
     l.off_bar = l.off_w + R * l.w_slot;
     l.off_misc = l.off_bar + 8 * SK_NUM_BARS;
     return l;
 }
-static_assert(sk_layout(SK_MAX_N, true, SK_MAX_N, false).xs >= SK_MIN_XS, "the x ring keeps at least three slots");
-static_assert(sk_layout(SK_MAX_N, true, SK_MAX_N, false).off_misc + 16 + 1024 <= SK_SMEM, "shared memory budget");
+static_assert(sk_layout(SK_MAX_N, true, SK_MAX_N, false, sk_x_slot(SK_TOKENS)).xs >= SK_MIN_XS,
+              "the x ring keeps at least three slots");
+static_assert(sk_layout(SK_MAX_N, true, SK_MAX_N, false, sk_x_slot(SK_TOKENS)).off_misc + 16 + 1024 <= SK_SMEM,
+              "shared memory budget");
+static_assert(sk_layout(SK_MAX_N, true, SK_MAX_N, false, sk_x_slot(1)).off_misc + 16 + 1024 <= SK_SMEM,
+              "shared memory budget (smallest slots, SK_MAX_XS of them)");
 // Whether a launch takes the short-K rings: its CTAs' K range is at most
 // SK_SHORT_STAGES stages and the layout still leaves four x slots.
-__host__ __device__ constexpr bool sk_short(int n_pad, bool bf16, int rows, int stages) {
-    return stages <= SK_SHORT_STAGES && sk_layout(n_pad, bf16, rows, true).xs >= 4;
+__host__ __device__ constexpr bool sk_short(int n_pad, bool bf16, int rows, int stages, int x_slot) {
+    return stages <= SK_SHORT_STAGES && sk_layout(n_pad, bf16, rows, true, x_slot).xs >= 4;
 }
 static_assert(SK_SMEM <= 232448, "opt-in shared memory per CTA");
-// The partial tile of one CTA overlays its x ring: [128 tokens][n_pad + 4] fp32
-// (the 4 extra floats per row spread the rows over the banks).
-static_assert(SK_TOKENS * (SK_MAX_N + 4) * 4 <= SK_MIN_XS * SK_X_SLOT, "partial tile fits the x ring");
+// The partial tile of one CTA overlays its x ring: [tm tokens][n_pad + 4] fp32
+// (the 4 extra floats per row spread the rows over the banks), within the
+// first SK_MIN_XS slots of at least tm * 128 bytes each.
+static_assert((SK_MAX_N + 4) * 4 <= SK_MIN_XS * 128, "partial tile fits the x ring");
 
 struct SkinnyArgs {
     const uint8_t *w;     // repacked Q4_K (one tile of R = N rows)
@@ -130,12 +138,13 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
                                                 ~static_cast<uintptr_t>(1023));
     const uint32_t warp = warp_id(), lane = lane_id();
     const bool bf16 = args.x_bf16 != 0;
-    const SkLayout L = sk_layout(args.n_pad, bf16, args.N, kShort);
+    const int tm = args.tm;
+    const int x_slot = sk_x_slot(tm);
+    const SkLayout L = sk_layout(args.n_pad, bf16, args.N, kShort, x_slot);
     constexpr int BS = sk_rings(kShort), WS = sk_rings(kShort);
     const int XS = L.xs;
     const int S = args.splits;
     const int rank = static_cast<int>(blockIdx.x);  // cluster rank along K
-    const int tm = args.tm;
     const int m0 = static_cast<int>(blockIdx.y) * tm;
     const int st0 = rank * args.stages;              // first 256-wide stage of this CTA
     const int nblk = 4 * args.stages;                // 64-wide K blocks of this CTA
@@ -150,7 +159,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     const uint32_t acc_full = b_empty + 8 * SK_MAX_RING, drain = acc_full + 8;
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + L.off_misc);  // [0] tensor memory, [1] abort
     const Ctl ctl{misc + 1, args.status, args.timeout_cycles, args.drain_cycles};
-    const int x_pre = min(XS, nblk), w_pre = min(WS, args.stages);  // copies started at set-up
+    const int x_pre = min(min(XS, SK_X_PRE), nblk), w_pre = min(WS, args.stages);  // copies started at set-up
     const uint32_t w_bytes = static_cast<uint32_t>(R) * Q4K_BLOCK_BYTES;
     const uint32_t x_bytes = static_cast<uint32_t>(tm) * 128u;  // one TMA box: tm rows of 64 values
 
@@ -180,16 +189,19 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         // first and its value used only after the copies are issued, so that its
         // latency (about 1 us once every CTA's copies are queued) overlaps theirs.
         const uint32_t status_now = *reinterpret_cast<volatile uint32_t *>(args.status);
-        // The first x tiles and weight stages start before the block-wide barrier
-        // (their slots are empty); this thread is also the x producer.
-        for (int j = 0; j < x_pre; ++j) {
-            mbar_arrive_expect_tx(x_full + 8 * j, x_bytes);
-            tma_load_2d(smem_u32(smem + j * SK_X_SLOT), &tmap_x, (4 * st0 + j) * CHUNK_K, m0, x_full + 8 * j);
-        }
+        // The first weight stages and x tiles start before the block-wide barrier
+        // (their slots are empty); this thread is also the x producer.  Weights
+        // first: their transform stands between the first x tile and its MMAs.
+        // At most SK_X_PRE x tiles here (more, issued one by one before the
+        // barrier, delayed every role: 1 us at M=4096, N=32, K=4096).
         for (int i = 0; i < w_pre; ++i) {
             mbar_arrive_expect_tx(w_full + 8 * i, w_bytes);
             bulk_copy_g2s(smem_u32(smem + L.off_w + i * L.w_slot), args.w + q4k_group_offset(args.K, 0, R, st0 + i),
                           w_bytes, w_full + 8 * i);
+        }
+        for (int j = 0; j < x_pre; ++j) {
+            mbar_arrive_expect_tx(x_full + 8 * j, x_bytes);
+            tma_load_2d(smem_u32(smem + j * x_slot), &tmap_x, (4 * st0 + j) * CHUNK_K, m0, x_full + 8 * j);
         }
         misc[1] = (status_now & kStatusTimeoutMask) ? 1u : 0u;
     }
@@ -214,7 +226,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
             for (; j < nblk; ++j) {
                 if (j >= XS && !wait_bar(x_empty + 8 * xs, ph ^ 1, ctl, SW_X_EMPTY)) break;
                 mbar_arrive_expect_tx(x_full + 8 * xs, x_bytes);
-                tma_load_2d(smem_u32(smem + xs * SK_X_SLOT), &tmap_x, (4 * st0 + j) * CHUNK_K, m0, x_full + 8 * xs);
+                tma_load_2d(smem_u32(smem + xs * x_slot), &tmap_x, (4 * st0 + j) * CHUNK_K, m0, x_full + 8 * xs);
                 if (++xs == XS) {
                     xs = 0;
                     ph ^= 1;
@@ -256,7 +268,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
                 for (int blk = 0; blk < 4; ++blk) {
                     if (!(ok = __all_sync(0xffffffffu, wait_bar(x_full + 8 * xs, xph, ctl, SW_X_FULL)))) break;
                     tc_fence_after();
-                    const uint64_t a_desc = smem_desc_sw128(smem_u32(smem + xs * SK_X_SLOT));
+                    const uint64_t a_desc = smem_desc_sw128(smem_u32(smem + xs * x_slot));
                     const uint64_t b_desc =
                         smem_desc_sw128(smem_u32(smem + L.off_b + bs * L.b_slot) + blk * b_blk);
                     if (elect_one()) {
@@ -346,11 +358,12 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         if (acc_ok) tc_fence_after();
     }
 
-    // The accumulator: warps 3..6 (lane quarters 3, 0, 1, 2) hold token rows
-    // 32q .. 32q+31 of the tile, n_pad columns each (bf16 x: the hi sums, then
-    // n_pad columns of lo sums, added here).  S == 1: straight to y.  S > 1:
-    // into this CTA's x ring, [row][n_pad + 4], for the cluster's reduction (every
-    // x tile has been consumed once the accumulator is complete).
+    // The accumulator: warps 3..6 (lane quarters 3, 0, 1, 2) hold rows 32q ..
+    // 32q+31 of the MMA's 128, n_pad columns each (bf16 x: the hi sums, then
+    // n_pad columns of lo sums, added here); rows from tm on are not the tile's
+    // and are dropped.  S == 1: straight to y.  S > 1: into this CTA's x ring,
+    // [row][n_pad + 4], for the cluster's reduction (every x tile has been
+    // consumed once the accumulator is complete).
     const int pstride = args.n_pad + 4;
     float *pbuf = reinterpret_cast<float *>(smem);
     if (warp >= SK_XFORM0) {
@@ -376,7 +389,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
                         for (int e = 0; e < 16; ++e)
                             if (c0 + e < args.N) yr[e] = __uint_as_float(v[e]);
                     }
-                } else {
+                } else if (row < tm) {
 #pragma unroll
                     for (int e = 0; e < 16; e += 4)
                         *reinterpret_cast<float4 *>(pbuf + row * pstride + c0 + e) =
@@ -599,7 +612,7 @@ int launch_skinny(const void *w, const void *x, bool x_bf16, float *y, int64_t M
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    const bool short_k = sk_short(a.n_pad, x_bf16, a.N, a.stages);
+    const bool short_k = sk_short(a.n_pad, x_bf16, a.N, a.stages, sk_x_slot(tm));
     if (cudaLaunchKernelEx(&cfg, short_k ? qwp_skinny_kernel<true> : qwp_skinny_kernel<false>, map, a) !=
         cudaSuccess) {
         cudaGetLastError();
