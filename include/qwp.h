@@ -394,8 +394,8 @@ QWP_API int qwp_decode_selected(int format, int64_t M, int64_t N, int64_t K);
  * it reads the device's properties but launches nothing).  `format`: 0 W4A16,
  * 1 Q4_K, 2 Q6_K.  plan_out[6] receives: [0] the kernel (1 the prefill kernel,
  * 2 the decode kernel, which leaves [1..5] at 0, 3 the skinny-N kernel, which
- * reports its split, clusters and token tile (at most 128 tokens; the plan of
- * bf16 activations) the same way and 1 unit per cluster); [1] the split-K factor S (the
+ * reports its split, clusters and token tile (at most 128 tokens) the same
+ * way and 1 unit per cluster); [1] the split-K factor S (the
  * cluster size); [2] the clusters launched; [3] the token tile (tokens per
  * unit); [4] the units (128-row tiles x token tiles); [5] the units per cluster
  * at most.  Returns QWP_OK, QWP_ERR_INVALID_ARG (NULL plan_out, a size below 1,

@@ -383,8 +383,7 @@ def gemm_plan(fmt: str, M: int, N: int, K: int) -> dict:
     """The launch a GEMM call of this shape gets on the current device: kernel
     ("prefill", "decode" or "skinny"), split-K factor, clusters, token tile, units
     and units per cluster (zero for the decode kernel; the skinny-N kernel reports
-    its cluster size, token tiles, tokens per tile (<= 128, the plan for bf16 x),
-    token tiles and 1)."""
+    its cluster size, token tiles, tokens per tile (<= 128), token tiles and 1)."""
     out = (ctypes.c_int32 * 6)()
     _check(library().qwp_gemm_plan(_PLAN_FORMATS[fmt], int(M), int(N), int(K), ctypes.cast(out, ctypes.c_void_p)),
            "qwp_gemm_plan")

@@ -1603,7 +1603,7 @@ extern "C" int qwp_gemm_plan(int format, int64_t M, int64_t N, int64_t K, int32_
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return QWP_ERR_CUDA;
-        if ((rc = skinny_plan(M, K, true, sms, S, tiles, tm))) return rc;  // the bf16-x entry point's plan
+        if ((rc = skinny_plan(M, K, sms, S, tiles, tm))) return rc;
         plan_out[0] = 3;
         plan_out[1] = S;
         plan_out[2] = static_cast<int32_t>(tiles);

@@ -67,7 +67,7 @@ constexpr int64_t SKINNY_MIN_TOKENS = 256;
 bool skinny_selected(int fmt, int64_t M, int64_t N, int64_t K);
 // Its launch: `splits` CTAs per cluster along K, `tiles` token tiles of `tm`
 // (<= 128) tokens.
-int skinny_plan(int64_t M, int64_t K, bool x_bf16, int sms, int &splits, int64_t &tiles, int &tm);
+int skinny_plan(int64_t M, int64_t K, int sms, int &splits, int64_t &tiles, int &tm);
 int launch_skinny(const void *w, const void *x, bool x_bf16, float *y, int64_t M, int64_t N, int64_t K,
                   cudaStream_t stream);
 

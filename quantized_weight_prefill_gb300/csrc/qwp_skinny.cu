@@ -532,16 +532,17 @@ bool skinny_selected(int fmt, int64_t M, int64_t N, int64_t K) {
 // Launch plan: S CTAs per cluster along K (a power of two up to 8 dividing the
 // 256-wide stages) and token tiles of tm <= 128 rows, cut so that the clusters run
 // in whole waves of resident clusters.  Per CTA and 64-wide K block the time is
-// the larger of its x stream (tm rows of 128 bytes) and its MMAs (128 rows
-// whatever tm is: two per K step for bf16 x), plus a fixed cost per wave and one
-// for the cluster reduction; the cheapest plan wins.  In units of the stream
-// time of one 128-byte row at the full-GPU rate (~3 ns on GB300): the MMAs of a
-// block cost 77 rows (bf16 x) or 39 (fp16 x), a wave or a reduction ~2 us.
-int skinny_plan(int64_t M, int64_t K, bool x_bf16, int sms, int &splits, int64_t &tiles, int &tm) {
+// the larger of its x stream (tm rows of 128 bytes) and a floor set by its MMAs
+// (128 rows whatever tm is), plus a fixed cost per wave and one for the cluster
+// reduction; the cheapest plan wins.  In units of the stream time of one
+// 128-byte row at the full-GPU rate (~3 ns on GB300): the floor is 77 rows, a
+// wave or a reduction ~2 us.  (Timed on GB300 at M = 1024 ... 32768, N = 32,
+// K = 4096, this picks the fastest of the forced plans at every size.)
+int skinny_plan(int64_t M, int64_t K, int sms, int &splits, int64_t &tiles, int &tm) {
     const int64_t nst = K / Q4K_BLOCK;
     int dummy = 0;
     if (sk_device_sms(dummy)) return QWP_ERR_CUDA;
-    const int64_t mma_rows = x_bf16 ? 77 : 39, fixed = 625;
+    const int64_t mma_rows = 77, fixed = 625;
     double best = 1e300;
     splits = 0;
     for (int S = 1; S <= 8 && nst % S == 0; S *= 2) {
@@ -572,7 +573,7 @@ int launch_skinny(const void *w, const void *x, bool x_bf16, float *y, int64_t M
     if ((rc = sk_device_sms(sms))) return rc;
     int S = 1, tm = SK_TOKENS;
     int64_t tiles = 0;
-    if ((rc = skinny_plan(M, K, x_bf16, sms, S, tiles, tm))) return rc;
+    if ((rc = skinny_plan(M, K, sms, S, tiles, tm))) return rc;
     SkEncodeTiledFn fn = sk_encode_fn();
     if (!fn) return QWP_ERR_CUDA;
     CUtensorMap map;
