@@ -75,7 +75,7 @@ extern "C" int q4k_gemm_noalloc(const void *w_tiled, const void *x, float *y, in
     if (dec_need && dec_need <= kDecodeScratchBytes)
         return launch_decode(DFMT_Q4K, w_tiled, nullptr, nullptr, x, true, y, M, N, K, 0, dec, kDecodeScratchBytes,
                              static_cast<cudaStream_t>(stream));
-    // The skinny-N kernel converts x in shared memory and allocates nothing.
+    // The skinny-N kernel reads bf16 x as it is and allocates nothing.
     if (skinny_selected(DFMT_Q4K, M, N, K))
         return launch_skinny(w_tiled, x, true, y, M, N, K, static_cast<cudaStream_t>(stream));
     // The conversion writes all M*K elements the GEMM reads, so nothing left
