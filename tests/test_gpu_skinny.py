@@ -77,8 +77,9 @@ def test_skinny_f16_against_oracle(M, N, K):
 
 
 def test_skinny_stress_shape_sampled_rows():
-    """The workload's skinny gate projection: M=4096, N=32, K=4096, every token row
-    of the first, last and two middle token tiles against the oracle."""
+    """The workload's skinny gate projection: M=4096, N=32, K=4096; token rows 0-127,
+    1920-2175 and the last 128 (spanning several token tiles and their boundaries,
+    the ragged last tile included) against the oracle."""
     M, N, K = 4096, 32, 4096
     blocks, w, xb, x = _setup(M, N, K, seed=601)
     y = qwp.q4k_gemm(w, x, N).cpu().numpy()
